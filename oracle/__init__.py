@@ -1,0 +1,156 @@
+"""fp64 CPU oracle for the batch-invariant linear layer and RMSNorm.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` are its only callers. The product library never
+imports, links or runs anything here, and this package imports nothing from
+the product (the seeded input generator ``bi_synth`` is the one module both
+sides use).
+
+The arithmetic lives in ``oracle.c`` (plain loops, fp64, one sequential sum per
+output element). This module compiles it with the host C compiler and wraps it
+with numpy arrays.
+
+Parity pins (see tests/test_oracle.py): every routine here is checked against
+brute force in exact rational arithmetic on small integer / dyadic inputs,
+closed forms and the format definitions; none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "_liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into _liboracle.so (OpenMP if the compiler has it).
+
+    -ffp-contract=off keeps every multiply and add separately rounded (no FMA
+    contraction), so results are identical on x86-64 and aarch64 hosts."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    cc = os.environ.get("CC", "gcc")
+    base = [cc, "-O2", "-ffp-contract=off", "-fno-fast-math", "-shared", "-fPIC", _SRC, "-o", _LIB + ".tmp", "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(_LIB + ".tmp", _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P, I64, D = ctypes.c_void_p, ctypes.c_int64, ctypes.c_double
+            lib.oracle_gemm_bf16.argtypes = [I64, I64, I64, P, I64, P, I64, P, I64]
+            lib.oracle_grouped_gemm_bf16.argtypes = [ctypes.c_int32, P, I64, I64, P, P, P]
+            lib.oracle_gemm_nvfp4.argtypes = [I64, I64, I64, P, P, P, P, D, P]
+            lib.oracle_rmsnorm.argtypes = [I64, I64, P, P, P, D, P, P]
+            lib.oracle_e2m1_value.argtypes = [ctypes.c_uint]
+            lib.oracle_e2m1_value.restype = D
+            lib.oracle_e4m3_value.argtypes = [ctypes.c_uint]
+            lib.oracle_e4m3_value.restype = D
+            lib.oracle_bf16_value.argtypes = [ctypes.c_uint16]
+            lib.oracle_bf16_value.restype = D
+            lib.oracle_bf16_round.argtypes = [D]
+            lib.oracle_bf16_round.restype = ctypes.c_uint16
+            lib.oracle_threads.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _p(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def threads() -> int:
+    """OpenMP threads the oracle's loops use."""
+    return int(_load().oracle_threads())
+
+
+def gemm_bf16(X: np.ndarray, W: np.ndarray) -> np.ndarray:
+    """Y = X W^T in fp64 from bf16 bit patterns X [M,K], W [N,K]."""
+    X, W = _c(X, np.uint16), _c(W, np.uint16)
+    M, K = X.shape
+    N, K2 = W.shape
+    assert K == K2
+    Y = np.zeros((M, N), dtype=np.float64)
+    if M and N:
+        _load().oracle_gemm_bf16(M, N, K, _p(X), K, _p(W), K, _p(Y), N)
+    return Y
+
+
+def grouped_gemm_bf16(X: np.ndarray, W: np.ndarray, offsets: np.ndarray) -> np.ndarray:
+    """Per-expert Y[r] = X[r] W[e]^T for rows r in [offsets[e], offsets[e+1])."""
+    X, W, off = _c(X, np.uint16), _c(W, np.uint16), _c(offsets, np.int32)
+    E, N, K = W.shape
+    rows = int(off[-1])
+    assert X.shape == (rows, K) and len(off) == E + 1
+    Y = np.zeros((rows, N), dtype=np.float64)
+    if rows and N:
+        _load().oracle_grouped_gemm_bf16(E, _p(off), N, K, _p(X), _p(W), _p(Y))
+    return Y
+
+
+def gemm_nvfp4(A, SA, B, SB, alpha) -> np.ndarray:
+    """Y = alpha * dequant(A) dequant(B)^T in fp64; scales row-major [rows, K/16]."""
+    A, SA, B, SB = (_c(t, np.uint8) for t in (A, SA, B, SB))
+    M, KB = A.shape
+    N = B.shape[0]
+    K = KB * 2
+    assert B.shape == (N, KB) and SA.shape == (M, K // 16) and SB.shape == (N, K // 16)
+    Y = np.zeros((M, N), dtype=np.float64)
+    if M and N:
+        _load().oracle_gemm_nvfp4(M, N, K, _p(A), _p(SA), _p(B), _p(SB), float(alpha), _p(Y))
+    return Y
+
+
+def rmsnorm(x, w, eps: float, residual=None):
+    """RMSNorm of bf16 rows (optionally after the residual add).
+
+    Returns (y fp64 [M,H], h_bits uint16 [M,H] or None), where h_bits is the
+    rounded sum bf16(x + residual) that the kernel writes back to residual."""
+    x, w = _c(x, np.uint16), _c(w, np.uint16)
+    M, H = x.shape
+    y = np.zeros((M, H), dtype=np.float64)
+    h = None
+    rp = None
+    if residual is not None:
+        residual = _c(residual, np.uint16)
+        h = np.zeros((M, H), dtype=np.uint16)
+        rp = _p(residual)
+    if M:
+        _load().oracle_rmsnorm(M, H, _p(x), rp, _p(w), float(eps), _p(y),
+                               _p(h) if h is not None else None)
+    return y, h
+
+
+def e2m1_value(code: int) -> float:
+    return float(_load().oracle_e2m1_value(code))
+
+
+def e4m3_value(code: int) -> float:
+    return float(_load().oracle_e4m3_value(code))
+
+
+def bf16_value(bits: int) -> float:
+    return float(_load().oracle_bf16_value(bits))
+
+
+def bf16_round(v: float) -> int:
+    return int(_load().oracle_bf16_round(float(v)))

@@ -1,0 +1,195 @@
+/*
+ * oracle.c -- plain, slow fp64 CPU oracle for the batch-invariant linear layer
+ * and RMSNorm.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing on the product path links, loads or calls
+ * this file; only the tests, the smoke check and the bench's CPU-baseline leg
+ * do. It shares no code, header, table or constant with the CUDA library.
+ *
+ * Every routine evaluates the plain definition of what the kernel computes, in
+ * fp64, on the same stored (bf16 / e2m1 / e4m3) values the kernel reads, with
+ * no blocking, fusion or reordering: loops run in index order. Rows are
+ * distributed over OpenMP threads (each output element is still one
+ * sequential sum), which changes nothing but wall time.
+ *
+ * Sources (web pages on batch invariance in vLLM serving):
+ *  - Batch invariance: a request's output does not depend on batch size or
+ *    on request order (vllm-ascend "Batch Invariance" guide, introduction).
+ *  - Linear layer Y = X W^T over nn.Linear weights; its NVFP4 form
+ *    alpha * (A_fp4 . sf_A)(B_fp4 . sf_B)^T with alpha = 1/(gs_A gs_B)
+ *    (vLLM PR #39912 "NVFP4 CUTLASS batch invariant mode", test code);
+ *    the dequantise-then-multiply reading is the "emulation" backend of the
+ *    same PR's kernel selector.
+ *  - RMSNorm after the residual add (vLLM PR #51292, fused all-reduce +
+ *    RMSNorm, Purpose / root-cause discussion). The pages give no formula;
+ *    the standard y = h / sqrt(mean(h^2) + eps) * w is used.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* bf16 is the upper half of an IEEE binary32; widening is exact. */
+static double bf16_to_double(uint16_t bits)
+{
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Round a double to the nearest bf16 (ties to even mantissa). bf16 keeps 8
+ * significant bits; its smallest exponent is that of binary32 (subnormal
+ * quantum 2^-133); values past the largest finite bf16 become infinity. */
+static uint16_t double_to_bf16(double v)
+{
+    if (isnan(v)) return 0x7FC0;
+    if (v == 0.0) return signbit(v) ? 0x8000 : 0x0000;
+    int e;
+    (void)frexp(fabs(v), &e);                  /* |v| = m * 2^e, m in [0.5, 1) */
+    int qexp = e - 8;                          /* quantum of an 8-bit significand */
+    if (qexp < -133) qexp = -133;
+    double q = ldexp(1.0, qexp);
+    double r = nearbyint(v / q) * q;           /* default rounding: nearest, ties even */
+    float f = (float)r;                        /* exact: r has <= 8 significant bits */
+    if (fabs(r) > 3.3895313892515355e38) f = signbit(r) ? -INFINITY : INFINITY;
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(u >> 16);
+}
+
+/* e2m1: sign bit 3, exponent bits 2..1 (bias 1), mantissa bit 0; exponent 0
+ * is subnormal (0 or 0.5). OCP Microscaling Formats spec, FP4 E2M1. */
+static double e2m1_to_double(unsigned code)
+{
+    unsigned s = (code >> 3) & 1u, e = (code >> 1) & 3u, m = code & 1u;
+    double mag = (e == 0) ? 0.5 * m : ldexp(1.0 + 0.5 * m, (int)e - 1);
+    return s ? -mag : mag;
+}
+
+/* e4m3 (FN): sign bit 7, exponent bits 6..3 (bias 7), mantissa bits 2..0;
+ * exponent 0 is subnormal (m/8 * 2^-6); S.1111.111 is NaN; no infinities.
+ * OCP 8-bit Floating Point spec, E4M3. */
+static double e4m3_to_double(unsigned code)
+{
+    unsigned s = (code >> 7) & 1u, e = (code >> 3) & 15u, m = code & 7u;
+    if (e == 15 && m == 7) return NAN;
+    double mag = (e == 0) ? ldexp(m / 8.0, -6) : ldexp(1.0 + m / 8.0, (int)e - 7);
+    return s ? -mag : mag;
+}
+
+/* Exported decoders (used by the format pins). */
+double oracle_e2m1_value(unsigned code) { return e2m1_to_double(code & 15u); }
+double oracle_e4m3_value(unsigned code) { return e4m3_to_double(code & 255u); }
+double oracle_bf16_value(uint16_t bits) { return bf16_to_double(bits); }
+uint16_t oracle_bf16_round(double v) { return double_to_bf16(v); }
+
+int oracle_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* Y[i][j] = sum_{k=0}^{K-1} X[i][k] * W[j][k]   (linear layer, Y = X W^T).
+ * X: bf16 [M][ldx], W: bf16 [N][ldw] (nn.Linear layout), Y: fp64 [M][ldy]. */
+void oracle_gemm_bf16(int64_t M, int64_t N, int64_t K,
+                      const uint16_t *X, int64_t ldx,
+                      const uint16_t *W, int64_t ldw,
+                      double *Y, int64_t ldy)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < M; ++i) {
+        for (int64_t j = 0; j < N; ++j) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                acc += bf16_to_double(X[i * ldx + k]) * bf16_to_double(W[j * ldw + k]);
+            Y[i * ldy + j] = acc;
+        }
+    }
+}
+
+/* Grouped (MoE expert) linear layers: rows offsets[e] .. offsets[e+1]-1 of X
+ * belong to expert e and are multiplied by that expert's weight W[e] ([N][K]).
+ * X: bf16 [offsets[E]][K], W: bf16 [E][N][K], Y: fp64 [offsets[E]][N]. */
+void oracle_grouped_gemm_bf16(int32_t E, const int32_t *offsets, int64_t N, int64_t K,
+                              const uint16_t *X, const uint16_t *W, double *Y)
+{
+    for (int32_t e = 0; e < E; ++e) {
+        const int64_t r0 = offsets[e], r1 = offsets[e + 1];
+        const uint16_t *We = W + (int64_t)e * N * K;
+#pragma omp parallel for schedule(static)
+        for (int64_t i = r0; i < r1; ++i) {
+            for (int64_t j = 0; j < N; ++j) {
+                double acc = 0.0;
+                for (int64_t k = 0; k < K; ++k)
+                    acc += bf16_to_double(X[i * K + k]) * bf16_to_double(We[j * K + k]);
+                Y[i * N + j] = acc;
+            }
+        }
+    }
+}
+
+/* Block-scaled NVFP4 linear layer, dequantised in fp64:
+ *   Y[i][j] = alpha * sum_k (a[i][k] * sa[i][k/16]) * (b[j][k] * sb[j][k/16])
+ * A: packed e2m1 [M][K/2] (element k in byte k/2, low nibble for even k),
+ * SA: e4m3 [M][K/16] row-major; B, SB likewise with N rows; Y fp64 [M][N]. */
+void oracle_gemm_nvfp4(int64_t M, int64_t N, int64_t K,
+                       const uint8_t *A, const uint8_t *SA,
+                       const uint8_t *B, const uint8_t *SB,
+                       double alpha, double *Y)
+{
+    const int64_t KB = K / 2, KS = K / 16;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < M; ++i) {
+        for (int64_t j = 0; j < N; ++j) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                unsigned abyte = A[i * KB + k / 2], bbyte = B[j * KB + k / 2];
+                unsigned ac = (k & 1) ? (abyte >> 4) : (abyte & 15u);
+                unsigned bc = (k & 1) ? (bbyte >> 4) : (bbyte & 15u);
+                double av = e2m1_to_double(ac) * e4m3_to_double(SA[i * KS + k / 16]);
+                double bv = e2m1_to_double(bc) * e4m3_to_double(SB[j * KS + k / 16]);
+                acc += av * bv;
+            }
+            Y[i * N + j] = alpha * acc;
+        }
+    }
+}
+
+/* RMSNorm with optional residual add, per row i:
+ *   h = residual ? bf16(x + residual) : x         (the stored, rounded sum)
+ *   y = h / sqrt( (1/H) sum_k h_k^2 + eps ) * w
+ * x, residual: bf16 [M][H]; w: bf16 [H]; y: fp64 [M][H];
+ * h_out (nullable): bf16 bits of h, what the kernel writes back to residual. */
+void oracle_rmsnorm(int64_t M, int64_t H, const uint16_t *x, const uint16_t *residual,
+                    const uint16_t *w, double eps, double *y, uint16_t *h_out)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < M; ++i) {
+        double ss = 0.0;
+        for (int64_t k = 0; k < H; ++k) {
+            double h;
+            if (residual) {
+                uint16_t hb = double_to_bf16(bf16_to_double(x[i * H + k]) +
+                                             bf16_to_double(residual[i * H + k]));
+                if (h_out) h_out[i * H + k] = hb;
+                h = bf16_to_double(hb);
+            } else {
+                h = bf16_to_double(x[i * H + k]);
+            }
+            ss += h * h;
+        }
+        double r = 1.0 / sqrt(ss / (double)H + eps);
+        for (int64_t k = 0; k < H; ++k) {
+            double h = residual ? bf16_to_double(double_to_bf16(bf16_to_double(x[i * H + k]) +
+                                                                bf16_to_double(residual[i * H + k])))
+                                : bf16_to_double(x[i * H + k]);
+            y[i * H + k] = h * r * bf16_to_double(w[k]);
+        }
+    }
+}

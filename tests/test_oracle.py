@@ -1,0 +1,259 @@
+"""Pins for the fp64 oracle (CPU only).
+
+Each test checks the oracle against something other than itself: brute force
+in exact rational arithmetic on small integer or dyadic inputs, closed forms,
+hand-worked fixtures under tests/golden/, the storage-format definitions, or an
+independent library routine. They are chosen so that a dropped term, a wrong
+sign or index, a transposed operand or a misplaced eps fails at least one.
+"""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import bi_synth as syn
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _frac(s: str):
+    return None if s == "NaN" else Fraction(s)
+
+
+def _bf16_frac(bits: int) -> Fraction:
+    return Fraction(float(syn.bf16_bits_to_f32(np.array([bits], dtype=np.uint16))[0]))
+
+
+# ------------------------------------------------------------------ formats
+
+def test_format_tables_match_golden():
+    n = 0
+    with open(os.path.join(GOLDEN, "formats.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if not line:
+                continue
+            fmt, code, val = line.split()
+            code = int(code, 16)
+            want = _frac(val)
+            got = oracle.e2m1_value(code) if fmt == "e2m1" else oracle.e4m3_value(code)
+            if want is None:
+                assert math.isnan(got)
+            else:
+                assert Fraction(got) == want, (fmt, hex(code), got, want)
+            n += 1
+    assert n >= 30
+
+
+def test_e4m3_matches_torch_float8():
+    torch = pytest.importorskip("torch")
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle.e4m3_value(int(c)) for c in codes])
+    nan = np.isnan(ref)
+    assert np.array_equal(nan, np.isnan(got))
+    assert np.array_equal(ref[~nan], got[~nan])
+
+
+def test_e2m1_structure():
+    vals = [oracle.e2m1_value(c) for c in range(16)]
+    assert vals[:8] == sorted(vals[:8])                   # positive codes increase
+    assert all(vals[c + 8] == -vals[c] for c in range(8))  # bit 3 is the sign
+    assert max(vals) == 6.0
+
+
+def test_bf16_round_golden():
+    with open(os.path.join(GOLDEN, "bf16_rounding.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if not line:
+                continue
+            v, bits = line.split()
+            assert oracle.bf16_round(float(Fraction(v))) == int(bits, 16), line
+
+
+def test_bf16_round_exhaustive_against_neighbours():
+    """Round-trip every positive finite bf16 and check midpoints between
+    neighbours go to the even pattern (ties-to-even, by construction)."""
+    bits = np.arange(0x0001, 0x7F80, 37, dtype=np.uint16)
+    for b in bits:
+        v = oracle.bf16_value(int(b))
+        assert oracle.bf16_round(v) == b
+        nxt = oracle.bf16_value(int(b) + 1)
+        mid = (Fraction(v) + Fraction(nxt)) / 2
+        want = b if b % 2 == 0 else b + 1
+        assert oracle.bf16_round(float(mid)) == want
+
+
+# -------------------------------------------------------------------- GEMM
+
+def _brute_gemm(X_bits, W_bits):
+    X = [[_bf16_frac(int(v)) for v in row] for row in X_bits]
+    W = [[_bf16_frac(int(v)) for v in row] for row in W_bits]
+    return [[sum(x * w for x, w in zip(xr, wr)) for wr in W] for xr in X]
+
+
+@pytest.mark.parametrize("M,N,K", [(5, 7, 64), (3, 11, 256), (1, 16, 48)])
+def test_gemm_exact_vs_bruteforce(M, N, K):
+    X = syn.integer_bf16(1, 0, (M, K))
+    W = syn.integer_bf16(1, 1, (N, K))
+    Y = oracle.gemm_bf16(X, W)
+    ref = _brute_gemm(X, W)
+    for i in range(M):
+        for j in range(N):
+            assert Fraction(Y[i, j]) == ref[i][j]
+
+
+def test_gemm_identity_and_onehot():
+    K = 32
+    X = syn.integer_bf16(2, 0, (6, K))
+    eye = syn.to_bf16_bits(np.eye(K, dtype=np.float32))
+    assert np.array_equal(oracle.gemm_bf16(X, eye), syn.bf16_bits_to_f32(X).astype(np.float64))
+    W = syn.integer_bf16(2, 1, (9, K))
+    for k in (0, 5, K - 1):
+        onehot = np.zeros((1, K), dtype=np.float32)
+        onehot[0, k] = 1.0
+        Y = oracle.gemm_bf16(syn.to_bf16_bits(onehot), W)
+        assert np.array_equal(Y[0], syn.bf16_bits_to_f32(W[:, k]).astype(np.float64))
+
+
+def test_gemm_close_to_numpy_fp64():
+    X, W = syn.gemm_inputs(17, 40, 256, seed=3)
+    Y = oracle.gemm_bf16(X, W)
+    ref = syn.bf16_bits_to_f32(X).astype(np.float64) @ syn.bf16_bits_to_f32(W).astype(np.float64).T
+    assert np.allclose(Y, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_gemm_rows_independent_of_batch():
+    """Oracle-level invariance: row i alone equals row i of the batch."""
+    X, W = syn.gemm_inputs(9, 24, 128, seed=4)
+    full = oracle.gemm_bf16(X, W)
+    for i in range(9):
+        assert np.array_equal(oracle.gemm_bf16(X[i:i + 1], W)[0], full[i])
+
+
+def test_grouped_vs_bruteforce():
+    E, N, K = 5, 6, 32
+    counts = [3, 0, 1, 4, 0]
+    off = syn.offsets_from_counts(counts)
+    X = syn.integer_bf16(5, 0, (int(off[-1]), K))
+    W = syn.integer_bf16(5, 1, (E, N, K))
+    Y = oracle.grouped_gemm_bf16(X, W, off)
+    for e in range(E):
+        for r in range(off[e], off[e + 1]):
+            ref = _brute_gemm(X[r:r + 1], W[e])[0]
+            assert [Fraction(v) for v in Y[r]] == ref
+
+
+# ------------------------------------------------------------------- NVFP4
+
+def _brute_nvfp4(A, SA, B, SB, alpha):
+    def deq(q, s, i, k):
+        byte = int(q[i, k // 2])
+        code = (byte >> 4) if k % 2 else (byte & 15)
+        return Fraction(oracle.e2m1_value(code)) * Fraction(oracle.e4m3_value(int(s[i, k // 16])))
+    M, N, K = A.shape[0], B.shape[0], A.shape[1] * 2
+    return [[Fraction(alpha) * sum(deq(A, SA, i, k) * deq(B, SB, j, k) for k in range(K))
+             for j in range(N)] for i in range(M)]
+
+
+def test_nvfp4_exact_vs_bruteforce():
+    g = syn.rng(7, 0)
+    M, N, K = 3, 5, 64
+    A = g.integers(0, 256, size=(M, K // 2), dtype=np.uint8)
+    B = g.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    SA = g.integers(0x30, 0x41, size=(M, K // 16), dtype=np.uint8)   # 0.5 .. 2
+    SB = g.integers(0x30, 0x41, size=(N, K // 16), dtype=np.uint8)
+    alpha = 0.25
+    Y = oracle.gemm_nvfp4(A, SA, B, SB, alpha)
+    ref = _brute_nvfp4(A, SA, B, SB, alpha)
+    for i in range(M):
+        for j in range(N):
+            assert Fraction(Y[i, j]) == ref[i][j]
+
+
+def test_nvfp4_nibble_order_and_scale_index():
+    """One nonzero element at an odd k in block 2: only the high nibble of
+    byte k/2 and scale k/16 may contribute."""
+    K = 64
+    A = np.zeros((1, K // 2), dtype=np.uint8)
+    B = np.zeros((1, K // 2), dtype=np.uint8)
+    k = 37                               # odd -> high nibble; block 37//16 = 2
+    A[0, k // 2] = 0x2 << 4              # +1.0 in the high nibble
+    B[0, k // 2] = (0x7 << 4) | 0x5      # +6.0 high, +3.0 low (k = 36)
+    SA = np.full((1, 4), 0x38, dtype=np.uint8)
+    SB = np.full((1, 4), 0x38, dtype=np.uint8)
+    SA[0, 2] = 0x40                      # 2.0 for block 2
+    SB[0, 1] = 0x48                      # a wrong block index would pick up 4.0
+    Y = oracle.gemm_nvfp4(A, SA, B, SB, 1.0)
+    assert Y[0, 0] == 1.0 * 2.0 * 6.0
+
+
+def test_nvfp4_unit_scales_integer_case():
+    """Unit scales, alpha 1: the result is a plain dot product of e2m1 values."""
+    g = syn.rng(8, 0)
+    codes_a = g.integers(0, 16, size=(2, 128))
+    codes_b = g.integers(0, 16, size=(4, 128))
+    pack = lambda c: (c[:, 0::2] | (c[:, 1::2] << 4)).astype(np.uint8)
+    one = lambda r: np.full((r, 8), 0x38, dtype=np.uint8)
+    Y = oracle.gemm_nvfp4(pack(codes_a), one(2), pack(codes_b), one(4), 1.0)
+    tab = syn._E2M1
+    val = lambda c: np.where(c >= 8, -tab[c & 7], tab[c & 7])
+    assert np.array_equal(Y, val(codes_a) @ val(codes_b).T)
+
+
+# ----------------------------------------------------------------- RMSNorm
+
+def test_rmsnorm_golden_cases():
+    with open(os.path.join(GOLDEN, "rmsnorm_cases.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if not line:
+                continue
+            _, eps, h, w, y = line.split()
+            h = np.array([float(v) for v in h.split(",")], dtype=np.float32)[None]
+            w = np.array([float(v) for v in w.split(",")], dtype=np.float32)
+            want = np.array([float(v) for v in y.split(",")])
+            got, _ = oracle.rmsnorm(syn.to_bf16_bits(h), syn.to_bf16_bits(w), float(eps))
+            assert np.allclose(got[0], want, rtol=1e-13, atol=1e-15), (line, got)
+
+
+@pytest.mark.parametrize("c", [1.0, 0.001, 37.5, -2.0])
+def test_rmsnorm_constant_row_closed_form(c):
+    H, eps = 64, 1e-6
+    x = syn.to_bf16_bits(np.full((1, H), c, dtype=np.float32))
+    w = syn.to_bf16_bits(np.linspace(0.5, 1.5, H).astype(np.float32))
+    cb = oracle.bf16_value(int(x[0, 0]))
+    y, _ = oracle.rmsnorm(x, w, eps)
+    want = cb / math.sqrt(cb * cb + eps) * syn.bf16_bits_to_f32(w).astype(np.float64)
+    assert np.allclose(y[0], want, rtol=1e-14, atol=0)
+
+
+def test_rmsnorm_scale_invariance():
+    x, _, w, _ = syn.rmsnorm_inputs(4, 256, seed=9, outlier_frac=0)
+    y1, _ = oracle.rmsnorm(x, w, 0.0)
+    x2 = syn.to_bf16_bits(syn.bf16_bits_to_f32(x) * np.float32(64.0))   # exact power-of-two scaling
+    y2, _ = oracle.rmsnorm(x2, w, 0.0)
+    assert np.allclose(y1, y2, rtol=1e-14, atol=1e-15)
+
+
+def test_rmsnorm_residual_is_rounded_sum():
+    x = syn.to_bf16_bits(np.array([[1.0, 1.0, 2.0, -3.0]], dtype=np.float32))
+    r = syn.to_bf16_bits(np.array([[2.0 ** -8, 3 * 2.0 ** -8, 2.0 ** -7, 0.5]], dtype=np.float32))
+    w = syn.to_bf16_bits(np.ones(4, dtype=np.float32))
+    y, h = oracle.rmsnorm(x, w, 1e-6, residual=r)
+    assert list(h[0]) == [0x3F80, 0x3F82, 0x4000, 0xC020]   # ties to even; 2+2^-7 -> 2; -2.5
+    hv = np.array([1.0, 1.0 + 2 ** -6, 2.0, -2.5])
+    want = hv / math.sqrt(np.mean(hv ** 2) + 1e-6)
+    assert np.allclose(y[0], want, rtol=1e-14)
+
+
+def test_rmsnorm_rows_independent():
+    x, res, w, _ = syn.rmsnorm_inputs(7, 128, seed=10)
+    full, hfull = oracle.rmsnorm(x, w, 1e-6, residual=res)
+    for i in range(7):
+        yi, hi = oracle.rmsnorm(x[i:i + 1], w, 1e-6, residual=res[i:i + 1])
+        assert np.array_equal(yi[0], full[i]) and np.array_equal(hi[0], hfull[i])
