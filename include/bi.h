@@ -1,0 +1,203 @@
+/*
+ * bi.h -- libbi: batch-invariant linear layers and RMSNorm for NVIDIA GB300 (sm_103a).
+ *
+ * Batch invariance (vllm-ascend "Batch Invariance" guide, introduction): the
+ * output for one request must not depend on how many other requests share the
+ * batch or on their order. For a linear layer that means every output element
+ * Y[i][j] is the same fp32 sum over k, in the same order, whatever the row
+ * count M, the row's position in the batch and whatever padding rows sit next
+ * to it. libbi gets there by construction:
+ *   - one tile shape, one MMA instruction shape and one K loop per (N, K):
+ *     nothing is chosen from M (vLLM PR #39912, "NVFP4 CUTLASS batch invariant
+ *     mode", fixes its tile scheduler for the same reason);
+ *   - no split-K, no stream-K, no atomics: each output element is reduced by
+ *     one CTA in ascending K order;
+ *   - the RMSNorm reduces each row over a fixed tree that depends only on H.
+ * There is no mode switch and no fallback path: every call is invariant, and
+ * an unsupported argument is an error, never a silent slower path.
+ *
+ * Conventions (all entry points):
+ *  - Pointers are DEVICE pointers owned by the caller, 16-byte aligned; leading
+ *    dimensions are in elements and must keep every row 16-byte aligned.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream). Calls are
+ *    asynchronous on it; argument errors are returned synchronously before
+ *    anything is launched; a failed launch returns BI_ERR_CUDA.
+ *  - libbi allocates no device memory per call and never synchronises inside
+ *    a compute call. It owns one status word per device, set by kernels whose
+ *    bounded waits ran out or that found invalid device-side data
+ *    (bi_device_status reads and clears it).
+ *  - Empty work (M == 0, rows == 0, N == 0) returns BI_OK and launches nothing.
+ *  - The current CUDA device must be an sm_103 GPU, else BI_ERR_ARCH.
+ */
+#ifndef LIBBI_BI_H
+#define LIBBI_BI_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define BI_API __attribute__((visibility("default")))
+#else
+#define BI_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    BI_OK = 0,
+    BI_ERR_INVALID_ARG = 1,   /* null pointer, negative size, bad offsets (host or device side) */
+    BI_ERR_UNSUPPORTED = 2,   /* a size outside what the kernels handle (e.g. K % 8 != 0) */
+    BI_ERR_MISALIGNED = 3,    /* pointer or leading dimension not 16-byte aligned */
+    BI_ERR_ARCH = 4,          /* current device is not sm_103 */
+    BI_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed */
+    BI_ERR_TIMEOUT = 6        /* a kernel's bounded wait ran out; its output is not valid */
+} bi_status;
+
+/* Opaque CUDA stream handle (cudaStream_t). */
+typedef void *bi_stream;
+
+/*
+ * bi_gemm_bf16 -- batch-invariant linear layer  Y = X W^T.
+ *
+ * The batch-invariant bf16 linear layer of the vLLM batch-invariance tracking
+ * issue (#27433, "Basic framework"); row i of Y equals what a call with that
+ * row alone returns, bit for bit (vLLM PR #39912, test
+ * test_nvfp4_gemm_batch_invariance, states the same property for NVFP4).
+ *
+ *   X  bf16 [M][ldx]  row-major activations (first K columns used)
+ *   W  bf16 [N][ldw]  row-major weights, nn.Linear layout (first K columns used)
+ *   Y  bf16 [M][ldy]  output, first N columns written; RNE from the fp32 sum
+ *   Y[i][j] = bf16( sum_{k ascending, 16-element MMA steps} X[i][k] * W[j][k] ), fp32 accumulate
+ *
+ * Requirements: M >= 0, N >= 0, K > 0; K % 8 == 0; N % 8 == 0; ldx, ldw, ldy
+ * multiples of 8 and >= K (ldy >= N); M, N, K < 2^31. Y must not overlap X or W.
+ */
+BI_API bi_status bi_gemm_bf16(const void *X, int64_t ldx, const void *W, int64_t ldw,
+                       void *Y, int64_t ldy, int64_t M, int64_t N, int64_t K,
+                       bi_stream stream);
+
+/*
+ * bi_grouped_gemm_bf16 -- batch-invariant MoE expert linear layers.
+ *
+ * For the MoE models the pages list as tested (Qwen3-30B-A3B, Qwen3-235B-A22B;
+ * vllm-ascend guide, Tested Models): rows are grouped by expert, and rows
+ * offsets[e] .. offsets[e+1]-1 of X are multiplied by expert e's weight:
+ *   Y[r][j] = bf16( sum_k X[r][k] * W[e][j][k] ),  same per-element order as bi_gemm_bf16,
+ * so a token's expert output does not depend on which tokens share its expert.
+ *
+ *   X        bf16 [rows][K]     expert-sorted activations (dense, ld = K)
+ *   W        bf16 [E][N][K]     expert weights (dense)
+ *   Y        bf16 [rows][N]     output (dense, ld = N)
+ *   expert_offsets  int32 [E+1] DEVICE array: 0 = offsets[0] <= ... <= offsets[E] = rows
+ *
+ * The offsets are read on the device (no host synchronisation). If they are
+ * not a non-decreasing sequence from 0 to `rows`, nothing is written and the
+ * device status becomes BI_ERR_INVALID_ARG (see bi_device_status).
+ * Requirements: 1 <= E <= 1024; K % 8 == 0; N % 8 == 0; E*N < 2^31.
+ */
+BI_API bi_status bi_grouped_gemm_bf16(const void *X, const void *W, void *Y,
+                               const int32_t *expert_offsets, int32_t E, int64_t rows,
+                               int64_t N, int64_t K, bi_stream stream);
+
+/*
+ * bi_gemm_nvfp4 -- batch-invariant block-scaled NVFP4 linear layer.
+ *
+ * vLLM PR #39912 ("NVFP4 CUTLASS batch invariant mode"): e2m1 values packed two
+ * per byte (K = 2 * packed_k), one e4m3 scale per 16 consecutive K elements,
+ * per-tensor global scales folded into alpha = 1 / (gs_A * gs_B):
+ *   Y[i][j] = bf16( alpha * sum_k (a[i][k] * sa[i][k/16]) * (b[j][k] * sb[j][k/16]) ), fp32 accumulate
+ *
+ *   A     u8 [M][K/2]  e2m1 codes, element k in byte k/2, low nibble for even k
+ *   B     u8 [N][K/2]  same, weights
+ *   A_sf  u8           e4m3 block scales of A in the interleaved 128x4 layout:
+ *                      scale (r, c) (row r, K block c = k/16) sits at byte
+ *                        ((r/128) * (C/4) + c/4) * 512 + (r%32)*16 + ((r%128)/32)*4 + c%4,
+ *                      C = K/16 (rounded up to a multiple of 4); the buffer holds
+ *                      ceil(M/128)*128 rows (padding rows may hold anything)
+ *   B_sf  u8           same layout for B (ceil(N/128)*128 rows)
+ *   Y     bf16 [M][N]  output (dense, ld = N)
+ * The page calls this scale layout "interleaved" without defining it; the
+ * layout above is the one Blackwell block-scaled MMAs read from tensor memory.
+ * Requirements: K % 64 == 0 and K >= 64; N % 8 == 0.
+ */
+BI_API bi_status bi_gemm_nvfp4(const uint8_t *A, const uint8_t *A_sf, const uint8_t *B,
+                        const uint8_t *B_sf, float alpha, void *Y,
+                        int64_t M, int64_t N, int64_t K, bi_stream stream);
+
+/*
+ * bi_rmsnorm -- RMSNorm with optional residual add and a fixed reduction tree.
+ *
+ * The RMSNorm that vLLM fuses with the tensor-parallel all-reduce (vLLM PR
+ * #51292, Purpose and root-cause discussion: its fused kernel reduces with
+ * shuffles and block reductions whose order varies run to run). Here each row
+ * is reduced by one warp: every lane sums the squares of its elements in
+ * index order, then a fixed xor-shuffle tree combines the 32 lane sums. The
+ * tree depends only on H.
+ *   h = residual ? bf16(x + residual) : x       (written back to residual)
+ *   out = bf16( h * (1 / sqrt(sum(h^2)/H + eps)) * w ),  fp32 arithmetic
+ *
+ *   x        bf16 [M][H]      input (dense)
+ *   residual bf16 [M][H]      NULLABLE; when given, updated in place to h
+ *   w        bf16 [H]         weight
+ *   out      bf16 [M][H]      output (dense); may be the same buffer as x
+ * Requirements: H % 8 == 0, 8 <= H <= 65536; eps >= 0.
+ */
+BI_API bi_status bi_rmsnorm(const void *x, void *residual, const void *w, void *out,
+                     int64_t M, int64_t H, float eps, bi_stream stream);
+
+/* Operation ids for bi_plan. */
+enum { BI_OP_GEMM_BF16 = 0, BI_OP_GROUPED_GEMM_BF16 = 1, BI_OP_GEMM_NVFP4 = 2, BI_OP_RMSNORM = 3 };
+
+/*
+ * bi_plan -- the launch plan a call with these sizes uses (host only, no GPU needed).
+ *
+ * Everything that decides the arithmetic (tile, MMA shape, K step, K-step
+ * count, split) depends on (N, K) or H only; tiles_m and grid also depend on M
+ * (or rows). For the grouped GEMM, M is the row capacity and the real tile
+ * count is decided on the device. num_sms = 0 means "the current device's SM
+ * count" (then a CUDA device is needed); pass e.g. 152 to plan without one.
+ */
+typedef struct {
+    int32_t op;
+    int32_t block_m, block_n, block_k;   /* CTA tile (rows, cols, K step); RMSNorm: rows per CTA, H, 8 */
+    int32_t mma_m, mma_n, mma_k;         /* tcgen05.mma instruction shape (0 for RMSNorm) */
+    int32_t k_steps;                     /* K steps per output tile (fixed by K) */
+    int32_t split_k;                     /* always 1: no split of the K reduction */
+    int32_t stages;                      /* shared-memory pipeline depth */
+    int32_t threads;                     /* threads per CTA */
+    int32_t smem_bytes;                  /* dynamic shared memory per CTA */
+    int64_t tiles_m, tiles_n;            /* output tiles (tiles_m depends on M) */
+    int32_t grid;                        /* CTAs launched (persistent GEMMs: <= SM count) */
+    int32_t reduce_tree;                 /* RMSNorm: elements per lane sum (ceil(H/256)*8) */
+} bi_plan_t;
+
+BI_API bi_status bi_plan(int32_t op, int64_t M, int64_t N, int64_t K, int32_t num_sms, bi_plan_t *out);
+
+/*
+ * bi_device_status -- synchronise `stream`, then read and clear the current
+ * device's status word. Returns BI_OK, BI_ERR_TIMEOUT (a bounded wait in a
+ * kernel ran out; that call's output is invalid), BI_ERR_INVALID_ARG (a
+ * kernel found invalid device-side data, e.g. MoE offsets) or BI_ERR_CUDA.
+ */
+BI_API bi_status bi_device_status(bi_stream stream);
+
+/*
+ * bi_check_wait_timeout -- launch one CTA that waits on a shared-memory
+ * barrier nobody arrives at, with a limit of `limit_us` microseconds
+ * (1 .. 2,000,000), then records BI_ERR_TIMEOUT in the status word and
+ * returns. Exercises the same bounded-wait path the GEMM kernels use; a
+ * following bi_device_status(stream) returns BI_ERR_TIMEOUT.
+ */
+BI_API bi_status bi_check_wait_timeout(uint32_t limit_us, bi_stream stream);
+
+/* Human-readable name of a status code (static string). */
+BI_API const char *bi_status_string(bi_status s);
+
+/* Library version: major*10000 + minor*100 + patch. */
+BI_API int32_t bi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LIBBI_BI_H */

@@ -1,0 +1,219 @@
+"""Python binding of libbi: batch-invariant linear layers and RMSNorm for GB300.
+
+Argument marshalling only: every function here checks dtypes and devices,
+takes data pointers, sizes and the current CUDA stream from torch tensors and
+calls the matching ``extern "C"`` entry point of ``libbi.so`` (declared in
+``include/bi.h``). All arithmetic runs in the library's sm_103a kernels; there
+is no CPU or PyTorch fallback. If the library is missing this module raises.
+
+Names follow the C ABI: ``gemm_bf16``, ``grouped_gemm_bf16``, ``gemm_nvfp4``,
+``rmsnorm``, ``plan``, ``device_status``, ``check_wait_timeout``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libbi.so")
+
+BI_OK, BI_ERR_INVALID_ARG, BI_ERR_UNSUPPORTED, BI_ERR_MISALIGNED, BI_ERR_ARCH, BI_ERR_CUDA, BI_ERR_TIMEOUT = range(7)
+OP_GEMM_BF16, OP_GROUPED_GEMM_BF16, OP_GEMM_NVFP4, OP_RMSNORM = range(4)
+
+_lock = threading.Lock()
+_lib = None
+
+
+class BiError(RuntimeError):
+    """A libbi call returned a non-OK status."""
+
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)}")
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [("op", ctypes.c_int32),
+                ("block_m", ctypes.c_int32), ("block_n", ctypes.c_int32), ("block_k", ctypes.c_int32),
+                ("mma_m", ctypes.c_int32), ("mma_n", ctypes.c_int32), ("mma_k", ctypes.c_int32),
+                ("k_steps", ctypes.c_int32), ("split_k", ctypes.c_int32), ("stages", ctypes.c_int32),
+                ("threads", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
+                ("tiles_m", ctypes.c_int64), ("tiles_n", ctypes.c_int64),
+                ("grid", ctypes.c_int32), ("reduce_tree", ctypes.c_int32)]
+
+    def as_dict(self) -> dict:
+        return {f: getattr(self, f) for f, _ in self._fields_}
+
+
+def load() -> ctypes.CDLL:
+    """Load libbi.so (built by ``__graft_entry__.build()``); raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libbi.so is not built ({LIB_PATH}); run __graft_entry__.build() first")
+        lib = ctypes.CDLL(LIB_PATH)
+        P, I64, I32, F = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float
+        sig = {
+            "bi_gemm_bf16": [P, I64, P, I64, P, I64, I64, I64, I64, P],
+            "bi_grouped_gemm_bf16": [P, P, P, P, I32, I64, I64, I64, P],
+            "bi_gemm_nvfp4": [P, P, P, P, F, P, I64, I64, I64, P],
+            "bi_rmsnorm": [P, P, P, P, I64, I64, F, P],
+            "bi_plan": [I32, I64, I64, I64, I32, ctypes.POINTER(Plan)],
+            "bi_device_status": [P],
+            "bi_check_wait_timeout": [ctypes.c_uint32, P],
+            "bi_status_string": [ctypes.c_int],
+            "bi_version": [],
+        }
+        for name, args in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_int
+        lib.bi_status_string.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load().bi_status_string(status).decode()
+
+
+def version() -> int:
+    return int(load().bi_version())
+
+
+def _check(status: int, where: str):
+    if status != BI_OK:
+        raise BiError(status, where)
+
+
+def _stream(stream=None):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev(t, dtype, name):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def gemm_bf16(X, W, Y=None, stream=None):
+    """Y[M,N] = X[M,K] W[N,K]^T (bf16 in/out, fp32 accumulate), batch-invariant.
+
+    X and W may be row-strided views (unit column stride); Y is allocated if None."""
+    import torch
+    _dev(X, torch.bfloat16, "X"), _dev(W, torch.bfloat16, "W")
+    if X.dim() != 2 or W.dim() != 2 or X.shape[1] != W.shape[1]:
+        raise ValueError(f"shape mismatch X{tuple(X.shape)} W{tuple(W.shape)}")
+    if X.stride(1) != 1 or W.stride(1) != 1:
+        raise ValueError("X and W need unit column stride")
+    M, K = X.shape
+    N = W.shape[0]
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    _dev(Y, torch.bfloat16, "Y")
+    if Y.shape != (M, N) or Y.stride(1) != 1:
+        raise ValueError("Y must be [M, N] with unit column stride")
+    _check(load().bi_gemm_bf16(_ptr(X), X.stride(0), _ptr(W), W.stride(0), _ptr(Y), Y.stride(0), M, N, K,
+                               _stream(stream)), "bi_gemm_bf16")
+    return Y
+
+
+def grouped_gemm_bf16(X, W, offsets, Y=None, stream=None):
+    """Per-expert Y[r] = X[r] W[e]^T for rows r in [offsets[e], offsets[e+1]).
+
+    X [rows,K], W [E,N,K] bf16 (contiguous); offsets int32 [E+1] on the device."""
+    import torch
+    _dev(X, torch.bfloat16, "X"), _dev(W, torch.bfloat16, "W"), _dev(offsets, torch.int32, "offsets")
+    if not (X.is_contiguous() and W.is_contiguous() and offsets.is_contiguous()):
+        raise ValueError("X, W and offsets must be contiguous")
+    E, N, K = W.shape
+    rows = X.shape[0]
+    if X.shape[1] != K or offsets.numel() != E + 1:
+        raise ValueError("shape mismatch")
+    if Y is None:
+        Y = torch.empty((rows, N), dtype=torch.bfloat16, device=X.device)
+    _dev(Y, torch.bfloat16, "Y")
+    if Y.shape != (rows, N) or not Y.is_contiguous():
+        raise ValueError("Y must be contiguous [rows, N]")
+    _check(load().bi_grouped_gemm_bf16(_ptr(X), _ptr(W), _ptr(Y), _ptr(offsets), E, rows, N, K, _stream(stream)),
+           "bi_grouped_gemm_bf16")
+    return Y
+
+
+def gemm_nvfp4(A, A_sf, B, B_sf, alpha: float, Y=None, stream=None):
+    """Y[M,N] = alpha * dequant(A) dequant(B)^T, e2m1 codes packed two per byte
+    (uint8 [rows, K/2]) with e4m3 block scales (uint8, interleaved 128x4 layout)."""
+    import torch
+    for t, n in ((A, "A"), (A_sf, "A_sf"), (B, "B"), (B_sf, "B_sf")):
+        _dev(t, torch.uint8, n)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    M, KB = A.shape
+    N = B.shape[0]
+    K = KB * 2
+    if B.shape[1] != KB:
+        raise ValueError("A and B disagree on K")
+    c4 = -(-(K // 16) // 4) * 4
+    if A_sf.numel() < -(-M // 128) * 128 * c4 or B_sf.numel() < -(-N // 128) * 128 * c4:
+        raise ValueError("scale buffers are smaller than the interleaved layout needs")
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    _dev(Y, torch.bfloat16, "Y")
+    if Y.shape != (M, N) or not Y.is_contiguous():
+        raise ValueError("Y must be contiguous [M, N]")
+    _check(load().bi_gemm_nvfp4(_ptr(A), _ptr(A_sf), _ptr(B), _ptr(B_sf), float(alpha), _ptr(Y), M, N, K,
+                                _stream(stream)), "bi_gemm_nvfp4")
+    return Y
+
+
+def rmsnorm(x, w, eps: float, residual=None, out=None, stream=None):
+    """out = bf16(h / sqrt(mean(h^2) + eps) * w), h = bf16(x + residual) (written
+    back to residual) or x. x, residual, out contiguous bf16 [M, H]; w bf16 [H]."""
+    import torch
+    _dev(x, torch.bfloat16, "x"), _dev(w, torch.bfloat16, "w")
+    if not x.is_contiguous() or not w.is_contiguous() or x.dim() != 2:
+        raise ValueError("x must be contiguous [M, H]; w contiguous [H]")
+    M, H = x.shape
+    if w.numel() != H:
+        raise ValueError("w must have H elements")
+    if residual is not None:
+        _dev(residual, torch.bfloat16, "residual")
+        if residual.shape != x.shape or not residual.is_contiguous():
+            raise ValueError("residual must be contiguous [M, H]")
+    if out is None:
+        out = torch.empty_like(x)
+    _dev(out, torch.bfloat16, "out")
+    if out.shape != x.shape or not out.is_contiguous():
+        raise ValueError("out must be contiguous [M, H]")
+    _check(load().bi_rmsnorm(_ptr(x), _ptr(residual) if residual is not None else None, _ptr(w), _ptr(out), M, H,
+                             float(eps), _stream(stream)), "bi_rmsnorm")
+    return out
+
+
+def plan(op: int, M: int, N: int, K: int, num_sms: int = 0) -> dict:
+    """Launch plan for these sizes (num_sms=0: the current device's SM count)."""
+    p = Plan()
+    _check(load().bi_plan(op, M, N, K, num_sms, ctypes.byref(p)), "bi_plan")
+    return p.as_dict()
+
+
+def device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status code."""
+    return int(load().bi_device_status(_stream(stream)))
+
+
+def check_wait_timeout(limit_us: int, stream=None):
+    """Launch the bounded-wait check kernel (see bi.h)."""
+    _check(load().bi_check_wait_timeout(limit_us, _stream(stream)), "bi_check_wait_timeout")

@@ -1,0 +1,214 @@
+// abi.cu -- the C ABI of libbi: argument checks, device facts, the device
+// status word, tensor-map encoding and the extern "C" entry points.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstring>
+#include <functional>
+#include <mutex>
+
+#include "bi_internal.h"
+
+namespace bi {
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// One status word per device; kernels or codes into it, bi_device_status
+// reads and clears it.
+__device__ unsigned g_status_word;
+
+struct DeviceSlot {
+    std::once_flag once;
+    DeviceInfo info;
+    bi_status init_status = BI_ERR_CUDA;
+    unsigned *status = nullptr;
+};
+DeviceSlot g_devices[kMaxDevices];
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+void init_device(int dev, DeviceSlot &slot) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&slot.info.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&slot.info.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess) {
+        slot.init_status = BI_ERR_CUDA;
+        return;
+    }
+    slot.info.is_sm103 = (major == 10 && minor == 3);
+    if (!slot.info.is_sm103) {
+        slot.init_status = BI_ERR_ARCH;
+        return;
+    }
+    void *addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess) {
+        slot.init_status = BI_ERR_CUDA;
+        return;
+    }
+    slot.status = static_cast<unsigned *>(addr);
+    slot.init_status = BI_OK;
+}
+
+}  // namespace
+
+bi_status current_device(int *dev, const DeviceInfo **info) {
+    if (cudaGetDevice(dev) != cudaSuccess || *dev < 0 || *dev >= kMaxDevices) return BI_ERR_CUDA;
+    DeviceSlot &slot = g_devices[*dev];
+    std::call_once(slot.once, init_device, *dev, std::ref(slot));
+    *info = &slot.info;
+    return slot.init_status;
+}
+
+unsigned *device_status_word() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    return g_devices[dev].status;
+}
+
+bi_status make_tmap_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, uint64_t inner,
+                       uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
+                       CUtensorMapSwizzle swizzle) {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (!g_encode) return BI_ERR_CUDA;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {row_stride_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, dtype, 2, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? BI_OK : BI_ERR_CUDA;
+}
+
+}  // namespace bi
+
+using namespace bi;
+
+namespace {
+constexpr int64_t kI32Max = 0x7FFFFFFF;
+inline cudaStream_t as_stream(bi_stream s) { return static_cast<cudaStream_t>(s); }
+}  // namespace
+
+extern "C" {
+
+bi_status bi_gemm_bf16(const void *X, int64_t ldx, const void *W, int64_t ldw, void *Y, int64_t ldy, int64_t M,
+                       int64_t N, int64_t K, bi_stream stream) {
+    if (M < 0 || N < 0 || K <= 0 || M >= kI32Max || N >= kI32Max || K >= kI32Max) return BI_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return BI_OK;
+    if (!X || !W || !Y) return BI_ERR_INVALID_ARG;
+    if (ldx < K || ldw < K || ldy < N) return BI_ERR_INVALID_ARG;
+    if (K % 8 != 0 || N % 8 != 0) return BI_ERR_UNSUPPORTED;
+    if (ldx % 8 != 0 || ldw % 8 != 0 || ldy % 8 != 0 || !aligned16(X) || !aligned16(W) || !aligned16(Y))
+        return BI_ERR_MISALIGNED;
+    return launch_gemm_bf16(X, ldx, W, ldw, Y, ldy, M, N, K, as_stream(stream));
+}
+
+bi_status bi_grouped_gemm_bf16(const void *X, const void *W, void *Y, const int32_t *expert_offsets, int32_t E,
+                               int64_t rows, int64_t N, int64_t K, bi_stream stream) {
+    if (E < 1 || E > 1024 || rows < 0 || N < 0 || K <= 0 || rows >= kI32Max || K >= kI32Max ||
+        static_cast<int64_t>(E) * N >= kI32Max)
+        return BI_ERR_INVALID_ARG;
+    if (rows == 0 || N == 0) return BI_OK;
+    if (!X || !W || !Y || !expert_offsets) return BI_ERR_INVALID_ARG;
+    if (K % 8 != 0 || N % 8 != 0) return BI_ERR_UNSUPPORTED;
+    if (!aligned16(X) || !aligned16(W) || !aligned16(Y) || (reinterpret_cast<uintptr_t>(expert_offsets) & 3u))
+        return BI_ERR_MISALIGNED;
+    return launch_grouped_gemm_bf16(X, W, Y, expert_offsets, E, rows, N, K, as_stream(stream));
+}
+
+bi_status bi_gemm_nvfp4(const uint8_t *A, const uint8_t *A_sf, const uint8_t *B, const uint8_t *B_sf, float alpha,
+                        void *Y, int64_t M, int64_t N, int64_t K, bi_stream stream) {
+    if (M < 0 || N < 0 || K <= 0 || M >= kI32Max || N >= kI32Max || K >= kI32Max) return BI_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return BI_OK;
+    if (!A || !A_sf || !B || !B_sf || !Y) return BI_ERR_INVALID_ARG;
+    if (K % 64 != 0 || N % 8 != 0) return BI_ERR_UNSUPPORTED;
+    if (!aligned16(A) || !aligned16(A_sf) || !aligned16(B) || !aligned16(B_sf) || !aligned16(Y))
+        return BI_ERR_MISALIGNED;
+    return launch_gemm_nvfp4(A, A_sf, B, B_sf, alpha, Y, M, N, K, as_stream(stream));
+}
+
+bi_status bi_rmsnorm(const void *x, void *residual, const void *w, void *out, int64_t M, int64_t H, float eps,
+                     bi_stream stream) {
+    if (M < 0 || H < 8 || H > 65536 || !(eps >= 0.0f)) return BI_ERR_INVALID_ARG;
+    if (M == 0) return BI_OK;
+    if (!x || !w || !out) return BI_ERR_INVALID_ARG;
+    if (H % 8 != 0) return BI_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(out) || (residual && !aligned16(residual)))
+        return BI_ERR_MISALIGNED;
+    int dev;
+    const DeviceInfo *info;
+    bi_status st = current_device(&dev, &info);
+    if (st != BI_OK) return st;
+    return launch_rmsnorm(x, residual, w, out, M, H, eps, as_stream(stream));
+}
+
+bi_status bi_plan(int32_t op, int64_t M, int64_t N, int64_t K, int32_t num_sms, bi_plan_t *out) {
+    if (!out || M < 0 || N < 0 || K < 0 || num_sms < 0) return BI_ERR_INVALID_ARG;
+    int sms = num_sms;
+    if (sms == 0) {
+        int dev;
+        const DeviceInfo *info;
+        bi_status st = current_device(&dev, &info);
+        if (st != BI_OK) return st;
+        sms = info->sm_count;
+    }
+    std::memset(out, 0, sizeof(*out));
+    switch (op) {
+        case BI_OP_GEMM_BF16: plan_gemm_bf16(M, N, K, sms, out); return BI_OK;
+        case BI_OP_GROUPED_GEMM_BF16: plan_grouped_gemm_bf16(M, N, K, sms, out); return BI_OK;
+        case BI_OP_GEMM_NVFP4: plan_gemm_nvfp4(M, N, K, sms, out); return BI_OK;
+        case BI_OP_RMSNORM: plan_rmsnorm(M, N, out); return BI_OK;   /* N carries H */
+        default: return BI_ERR_INVALID_ARG;
+    }
+}
+
+bi_status bi_device_status(bi_stream stream) {
+    int dev;
+    const DeviceInfo *info;
+    bi_status st = current_device(&dev, &info);
+    if (st != BI_OK) return st;
+    if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return BI_ERR_CUDA;
+    unsigned word = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&word, g_status_word, sizeof word) != cudaSuccess) return BI_ERR_CUDA;
+    if (word && cudaMemcpyToSymbol(g_status_word, &zero, sizeof zero) != cudaSuccess) return BI_ERR_CUDA;
+    if (word & kDevTimeout) return BI_ERR_TIMEOUT;
+    if (word & kDevBadOffsets) return BI_ERR_INVALID_ARG;
+    return BI_OK;
+}
+
+bi_status bi_check_wait_timeout(uint32_t limit_us, bi_stream stream) {
+    if (limit_us < 1 || limit_us > 2000000) return BI_ERR_INVALID_ARG;
+    int dev;
+    const DeviceInfo *info;
+    bi_status st = current_device(&dev, &info);
+    if (st != BI_OK) return st;
+    return launch_wait_timeout_check(limit_us, as_stream(stream));
+}
+
+const char *bi_status_string(bi_status s) {
+    switch (s) {
+        case BI_OK: return "BI_OK";
+        case BI_ERR_INVALID_ARG: return "BI_ERR_INVALID_ARG";
+        case BI_ERR_UNSUPPORTED: return "BI_ERR_UNSUPPORTED";
+        case BI_ERR_MISALIGNED: return "BI_ERR_MISALIGNED";
+        case BI_ERR_ARCH: return "BI_ERR_ARCH";
+        case BI_ERR_CUDA: return "BI_ERR_CUDA";
+        case BI_ERR_TIMEOUT: return "BI_ERR_TIMEOUT";
+        default: return "BI_ERR_UNKNOWN";
+    }
+}
+
+int32_t bi_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,53 @@
+// bi_internal.h -- host-side helpers shared by the libbi translation units.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/bi.h"
+
+namespace bi {
+
+// Device status codes (or-ed into the per-device status word by kernels).
+constexpr unsigned kDevTimeout = 1u;      // a bounded wait ran out
+constexpr unsigned kDevBadOffsets = 2u;   // MoE expert offsets were not 0 <= ... <= rows
+
+// Per-device facts, looked up once per device.
+struct DeviceInfo {
+    int sm_count = 0;
+    int max_smem_optin = 0;
+    bool is_sm103 = false;
+};
+
+// Current device's info; returns BI_ERR_ARCH / BI_ERR_CUDA on failure.
+bi_status current_device(int *dev, const DeviceInfo **info);
+
+// Address of this device's status word (library-owned, one per device).
+unsigned *device_status_word();
+
+// Encode a 2-D row-major tensor map (inner dimension first).
+bi_status make_tmap_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, uint64_t inner,
+                       uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
+                       CUtensorMapSwizzle swizzle);
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Kernel launchers (defined in the .cu files); arguments already validated.
+bi_status launch_gemm_bf16(const void *X, int64_t ldx, const void *W, int64_t ldw, void *Y, int64_t ldy,
+                           int64_t M, int64_t N, int64_t K, cudaStream_t s);
+bi_status launch_grouped_gemm_bf16(const void *X, const void *W, void *Y, const int32_t *offsets, int32_t E,
+                                   int64_t rows, int64_t N, int64_t K, cudaStream_t s);
+bi_status launch_gemm_nvfp4(const uint8_t *A, const uint8_t *A_sf, const uint8_t *B, const uint8_t *B_sf,
+                            float alpha, void *Y, int64_t M, int64_t N, int64_t K, cudaStream_t s);
+bi_status launch_rmsnorm(const void *x, void *residual, const void *w, void *out, int64_t M, int64_t H,
+                         float eps, cudaStream_t s);
+bi_status launch_wait_timeout_check(uint32_t limit_us, cudaStream_t s);
+
+// Plans (M-independent except tiles_m and grid).
+void plan_gemm_bf16(int64_t M, int64_t N, int64_t K, int sms, bi_plan_t *p);
+void plan_grouped_gemm_bf16(int64_t rows, int64_t N, int64_t K, int sms, bi_plan_t *p);
+void plan_gemm_nvfp4(int64_t M, int64_t N, int64_t K, int sms, bi_plan_t *p);
+void plan_rmsnorm(int64_t M, int64_t H, bi_plan_t *p);
+
+}  // namespace bi

@@ -65,6 +65,7 @@ def _load():
             lib.oracle_bf16_value.restype = D
             lib.oracle_bf16_round.argtypes = [D]
             lib.oracle_bf16_round.restype = ctypes.c_uint16
+            lib.oracle_bf16_round_array.argtypes = [I64, P, P]
             lib.oracle_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -154,3 +155,12 @@ def bf16_value(bits: int) -> float:
 
 def bf16_round(v: float) -> int:
     return int(_load().oracle_bf16_round(float(v)))
+
+
+def bf16_round_array(v: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns (round to nearest even) of an fp64 array."""
+    v = _c(v, np.float64)
+    out = np.zeros(v.shape, dtype=np.uint16)
+    if v.size:
+        _load().oracle_bf16_round_array(v.size, _p(v), _p(out))
+    return out

@@ -86,6 +86,12 @@ double oracle_e4m3_value(unsigned code) { return e4m3_to_double(code & 255u); }
 double oracle_bf16_value(uint16_t bits) { return bf16_to_double(bits); }
 uint16_t oracle_bf16_round(double v) { return double_to_bf16(v); }
 
+/* Round n doubles to bf16 bit patterns (same rule as double_to_bf16). */
+void oracle_bf16_round_array(int64_t n, const double *v, uint16_t *out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = double_to_bf16(v[i]);
+}
+
 int oracle_threads(void)
 {
 #ifdef _OPENMP

@@ -1,0 +1,122 @@
+"""The C ABI: the library loads, exports every symbol bi.h declares, plans on
+the host, and rejects bad arguments before touching a GPU (CPU only)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "bi.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from invariant_deterministic_bi_gb300 import _build
+    _build.build()
+    import invariant_deterministic_bi_gb300 as m
+    return m
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:BI_API\s+)?(?:bi_status|const char \*|int32_t)\s*(bi_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_calls():
+    names = declared_functions()
+    for n in ["bi_gemm_bf16", "bi_grouped_gemm_bf16", "bi_gemm_nvfp4", "bi_rmsnorm", "bi_plan",
+              "bi_device_status", "bi_status_string", "bi_version", "bi_check_wait_timeout"]:
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    so = lib.load()
+    out = subprocess.run(["nm", "-D", "--defined-only", lib.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\sT\s(\w+)$", out, re.M))
+    for n in declared_functions():
+        assert hasattr(so, n), n
+        assert n in exported, n
+    # nothing but the C ABI is exported from our own code
+    ours = {s for s in exported if s.startswith("bi_") or s.startswith("_ZN2bi")}
+    assert ours == set(declared_functions())
+
+
+def test_status_strings(lib):
+    assert lib.status_string(lib.BI_OK) == "BI_OK"
+    assert lib.status_string(lib.BI_ERR_TIMEOUT) == "BI_ERR_TIMEOUT"
+    assert lib.version() >= 100
+
+
+def _plan(lib, op, M, N, K):
+    return lib.plan(op, M, N, K, num_sms=152)
+
+
+@pytest.mark.parametrize("N,K", [(512, 256), (6144, 4096), (24576, 4096), (4096, 12288), (264, 72)])
+def test_gemm_plan_independent_of_M(lib, N, K):
+    keys = ["block_m", "block_n", "block_k", "mma_m", "mma_n", "mma_k", "k_steps", "split_k", "stages",
+            "threads", "smem_bytes", "tiles_n"]
+    base = _plan(lib, lib.OP_GEMM_BF16, 1, N, K)
+    for M in [1, 2, 7, 64, 127, 128, 129, 513, 4096, 8192, 65536]:
+        p = _plan(lib, lib.OP_GEMM_BF16, M, N, K)
+        assert {k: p[k] for k in keys} == {k: base[k] for k in keys}
+        assert p["tiles_m"] == -(-M // 128) and p["split_k"] == 1
+        assert 1 <= p["grid"] <= 152
+    assert base["k_steps"] == -(-K // 64)
+
+
+def test_grouped_and_nvfp4_and_rmsnorm_plans_independent_of_M(lib):
+    for op, N, K in [(lib.OP_GROUPED_GEMM_BF16, 1536, 2048), (lib.OP_GROUPED_GEMM_BF16, 2048, 768),
+                     (lib.OP_GEMM_NVFP4, 14336, 4096), (lib.OP_RMSNORM, 4096, 0)]:
+        ps = [_plan(lib, op, M, N, K) for M in [1, 3, 128, 4097, 16384]]
+        for p in ps:
+            for k in ["block_n", "block_k", "mma_m", "mma_n", "mma_k", "k_steps", "split_k", "reduce_tree"]:
+                assert p[k] == ps[0][k], (op, k)
+
+
+def test_rmsnorm_plan_tree(lib):
+    p = _plan(lib, lib.OP_RMSNORM, 16384, 4096, 0)
+    assert p["reduce_tree"] == 128 and p["block_m"] == 8
+
+
+FAKE = 0x10000   # never dereferenced: every call below fails validation first
+
+
+@pytest.mark.parametrize("args,want", [
+    ((FAKE, 256, FAKE, 256, FAKE, 512, -1, 512, 256), 1),          # M < 0
+    ((FAKE, 256, FAKE, 256, FAKE, 512, 4, 512, 0), 1),             # K == 0
+    ((None, 256, FAKE, 256, FAKE, 512, 4, 512, 256), 1),           # null X
+    ((FAKE, 100, FAKE, 256, FAKE, 512, 4, 512, 256), 1),           # ldx < K
+    ((FAKE, 256, FAKE, 256, FAKE, 512, 4, 512, 250), 2),           # K % 8
+    ((FAKE, 256, FAKE, 256, FAKE, 516, 4, 516, 256), 2),           # N % 8
+    ((FAKE + 8, 256, FAKE, 256, FAKE, 512, 4, 512, 256), 3),       # misaligned X
+    ((FAKE, 260, FAKE, 256, FAKE, 512, 4, 512, 256), 3),           # ldx row stride not 16-byte
+])
+def test_gemm_bf16_rejects_bad_arguments(lib, args, want):
+    so = lib.load()
+    assert so.bi_gemm_bf16(*args, None) == want
+
+
+def test_empty_work_is_ok_without_launch(lib):
+    so = lib.load()
+    assert so.bi_gemm_bf16(FAKE, 256, FAKE, 256, FAKE, 512, 0, 512, 256, None) == 0
+    assert so.bi_grouped_gemm_bf16(FAKE, FAKE, FAKE, FAKE, 128, 0, 1536, 2048, None) == 0
+    assert so.bi_gemm_nvfp4(FAKE, FAKE, FAKE, FAKE, ctypes.c_float(1.0), FAKE, 0, 64, 128, None) == 0
+    assert so.bi_rmsnorm(FAKE, None, FAKE, FAKE, 0, 4096, ctypes.c_float(1e-6), None) == 0
+
+
+def test_other_calls_reject_bad_arguments(lib):
+    so = lib.load()
+    f = ctypes.c_float
+    assert so.bi_grouped_gemm_bf16(FAKE, FAKE, FAKE, FAKE, 0, 8, 64, 64, None) == 1        # E < 1
+    assert so.bi_grouped_gemm_bf16(FAKE, FAKE, FAKE, FAKE, 2000, 8, 64, 64, None) == 1     # E > 1024
+    assert so.bi_grouped_gemm_bf16(FAKE, FAKE, FAKE, FAKE + 2, 4, 8, 64, 64, None) == 3    # offsets align
+    assert so.bi_gemm_nvfp4(FAKE, FAKE, FAKE, FAKE, f(1.0), FAKE, 4, 64, 96, None) == 2    # K % 64
+    assert so.bi_gemm_nvfp4(FAKE, FAKE + 4, FAKE, FAKE, f(1.0), FAKE, 4, 64, 128, None) == 3
+    assert so.bi_rmsnorm(FAKE, None, FAKE, FAKE, 4, 4, f(1e-6), None) == 1                 # H < 8
+    assert so.bi_rmsnorm(FAKE, None, FAKE, FAKE, 4, 4100, f(1e-6), None) == 2              # H % 8
+    assert so.bi_rmsnorm(FAKE, None, FAKE, FAKE, 4, 4096, f(-1.0), None) == 1              # eps < 0
+    assert so.bi_rmsnorm(FAKE, FAKE + 8, FAKE, FAKE, 4, 4096, f(1e-6), None) == 3          # residual align
+    assert so.bi_check_wait_timeout(0, None) == 1
+    assert so.bi_plan(99, 1, 1, 1, 152, ctypes.byref(lib.Plan())) == 1

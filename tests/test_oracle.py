@@ -75,6 +75,11 @@ def test_bf16_round_golden():
             assert oracle.bf16_round(float(Fraction(v))) == int(bits, 16), line
 
 
+def test_bf16_round_array_matches_scalar():
+    v = np.array([1.0, 257 / 256, 259 / 256, -3.0, 1 / 3, 65408.0, 0.0, 1e-40, -2.5e38])
+    assert [int(b) for b in oracle.bf16_round_array(v)] == [oracle.bf16_round(x) for x in v]
+
+
 def test_bf16_round_exhaustive_against_neighbours():
     """Round-trip every positive finite bf16 and check midpoints between
     neighbours go to the even pattern (ties-to-even, by construction)."""
