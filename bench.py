@@ -1,0 +1,584 @@
+"""Benchmark of the batch-invariant linear layer and RMSNorm (libbi) on GB300.
+
+Headline step (one pass of the hot path over one batch, Qwen3-8B-shaped
+decoder-layer linears at M = 8192 tokens, bf16, synthetic N(0,1) activations and
+N(0, 0.02^2) weights):
+    RMSNorm + residual add [M, 4096]   -> qkv     Y = X W^T  K=4096  N=6144
+    RMSNorm + residual add [M, 4096]   -> gate_up Y = X W^T  K=4096  N=24576
+    down   Y = X W^T  K=12288 N=4096   (X = first 12288 columns of gate_up's output)
+value = GEMM FLOPs of the step / device time of the step (TFLOP/s); the step's
+working set (> 1 GB of weights and activations) is far larger than the 129 MB
+L2, so back-to-back steps do not hit in L2.
+
+Also reported on the same line: the roofline of the dominant kernel
+(bi_gemm_bf16), an end-to-end number through host buffers, the fp64 CPU oracle
+timed on a bounded sample, and per-row measurements (M sweep vs cuBLAS,
+RMSNorm GB/s vs torch, MoE grouped GEMM, NVFP4 GEMM when present).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+With N > 1 (torchrun) every rank runs an independent replica (no collectives).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+M_STEP = 8192
+H = 4096
+EPS = 1e-6
+LAYERS = {"qkv": (6144, 4096), "gate_up": (24576, 4096), "down": (4096, 12288)}
+M_SWEEP = [1, 7, 64, 513, 4096, 8192]
+RMS_SWEEP = [1, 3, 128, 4097, 16384]
+METRIC = "batch-invariant GEMM TFLOP/s vs M (% bf16 peak); RMSNorm HBM GB/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+NOMINAL_HBM_GBS = 8000.0
+
+
+def step_flops(M: int) -> float:
+    return sum(2.0 * M * n * k for n, k in LAYERS.values())
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------- distributed
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class Dist:
+    def __init__(self, world, rank, backend):
+        self.world, self.rank = world, rank
+        self.pg = None
+        if world > 1:
+            import torch.distributed as dist
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, v: float) -> float:
+        if not self.pg:
+            return v
+        import torch
+        t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# --------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"bi_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.06)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if not self.proc or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx = float(parts[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- our arm
+
+def bf16_dev(bits):
+    import numpy as np
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def make_step_inputs(M: int, seed: int = 0):
+    """Synthetic Qwen3-8B-shaped inputs (bf16, device resident)."""
+    import bi_synth as syn
+    d = {}
+    x, res, w1, _ = syn.rmsnorm_inputs(M, H, seed=seed, outlier_frac=0.0)
+    x2, _, w2, _ = syn.rmsnorm_inputs(M, H, seed=seed + 1, outlier_frac=0.0)
+    d["x"], d["x2"], d["res"], d["w1"], d["w2"] = map(bf16_dev, (x, x2, res, w1, w2))
+    for i, (name, (n, k)) in enumerate(LAYERS.items()):
+        d["W_" + name] = bf16_dev(syn.to_bf16_bits(syn.normal_rows(seed + 10 + i, syn.TID_W, n, k, std=0.02)))
+    return d
+
+
+class Step:
+    """One pass of the hot path; optional per-GEMM events for the roofline."""
+
+    def __init__(self, bi, inp, M):
+        import torch
+        self.bi, self.inp, self.M = bi, inp, M
+        self.h1 = torch.empty((M, H), dtype=torch.bfloat16, device="cuda")
+        self.h2 = torch.empty_like(self.h1)
+        self.qkv = torch.empty((M, LAYERS["qkv"][0]), dtype=torch.bfloat16, device="cuda")
+        self.gu = torch.empty((M, LAYERS["gate_up"][0]), dtype=torch.bfloat16, device="cuda")
+        self.dn = torch.empty((M, LAYERS["down"][0]), dtype=torch.bfloat16, device="cuda")
+        self.gemm_events = []
+
+    def __call__(self, events=False):
+        import torch
+        bi, d = self.bi, self.inp
+        ev = (lambda: torch.cuda.Event(enable_timing=True)) if events else None
+
+        def gemm(X, W, Y):
+            if events:
+                a, b = ev(), ev()
+                a.record()
+                bi.gemm_bf16(X, W, Y=Y)
+                b.record()
+                self.gemm_events.append((a, b))
+            else:
+                bi.gemm_bf16(X, W, Y=Y)
+
+        bi.rmsnorm(d["x"], d["w1"], EPS, residual=d["res"], out=self.h1)
+        gemm(self.h1, d["W_qkv"], self.qkv)
+        bi.rmsnorm(d["x2"], d["w2"], EPS, residual=d["res"], out=self.h2)
+        gemm(self.h2, d["W_gate_up"], self.gu)
+        gemm(self.gu[:, :LAYERS["down"][1]], d["W_down"], self.dn)
+
+
+def time_fn(fn, reps: int, warm: int = 3) -> float:
+    """Mean device time (ms) of fn() over reps back-to-back calls (CUDA events)."""
+    import torch
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def rotate(inputs_list):
+    """Cycle through several input sets so consecutive calls miss in L2."""
+    state = {"i": 0}
+
+    def nxt():
+        v = inputs_list[state["i"] % len(inputs_list)]
+        state["i"] += 1
+        return v
+    return nxt
+
+
+def gemm_sweep(bi, peaks):
+    """TFLOP/s of bi_gemm_bf16 vs M for each layer, against cuBLAS (torch.matmul)."""
+    import torch
+    import bi_synth as syn
+    rows = []
+    for name, (n, k) in LAYERS.items():
+        Ws = [bf16_dev(syn.to_bf16_bits(syn.normal_rows(20 + j, syn.TID_W, n, k, std=0.02))) for j in range(2)]
+        Xmax = bf16_dev(syn.to_bf16_bits(syn.normal_rows(0, syn.TID_X, max(M_SWEEP), k)))
+        for M in M_SWEEP:
+            X = Xmax[:M]
+            Y = torch.empty((M, n), dtype=torch.bfloat16, device="cuda")
+            wsel = rotate(Ws)
+            reps = 50 if M <= 513 else 10
+            t_bi = time_fn(lambda: bi.gemm_bf16(X, wsel(), Y=Y), reps)
+            wsel2 = rotate(Ws)
+            t_cb = time_fn(lambda: torch.matmul(X, wsel2().t(), out=Y), reps)
+            flops = 2.0 * M * n * k
+            tf = flops / (t_bi * 1e-3) / 1e12
+            rows.append({"layer": name, "M": M, "N": n, "K": k, "us": round(t_bi * 1e3, 2),
+                         "tflops": round(tf, 1), "frac_bf16_peak": round(tf / peaks["bf16_tflops"], 3),
+                         "weight_gbs": round(2.0 * n * k / (t_bi * 1e-3) / 1e9, 0),
+                         "cublas_us": round(t_cb * 1e3, 2), "cost_vs_cublas": round(t_bi / t_cb, 3)})
+        del Ws, Xmax
+        torch.cuda.empty_cache()
+    # is cuBLAS itself batch-invariant here? (informational)
+    n, k = LAYERS["qkv"]
+    W = bf16_dev(syn.to_bf16_bits(syn.normal_rows(20, syn.TID_W, n, k, std=0.02)))
+    X = bf16_dev(syn.to_bf16_bits(syn.normal_rows(0, syn.TID_X, 4096, k)))
+    full = torch.matmul(X, W.t())
+    one = torch.matmul(X[:1], W.t())
+    cublas_inv = bool(torch.equal(full[0], one[0]))
+    return rows, cublas_inv
+
+
+def rmsnorm_sweep(bi, peaks):
+    import torch
+    import bi_synth as syn
+    rows = []
+    for with_res in (True, False):
+        for M in RMS_SWEEP:
+            sets = []
+            nsets = max(1, min(4, (512 << 20) // max(1, 8 * M * H)))
+            for j in range(nsets):
+                x, res, w, _ = syn.rmsnorm_inputs(M, H, seed=j)
+                sets.append((bf16_dev(x), bf16_dev(res) if with_res else None, bf16_dev(w),
+                             torch.empty((M, H), dtype=torch.bfloat16, device="cuda")))
+            sel = rotate(sets)
+
+            def ours():
+                x, r, w, o = sel()
+                bi.rmsnorm(x, w, EPS, residual=r, out=o)
+            sel2 = rotate(sets)
+
+            def theirs():
+                x, r, w, o = sel2()
+                if r is not None:
+                    r.add_(x)
+                    torch.nn.functional.rms_norm(r, (H,), w, EPS)
+                else:
+                    torch.nn.functional.rms_norm(x, (H,), w, EPS)
+            reps = 200 if M <= 128 else 30
+            t = time_fn(ours, reps)
+            t2 = time_fn(theirs, reps)
+            nbytes = (8 if with_res else 4) * M * H + 2 * H
+            gbs = nbytes / (t * 1e-3) / 1e9
+            rows.append({"M": M, "H": H, "residual": with_res, "us": round(t * 1e3, 2), "gbs": round(gbs, 0),
+                         "frac_hbm_measured": round(gbs / peaks["hbm_gbs"], 3),
+                         "frac_hbm_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 3),
+                         "torch_us": round(t2 * 1e3, 2), "cost_vs_torch": round(t / t2, 3)})
+            del sets
+    return rows
+
+
+MOE_E, MOE_TOPK = 128, 8
+MOE_LAYERS = {"gate_up": (1536, 2048), "down": (2048, 768)}
+MOE_T = [1, 64, 512, 8192]
+
+
+def moe_inputs(layer: str, T: int, seed: int = 0, W=None):
+    """Qwen3-30B-A3B-shaped expert inputs: top-8 of 128 experts from seeded
+    router logits; rows grouped by expert (device tensors)."""
+    import bi_synth as syn
+    n, k = MOE_LAYERS[layer]
+    tok, exp, off, _ = syn.moe_routing(T, MOE_E, MOE_TOPK, seed=seed)
+    if layer == "gate_up":
+        X = syn.to_bf16_bits(syn.normal_rows(seed, syn.TID_HIDDEN, T, k))[tok]
+    else:
+        X = syn.to_bf16_bits(syn.normal_rows(seed, syn.TID_DOWN_IN, T * MOE_TOPK, k))
+    if W is None:
+        W = bf16_dev(syn.moe_weights(MOE_E, n, k, seed=seed,
+                                     tensor_id=syn.TID_W1 if layer == "gate_up" else syn.TID_W2))
+    import torch
+    return bf16_dev(X), W, torch.from_numpy(off).cuda(), exp
+
+
+def moe_sweep(bi, peaks):
+    """Grouped expert GEMM throughput vs tokens, against torch's grouped GEMM."""
+    import torch
+    rows = []
+    for layer, (n, k) in MOE_LAYERS.items():
+        W = None
+        for T in MOE_T:
+            X, W, off, exp = moe_inputs(layer, T, W=W)
+            Y = torch.empty((X.shape[0], n), dtype=torch.bfloat16, device="cuda")
+            t = time_fn(lambda: bi.grouped_gemm_bf16(X, W, off, Y=Y), 20 if T <= 512 else 5)
+            flops = 2.0 * X.shape[0] * n * k
+            touched = len(set(exp.tolist()))
+            nbytes = 2.0 * (touched * n * k + X.shape[0] * (k + n))
+            r = {"layer": layer, "T": T, "rows": int(X.shape[0]), "experts_touched": touched, "us": round(t * 1e3, 2),
+                 "tflops": round(flops / (t * 1e-3) / 1e12, 1),
+                 "frac_bf16_peak": round(flops / (t * 1e-3) / 1e12 / peaks["bf16_tflops"], 3),
+                 "gbs": round(nbytes / (t * 1e-3) / 1e9, 0),
+                 "frac_hbm_measured": round(nbytes / (t * 1e-3) / 1e9 / peaks["hbm_gbs"], 3)}
+            try:
+                Wt = W.transpose(1, 2)
+                ends = off[1:].contiguous()
+                torch._grouped_mm(X, Wt, offs=ends)
+                t2 = time_fn(lambda: torch._grouped_mm(X, Wt, offs=ends), 20 if T <= 512 else 5)
+                r["torch_grouped_mm_us"] = round(t2 * 1e3, 2)
+                r["cost_vs_torch"] = round(t / t2, 3)
+            except Exception as e:  # not every torch build has a bf16 grouped GEMM for this arch
+                r["torch_grouped_mm_us"] = None
+                r["torch_note"] = type(e).__name__
+            rows.append(r)
+        del W
+        torch.cuda.empty_cache()
+    return rows
+
+
+def cpu_baseline(rows: int):
+    """The fp64 oracle on a bounded sample of the step: `rows` rows of every
+    GEMM of the step and of both RMSNorms, on the host's cores."""
+    import numpy as np
+    import bi_synth as syn
+    import oracle
+    x, res, w, _ = syn.rmsnorm_inputs(rows, H, seed=0, outlier_frac=0.0)
+    Ws = {name: syn.to_bf16_bits(syn.normal_rows(10 + i, syn.TID_W, n, k, std=0.02))
+          for i, (name, (n, k)) in enumerate(LAYERS.items())}
+    Xd = syn.to_bf16_bits(syn.normal_rows(0, syn.TID_X, rows, LAYERS["down"][1]))
+    t0 = time.perf_counter()
+    y1, h = oracle.rmsnorm(x, w, EPS, residual=res)
+    oracle.gemm_bf16(oracle.bf16_round_array(y1), Ws["qkv"])
+    y2, _ = oracle.rmsnorm(x, w, EPS, residual=h)
+    oracle.gemm_bf16(oracle.bf16_round_array(y2), Ws["gate_up"])
+    oracle.gemm_bf16(Xd, Ws["down"])
+    dt = time.perf_counter() - t0
+    return step_flops(rows) / dt / 1e12, dt, oracle.threads()
+
+
+def run_ours(args, dist):
+    import torch
+    import invariant_deterministic_bi_gb300 as bi
+    bi.load()
+    peaks, peak_src = load_peaks()
+    M = M_STEP
+    inp = make_step_inputs(M, seed=dist.rank)
+    step = Step(bi, inp, M)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = bi.device_status()
+    if st != bi.BI_OK:
+        raise RuntimeError(f"device status after warm-up: {bi.status_string(st)}")
+
+    # ---- timed region: K steps back to back, events around each GEMM launch
+    dist.barrier()
+    torch.cuda.synchronize()
+    t0e, t1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        t0e.record()
+        for _ in range(args.steps):
+            step(events=True)
+        t1e.record()
+        torch.cuda.synchronize()
+    dist.barrier()
+    ms_total = dist.max(t0e.elapsed_time(t1e))
+    clocks = clk.summary()
+    gemm_ms = [a.elapsed_time(b) for a, b in step.gemm_events]
+    st = bi.device_status()
+    if st != bi.BI_OK:
+        raise RuntimeError(f"device status after timed steps: {bi.status_string(st)}")
+
+    ms_per_step = ms_total / args.steps
+    flops = step_flops(M)
+    value = flops * dist.world / (ms_per_step * 1e-3) / 1e12
+    launches_per_step = 5
+    gemm_flops_per_launch = flops / 3
+    gemm_avg_ms = sum(gemm_ms) / len(gemm_ms)
+    achieved = gemm_flops_per_launch / (gemm_avg_ms * 1e-3) / 1e12
+    roofline = {"kernel": "bi_gemm_bf16 (qkv, gate_up, down launches of the step)", "bound": "tensor",
+                "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(achieved / peaks["bf16_tflops"], 3),
+                "peak_source": f"{peak_src} bf16 burst (cuBLAS 8192^3)", "traffic": None}
+
+    # ---- end to end: host buffers in, results out, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        hx = torch.empty_like(inp["x"], device="cpu").pin_memory()
+        hx2 = torch.empty_like(inp["x2"], device="cpu").pin_memory()
+        hres = torch.empty_like(inp["res"], device="cpu").pin_memory()
+        hx.copy_(inp["x"].cpu()), hx2.copy_(inp["x2"].cpu()), hres.copy_(inp["res"].cpu())
+        hq = torch.empty_like(step.qkv, device="cpu").pin_memory()
+        hd = torch.empty_like(step.dn, device="cpu").pin_memory()
+        k_e2e = max(3, args.steps // 4)
+
+        def e2e_step():
+            inp["x"].copy_(hx, non_blocking=True)
+            inp["x2"].copy_(hx2, non_blocking=True)
+            inp["res"].copy_(hres, non_blocking=True)
+            step()
+            hq.copy_(step.qkv, non_blocking=True)
+            hd.copy_(step.dn, non_blocking=True)
+        e2e_step()
+        torch.cuda.synchronize()
+        dist.barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(k_e2e):
+            e2e_step()
+        b.record()
+        torch.cuda.synchronize()
+        ms = dist.max(a.elapsed_time(b)) / k_e2e
+        h2d = 3 * inp["x"].numel() * 2
+        d2h = (step.qkv.numel() + step.dn.numel()) * 2
+        e2e = {"value": round(flops * dist.world / (ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
+               "ms_per_step": round(ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    breakdown = {}
+    if not args.no_breakdown and dist.rank == 0:
+        rows, cublas_inv = gemm_sweep(bi, peaks)
+        breakdown["gemm_bf16_vs_M"] = rows
+        breakdown["cublas_row0_equal_M1_vs_M4096"] = cublas_inv
+        breakdown["rmsnorm"] = rmsnorm_sweep(bi, peaks)
+        breakdown["grouped_gemm_bf16_moe"] = moe_sweep(bi, peaks)
+        if bi.device_status() != bi.BI_OK:
+            raise RuntimeError("device status after breakdown")
+
+    cpu = None
+    if dist.rank == 0 and not args.no_cpu:
+        v, dt, cores = cpu_baseline(args.cpu_rows)
+        cpu = {"value": round(v, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": f"{args.cpu_rows} rows of the step (2 RMSNorm rows + qkv/gate_up/down GEMM rows), "
+                         f"fp64, {dt:.1f} s"}
+
+    line = {"metric": METRIC, "value": round(value, 1), "unit": "TFLOP/s", "n_gpus": dist.world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) activations, N(0,0.02^2) weights; no model weights)",
+            "config": {"workload": "Qwen3-8B-shaped decoder-layer linears at M=8192: RMSNorm+residual -> qkv "
+                                   "(4096->6144) -> RMSNorm+residual -> gate_up (4096->24576) -> down (12288->4096)",
+                       "M": M, "hidden": H, "parallelism": f"replicas x{dist.world}",
+                       "l2": "no flush: each step streams > 1 GB (weights 352 MB + activations), L2 is 129 MB"},
+            "roofline": roofline, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks, "cpu_baseline": cpu, "breakdown": breakdown}
+    return line
+
+
+# ------------------------------------------------------------ reference arm
+
+def run_reference(args, dist):
+    """The fp64 CPU oracle timed as the reference arm, on a bounded sample per step."""
+    if dist.rank != 0:
+        return None
+    rows = args.ref_rows
+    for _ in range(args.warmup):
+        cpu_baseline(rows)
+    t = 0.0
+    for _ in range(args.steps):
+        _, dt, cores = cpu_baseline(rows)
+        t += dt
+    ms = t / args.steps * 1e3
+    v = step_flops(rows) / (ms * 1e-3) / 1e12
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TFLOP/s", "n_gpus": dist.world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "Qwen3-8B-shaped decoder-layer linears (same step), "
+                                   f"bounded sample of {rows} rows per step", "M": rows, "hidden": H},
+            "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{rows} rows of the step per step"},
+            "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def profile_case(spec: str, reps: int):
+    """Run one kernel configuration `reps` times (for ncu captures); no output line.
+    spec: gemm:<qkv|gate_up|down>:<M> | rmsnorm:<M>:<0|1 residual> | grouped:<gate_up|down>:<T>"""
+    import torch
+    import bi_synth as syn
+    import invariant_deterministic_bi_gb300 as bi
+    bi.load()
+    kind, *rest = spec.split(":")
+    if kind == "gemm":
+        n, k = LAYERS[rest[0]]
+        M = int(rest[1])
+        X = bf16_dev(syn.to_bf16_bits(syn.normal_rows(0, syn.TID_X, M, k)))
+        W = bf16_dev(syn.to_bf16_bits(syn.normal_rows(0, syn.TID_W, n, k, std=0.02)))
+        Y = torch.empty((M, n), dtype=torch.bfloat16, device="cuda")
+        fn = lambda: bi.gemm_bf16(X, W, Y=Y)
+    elif kind == "rmsnorm":
+        M, res = int(rest[0]), rest[1] == "1"
+        x, r, w, _ = syn.rmsnorm_inputs(M, H, seed=0)
+        xd, rd, wd = bf16_dev(x), (bf16_dev(r) if res else None), bf16_dev(w)
+        out = torch.empty_like(xd)
+        fn = lambda: bi.rmsnorm(xd, wd, EPS, residual=rd, out=out)
+    elif kind == "grouped":
+        X, W, off, _ = moe_inputs(rest[0], int(rest[1]))
+        Y = torch.empty((X.shape[0], W.shape[1]), dtype=torch.bfloat16, device="cuda")
+        fn = lambda: bi.grouped_gemm_bf16(X, W, off, Y=Y)
+    else:
+        raise SystemExit(f"unknown profile case {spec}")
+    for _ in range(reps):
+        fn()
+    torch.cuda.synchronize()
+    st = bi.device_status()
+    if st != bi.BI_OK:
+        raise SystemExit(f"device status {bi.status_string(st)}")
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-breakdown", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=192)
+    ap.add_argument("--ref-rows", type=int, default=2)
+    ap.add_argument("--profile", default=None, help="run one kernel case only (see profile_case)")
+    ap.add_argument("--reps", type=int, default=4)
+    args = ap.parse_args()
+    if args.profile:
+        profile_case(args.profile, args.reps)
+        return
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        if rank != 0:          # the CPU oracle runs once, on rank 0
+            return
+        line = run_reference(args, Dist(1, 0, None))
+        line["n_gpus"] = world
+        print(json.dumps(line), flush=True)
+        return
+    import torch
+    torch.cuda.set_device(local)
+    dist = Dist(world, rank, "nccl")
+    line = run_ours(args, dist)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    dist.close()
+
+
+if __name__ == "__main__":
+    main()
