@@ -340,20 +340,92 @@ def moe_sweep(bi, peaks):
                  "frac_bf16_peak": round(flops / (t * 1e-3) / 1e12 / peaks["bf16_tflops"], 3),
                  "gbs": round(nbytes / (t * 1e-3) / 1e9, 0),
                  "frac_hbm_measured": round(nbytes / (t * 1e-3) / 1e9 / peaks["hbm_gbs"], 3)}
-            try:
-                Wt = W.transpose(1, 2)
-                ends = off[1:].contiguous()
-                torch._grouped_mm(X, Wt, offs=ends)
-                t2 = time_fn(lambda: torch._grouped_mm(X, Wt, offs=ends), 20 if T <= 512 else 5)
-                r["torch_grouped_mm_us"] = round(t2 * 1e3, 2)
-                r["cost_vs_torch"] = round(t / t2, 3)
-            except Exception as e:  # not every torch build has a bf16 grouped GEMM for this arch
-                r["torch_grouped_mm_us"] = None
-                r["torch_note"] = type(e).__name__
+            # non-invariant library reference: one cuBLAS matmul per non-empty expert
+            offh = off.cpu().tolist()
+            segs = [(e, offh[e], offh[e + 1]) for e in range(MOE_E) if offh[e + 1] > offh[e]]
+
+            def per_expert():
+                for e, a, b in segs:
+                    torch.matmul(X[a:b], W[e].t(), out=Y[a:b])
+            t2 = time_fn(per_expert, 20 if T <= 512 else 5)
+            r["cublas_per_expert_us"] = round(t2 * 1e3, 2)
+            r["cost_vs_cublas_per_expert"] = round(t / t2, 3)
             rows.append(r)
         del W
         torch.cuda.empty_cache()
     return rows
+
+
+NVFP4_N, NVFP4_K = 14336, 4096
+NVFP4_M = [1, 16, 256, 4096]
+
+
+def torch_nvfp4_mm(A, SA_il, B, SB_il, M, N, K):
+    """cuBLASLt NVFP4 GEMM through torch._scaled_mm (not batch-invariant by
+    contract); returns a callable, or None when this torch build lacks it."""
+    import torch
+    try:
+        a = A.view(torch.float4_e2m1fn_x2)
+        b = B.view(torch.float4_e2m1fn_x2).t()
+        rp = lambda r: -(-r // 128) * 128
+        cp = -(-(K // 16) // 4) * 4
+        sa = SA_il.view(torch.float8_e4m3fn)[: rp(M) * cp].view(rp(M), cp)
+        sb = SB_il.view(torch.float8_e4m3fn)[: rp(N) * cp].view(rp(N), cp)
+        fn = lambda: torch._scaled_mm(a, b, sa, sb, out_dtype=torch.bfloat16)
+    except Exception:
+        return None
+    try:
+        fn()
+    except RuntimeError:     # argument rejected on the host: not available here
+        return None
+    torch.cuda.synchronize()  # a device error here is not swallowed
+    return fn
+
+
+def nvfp4_sweep(bi, peaks):
+    """bi_gemm_nvfp4 vs M at K=4096, N=14336, against cuBLASLt NVFP4 via torch."""
+    import torch
+    import bi_synth as syn
+    d = syn.nvfp4_inputs(max(NVFP4_M), NVFP4_N, NVFP4_K, seed=0)
+    Bd, SBd = torch.from_numpy(d["B"]).cuda(), torch.from_numpy(d["SB_il"]).cuda()
+    rows, fp4_peak, peak_note = [], None, "unmeasured"
+    # dense fp4 peak on this GPU: cuBLASLt NVFP4 at 8192^3, if torch exposes it
+    if os.environ.get("BI_BENCH_CUBLASLT_FP4", "0") == "1":
+        g = torch.Generator(device="cuda").manual_seed(0)
+        big = torch.randint(0, 256, (8192, 4096), dtype=torch.uint8, device="cuda", generator=g)
+        sc = torch.full((8192 * 512,), 0x38, dtype=torch.uint8, device="cuda")
+        f = torch_nvfp4_mm(big, sc, big, sc, 8192, 8192, 8192)
+        if f is not None:
+            t = time_fn(f, 20)
+            fp4_peak = 2.0 * 8192 ** 3 / (t * 1e-3) / 1e12
+            peak_note = "measured: cuBLASLt NVFP4 8192^3 via torch._scaled_mm (burst)"
+        del big, sc
+    if fp4_peak is None:
+        fp4_peak = peaks["bf16_tflops"] * 6.0
+        peak_note = "measured bf16 peak x 6 (nominal fp4/bf16 dense ratio 13.5/2.25)"
+    for M in NVFP4_M:
+        A = torch.from_numpy(d["A"][:M].copy()).cuda()
+        SA = torch.from_numpy(syn.swizzle_block_scales(d["SA"][:M])).cuda()
+        Y = torch.empty((M, NVFP4_N), dtype=torch.bfloat16, device="cuda")
+        t = time_fn(lambda: bi.gemm_nvfp4(A, SA, Bd, SBd, float(d["alpha"]), Y=Y), 50 if M <= 256 else 10)
+        flops = 2.0 * M * NVFP4_N * NVFP4_K
+        nbytes = (M + NVFP4_N) * NVFP4_K * (0.5 + 1 / 16) + 2 * M * NVFP4_N
+        r = {"M": M, "N": NVFP4_N, "K": NVFP4_K, "us": round(t * 1e3, 2),
+             "tflops": round(flops / (t * 1e-3) / 1e12, 1),
+             "frac_fp4_peak": round(flops / (t * 1e-3) / 1e12 / fp4_peak, 3),
+             "gbs": round(nbytes / (t * 1e-3) / 1e9, 0),
+             "frac_hbm_measured": round(nbytes / (t * 1e-3) / 1e9 / peaks["hbm_gbs"], 3)}
+        f = torch_nvfp4_mm(A, SA, Bd, SBd, M, NVFP4_N, NVFP4_K) if os.environ.get("BI_BENCH_CUBLASLT_FP4") == "1" \
+            else None
+        if f is not None:
+            t2 = time_fn(f, 50 if M <= 256 else 10)
+            r["cublaslt_us"] = round(t2 * 1e3, 2)
+            r["cost_vs_cublaslt"] = round(t / t2, 3)
+            ours = Y.float()
+            theirs = f().float() * float(d["alpha"])
+            r["max_rel_diff_vs_cublaslt"] = float(((ours - theirs).abs() / (theirs.abs() + 1)).max())
+        rows.append(r)
+    return {"fp4_peak_tflops": round(fp4_peak, 1), "fp4_peak_source": peak_note, "rows": rows}
 
 
 def cpu_baseline(rows: int):
@@ -461,6 +533,7 @@ def run_ours(args, dist):
         breakdown["cublas_row0_equal_M1_vs_M4096"] = cublas_inv
         breakdown["rmsnorm"] = rmsnorm_sweep(bi, peaks)
         breakdown["grouped_gemm_bf16_moe"] = moe_sweep(bi, peaks)
+        breakdown["gemm_nvfp4"] = nvfp4_sweep(bi, peaks)
         if bi.device_status() != bi.BI_OK:
             raise RuntimeError("device status after breakdown")
 
@@ -530,15 +603,21 @@ def profile_case(spec: str, reps: int):
         xd, rd, wd = bf16_dev(x), (bf16_dev(r) if res else None), bf16_dev(w)
         out = torch.empty_like(xd)
         fn = lambda: bi.rmsnorm(xd, wd, EPS, residual=rd, out=out)
+    elif kind == "nvfp4":
+        M = int(rest[0])
+        d = syn.nvfp4_inputs(M, NVFP4_N, NVFP4_K, seed=0)
+        A, SA = torch.from_numpy(d["A"]).cuda(), torch.from_numpy(d["SA_il"]).cuda()
+        B, SB = torch.from_numpy(d["B"]).cuda(), torch.from_numpy(d["SB_il"]).cuda()
+        Y = torch.empty((M, NVFP4_N), dtype=torch.bfloat16, device="cuda")
+        fn = lambda: bi.gemm_nvfp4(A, SA, B, SB, float(d["alpha"]), Y=Y)
     elif kind == "grouped":
         X, W, off, _ = moe_inputs(rest[0], int(rest[1]))
         Y = torch.empty((X.shape[0], W.shape[1]), dtype=torch.bfloat16, device="cuda")
         fn = lambda: bi.grouped_gemm_bf16(X, W, off, Y=Y)
     else:
         raise SystemExit(f"unknown profile case {spec}")
-    for _ in range(reps):
-        fn()
-    torch.cuda.synchronize()
+    ms = time_fn(fn, reps, warm=1)
+    print(json.dumps({"profile": spec, "reps": reps, "us_per_call": round(ms * 1e3, 2)}), flush=True)
     st = bi.device_status()
     if st != bi.BI_OK:
         raise SystemExit(f"device status {bi.status_string(st)}")

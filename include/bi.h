@@ -131,9 +131,10 @@ BI_API bi_status bi_gemm_nvfp4(const uint8_t *A, const uint8_t *A_sf, const uint
  * The RMSNorm that vLLM fuses with the tensor-parallel all-reduce (vLLM PR
  * #51292, Purpose and root-cause discussion: its fused kernel reduces with
  * shuffles and block reductions whose order varies run to run). Here each row
- * is reduced by one warp: every lane sums the squares of its elements in
- * index order, then a fixed xor-shuffle tree combines the 32 lane sums. The
- * tree depends only on H.
+ * is reduced by one CTA over a fixed tree that depends only on H: every thread
+ * sums the squares of its elements in index order, a fixed xor-shuffle
+ * butterfly combines each warp's 32 sums, and the warp sums are added in warp
+ * order.
  *   h = residual ? bf16(x + residual) : x       (written back to residual)
  *   out = bf16( h * (1 / sqrt(sum(h^2)/H + eps)) * w ),  fp32 arithmetic
  *
@@ -160,16 +161,16 @@ enum { BI_OP_GEMM_BF16 = 0, BI_OP_GROUPED_GEMM_BF16 = 1, BI_OP_GEMM_NVFP4 = 2, B
  */
 typedef struct {
     int32_t op;
-    int32_t block_m, block_n, block_k;   /* CTA tile (rows, cols, K step); RMSNorm: rows per CTA, H, 8 */
+    int32_t block_m, block_n, block_k;   /* CTA tile (rows, cols, K step); RMSNorm: 1 row per CTA, H, 8 */
     int32_t mma_m, mma_n, mma_k;         /* tcgen05.mma instruction shape (0 for RMSNorm) */
-    int32_t k_steps;                     /* K steps per output tile (fixed by K) */
+    int32_t k_steps;                     /* K steps per output tile (fixed by K); RMSNorm: vectors per thread */
     int32_t split_k;                     /* always 1: no split of the K reduction */
     int32_t stages;                      /* shared-memory pipeline depth */
     int32_t threads;                     /* threads per CTA */
     int32_t smem_bytes;                  /* dynamic shared memory per CTA */
     int64_t tiles_m, tiles_n;            /* output tiles (tiles_m depends on M) */
     int32_t grid;                        /* CTAs launched (persistent GEMMs: <= SM count) */
-    int32_t reduce_tree;                 /* RMSNorm: elements per lane sum (ceil(H/256)*8) */
+    int32_t reduce_tree;                 /* RMSNorm: elements each thread sums in index order */
 } bi_plan_t;
 
 BI_API bi_status bi_plan(int32_t op, int64_t M, int64_t N, int64_t K, int32_t num_sms, bi_plan_t *out);

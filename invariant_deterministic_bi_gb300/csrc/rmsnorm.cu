@@ -4,17 +4,22 @@
 // fuse_allreduce_rms under VLLM_BATCH_INVARIANT") turns off reduces with
 // shuffles and block reductions in an order that varies from run to run.
 // Here the order is a function of H alone:
-//   - one warp owns one row; lane l owns the 16-byte vectors l, l+32, l+64, ...
-//     (8 bf16 each) and sums the squares of its elements in index order (fp32);
-//   - the 32 lane sums are combined by the xor-shuffle butterfly 16, 8, 4, 2, 1,
-//     which leaves the same total in every lane (fp32 addition commutes).
-// Rows never interact, so a row's output does not depend on M or on which
-// warp or CTA processes it.
+//   - one CTA of T threads owns one row (T = 128 for H <= 16384, 512 above);
+//     thread t owns the 16-byte vectors t, t+T, t+2T, ... (8 bf16 each) and
+//     sums the squares of its elements in index order (fp32 FMA);
+//   - each warp combines its 32 thread sums with the xor-shuffle butterfly
+//     16, 8, 4, 2, 1 (every lane ends with the same value: fp32 addition
+//     commutes);
+//   - thread 0 adds the warp sums in warp order through shared memory and
+//     broadcasts the total.
+// Rows never interact, so a row's output does not depend on M or on which CTA
+// processes it.
 //
-// Memory: 128-bit loads and stores, coalesced across the warp (lane l reads
-// bytes 16l .. 16l+15 of each 512-byte segment); x and residual are streamed
-// (evict-first), the weight row stays cached. For H <= 8192 the row lives in
-// registers between the two passes; larger H re-reads it.
+// Memory: 128-bit loads and stores, coalesced (thread t reads bytes 16t ..
+// 16t+15 of each 16T-byte segment). With 4 vectors per thread at H = 4096 the
+// kernel needs few registers, so 16 CTAs (64 warps) fit on an SM and every SM
+// keeps ~256 KB of loads in flight. x and residual are streamed (evict-first);
+// the weight row stays cached.
 #include <cuda_bf16.h>
 
 #include "bi_internal.h"
@@ -22,9 +27,6 @@
 
 namespace bi {
 namespace {
-
-constexpr int kRowsPerCta = 8;   // 8 warps, one row each
-constexpr int kThreads = 32 * kRowsPerCta;
 
 __device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
@@ -64,94 +66,107 @@ __device__ __forceinline__ uint4 scale(uint4 h, uint4 w, float r) {
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-__device__ __forceinline__ float row_scale(float ss, int H, float eps) {
+// 1 / sqrt(sum/H + eps) for the whole CTA: warp butterflies, then the warp sums
+// in warp order. `red` holds T/32 + 1 floats.
+template <int T>
+__device__ __forceinline__ float row_scale(float ss, int H, float eps, float *red) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    return __fdiv_rn(1.0f, __fsqrt_rn(__fdiv_rn(ss, static_cast<float>(H)) + eps));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float total = red[0];
+#pragma unroll
+        for (int w = 1; w < T / 32; ++w) total += red[w];
+        red[T / 32] = __fdiv_rn(1.0f, __fsqrt_rn(__fdiv_rn(total, static_cast<float>(H)) + eps));
+    }
+    __syncthreads();
+    return red[T / 32];
 }
 
-// Row held in registers: VPL vectors per lane (H <= 256 * VPL).
-template <int VPL, bool RESIDUAL>
-__global__ void __launch_bounds__(kThreads)
-rmsnorm_reg_kernel(const uint4 *x, uint4 *residual, const uint4 *__restrict__ w, uint4 *out, int64_t M,
-                   int H, float eps) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+// One row per CTA; VPT vectors per thread (H <= 8 * T * VPT).
+template <int T, int VPT, bool RESIDUAL>
+__global__ void __launch_bounds__(T)
+rmsnorm_kernel(const uint4 *x, uint4 *residual, const uint4 *__restrict__ w, uint4 *out, int H, float eps) {
+    __shared__ float red[T / 32 + 1];
+    const int64_t row = blockIdx.x;
     const int nvec = H >> 3;
-    for (int64_t row = static_cast<int64_t>(blockIdx.x) * kRowsPerCta + warp; row < M;
-         row += static_cast<int64_t>(gridDim.x) * kRowsPerCta) {
-        const uint4 *xr = x + row * nvec;
-        uint4 *rr = RESIDUAL ? residual + row * nvec : nullptr;
-        uint4 h[VPL];
-        float ss = 0.0f;
+    const int t = threadIdx.x;
+    const uint4 *xr = x + row * nvec;
+    uint4 *rr = RESIDUAL ? residual + row * nvec : nullptr;
+    uint4 h[VPT];
 #pragma unroll
-        for (int i = 0; i < VPL; ++i) {
-            const int j = lane + 32 * i;
-            if (j < nvec) {
-                h[i] = __ldcs(xr + j);
-                if (RESIDUAL) h[i] = add_round(h[i], __ldcs(rr + j));
-            }
+    for (int i = 0; i < VPT; ++i) {
+        const int j = t + T * i;
+        if (j < nvec) {
+            h[i] = __ldcs(xr + j);
+            if (RESIDUAL) h[i] = add_round(h[i], __ldcs(rr + j));
         }
+    }
+    float ss = 0.0f;
 #pragma unroll
-        for (int i = 0; i < VPL; ++i) {
-            const int j = lane + 32 * i;
-            if (j < nvec) {
-                if (RESIDUAL) __stcs(rr + j, h[i]);
-                ss = sum_squares(h[i], ss);
-            }
+    for (int i = 0; i < VPT; ++i) {
+        const int j = t + T * i;
+        if (j < nvec) {
+            if (RESIDUAL) __stcs(rr + j, h[i]);
+            ss = sum_squares(h[i], ss);
         }
-        const float r = row_scale(ss, H, eps);
-        uint4 *orow = out + row * nvec;
+    }
+    const float r = row_scale<T>(ss, H, eps, red);
+    uint4 *orow = out + row * nvec;
 #pragma unroll
-        for (int i = 0; i < VPL; ++i) {
-            const int j = lane + 32 * i;
-            if (j < nvec) __stcs(orow + j, scale(h[i], __ldg(w + j), r));
-        }
+    for (int i = 0; i < VPT; ++i) {
+        const int j = t + T * i;
+        if (j < nvec) __stcs(orow + j, scale(h[i], __ldg(w + j), r));
     }
 }
 
-// Any H: the first pass stores h (to residual) and sums; the second re-reads h.
-template <bool RESIDUAL>
-__global__ void __launch_bounds__(kThreads)
-rmsnorm_loop_kernel(const uint4 *x, uint4 *residual, const uint4 *__restrict__ w, uint4 *out, int64_t M, int H,
-                    float eps) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nvec = H >> 3;
-    for (int64_t row = static_cast<int64_t>(blockIdx.x) * kRowsPerCta + warp; row < M;
-         row += static_cast<int64_t>(gridDim.x) * kRowsPerCta) {
-        const uint4 *xr = x + row * nvec;
-        uint4 *rr = RESIDUAL ? residual + row * nvec : nullptr;
-        float ss = 0.0f;
-        for (int j = lane; j < nvec; j += 32) {
-            uint4 h = xr[j];
-            if (RESIDUAL) {
-                h = add_round(h, rr[j]);
-                rr[j] = h;
-            }
-            ss = sum_squares(h, ss);
-        }
-        const float r = row_scale(ss, H, eps);
-        const uint4 *hr = RESIDUAL ? rr : xr;
-        uint4 *orow = out + row * nvec;
-        for (int j = lane; j < nvec; j += 32) orow[j] = scale(hr[j], __ldg(w + j), r);
+// Threads per row and vectors per thread, chosen from H alone.
+struct RowShape {
+    int threads, vpt;
+};
+RowShape row_shape(int64_t H) {
+    const int64_t nvec = H / 8;
+    if (nvec <= 128 * 16) {
+        int vpt = 1;
+        while (128 * vpt < nvec) vpt *= 2;
+        return {128, vpt};
     }
+    int vpt = 1;
+    while (512 * vpt < nvec) vpt *= 2;
+    return {512, vpt};
+}
+
+template <int T, int VPT, bool RES>
+bi_status launch_one(const void *x, void *residual, const void *w, void *out, int64_t M, int64_t H, float eps,
+                     cudaStream_t s) {
+    rmsnorm_kernel<T, VPT, RES><<<static_cast<unsigned>(M), T, 0, s>>>(
+        static_cast<const uint4 *>(x), static_cast<uint4 *>(residual), static_cast<const uint4 *>(w),
+        static_cast<uint4 *>(out), static_cast<int>(H), eps);
+    return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
 }
 
 template <bool RES>
 bi_status launch_res(const void *x, void *residual, const void *w, void *out, int64_t M, int64_t H, float eps,
-                     int grid, cudaStream_t s) {
-    auto X = static_cast<const uint4 *>(x);
-    auto R = static_cast<uint4 *>(residual);
-    auto Wt = static_cast<const uint4 *>(w);
-    auto O = static_cast<uint4 *>(out);
-    const int h = static_cast<int>(H);
-    if (H <= 256) rmsnorm_reg_kernel<1, RES><<<grid, kThreads, 0, s>>>(X, R, Wt, O, M, h, eps);
-    else if (H <= 512) rmsnorm_reg_kernel<2, RES><<<grid, kThreads, 0, s>>>(X, R, Wt, O, M, h, eps);
-    else if (H <= 1024) rmsnorm_reg_kernel<4, RES><<<grid, kThreads, 0, s>>>(X, R, Wt, O, M, h, eps);
-    else if (H <= 2048) rmsnorm_reg_kernel<8, RES><<<grid, kThreads, 0, s>>>(X, R, Wt, O, M, h, eps);
-    else if (H <= 4096) rmsnorm_reg_kernel<16, RES><<<grid, kThreads, 0, s>>>(X, R, Wt, O, M, h, eps);
-    else if (H <= 8192) rmsnorm_reg_kernel<32, RES><<<grid, kThreads, 0, s>>>(X, R, Wt, O, M, h, eps);
-    else rmsnorm_loop_kernel<RES><<<grid, kThreads, 0, s>>>(X, R, Wt, O, M, h, eps);
-    return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
+                     cudaStream_t s) {
+    const RowShape rs = row_shape(H);
+    if (rs.threads == 128) {
+        switch (rs.vpt) {
+            case 1: return launch_one<128, 1, RES>(x, residual, w, out, M, H, eps, s);
+            case 2: return launch_one<128, 2, RES>(x, residual, w, out, M, H, eps, s);
+            case 4: return launch_one<128, 4, RES>(x, residual, w, out, M, H, eps, s);
+            case 8: return launch_one<128, 8, RES>(x, residual, w, out, M, H, eps, s);
+            default: return launch_one<128, 16, RES>(x, residual, w, out, M, H, eps, s);
+        }
+    }
+    switch (rs.vpt) {
+        case 1: return launch_one<512, 1, RES>(x, residual, w, out, M, H, eps, s);
+        case 2: return launch_one<512, 2, RES>(x, residual, w, out, M, H, eps, s);
+        case 4: return launch_one<512, 4, RES>(x, residual, w, out, M, H, eps, s);
+        case 8: return launch_one<512, 8, RES>(x, residual, w, out, M, H, eps, s);
+        default: return launch_one<512, 16, RES>(x, residual, w, out, M, H, eps, s);
+    }
 }
 
 __global__ void wait_timeout_check_kernel(unsigned *status, unsigned long long limit_ns) {
@@ -167,29 +182,27 @@ __global__ void wait_timeout_check_kernel(unsigned *status, unsigned long long l
 }  // namespace
 
 void plan_rmsnorm(int64_t M, int64_t H, bi_plan_t *pl) {
+    const RowShape rs = row_shape(H);
     pl->op = BI_OP_RMSNORM;
-    pl->block_m = kRowsPerCta;
+    pl->block_m = 1;                               // rows per CTA
     pl->block_n = static_cast<int32_t>(H);
-    pl->block_k = 8;
+    pl->block_k = 8;                               // elements per vector
     pl->mma_m = pl->mma_n = pl->mma_k = 0;
-    pl->k_steps = static_cast<int32_t>((H / 8 + 31) / 32);
+    pl->k_steps = rs.vpt;                          // vectors per thread
     pl->split_k = 1;
     pl->stages = 1;
-    pl->threads = kThreads;
-    pl->smem_bytes = 0;
-    pl->tiles_m = (M + kRowsPerCta - 1) / kRowsPerCta;
+    pl->threads = rs.threads;
+    pl->smem_bytes = static_cast<int32_t>((rs.threads / 32 + 1) * 4);
+    pl->tiles_m = M;
     pl->tiles_n = 1;
-    const int64_t max_grid = 1 << 20;
-    pl->grid = static_cast<int32_t>(pl->tiles_m < max_grid ? pl->tiles_m : max_grid);
-    pl->reduce_tree = static_cast<int32_t>(((H / 8 + 31) / 32) * 8);
+    pl->grid = static_cast<int32_t>(M);
+    pl->reduce_tree = rs.vpt * 8;                  // elements each thread sums in order
 }
 
 bi_status launch_rmsnorm(const void *x, void *residual, const void *w, void *out, int64_t M, int64_t H, float eps,
                          cudaStream_t s) {
-    bi_plan_t pl;
-    plan_rmsnorm(M, H, &pl);
-    return residual ? launch_res<true>(x, residual, w, out, M, H, eps, pl.grid, s)
-                    : launch_res<false>(x, residual, w, out, M, H, eps, pl.grid, s);
+    return residual ? launch_res<true>(x, residual, w, out, M, H, eps, s)
+                    : launch_res<false>(x, residual, w, out, M, H, eps, s);
 }
 
 bi_status launch_wait_timeout_check(uint32_t limit_us, cudaStream_t s) {

@@ -77,7 +77,8 @@ def test_grouped_and_nvfp4_and_rmsnorm_plans_independent_of_M(lib):
 
 def test_rmsnorm_plan_tree(lib):
     p = _plan(lib, lib.OP_RMSNORM, 16384, 4096, 0)
-    assert p["reduce_tree"] == 128 and p["block_m"] == 8
+    assert p["reduce_tree"] == 32 and p["threads"] == 128 and p["block_m"] == 1 and p["grid"] == 16384
+    assert _plan(lib, lib.OP_RMSNORM, 5, 65536, 0)["threads"] == 512
 
 
 FAKE = 0x10000   # never dereferenced: every call below fails validation first

@@ -48,6 +48,13 @@ def test_e2m1_encode_rounding():
     assert got == [0.0, 1.0, 2.0, 4.0, 4.0, 0.0, -4.0, 6.0, 6.0, 1.0, 0.0]
 
 
+def test_e2m1_fast_encoder_matches_search():
+    g = syn.rng(5, 0)
+    v = np.concatenate([g.uniform(-6.5, 6.5, 200000).astype(np.float32),
+                        np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -0.25, -5.0, 0.0, -0.0], np.float32)])
+    assert np.array_equal(syn.e2m1_encode(v), syn.e2m1_encode_by_search(v))
+
+
 def test_e4m3_encode_roundtrip_and_saturation():
     codes = np.arange(0, 127, dtype=np.uint8)
     vals = np.array([oracle.e4m3_value(int(c)) for c in codes])
