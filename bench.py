@@ -201,18 +201,37 @@ class Step:
         gemm(self.gu[:, :LAYERS["down"][1]], d["W_down"], self.dn)
 
 
-def time_fn(fn, reps: int, warm: int = 3) -> float:
-    """Mean device time (ms) of fn() over reps back-to-back calls (CUDA events)."""
+def time_fn(fn, reps: int, warm: int = 3, graph: bool = True) -> float:
+    """Mean device time (ms) of fn() over reps back-to-back calls, CUDA events
+    around one replay of a CUDA graph holding the reps calls (so small calls
+    are not timed at the host's launch rate). graph=False times eager calls."""
     import torch
     for _ in range(warm):
         fn()
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if not graph:
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g):
+            for _ in range(reps):
+                fn()
+    torch.cuda.current_stream().wait_stream(side)
+    g.replay()
+    torch.cuda.synchronize()
     a.record()
-    for _ in range(reps):
-        fn()
+    g.replay()
     b.record()
     torch.cuda.synchronize()
+    del g
     return a.elapsed_time(b) / reps
 
 

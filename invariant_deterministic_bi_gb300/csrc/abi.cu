@@ -69,6 +69,18 @@ unsigned *device_status_word() {
     return g_devices[dev].status;
 }
 
+bi_status ensure_smem_attr(const void *kernel, int bytes, unsigned long long *done) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return BI_ERR_CUDA;
+    const unsigned long long bit = 1ull << dev;
+    auto *flag = reinterpret_cast<std::atomic<unsigned long long> *>(done);
+    if (flag->load(std::memory_order_acquire) & bit) return BI_OK;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+        return BI_ERR_CUDA;
+    flag->fetch_or(bit, std::memory_order_acq_rel);
+    return BI_OK;
+}
+
 bi_status make_tmap_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, uint64_t inner,
                        uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
                        CUtensorMapSwizzle swizzle) {

@@ -33,6 +33,10 @@ bi_status make_tmap_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Raise a kernel's dynamic shared-memory limit once per device. `done` is a
+// per-kernel bitmask of devices already configured.
+bi_status ensure_smem_attr(const void *kernel, int bytes, unsigned long long *done);
+
 // Kernel launchers (defined in the .cu files); arguments already validated.
 bi_status launch_gemm_bf16(const void *X, int64_t ldx, const void *W, int64_t ldw, void *Y, int64_t ldy,
                            int64_t M, int64_t N, int64_t K, cudaStream_t s);

@@ -296,8 +296,8 @@ template <bool GROUPED>
 bi_status launch(const CUtensorMap &ta, const CUtensorMap &tb, const Params &p, int grid, cudaStream_t s) {
     using C = Cfg<kBN, kStages>;
     auto kern = gemm_bf16_kernel<kBN, kStages, GROUPED>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) != cudaSuccess)
-        return BI_ERR_CUDA;
+    static unsigned long long configured = 0;
+    if (ensure_smem_attr(reinterpret_cast<const void *>(kern), C::kSmem, &configured) != BI_OK) return BI_ERR_CUDA;
     kern<<<grid, kThreads, C::kSmem, s>>>(ta, tb, p);
     return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
 }

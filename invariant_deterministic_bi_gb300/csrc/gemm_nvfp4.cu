@@ -311,7 +311,8 @@ bi_status launch_gemm_nvfp4(const uint8_t *A, const uint8_t *A_sf, const uint8_t
     p.atoms_per_rowblock = static_cast<int32_t>(K / kMmaK);
     p.sfb_rowblocks = static_cast<int32_t>((N + 127) / 128);
     p.status = device_status_word();
-    if (cudaFuncSetAttribute(gemm_nvfp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
+    static unsigned long long configured = 0;
+    if (ensure_smem_attr(reinterpret_cast<const void *>(gemm_nvfp4_kernel), kSmem, &configured) != BI_OK)
         return BI_ERR_CUDA;
     gemm_nvfp4_kernel<<<pl.grid, kThreads, kSmem, s>>>(ta, tb, p);
     return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
