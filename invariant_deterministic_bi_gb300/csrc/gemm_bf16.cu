@@ -1,5 +1,7 @@
-// gemm_bf16.cu -- batch-invariant bf16 linear layer (dense and MoE-grouped) on tcgen05.
+// gemm_bf16.cu -- batch-invariant MoE-grouped bf16 linear layers on tcgen05 (single-CTA tiles).
 //
+// (Dense Y = X W^T uses the CTA-pair kernel in gemm_bf16_pair.cu; expert groups
+// are often a few hundred rows, where 128-row tiles waste less.)
 // One persistent, warp-specialised kernel per (BN, stages) configuration:
 //   warp 0      TMA producer: A tile [128 x 64] and B tile [BN x 64] per K step
 //               into a STAGES-deep shared-memory ring (128-byte swizzle);
@@ -304,9 +306,9 @@ bi_status launch(const CUtensorMap &ta, const CUtensorMap &tb, const Params &p, 
 
 }  // namespace
 
-void plan_gemm_bf16(int64_t M, int64_t N, int64_t K, int sms, bi_plan_t *pl) {
+void plan_grouped_gemm_bf16(int64_t rows, int64_t N, int64_t K, int sms, bi_plan_t *pl) {
     using C = Cfg<kBN, kStages>;
-    pl->op = BI_OP_GEMM_BF16;
+    pl->op = BI_OP_GROUPED_GEMM_BF16;
     pl->block_m = kBM; pl->block_n = kBN; pl->block_k = kBK;
     pl->mma_m = kBM; pl->mma_n = kBN; pl->mma_k = kMmaK;
     pl->k_steps = static_cast<int32_t>((K + kBK - 1) / kBK);
@@ -314,40 +316,10 @@ void plan_gemm_bf16(int64_t M, int64_t N, int64_t K, int sms, bi_plan_t *pl) {
     pl->stages = kStages;
     pl->threads = kThreads;
     pl->smem_bytes = C::kSmem;
-    pl->tiles_m = (M + kBM - 1) / kBM;
+    pl->tiles_m = (rows + kBM - 1) / kBM;   // without the per-expert partial tiles
     pl->tiles_n = (N + kBN - 1) / kBN;
-    const int64_t tiles = pl->tiles_m * pl->tiles_n;
-    pl->grid = static_cast<int32_t>(tiles < sms ? tiles : sms);
+    pl->grid = sms;                         // the tile count is only known on the device
     pl->reduce_tree = 0;
-}
-
-void plan_grouped_gemm_bf16(int64_t rows, int64_t N, int64_t K, int sms, bi_plan_t *pl) {
-    plan_gemm_bf16(rows, N, K, sms, pl);
-    pl->op = BI_OP_GROUPED_GEMM_BF16;
-    pl->grid = sms;   // the tile count is only known on the device
-}
-
-bi_status launch_gemm_bf16(const void *X, int64_t ldx, const void *W, int64_t ldw, void *Y, int64_t ldy,
-                           int64_t M, int64_t N, int64_t K, cudaStream_t s) {
-    int dev;
-    const DeviceInfo *info;
-    bi_status st = current_device(&dev, &info);
-    if (st != BI_OK) return st;
-    CUtensorMap ta, tb;
-    st = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, K, M, ldx * 2, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
-    if (st != BI_OK) return st;
-    st = make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, K, N, ldw * 2, kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B);
-    if (st != BI_OK) return st;
-    bi_plan_t pl;
-    plan_gemm_bf16(M, N, K, info->sm_count, &pl);
-    Params p{};
-    p.Y = static_cast<uint8_t *>(Y);
-    p.ldy = ldy;
-    p.M = static_cast<int32_t>(M);
-    p.N = static_cast<int32_t>(N);
-    p.K = static_cast<int32_t>(K);
-    p.status = device_status_word();
-    return launch<false>(ta, tb, p, pl.grid, s);
 }
 
 bi_status launch_grouped_gemm_bf16(const void *X, const void *W, void *Y, const int32_t *offsets, int32_t E,

@@ -1,0 +1,289 @@
+// gemm_bf16_pair.cu -- batch-invariant dense bf16 linear layer on CTA pairs (tcgen05 cta_group::2).
+//
+// Y = X W^T with 256 x 256 output tiles, each computed by a cluster of two CTAs
+// on two SMs:
+//   - each CTA's warp 0 TMA-loads its own 128 rows of the A tile and its own
+//     half (128 rows) of the B tile per 64-wide K step into a 6-stage ring;
+//     both CTAs' copies complete on the even (leader) CTA's "full" barrier;
+//   - one thread of the leader issues tcgen05.mma.cta_group::2 (256 x 256 x 16):
+//     the tensor cores of both SMs read A rows from their own CTA and the two
+//     B halves from both, and each CTA's 128 accumulator rows land in its own
+//     tensor memory (two accumulators of 256 columns, so the epilogue of one
+//     tile overlaps the main loop of the next);
+//   - the leader's commits are multicast to both CTAs' barriers (stage free,
+//     accumulator ready); both CTAs' epilogue warps read their own rows and
+//     report back to the leader's "accumulator empty" barrier.
+// Against the single-CTA 128 x 256 tile this halves the B bytes each SM loads
+// and reads from shared memory per MMA (64 instead of 96 bytes per clock at
+// full rate) and cuts L2-to-SM traffic per output by a third.
+//
+// Batch invariance: the tile shape, MMA instruction and K order (64-wide K
+// steps, four 16-wide MMA steps each, ascending, from zero) are the same for
+// every M; rows never interact; only which pair computes which tile depends on M.
+#include <cuda_bf16.h>
+
+#include "bi_internal.h"
+#include "bi_ptx.cuh"
+
+namespace bi {
+namespace {
+
+constexpr int kBM = 256;       // pair tile rows (128 per CTA)
+constexpr int kHalf = 128;     // rows per CTA of A, and of B
+constexpr int kBN = 256;       // pair tile columns = MMA N
+constexpr int kBK = 64;
+constexpr int kMmaK = 16;
+constexpr int kStages = 6;
+constexpr int kThreads = 192;
+constexpr int kGroupM = 8;     // 8 pair tiles (2048 rows) per raster band
+constexpr int kABytes = kHalf * kBK * 2;
+constexpr int kBBytes = kHalf * kBK * 2;
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kBarBytes = 256;
+constexpr int kSmem = 1024 + kStages * kStageBytes + kBarBytes;
+constexpr int kTmemCols = 512;
+
+struct Params {
+    uint8_t *Y;
+    int64_t ldy;
+    int32_t M, N, K;
+    unsigned *status;
+};
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                      const Params p) {
+    constexpr uint32_t kIdesc = idesc_bf16(kBM, kBN);
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + kStages * kABytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes);
+    uint64_t *empty = full + kStages;
+    uint64_t *tfull = empty + kStages;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *drain = tempty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();          // 0: leader (issues the MMAs)
+    const int pair = static_cast<int>(blockIdx.x >> 1), npairs = static_cast<int>(gridDim.x >> 1);
+    const int num_m = (p.M + kBM - 1) / kBM;
+    const int num_n = (p.N + kBN - 1) / kBN;
+    const int total = num_m * num_n;
+    const int k_steps = (p.K + kBK - 1) / kBK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 8);   // 4 epilogue warps in each CTA
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_slot, kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync();                      // both CTAs' barriers exist, TMEM allocated
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    auto tile_of = [&](int t, int &mb, int &nb) {
+        const int per_group = kGroupM * num_n;
+        const int g = t / per_group;
+        const int first = g * kGroupM;
+        const int gm = min(kGroupM, num_m - first);
+        const int local = t - g * per_group;
+        mb = first + local % gm;
+        nb = local / gm;
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer (both CTAs)
+        if (lane == 0) {
+            const uint32_t full_leader = mapa_shared(smem_u32(full), 0);
+            int stage = 0;
+            uint32_t phase = 0, issued = 0, issued_phase = 0;
+            bool ok = true;
+            for (int t = pair; t < total && ok; t += npairs) {
+                int mb, nb;
+                tile_of(t, mb, nb);
+                const int a_row = mb * kBM + static_cast<int>(rank) * kHalf;
+                const int b_row = nb * kBN + static_cast<int>(rank) * kHalf;
+                for (int kb = 0; kb < k_steps; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
+                    if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes);
+                    const uint32_t bar = full_leader + stage * 8;
+                    tma_load_2d_pair_bar(sA + stage * kABytes, &tmA, bar, kb * kBK, a_row);
+                    tma_load_2d_pair_bar(sB + stage * kBBytes, &tmB, bar, kb * kBK, b_row);
+                    issued |= 1u << stage;
+                    issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                }
+            }
+            for (int i = 0; i < kStages && ok; ++i) {   // every stage released by the MMAs
+                if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) ok = false;
+                if (++stage == kStages) { stage = 0; phase ^= 1u; }
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                atomicOr(p.status, kDevTimeout);
+                // The leader's full barriers count both CTAs' bytes: waiting on
+                // them lets every copy of the pair in flight land.
+                if (rank == 0)
+                    for (int s = 0; s < kStages; ++s)
+                        if ((issued >> s) & 1u) mbar_wait(&full[s], (issued_phase >> s) & 1u, nullptr);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer (leader only)
+        if (lane == 0 && rank == 0) {
+            int stage = 0, it = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int t = pair; t < total && ok; t += npairs, ++it) {
+                const int acc = it & 1;
+                const uint32_t acc_phase = (it >> 1) & 1;
+                if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kBN);
+                for (int kb = 0; kb < k_steps; ++kb) {
+                    if (!mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(sA + stage * kABytes);
+                    const uint32_t b0 = smem_u32(sB + stage * kBBytes);
+#pragma unroll
+                    for (int k = 0; k < kBK / kMmaK; ++k)
+                        mma_bf16_pair(d, sdesc_k_sw128(a0 + k * kMmaK * 2), sdesc_k_sw128(b0 + k * kMmaK * 2), kIdesc,
+                                      (kb | k) != 0);
+                    tc_commit_pair(&empty[stage], 0x3);
+                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                tc_commit_pair(&tfull[acc], 0x3);
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                atomicOr(p.status, kDevTimeout);
+                tc_commit_pair(drain, 0x1);
+                mbar_wait(drain, 0, nullptr);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ epilogue (both CTAs)
+        const int q = warp & 3;
+        const int r_in_tile = static_cast<int>(rank) * kHalf + q * 32 + lane;
+        const uint32_t tempty_leader = mapa_shared(smem_u32(tempty), 0);
+        int it = 0;
+        for (int t = pair; t < total; t += npairs, ++it) {
+            const int acc = it & 1;
+            const uint32_t acc_phase = (it >> 1) & 1;
+            int mb, nb;
+            tile_of(t, mb, nb);
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait(&tfull[acc], acc_phase, abort_flag) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0) {
+                    *abort_flag = 1;
+                    atomicOr(p.status, kDevTimeout);
+                }
+                break;
+            }
+            tc_fence_after();
+            const int64_t row = static_cast<int64_t>(mb) * kBM + r_in_tile;
+            const int n0 = nb * kBN;
+            const bool valid = row < p.M;
+            uint8_t *yrow = p.Y + (row * p.ldy + n0) * 2;
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
+#pragma unroll 1
+            for (int c = 0; c < kBN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(taddr + c * 32, r);
+                tmem_wait_ld();
+                if (valid) {
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        if (n0 + c * 32 + g * 8 < p.N)
+                            st_global_v4(yrow + (c * 32 + g * 8) * 2, pack_bf16x2(r[8 * g + 0], r[8 * g + 1]),
+                                         pack_bf16x2(r[8 * g + 2], r[8 * g + 3]),
+                                         pack_bf16x2(r[8 * g + 4], r[8 * g + 5]),
+                                         pack_bf16x2(r[8 * g + 6], r[8 * g + 7]));
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(tempty_leader + acc * 8);
+        }
+    }
+
+    tc_fence_before();
+    cluster_sync();                      // no CTA leaves while its peer may still signal it
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, kTmemCols);
+    }
+}
+
+}  // namespace
+
+void plan_gemm_bf16(int64_t M, int64_t N, int64_t K, int sms, bi_plan_t *pl) {
+    pl->op = BI_OP_GEMM_BF16;
+    pl->block_m = kBM; pl->block_n = kBN; pl->block_k = kBK;
+    pl->mma_m = kBM; pl->mma_n = kBN; pl->mma_k = kMmaK;
+    pl->k_steps = static_cast<int32_t>((K + kBK - 1) / kBK);
+    pl->split_k = 1;
+    pl->stages = kStages;
+    pl->threads = kThreads;
+    pl->smem_bytes = kSmem;
+    pl->tiles_m = (M + kBM - 1) / kBM;
+    pl->tiles_n = (N + kBN - 1) / kBN;
+    const int64_t tiles = pl->tiles_m * pl->tiles_n;
+    const int64_t pairs = sms / 2;
+    pl->grid = static_cast<int32_t>(2 * (tiles < pairs ? tiles : pairs));
+    pl->reduce_tree = 0;
+}
+
+bi_status launch_gemm_bf16(const void *X, int64_t ldx, const void *W, int64_t ldw, void *Y, int64_t ldy,
+                           int64_t M, int64_t N, int64_t K, cudaStream_t s) {
+    int dev;
+    const DeviceInfo *info;
+    bi_status st = current_device(&dev, &info);
+    if (st != BI_OK) return st;
+    CUtensorMap ta, tb;
+    st = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, K, M, ldx * 2, kBK, kHalf, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != BI_OK) return st;
+    st = make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, K, N, ldw * 2, kBK, kHalf, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != BI_OK) return st;
+    bi_plan_t pl;
+    plan_gemm_bf16(M, N, K, info->sm_count, &pl);
+    Params p{};
+    p.Y = static_cast<uint8_t *>(Y);
+    p.ldy = ldy;
+    p.M = static_cast<int32_t>(M);
+    p.N = static_cast<int32_t>(N);
+    p.K = static_cast<int32_t>(K);
+    p.status = device_status_word();
+    static unsigned long long configured = 0;
+    if (ensure_smem_attr(reinterpret_cast<const void *>(gemm_bf16_pair_kernel), kSmem, &configured) != BI_OK)
+        return BI_ERR_CUDA;
+    gemm_bf16_pair_kernel<<<pl.grid, kThreads, kSmem, s>>>(ta, tb, p);
+    return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
+}
+
+}  // namespace bi

@@ -66,6 +66,11 @@ def _load():
             lib.oracle_bf16_round.argtypes = [D]
             lib.oracle_bf16_round.restype = ctypes.c_uint16
             lib.oracle_bf16_round_array.argtypes = [I64, P, P]
+            lib.oracle_quantize_nvfp4.argtypes = [I64, I64, P, ctypes.c_float, P, P]
+            lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+            lib.oracle_e4m3_encode.restype = ctypes.c_uint
+            lib.oracle_e2m1_encode.argtypes = [ctypes.c_float]
+            lib.oracle_e2m1_encode.restype = ctypes.c_uint
             lib.oracle_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -139,6 +144,28 @@ def rmsnorm(x, w, eps: float, residual=None):
         _load().oracle_rmsnorm(M, H, _p(x), rp, _p(w), float(eps), _p(y),
                                _p(h) if h is not None else None)
     return y, h
+
+
+def quantize_nvfp4(X: np.ndarray, gs: float):
+    """NVFP4 quantisation of bf16 rows X [M,K] with global scale gs (fp32 arithmetic).
+
+    Returns (packed e2m1 codes u8 [M, K/2], e4m3 block scales u8 [M, K/16] row-major)."""
+    X = _c(X, np.uint16)
+    M, K = X.shape
+    assert K % 16 == 0
+    Q = np.zeros((M, K // 2), dtype=np.uint8)
+    S = np.zeros((M, K // 16), dtype=np.uint8)
+    if M:
+        _load().oracle_quantize_nvfp4(M, K, _p(X), float(np.float32(gs)), _p(Q), _p(S))
+    return Q, S
+
+
+def e4m3_encode(v: float) -> int:
+    return int(_load().oracle_e4m3_encode(float(v)))
+
+
+def e2m1_encode(v: float) -> int:
+    return int(_load().oracle_e2m1_encode(float(v)))
 
 
 def e2m1_value(code: int) -> float:

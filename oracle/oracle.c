@@ -167,6 +167,80 @@ void oracle_gemm_nvfp4(int64_t M, int64_t N, int64_t K,
     }
 }
 
+/* ---- NVFP4 quantisation of activations (scaled_fp4_quant in the page's test).
+ * Per row r and 16-element block b, with the per-tensor global scale gs:
+ *   amax = max |x| over the block                          (exact)
+ *   s    = e4m3_rne_satfinite( (amax / 6) * gs )           (fp32 ops, then encode)
+ *   q_k  = e2m1_rne( clamp( (x_k * gs) / value(s), -6, 6 ) )   (fp32 ops), q = 0 if value(s) == 0
+ * Floating point decides integer codes here, so the arithmetic is binary32
+ * (the precision the kernel uses), one rounding per operation (-ffp-contract=off).
+ * Encoders are written from the format definitions: round to the nearest
+ * representable value by binade (quantum 2^(e - mantissa bits)), ties to even. */
+
+/* Round half to even of a non-negative float that is an exact multiple of 1/2. */
+static float rne_halves(float v) { return nearbyintf(v); }
+
+static unsigned e4m3_encode_satfinite(float v) /* v >= 0 */
+{
+    if (!(v < 448.0f)) return 0x7Eu;                  /* saturate (also +inf) */
+    if (v < ldexpf(1.0f, -6)) {                       /* subnormal binade: quantum 2^-9 */
+        float m = rne_halves(v * 512.0f);             /* exact scaling by a power of two */
+        return (unsigned)m;                           /* m == 8 is 2^-6, code 0x08 */
+    }
+    int e;
+    (void)frexpf(v, &e);                              /* v = f * 2^e, f in [0.5, 1) */
+    e -= 1;                                           /* v in [2^e, 2^(e+1)) */
+    float m = rne_halves(ldexpf(v, 3 - e));           /* significand in [8, 16] */
+    if (m == 16.0f) { m = 8.0f; e += 1; }
+    if (e > 8) return 0x7Eu;
+    return ((unsigned)(e + 7) << 3) | ((unsigned)m - 8u);
+}
+
+static unsigned e2m1_encode_mag(float a) /* 0 <= a <= 6 */
+{
+    if (a < 2.0f) return (unsigned)rne_halves(a * 2.0f);            /* quantum 0.5: codes 0..4 */
+    if (a < 4.0f) return 2u + (unsigned)rne_halves(a);              /* quantum 1: 2,3,4 -> codes 4,5,6 */
+    return 4u + (unsigned)rne_halves(a * 0.5f);                     /* quantum 2: 2,3 -> codes 6,7 */
+}
+
+unsigned oracle_e4m3_encode(float v) { return e4m3_encode_satfinite(v); }
+unsigned oracle_e2m1_encode(float v)
+{
+    unsigned c = e2m1_encode_mag(fminf(fabsf(v), 6.0f));
+    return (v < 0.0f && c != 0u) ? (c | 8u) : c;
+}
+
+/* X: bf16 [M][K]; Q: packed e2m1 [M][K/2] (low nibble = even k); S: e4m3 [M][K/16]. */
+void oracle_quantize_nvfp4(int64_t M, int64_t K, const uint16_t *X, float gs, uint8_t *Q, uint8_t *S)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < M; ++i) {
+        for (int64_t b = 0; b < K / 16; ++b) {
+            float amax = 0.0f;
+            for (int k = 0; k < 16; ++k) {
+                float a = fabsf((float)bf16_to_double(X[i * K + b * 16 + k]));
+                if (a > amax) amax = a;
+            }
+            volatile float t = amax / 6.0f;               /* keep the two roundings separate */
+            unsigned s = e4m3_encode_satfinite(t * gs);
+            float sv = (float)e4m3_to_double(s);
+            S[i * (K / 16) + b] = (uint8_t)s;
+            for (int k = 0; k < 16; k += 2) {
+                unsigned c[2];
+                for (int h = 0; h < 2; ++h) {
+                    float x = (float)bf16_to_double(X[i * K + b * 16 + k + h]);
+                    if (sv == 0.0f) { c[h] = 0u; continue; }
+                    volatile float xs = x * gs;
+                    float y = xs / sv;
+                    y = fminf(fmaxf(y, -6.0f), 6.0f);
+                    c[h] = oracle_e2m1_encode(y);
+                }
+                Q[i * (K / 2) + (b * 16 + k) / 2] = (uint8_t)(c[0] | (c[1] << 4));
+            }
+        }
+    }
+}
+
 /* RMSNorm with optional residual add, per row i:
  *   h = residual ? bf16(x + residual) : x         (the stored, rounded sum)
  *   y = h / sqrt( (1/H) sum_k h_k^2 + eps ) * w

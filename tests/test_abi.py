@@ -61,8 +61,8 @@ def test_gemm_plan_independent_of_M(lib, N, K):
     for M in [1, 2, 7, 64, 127, 128, 129, 513, 4096, 8192, 65536]:
         p = _plan(lib, lib.OP_GEMM_BF16, M, N, K)
         assert {k: p[k] for k in keys} == {k: base[k] for k in keys}
-        assert p["tiles_m"] == -(-M // 128) and p["split_k"] == 1
-        assert 1 <= p["grid"] <= 152
+        assert p["tiles_m"] == -(-M // p["block_m"]) and p["split_k"] == 1
+        assert 2 <= p["grid"] <= 152 and p["grid"] % 2 == 0      # CTA pairs
     assert base["k_steps"] == -(-K // 64)
 
 

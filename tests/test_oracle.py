@@ -210,6 +210,80 @@ def test_nvfp4_unit_scales_integer_case():
     assert np.array_equal(Y, val(codes_a) @ val(codes_b).T)
 
 
+# ----------------------------------------------------------- quantiser
+
+def test_quantize_golden_blocks():
+    n = 0
+    with open(os.path.join(GOLDEN, "nvfp4_quant_cases.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if not line:
+                continue
+            case, gs, xs, sc, qb = line.split()
+            x = np.array([float(v) for v in xs.split(",")], dtype=np.float32)[None]
+            Xb = syn.to_bf16_bits(x)
+            assert np.array_equal(syn.bf16_bits_to_f32(Xb), x), "fixture values must be exact in bf16"
+            Q, S = oracle.quantize_nvfp4(Xb, float(gs))
+            assert int(S[0, 0]) == int(sc, 16), (case, hex(int(S[0, 0])))
+            assert [int(b) for b in Q[0]] == [int(v, 16) for v in qb.split(",")], (case, [hex(b) for b in Q[0]])
+            n += 1
+    assert n == 5
+
+
+def test_e4m3_encoder_roundtrip_ties_saturation():
+    for c in range(0x7F):
+        v = oracle.e4m3_value(c)
+        assert oracle.e4m3_encode(v) == c
+        if c < 0x7E:
+            mid = (Fraction(v) + Fraction(oracle.e4m3_value(c + 1))) / 2
+            assert oracle.e4m3_encode(float(mid)) == (c if c % 2 == 0 else c + 1)
+    for v in (448.0, 460.0, 1e6, float("inf")):
+        assert oracle.e4m3_encode(v) == 0x7E
+
+
+def test_e4m3_encoder_matches_torch_in_range():
+    torch = pytest.importorskip("torch")
+    g = syn.rng(31, 0)
+    v = np.exp(g.uniform(np.log(2.0 ** -10), np.log(440.0), 20000)).astype(np.float32)
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_encode(float(x)) for x in v], dtype=np.uint8)
+    assert np.array_equal(got, ref)
+
+
+def test_e2m1_encoder_ties_and_clamp():
+    cases = {0.0: 0, 0.24: 0, 0.25: 0, 0.26: 1, 0.75: 2, 1.25: 2, 1.75: 4, 2.5: 4, 3.5: 6,
+             5.0: 6, 5.01: 7, 6.0: 7, 9.0: 7, -0.25: 0, -0.3: 9, -5.0: 14}
+    for v, c in cases.items():
+        assert oracle.e2m1_encode(v) == c, v
+
+
+def test_quantize_agrees_with_generator_quantiser():
+    """Two independent implementations of the same reading (this oracle and
+    the input generator) agree code for code on random data."""
+    x = syn.bf16_bits_to_f32(syn.to_bf16_bits(syn.normal_rows(4, 0, 64, 512)))
+    x[3] *= 40.0
+    x[5, :16] = 0.0
+    x = syn.bf16_bits_to_f32(syn.to_bf16_bits(x))
+    gs = syn.nvfp4_global_scale(x)
+    Q, S = oracle.quantize_nvfp4(syn.to_bf16_bits(x), gs)
+    Qg, Sg = syn.nvfp4_quantize(x, gs)
+    assert np.array_equal(S, Sg) and np.array_equal(Q, Qg)
+
+
+def test_quantize_dequant_error_bound():
+    x = syn.bf16_bits_to_f32(syn.to_bf16_bits(syn.normal_rows(5, 0, 16, 256)))
+    gs = syn.nvfp4_global_scale(x)
+    Q, S = oracle.quantize_nvfp4(syn.to_bf16_bits(x), gs)
+    for i in range(16):
+        for k in range(256):
+            code = (int(Q[i, k // 2]) >> 4) if k % 2 else (int(Q[i, k // 2]) & 15)
+            s = oracle.e4m3_value(int(S[i, k // 16]))
+            deq = oracle.e2m1_value(code) * s / float(gs)
+            amax = np.abs(x[i, (k // 16) * 16:(k // 16) * 16 + 16]).max()
+            # half the largest e2m1 step (1.0 of 6 units) times the block scale, plus scale rounding
+            assert abs(deq - x[i, k]) <= amax / 6 * 1.07 + 1e-7
+
+
 # ----------------------------------------------------------------- RMSNorm
 
 def test_rmsnorm_golden_cases():
