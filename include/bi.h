@@ -126,6 +126,26 @@ BI_API bi_status bi_gemm_nvfp4(const uint8_t *A, const uint8_t *A_sf, const uint
                         int64_t M, int64_t N, int64_t K, bi_stream stream);
 
 /*
+ * bi_quantize_nvfp4 -- NVFP4 quantisation of bf16 activations for bi_gemm_nvfp4.
+ *
+ * The activation quantiser of vLLM PR #39912's test (scaled_fp4_quant with
+ * the tensor's global scale). Per row and 16-element block, with gs = global_scale:
+ *   s = e4m3( (amax / 6) * gs )       fp32 arithmetic, round to nearest even, saturating at 448
+ *   q = e2m1( (x * gs) / value(s) )   round to nearest even, saturating at 6; q = 0 where value(s) = 0
+ * A zero magnitude is stored as code 0 (never code 8). Row-local: a row's
+ * codes and scales do not depend on the other rows (the global scale is an
+ * input, computed once for the whole tensor as in the page's test).
+ *
+ *   X     bf16 [M][ldx]   activations (first K columns used)
+ *   Q     u8   [M][K/2]   packed e2m1 codes, element k in byte k/2, low nibble for even k
+ *   Q_sf  u8              e4m3 scales in the interleaved 128x4 layout of bi_gemm_nvfp4;
+ *                         the buffer holds ceil(M/128)*128 rows, rows >= M are not written
+ * Requirements: K % 64 == 0, K > 0; ldx % 8 == 0, ldx >= K; global_scale finite and > 0.
+ */
+BI_API bi_status bi_quantize_nvfp4(const void *X, int64_t ldx, float global_scale, uint8_t *Q, uint8_t *Q_sf,
+                                   int64_t M, int64_t K, bi_stream stream);
+
+/*
  * bi_rmsnorm -- RMSNorm with optional residual add and a fixed reduction tree.
  *
  * The RMSNorm that vLLM fuses with the tensor-parallel all-reduce (vLLM PR
@@ -148,7 +168,8 @@ BI_API bi_status bi_rmsnorm(const void *x, void *residual, const void *w, void *
                      int64_t M, int64_t H, float eps, bi_stream stream);
 
 /* Operation ids for bi_plan. */
-enum { BI_OP_GEMM_BF16 = 0, BI_OP_GROUPED_GEMM_BF16 = 1, BI_OP_GEMM_NVFP4 = 2, BI_OP_RMSNORM = 3 };
+enum { BI_OP_GEMM_BF16 = 0, BI_OP_GROUPED_GEMM_BF16 = 1, BI_OP_GEMM_NVFP4 = 2, BI_OP_RMSNORM = 3,
+       BI_OP_QUANTIZE_NVFP4 = 4 };
 
 /*
  * bi_plan -- the launch plan a call with these sizes uses (host only, no GPU needed).

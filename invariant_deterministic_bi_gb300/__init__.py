@@ -7,7 +7,7 @@ calls the matching ``extern "C"`` entry point of ``libbi.so`` (declared in
 is no CPU or PyTorch fallback. If the library is missing this module raises.
 
 Names follow the C ABI: ``gemm_bf16``, ``grouped_gemm_bf16``, ``gemm_nvfp4``,
-``rmsnorm``, ``plan``, ``device_status``, ``check_wait_timeout``.
+``quantize_nvfp4``, ``rmsnorm``, ``plan``, ``device_status``, ``check_wait_timeout``.
 """
 from __future__ import annotations
 
@@ -19,7 +19,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libbi.so")
 
 BI_OK, BI_ERR_INVALID_ARG, BI_ERR_UNSUPPORTED, BI_ERR_MISALIGNED, BI_ERR_ARCH, BI_ERR_CUDA, BI_ERR_TIMEOUT = range(7)
-OP_GEMM_BF16, OP_GROUPED_GEMM_BF16, OP_GEMM_NVFP4, OP_RMSNORM = range(4)
+OP_GEMM_BF16, OP_GROUPED_GEMM_BF16, OP_GEMM_NVFP4, OP_RMSNORM, OP_QUANTIZE_NVFP4 = range(5)
 
 _lock = threading.Lock()
 _lib = None
@@ -61,6 +61,7 @@ def load() -> ctypes.CDLL:
             "bi_grouped_gemm_bf16": [P, P, P, P, I32, I64, I64, I64, P],
             "bi_gemm_nvfp4": [P, P, P, P, F, P, I64, I64, I64, P],
             "bi_rmsnorm": [P, P, P, P, I64, I64, F, P],
+            "bi_quantize_nvfp4": [P, I64, F, P, P, I64, I64, P],
             "bi_plan": [I32, I64, I64, I64, I32, ctypes.POINTER(Plan)],
             "bi_device_status": [P],
             "bi_check_wait_timeout": [ctypes.c_uint32, P],
@@ -176,6 +177,28 @@ def gemm_nvfp4(A, A_sf, B, B_sf, alpha: float, Y=None, stream=None):
     _check(load().bi_gemm_nvfp4(_ptr(A), _ptr(A_sf), _ptr(B), _ptr(B_sf), float(alpha), _ptr(Y), M, N, K,
                                 _stream(stream)), "bi_gemm_nvfp4")
     return Y
+
+
+def quantize_nvfp4(X, global_scale: float, Q=None, Q_sf=None, stream=None):
+    """NVFP4-quantise bf16 rows X [M, K] with a per-tensor global scale.
+
+    Returns (Q uint8 [M, K/2] packed e2m1, Q_sf uint8 interleaved 128x4 scales
+    for ceil(M/128)*128 rows), ready for gemm_nvfp4."""
+    import torch
+    _dev(X, torch.bfloat16, "X")
+    if X.dim() != 2 or X.stride(1) != 1:
+        raise ValueError("X must be [M, K] with unit column stride")
+    M, K = X.shape
+    if Q is None:
+        Q = torch.empty((M, K // 2), dtype=torch.uint8, device=X.device)
+    if Q_sf is None:
+        Q_sf = torch.zeros(-(-M // 128) * 128 * (K // 16), dtype=torch.uint8, device=X.device)
+    _dev(Q, torch.uint8, "Q"), _dev(Q_sf, torch.uint8, "Q_sf")
+    if Q.shape != (M, K // 2) or not Q.is_contiguous() or Q_sf.numel() < -(-M // 128) * 128 * (K // 16):
+        raise ValueError("output buffers have the wrong size")
+    _check(load().bi_quantize_nvfp4(_ptr(X), X.stride(0), float(global_scale), _ptr(Q), _ptr(Q_sf), M, K,
+                                    _stream(stream)), "bi_quantize_nvfp4")
+    return Q, Q_sf
 
 
 def rmsnorm(x, w, eps: float, residual=None, out=None, stream=None):

@@ -150,6 +150,17 @@ bi_status bi_gemm_nvfp4(const uint8_t *A, const uint8_t *A_sf, const uint8_t *B,
     return launch_gemm_nvfp4(A, A_sf, B, B_sf, alpha, Y, M, N, K, as_stream(stream));
 }
 
+bi_status bi_quantize_nvfp4(const void *X, int64_t ldx, float global_scale, uint8_t *Q, uint8_t *Q_sf, int64_t M,
+                            int64_t K, bi_stream stream) {
+    if (M < 0 || K <= 0 || M >= kI32Max || K >= kI32Max || !(global_scale > 0.0f) || !(global_scale < 3.5e38f))
+        return BI_ERR_INVALID_ARG;
+    if (M == 0) return BI_OK;
+    if (!X || !Q || !Q_sf || ldx < K) return BI_ERR_INVALID_ARG;
+    if (K % 64 != 0) return BI_ERR_UNSUPPORTED;
+    if (ldx % 8 != 0 || !aligned16(X) || !aligned16(Q) || !aligned16(Q_sf)) return BI_ERR_MISALIGNED;
+    return launch_quantize_nvfp4(X, ldx, global_scale, Q, Q_sf, M, K, as_stream(stream));
+}
+
 bi_status bi_rmsnorm(const void *x, void *residual, const void *w, void *out, int64_t M, int64_t H, float eps,
                      bi_stream stream) {
     if (M < 0 || H < 8 || H > 65536 || !(eps >= 0.0f)) return BI_ERR_INVALID_ARG;
@@ -180,6 +191,17 @@ bi_status bi_plan(int32_t op, int64_t M, int64_t N, int64_t K, int32_t num_sms, 
         case BI_OP_GEMM_BF16: plan_gemm_bf16(M, N, K, sms, out); return BI_OK;
         case BI_OP_GROUPED_GEMM_BF16: plan_grouped_gemm_bf16(M, N, K, sms, out); return BI_OK;
         case BI_OP_GEMM_NVFP4: plan_gemm_nvfp4(M, N, K, sms, out); return BI_OK;
+        case BI_OP_QUANTIZE_NVFP4:
+            out->op = BI_OP_QUANTIZE_NVFP4;
+            out->block_m = 1; out->block_n = 64; out->block_k = 16;   /* 64 elements (4 scale blocks) per thread */
+            out->k_steps = static_cast<int32_t>(K / 64);
+            out->split_k = 1; out->stages = 1; out->threads = 256;
+            out->tiles_m = M; out->tiles_n = K / 64;
+            {
+                const int64_t g = (M * (K / 64) + 255) / 256, cap = static_cast<int64_t>(sms) * 8;
+                out->grid = static_cast<int32_t>(g < cap ? g : cap);
+            }
+            return BI_OK;   /* N unused, K = columns */
         case BI_OP_RMSNORM: plan_rmsnorm(M, N, out); return BI_OK;   /* N carries H */
         default: return BI_ERR_INVALID_ARG;
     }

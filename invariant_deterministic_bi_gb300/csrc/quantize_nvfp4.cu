@@ -1,0 +1,127 @@
+// quantize_nvfp4.cu -- NVFP4 quantisation of bf16 activations (row-local, batch-invariant).
+//
+// The activation quantiser that feeds the NVFP4 linear layer in vLLM PR #39912
+// ("NVFP4 CUTLASS batch invariant mode", test code: scaled_fp4_quant with the
+// tensor's global scale). Per row and 16-element block, with global scale gs:
+//   s = e4m3( (amax / 6) * gs )        round to nearest even, saturating at 448
+//   q = e2m1( (x * gs) / value(s) )    round to nearest even, saturating at 6; q = 0 if value(s) = 0
+// Every output depends only on its own row and gs, so a row quantises to the
+// same bytes whatever the batch. Zero magnitudes are stored as code 0 (never
+// the negative-zero code 8).
+//
+// One thread per 64 elements (four blocks): 128-byte coalesced loads, 32 bytes
+// of packed codes and one 32-bit word of four scales, written straight into
+// the interleaved 128x4 scale layout bi_gemm_nvfp4 reads.
+#include <cuda_bf16.h>
+
+#include "bi_internal.h"
+#include "bi_ptx.cuh"
+
+namespace bi {
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// fp32 -> e4m3 (satfinite, round to nearest even), one byte.
+__device__ __forceinline__ uint32_t to_e4m3(float v) {
+    uint16_t out;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(out) : "f"(0.0f), "f"(v));
+    return out & 0xFFu;
+}
+
+// e4m3 byte -> fp32 (exact, through f16).
+__device__ __forceinline__ float from_e4m3(uint32_t code) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(code)));
+    float f;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.f32.f16 %0, lo;\n\t}" : "=f"(f) : "r"(h2));
+    return f;
+}
+
+// Eight fp32 -> eight e2m1 nibbles (element 2i in the low nibble of byte i).
+__device__ __forceinline__ uint32_t to_e2m1x8(const float (&y)[8]) {
+    uint32_t out;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+        : "=r"(out)
+        : "f"(y[0]), "f"(y[1]), "f"(y[2]), "f"(y[3]), "f"(y[4]), "f"(y[5]), "f"(y[6]), "f"(y[7]));
+    // clear the sign of every nibble whose magnitude is zero
+    const uint32_t mag = out & 0x77777777u;
+    const uint32_t nz = (mag | (mag >> 1) | (mag >> 2)) & 0x11111111u;
+    return mag | (out & (nz << 3));
+}
+
+__global__ void __launch_bounds__(kThreads)
+quantize_nvfp4_kernel(const uint4 *__restrict__ X, int64_t ldx_vec, uint8_t *__restrict__ Q, uint8_t *__restrict__ SF,
+                      int64_t M, int K, float gs) {
+    const int groups = K / 64;                       // 64-element groups per row = scale words per row
+    const int64_t total = M * groups;
+    for (int64_t gid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; gid < total;
+         gid += static_cast<int64_t>(gridDim.x) * kThreads) {
+        const int64_t r = gid / groups;
+        const int g = static_cast<int>(gid - r * groups);
+        const uint4 *src = X + r * ldx_vec + g * 8;
+        uint4 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = __ldcs(src + i);
+        uint32_t codes[8];
+        uint32_t scale_word = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            float x[16];
+            const uint32_t w[8] = {v[2 * b].x, v[2 * b].y, v[2 * b].z, v[2 * b].w,
+                                   v[2 * b + 1].x, v[2 * b + 1].y, v[2 * b + 1].z, v[2 * b + 1].w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                x[2 * i] = bf_lo(w[i]);
+                x[2 * i + 1] = bf_hi(w[i]);
+            }
+            float amax = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+            const uint32_t s = to_e4m3(__fmul_rn(__fdiv_rn(amax, 6.0f), gs));
+            const float sv = from_e4m3(s);
+            scale_word |= s << (8 * b);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                float y[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    y[i] = sv == 0.0f ? 0.0f : __fdiv_rn(__fmul_rn(x[8 * h + i], gs), sv);
+                codes[2 * b + h] = to_e2m1x8(y);
+            }
+        }
+        uint4 *dst = reinterpret_cast<uint4 *>(Q + r * (K / 2) + g * 32);
+        __stcs(dst, make_uint4(codes[0], codes[1], codes[2], codes[3]));
+        __stcs(dst + 1, make_uint4(codes[4], codes[5], codes[6], codes[7]));
+        const int64_t atom = (r / 128) * groups + g;
+        const int64_t off = atom * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4;
+        *reinterpret_cast<uint32_t *>(SF + off) = scale_word;
+    }
+}
+
+}  // namespace
+
+bi_status launch_quantize_nvfp4(const void *X, int64_t ldx, float gs, uint8_t *Q, uint8_t *Q_sf, int64_t M, int64_t K,
+                                cudaStream_t s) {
+    int dev;
+    const DeviceInfo *info;
+    bi_status st = current_device(&dev, &info);
+    if (st != BI_OK) return st;
+    const int64_t threads = M * (K / 64);
+    int64_t grid = (threads + kThreads - 1) / kThreads;
+    const int64_t cap = static_cast<int64_t>(info->sm_count) * 8;
+    if (grid > cap) grid = cap;
+    quantize_nvfp4_kernel<<<static_cast<unsigned>(grid), kThreads, 0, s>>>(
+        static_cast<const uint4 *>(X), ldx / 8, Q, Q_sf, M, static_cast<int>(K), gs);
+    return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
+}
+
+}  // namespace bi

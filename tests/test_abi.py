@@ -26,7 +26,7 @@ def declared_functions():
 
 def test_header_declares_the_calls():
     names = declared_functions()
-    for n in ["bi_gemm_bf16", "bi_grouped_gemm_bf16", "bi_gemm_nvfp4", "bi_rmsnorm", "bi_plan",
+    for n in ["bi_gemm_bf16", "bi_grouped_gemm_bf16", "bi_gemm_nvfp4", "bi_rmsnorm", "bi_plan", "bi_quantize_nvfp4",
               "bi_device_status", "bi_status_string", "bi_version", "bi_check_wait_timeout"]:
         assert n in names
 
@@ -119,5 +119,10 @@ def test_other_calls_reject_bad_arguments(lib):
     assert so.bi_rmsnorm(FAKE, None, FAKE, FAKE, 4, 4100, f(1e-6), None) == 2              # H % 8
     assert so.bi_rmsnorm(FAKE, None, FAKE, FAKE, 4, 4096, f(-1.0), None) == 1              # eps < 0
     assert so.bi_rmsnorm(FAKE, FAKE + 8, FAKE, FAKE, 4, 4096, f(1e-6), None) == 3          # residual align
+    assert so.bi_quantize_nvfp4(FAKE, 128, f(1.0), FAKE, FAKE, 4, 96, None) == 2           # K % 64
+    assert so.bi_quantize_nvfp4(FAKE, 128, f(0.0), FAKE, FAKE, 4, 128, None) == 1          # scale <= 0
+    assert so.bi_quantize_nvfp4(FAKE, 100, f(1.0), FAKE, FAKE, 4, 128, None) == 1          # ldx < K
+    assert so.bi_quantize_nvfp4(FAKE, 136, f(1.0), FAKE + 8, FAKE, 4, 128, None) == 3      # Q align
+    assert so.bi_quantize_nvfp4(FAKE, 128, f(1.0), FAKE, FAKE, 0, 128, None) == 0          # empty
     assert so.bi_check_wait_timeout(0, None) == 1
     assert so.bi_plan(99, 1, 1, 1, 152, ctypes.byref(lib.Plan())) == 1
