@@ -447,6 +447,37 @@ def nvfp4_sweep(bi, peaks):
     return {"fp4_peak_tflops": round(fp4_peak, 1), "fp4_peak_source": peak_note, "rows": rows}
 
 
+QUANT_M = [1, 16, 256, 4096, 16384]
+
+
+def quant_sweep(bi, peaks):
+    """bi_quantize_nvfp4 at K=4096: HBM GB/s (reads 2 B, writes 0.5 + 1/16 B per element)."""
+    import torch
+    import bi_synth as syn
+    K = NVFP4_K
+    rows = []
+    for M in QUANT_M:
+        nsets = max(1, min(4, (512 << 20) // (2 * M * K)))
+        sets = []
+        for j in range(nsets):
+            X = bf16_dev(syn.to_bf16_bits(syn.normal_rows(j, syn.TID_FP4_A, M, K)))
+            Q = torch.empty((M, K // 2), dtype=torch.uint8, device="cuda")
+            S = torch.zeros(-(-M // 128) * 128 * (K // 16), dtype=torch.uint8, device="cuda")
+            sets.append((X, Q, S))
+        sel = rotate(sets)
+
+        def call():
+            X, Q, S = sel()
+            bi.quantize_nvfp4(X, 1.0, Q=Q, Q_sf=S)
+        t = time_fn(call, 200 if M <= 256 else 30)
+        nbytes = M * K * (2 + 0.5 + 1 / 16)
+        gbs = nbytes / (t * 1e-3) / 1e9
+        rows.append({"M": M, "K": K, "us": round(t * 1e3, 2), "gbs": round(gbs, 0),
+                     "frac_hbm_measured": round(gbs / peaks["hbm_gbs"], 3)})
+        del sets
+    return rows
+
+
 def cpu_baseline(rows: int):
     """The fp64 oracle on a bounded sample of the step: `rows` rows of every
     GEMM of the step and of both RMSNorms, on the host's cores."""
@@ -553,6 +584,7 @@ def run_ours(args, dist):
         breakdown["rmsnorm"] = rmsnorm_sweep(bi, peaks)
         breakdown["grouped_gemm_bf16_moe"] = moe_sweep(bi, peaks)
         breakdown["gemm_nvfp4"] = nvfp4_sweep(bi, peaks)
+        breakdown["quantize_nvfp4"] = quant_sweep(bi, peaks)
         if bi.device_status() != bi.BI_OK:
             raise RuntimeError("device status after breakdown")
 
@@ -629,6 +661,12 @@ def profile_case(spec: str, reps: int):
         B, SB = torch.from_numpy(d["B"]).cuda(), torch.from_numpy(d["SB_il"]).cuda()
         Y = torch.empty((M, NVFP4_N), dtype=torch.bfloat16, device="cuda")
         fn = lambda: bi.gemm_nvfp4(A, SA, B, SB, float(d["alpha"]), Y=Y)
+    elif kind == "quant":
+        M = int(rest[0])
+        X = bf16_dev(syn.to_bf16_bits(syn.normal_rows(0, syn.TID_FP4_A, M, NVFP4_K)))
+        Q = torch.empty((M, NVFP4_K // 2), dtype=torch.uint8, device="cuda")
+        S = torch.zeros(-(-M // 128) * 128 * (NVFP4_K // 16), dtype=torch.uint8, device="cuda")
+        fn = lambda: bi.quantize_nvfp4(X, 1.0, Q=Q, Q_sf=S)
     elif kind == "grouped":
         X, W, off, _ = moe_inputs(rest[0], int(rest[1]))
         Y = torch.empty((X.shape[0], W.shape[1]), dtype=torch.bfloat16, device="cuda")
