@@ -67,6 +67,10 @@ def _load():
             lib.oracle_bf16_round.restype = ctypes.c_uint16
             lib.oracle_bf16_round_array.argtypes = [I64, P, P]
             lib.oracle_quantize_nvfp4.argtypes = [I64, I64, P, ctypes.c_float, P, P]
+            lib.oracle_moe_topk_softmax.argtypes = [I64, ctypes.c_int32, ctypes.c_int32, P, ctypes.c_int, P, P]
+            lib.oracle_moe_align.argtypes = [I64, ctypes.c_int32, ctypes.c_int32, P, P, P, P]
+            lib.oracle_silu_mul.argtypes = [I64, I64, P, P]
+            lib.oracle_moe_combine.argtypes = [I64, ctypes.c_int32, I64, P, P, P, P]
             lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
             lib.oracle_e4m3_encode.restype = ctypes.c_uint
             lib.oracle_e2m1_encode.argtypes = [ctypes.c_float]
@@ -158,6 +162,52 @@ def quantize_nvfp4(X: np.ndarray, gs: float):
     if M:
         _load().oracle_quantize_nvfp4(M, K, _p(X), float(np.float32(gs)), _p(Q), _p(S))
     return Q, S
+
+
+def moe_topk_softmax(logits: np.ndarray, k: int, renormalize: bool = True):
+    """Top-k experts per token (ties to the lower index) and their softmax
+    weights (fp64), optionally renormalised over the k chosen."""
+    logits = _c(logits, np.float32)
+    T, E = logits.shape
+    assert 1 <= k <= E <= 4096
+    ids = np.zeros((T, k), dtype=np.int32)
+    w = np.zeros((T, k), dtype=np.float64)
+    if T:
+        _load().oracle_moe_topk_softmax(T, E, k, _p(logits), int(bool(renormalize)), _p(ids), _p(w))
+    return ids, w
+
+
+def moe_align(ids: np.ndarray, E: int):
+    """Group (token, rank) pairs by expert, stably by token: (offsets [E+1],
+    row_token [T*k], pos [T, k])."""
+    ids = _c(ids, np.int32)
+    T, k = ids.shape
+    off = np.zeros(E + 1, dtype=np.int32)
+    row_token = np.zeros(T * k, dtype=np.int32)
+    pos = np.zeros((T, k), dtype=np.int32)
+    _load().oracle_moe_align(T, k, E, _p(ids), _p(off), _p(row_token), _p(pos))
+    return off, row_token, pos
+
+
+def silu_mul(gu: np.ndarray) -> np.ndarray:
+    """act = silu(gate) * up for bf16 rows [gate | up] (fp64)."""
+    gu = _c(gu, np.uint16)
+    R, I2 = gu.shape
+    act = np.zeros((R, I2 // 2), dtype=np.float64)
+    if R:
+        _load().oracle_silu_mul(R, I2 // 2, _p(gu), _p(act))
+    return act
+
+
+def moe_combine(Y: np.ndarray, pos: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """out[t] = sum_i w[t,i] * Y[pos[t,i]] in rank order (fp64)."""
+    Y, pos, w = _c(Y, np.uint16), _c(pos, np.int32), _c(w, np.float64)
+    T, k = pos.shape
+    H = Y.shape[1]
+    out = np.zeros((T, H), dtype=np.float64)
+    if T:
+        _load().oracle_moe_combine(T, k, H, _p(Y), _p(pos), _p(w), _p(out))
+    return out
 
 
 def e4m3_encode(v: float) -> int:

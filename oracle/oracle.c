@@ -241,6 +241,93 @@ void oracle_quantize_nvfp4(int64_t M, int64_t K, const uint16_t *X, float gs, ui
     }
 }
 
+/* ---- MoE layer surroundings (the MoE models listed as tested on the vllm-ascend
+ * "Batch Invariance" guide: Qwen3-30B-A3B, Qwen3-235B-A22B).
+ *
+ * Routing, per token t with router logits l[t][0..E-1] (fp32):
+ *   ids  = the k experts with the largest logits, larger first, ties to the
+ *          lower expert index (softmax is monotonic, so these are also the
+ *          k largest softmax probabilities);
+ *   p_e  = exp(l_e - max l) / sum_j exp(l_j - max l)   (fp64)
+ *   w_i  = p_{ids[i]}, divided by sum_i p_{ids[i]} when renormalize != 0. */
+void oracle_moe_topk_softmax(int64_t T, int32_t E, int32_t k, const float *logits, int renormalize,
+                             int32_t *ids, double *w)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        const float *l = logits + t * E;
+        double mx = -INFINITY;
+        for (int32_t e = 0; e < E; ++e)
+            if ((double)l[e] > mx) mx = (double)l[e];
+        double sum = 0.0;
+        for (int32_t e = 0; e < E; ++e) sum += exp((double)l[e] - mx);
+        /* selection: repeatedly take the largest remaining logit, lowest index on ties */
+        unsigned char taken[4096];
+        for (int32_t e = 0; e < E; ++e) taken[e] = 0;
+        double wsum = 0.0;
+        for (int32_t i = 0; i < k; ++i) {
+            int32_t best = -1;
+            for (int32_t e = 0; e < E; ++e)
+                if (!taken[e] && (best < 0 || l[e] > l[best])) best = e;
+            taken[best] = 1;
+            ids[t * k + i] = best;
+            w[t * k + i] = exp((double)l[best] - mx) / sum;
+            wsum += w[t * k + i];
+        }
+        if (renormalize)
+            for (int32_t i = 0; i < k; ++i) w[t * k + i] /= wsum;
+    }
+}
+
+/* Group the T*k (token, rank) pairs by expert, stably by token:
+ * offsets[e] = number of pairs with expert < e; within expert e the pairs
+ * appear in increasing token order. row_token[r] = token of sorted row r,
+ * pos[t][i] = sorted row of pair (t, i). */
+void oracle_moe_align(int64_t T, int32_t k, int32_t E, const int32_t *ids, int32_t *offsets, int32_t *row_token,
+                      int32_t *pos)
+{
+    for (int32_t e = 0; e <= E; ++e) offsets[e] = 0;
+    for (int64_t t = 0; t < T; ++t)
+        for (int32_t i = 0; i < k; ++i) offsets[ids[t * k + i] + 1] += 1;
+    for (int32_t e = 0; e < E; ++e) offsets[e + 1] += offsets[e];
+    for (int32_t e = 0; e < E; ++e) {
+        int32_t r = offsets[e];
+        for (int64_t t = 0; t < T; ++t)
+            for (int32_t i = 0; i < k; ++i)
+                if (ids[t * k + i] == e) {
+                    row_token[r] = (int32_t)t;
+                    pos[t * k + i] = r;
+                    ++r;
+                }
+    }
+}
+
+/* act[r][j] = silu(g) * u with g = gu[r][j], u = gu[r][I + j], silu(g) = g / (1 + exp(-g)). */
+void oracle_silu_mul(int64_t R, int64_t I, const uint16_t *gu, double *act)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t j = 0; j < I; ++j) {
+            double g = bf16_to_double(gu[r * 2 * I + j]);
+            double u = bf16_to_double(gu[r * 2 * I + I + j]);
+            act[r * I + j] = g / (1.0 + exp(-g)) * u;
+        }
+}
+
+/* out[t][h] = sum_{i=0}^{k-1} w[t][i] * Y[pos[t][i]][h]   (rank order i = 0..k-1). */
+void oracle_moe_combine(int64_t T, int32_t k, int64_t H, const uint16_t *Y, const int32_t *pos, const double *w,
+                        double *out)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t h = 0; h < H; ++h) {
+            double acc = 0.0;
+            for (int32_t i = 0; i < k; ++i)
+                acc += w[t * k + i] * bf16_to_double(Y[(int64_t)pos[t * k + i] * H + h]);
+            out[t * H + h] = acc;
+        }
+}
+
 /* RMSNorm with optional residual add, per row i:
  *   h = residual ? bf16(x + residual) : x         (the stored, rounded sum)
  *   y = h / sqrt( (1/H) sum_k h_k^2 + eps ) * w

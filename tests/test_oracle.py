@@ -284,6 +284,68 @@ def test_quantize_dequant_error_bound():
             assert abs(deq - x[i, k]) <= amax / 6 * 1.07 + 1e-7
 
 
+# ------------------------------------------------------------- MoE layer
+
+def test_topk_softmax_hand_worked():
+    """logits [1, 3, 3, 0], k = 2: experts 1 and 2 tie, the lower index comes
+    first; renormalised weights are 1/2 each; raw softmax weights are
+    e^3 / (e + 2 e^3 + 1)."""
+    l = np.array([[1.0, 3.0, 3.0, 0.0]], dtype=np.float32)
+    ids, w = oracle.moe_topk_softmax(l, 2, renormalize=True)
+    assert ids.tolist() == [[1, 2]] and np.allclose(w, 0.5, rtol=0, atol=1e-15)
+    ids, w = oracle.moe_topk_softmax(l, 2, renormalize=False)
+    p = math.exp(3) / (math.e + 2 * math.exp(3) + 1)
+    assert np.allclose(w, p, rtol=1e-14)
+
+
+def test_topk_softmax_vs_numpy_scipy():
+    scipy = pytest.importorskip("scipy.special")
+    l = syn.normal_rows(6, 0, 50, 128)
+    l[3, 10] = l[3, 20] = l[3].max() + 1     # an exact tie at the top
+    ids, w = oracle.moe_topk_softmax(l, 8, renormalize=False)
+    ref_ids = np.argsort(-l, axis=1, kind="stable")[:, :8]
+    assert np.array_equal(ids, ref_ids)
+    p = scipy.softmax(l.astype(np.float64), axis=1)
+    assert np.allclose(w, np.take_along_axis(p, ref_ids, axis=1), rtol=1e-12)
+    ids2, w2 = oracle.moe_topk_softmax(l, 8, renormalize=True)
+    assert np.array_equal(ids2, ids) and np.allclose(w2.sum(axis=1), 1.0, rtol=1e-14)
+
+
+def test_align_matches_stable_sort_and_inverts():
+    T, E, k = 300, 128, 8
+    tok, exp, off, ids = syn.moe_routing(T, E, k, seed=7)
+    o_off, o_row_token, o_pos = oracle.moe_align(ids, E)
+    assert np.array_equal(o_off, off) and np.array_equal(o_row_token, tok)
+    flat = o_pos.reshape(-1)
+    assert sorted(flat.tolist()) == list(range(T * k))       # a bijection
+    for t in range(T):
+        for i in range(k):
+            r = o_pos[t, i]
+            assert o_row_token[r] == t and off[ids[t, i]] <= r < off[ids[t, i] + 1]
+
+
+def test_silu_mul_closed_forms():
+    scipy = pytest.importorskip("scipy.special")
+    g = np.array([[0.0, 1.0, -2.0, 10.0, -30.0, 0.5, 3.0, -0.25]], dtype=np.float32)
+    u = np.array([[5.0, 2.0, 1.0, 0.5, 4.0, -1.0, 0.0, 8.0]], dtype=np.float32)
+    gu = syn.to_bf16_bits(np.concatenate([g, u], axis=1))
+    act = oracle.silu_mul(gu)
+    gd, ud = g.astype(np.float64), u.astype(np.float64)
+    assert act[0, 0] == 0.0 and act[0, 6] == 0.0
+    assert np.allclose(act, gd * scipy.expit(gd) * ud, rtol=1e-14, atol=0)
+
+
+def test_combine_bruteforce():
+    Y = syn.integer_bf16(8, 0, (12, 16), lo=-4, hi=4)
+    pos = np.array([[3, 0, 7], [11, 2, 2], [5, 6, 1]], dtype=np.int32)
+    w = np.array([[0.5, 0.25, 0.125], [1.0, -0.5, 0.5], [0.0, 2.0, 0.75]])
+    out = oracle.moe_combine(Y, pos, w)
+    Yf = syn.bf16_bits_to_f32(Y).astype(np.float64)
+    for t in range(3):
+        ref = sum(Fraction(w[t, i]) * np.array([Fraction(v) for v in Yf[pos[t, i]]]) for i in range(3))
+        assert [Fraction(v) for v in out[t]] == list(ref)
+
+
 # ----------------------------------------------------------------- RMSNorm
 
 def test_rmsnorm_golden_cases():
