@@ -146,6 +146,65 @@ BI_API bi_status bi_quantize_nvfp4(const void *X, int64_t ldx, float global_scal
                                    int64_t M, int64_t K, bi_stream stream);
 
 /*
+ * ---- The MoE layer around bi_grouped_gemm_bf16 (MoE models listed as tested
+ * on the vllm-ascend "Batch Invariance" guide: Qwen3-30B-A3B, Qwen3-235B-A22B).
+ * A layer is: bi_moe_topk_softmax -> bi_moe_align -> bi_moe_gather ->
+ * bi_grouped_gemm_bf16 (gate_up) -> bi_silu_mul -> bi_grouped_gemm_bf16 (down)
+ * -> bi_moe_combine. Every value a token sees is computed from that token's
+ * data alone, in fixed orders, so its output does not depend on the other
+ * tokens in the batch. None of these calls uses atomics for results.
+ */
+
+/*
+ * bi_moe_topk_softmax -- router: for each token t, the k experts with the
+ * largest logits (larger first; ties go to the lower expert index) and their
+ * softmax probabilities p_e = exp(l_e - max l) / sum_j exp(l_j - max l) (fp32),
+ * divided by their sum when renormalize != 0.
+ *   logits        f32 [T][E]      (device)
+ *   topk_ids      i32 [T][k]      output
+ *   topk_weights  f32 [T][k]      output
+ * Requirements: 1 <= E <= 1024, 1 <= k <= min(E, 32).
+ */
+BI_API bi_status bi_moe_topk_softmax(const float *logits, int64_t T, int32_t E, int32_t k, int32_t renormalize,
+                                     int32_t *topk_ids, float *topk_weights, bi_stream stream);
+
+/*
+ * bi_moe_align -- group the T*k (token, rank) pairs by expert, stably by
+ * token: expert_offsets[e] = number of pairs routed to experts < e (E+1
+ * entries); within an expert, pairs appear in increasing token order.
+ * row_token[r] = token of sorted row r (T*k entries); pos[t][i] = sorted row
+ * of pair (t, i) (T*k entries). Deterministic (block scans, no atomics).
+ * An id outside [0, E) is skipped and the device status becomes
+ * BI_ERR_INVALID_ARG. Requirements: 1 <= E <= 1024, k >= 1.
+ */
+BI_API bi_status bi_moe_align(const int32_t *topk_ids, int64_t T, int32_t k, int32_t E, int32_t *expert_offsets,
+                              int32_t *row_token, int32_t *pos, bi_stream stream);
+
+/*
+ * bi_moe_gather -- X_sorted[r] = hidden[row_token[r]] for r < rows.
+ *   hidden bf16 [T][H], X_sorted bf16 [rows][H] (dense); H % 8 == 0.
+ * A token index outside [0, T) is skipped (status BI_ERR_INVALID_ARG).
+ */
+BI_API bi_status bi_moe_gather(const void *hidden, int64_t T, int64_t H, const int32_t *row_token, int64_t rows,
+                               void *X_sorted, bi_stream stream);
+
+/*
+ * bi_silu_mul -- act[r][j] = bf16( silu(g) * u ), g = gate_up[r][j],
+ * u = gate_up[r][I + j], silu(g) = g / (1 + exp(-g)), fp32 arithmetic.
+ *   gate_up bf16 [rows][2I] ([gate | up]), act bf16 [rows][I]; I % 8 == 0.
+ */
+BI_API bi_status bi_silu_mul(const void *gate_up, int64_t rows, int64_t I, void *act, bi_stream stream);
+
+/*
+ * bi_moe_combine -- out[t] = bf16( sum_{i=0}^{k-1} w[t][i] * Y_sorted[pos[t][i]] ),
+ * fp32 fused multiply-adds in top-k rank order i = 0, 1, ..., k-1.
+ *   Y_sorted bf16 [rows][H], pos i32 [T][k], topk_weights f32 [T][k], out bf16 [T][H].
+ * A row index outside [0, rows) is skipped (status BI_ERR_INVALID_ARG). H % 8 == 0.
+ */
+BI_API bi_status bi_moe_combine(const void *Y_sorted, int64_t rows, const int32_t *pos, const float *topk_weights,
+                                int64_t T, int32_t k, int64_t H, void *out, bi_stream stream);
+
+/*
  * bi_rmsnorm -- RMSNorm with optional residual add and a fixed reduction tree.
  *
  * The RMSNorm that vLLM fuses with the tensor-parallel all-reduce (vLLM PR

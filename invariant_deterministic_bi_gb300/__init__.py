@@ -62,6 +62,11 @@ def load() -> ctypes.CDLL:
             "bi_gemm_nvfp4": [P, P, P, P, F, P, I64, I64, I64, P],
             "bi_rmsnorm": [P, P, P, P, I64, I64, F, P],
             "bi_quantize_nvfp4": [P, I64, F, P, P, I64, I64, P],
+            "bi_moe_topk_softmax": [P, I64, I32, I32, I32, P, P, P],
+            "bi_moe_align": [P, I64, I32, I32, P, P, P, P],
+            "bi_moe_gather": [P, I64, I64, P, I64, P, P],
+            "bi_silu_mul": [P, I64, I64, P, P],
+            "bi_moe_combine": [P, I64, P, P, I64, I32, I64, P, P],
             "bi_plan": [I32, I64, I64, I64, I32, ctypes.POINTER(Plan)],
             "bi_device_status": [P],
             "bi_check_wait_timeout": [ctypes.c_uint32, P],
@@ -199,6 +204,71 @@ def quantize_nvfp4(X, global_scale: float, Q=None, Q_sf=None, stream=None):
     _check(load().bi_quantize_nvfp4(_ptr(X), X.stride(0), float(global_scale), _ptr(Q), _ptr(Q_sf), M, K,
                                     _stream(stream)), "bi_quantize_nvfp4")
     return Q, Q_sf
+
+
+def moe_topk_softmax(logits, k: int, renormalize: bool = True, stream=None):
+    """Router: (topk_ids int32 [T, k], topk_weights float32 [T, k]) from float32 logits [T, E]."""
+    import torch
+    _dev(logits, torch.float32, "logits")
+    if logits.dim() != 2 or not logits.is_contiguous():
+        raise ValueError("logits must be contiguous [T, E]")
+    T, E = logits.shape
+    ids = torch.empty((T, k), dtype=torch.int32, device=logits.device)
+    w = torch.empty((T, k), dtype=torch.float32, device=logits.device)
+    _check(load().bi_moe_topk_softmax(_ptr(logits), T, E, k, int(bool(renormalize)), _ptr(ids), _ptr(w),
+                                      _stream(stream)), "bi_moe_topk_softmax")
+    return ids, w
+
+
+def moe_align(topk_ids, E: int, stream=None):
+    """(expert_offsets int32 [E+1], row_token int32 [T*k], pos int32 [T, k])."""
+    import torch
+    _dev(topk_ids, torch.int32, "topk_ids")
+    T, k = topk_ids.shape
+    off = torch.empty(E + 1, dtype=torch.int32, device=topk_ids.device)
+    row_token = torch.empty(T * k, dtype=torch.int32, device=topk_ids.device)
+    pos = torch.empty((T, k), dtype=torch.int32, device=topk_ids.device)
+    _check(load().bi_moe_align(_ptr(topk_ids.contiguous()), T, k, E, _ptr(off), _ptr(row_token), _ptr(pos),
+                               _stream(stream)), "bi_moe_align")
+    return off, row_token, pos
+
+
+def moe_gather(hidden, row_token, out=None, stream=None):
+    """X_sorted[r] = hidden[row_token[r]]."""
+    import torch
+    _dev(hidden, torch.bfloat16, "hidden"), _dev(row_token, torch.int32, "row_token")
+    T, H = hidden.shape
+    rows = row_token.numel()
+    if out is None:
+        out = torch.empty((rows, H), dtype=torch.bfloat16, device=hidden.device)
+    _check(load().bi_moe_gather(_ptr(hidden), T, H, _ptr(row_token), rows, _ptr(out), _stream(stream)),
+           "bi_moe_gather")
+    return out
+
+
+def silu_mul(gate_up, out=None, stream=None):
+    """act = silu(gate) * up for bf16 rows [gate | up]."""
+    import torch
+    _dev(gate_up, torch.bfloat16, "gate_up")
+    rows, I2 = gate_up.shape
+    if out is None:
+        out = torch.empty((rows, I2 // 2), dtype=torch.bfloat16, device=gate_up.device)
+    _check(load().bi_silu_mul(_ptr(gate_up), rows, I2 // 2, _ptr(out), _stream(stream)), "bi_silu_mul")
+    return out
+
+
+def moe_combine(Y_sorted, pos, topk_weights, out=None, stream=None):
+    """out[t] = sum_i w[t, i] * Y_sorted[pos[t, i]] in rank order (fp32), bf16."""
+    import torch
+    _dev(Y_sorted, torch.bfloat16, "Y_sorted"), _dev(pos, torch.int32, "pos")
+    _dev(topk_weights, torch.float32, "topk_weights")
+    rows, H = Y_sorted.shape
+    T, k = pos.shape
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=Y_sorted.device)
+    _check(load().bi_moe_combine(_ptr(Y_sorted), rows, _ptr(pos), _ptr(topk_weights), T, k, H, _ptr(out),
+                                 _stream(stream)), "bi_moe_combine")
+    return out
 
 
 def rmsnorm(x, w, eps: float, residual=None, out=None, stream=None):

@@ -161,6 +161,66 @@ bi_status bi_quantize_nvfp4(const void *X, int64_t ldx, float global_scale, uint
     return launch_quantize_nvfp4(X, ldx, global_scale, Q, Q_sf, M, K, as_stream(stream));
 }
 
+namespace {
+inline bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+bi_status require_device() {
+    int dev;
+    const DeviceInfo *info;
+    return current_device(&dev, &info);
+}
+}  // namespace
+
+bi_status bi_moe_topk_softmax(const float *logits, int64_t T, int32_t E, int32_t k, int32_t renormalize,
+                              int32_t *topk_ids, float *topk_weights, bi_stream stream) {
+    if (T < 0 || T >= kI32Max || E < 1 || E > 1024 || k < 1 || k > 32 || k > E) return BI_ERR_INVALID_ARG;
+    if (T == 0) return BI_OK;
+    if (!logits || !topk_ids || !topk_weights) return BI_ERR_INVALID_ARG;
+    if (!aligned4(logits) || !aligned4(topk_ids) || !aligned4(topk_weights)) return BI_ERR_MISALIGNED;
+    bi_status st = require_device();
+    if (st != BI_OK) return st;
+    return launch_moe_topk_softmax(logits, T, E, k, renormalize, topk_ids, topk_weights, as_stream(stream));
+}
+
+bi_status bi_moe_align(const int32_t *topk_ids, int64_t T, int32_t k, int32_t E, int32_t *expert_offsets,
+                       int32_t *row_token, int32_t *pos, bi_stream stream) {
+    if (T < 0 || k < 1 || E < 1 || E > 1024 || T * k >= kI32Max) return BI_ERR_INVALID_ARG;
+    if (!topk_ids || !expert_offsets || !row_token || !pos) return BI_ERR_INVALID_ARG;
+    if (!aligned4(topk_ids) || !aligned4(expert_offsets) || !aligned4(row_token) || !aligned4(pos))
+        return BI_ERR_MISALIGNED;
+    return launch_moe_align(topk_ids, T, k, E, expert_offsets, row_token, pos, as_stream(stream));
+}
+
+bi_status bi_moe_gather(const void *hidden, int64_t T, int64_t H, const int32_t *row_token, int64_t rows,
+                        void *X_sorted, bi_stream stream) {
+    if (T < 0 || H < 8 || rows < 0 || rows >= kI32Max) return BI_ERR_INVALID_ARG;
+    if (rows == 0) return BI_OK;
+    if (!hidden || !row_token || !X_sorted) return BI_ERR_INVALID_ARG;
+    if (H % 8 != 0) return BI_ERR_UNSUPPORTED;
+    if (!aligned16(hidden) || !aligned16(X_sorted) || !aligned4(row_token)) return BI_ERR_MISALIGNED;
+    return launch_moe_gather(hidden, T, H, row_token, rows, X_sorted, as_stream(stream));
+}
+
+bi_status bi_silu_mul(const void *gate_up, int64_t rows, int64_t I, void *act, bi_stream stream) {
+    if (rows < 0 || I < 8) return BI_ERR_INVALID_ARG;
+    if (rows == 0) return BI_OK;
+    if (!gate_up || !act) return BI_ERR_INVALID_ARG;
+    if (I % 8 != 0) return BI_ERR_UNSUPPORTED;
+    if (!aligned16(gate_up) || !aligned16(act)) return BI_ERR_MISALIGNED;
+    return launch_silu_mul(gate_up, rows, I, act, as_stream(stream));
+}
+
+bi_status bi_moe_combine(const void *Y_sorted, int64_t rows, const int32_t *pos, const float *topk_weights,
+                         int64_t T, int32_t k, int64_t H, void *out, bi_stream stream) {
+    if (rows < 0 || T < 0 || T >= kI32Max || k < 1 || H < 8) return BI_ERR_INVALID_ARG;
+    if (T == 0) return BI_OK;
+    if (!Y_sorted || !pos || !topk_weights || !out) return BI_ERR_INVALID_ARG;
+    if (H % 8 != 0) return BI_ERR_UNSUPPORTED;
+    if (!aligned16(Y_sorted) || !aligned16(out) || !aligned4(pos) || !aligned4(topk_weights)) return BI_ERR_MISALIGNED;
+    bi_status st = require_device();
+    if (st != BI_OK) return st;
+    return launch_moe_combine(Y_sorted, rows, pos, topk_weights, T, k, H, out, as_stream(stream));
+}
+
 bi_status bi_rmsnorm(const void *x, void *residual, const void *w, void *out, int64_t M, int64_t H, float eps,
                      bi_stream stream) {
     if (M < 0 || H < 8 || H > 65536 || !(eps >= 0.0f)) return BI_ERR_INVALID_ARG;

@@ -46,6 +46,15 @@ bi_status launch_gemm_nvfp4(const uint8_t *A, const uint8_t *A_sf, const uint8_t
                             float alpha, void *Y, int64_t M, int64_t N, int64_t K, cudaStream_t s);
 bi_status launch_quantize_nvfp4(const void *X, int64_t ldx, float gs, uint8_t *Q, uint8_t *Q_sf, int64_t M, int64_t K,
                                 cudaStream_t s);
+bi_status launch_moe_topk_softmax(const float *logits, int64_t T, int32_t E, int32_t k, int32_t renorm, int32_t *ids,
+                                  float *w, cudaStream_t s);
+bi_status launch_moe_align(const int32_t *ids, int64_t T, int32_t k, int32_t E, int32_t *offsets, int32_t *row_token,
+                           int32_t *pos, cudaStream_t s);
+bi_status launch_moe_gather(const void *hidden, int64_t T, int64_t H, const int32_t *row_token, int64_t rows,
+                            void *out, cudaStream_t s);
+bi_status launch_silu_mul(const void *gate_up, int64_t rows, int64_t I, void *act, cudaStream_t s);
+bi_status launch_moe_combine(const void *Y, int64_t rows, const int32_t *pos, const float *w, int64_t T, int32_t k,
+                             int64_t H, void *out, cudaStream_t s);
 bi_status launch_rmsnorm(const void *x, void *residual, const void *w, void *out, int64_t M, int64_t H,
                          float eps, cudaStream_t s);
 bi_status launch_wait_timeout_check(uint32_t limit_us, cudaStream_t s);

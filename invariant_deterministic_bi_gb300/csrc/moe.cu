@@ -1,0 +1,281 @@
+// moe.cu -- the batch-invariant MoE layer around bi_grouped_gemm_bf16:
+// routing (top-k softmax), expert alignment, gather, SiLU-mul and the
+// weighted combine, for the MoE models the vllm-ascend "Batch Invariance"
+// guide lists as tested (Qwen3-30B-A3B, Qwen3-235B-A22B).
+//
+// Invariance: routing, gather, SiLU-mul and combine are per token (or per
+// row) with fixed reduction orders; the alignment only decides *where* a
+// token's rows sit, never their values; the combine adds a token's k expert
+// outputs in top-k rank order. So a token's layer output does not depend on
+// which tokens share the batch. No atomics anywhere (the alignment uses
+// per-expert block scans), so every buffer is the same bits run to run.
+#include <cuda_bf16.h>
+
+#include "bi_internal.h"
+#include "bi_ptx.cuh"
+
+namespace bi {
+namespace {
+
+__device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// --------------------------------------------------------------- routing
+// One warp per token. Lane l holds logits l, l+32, ...; max and the sum of
+// exponentials use fixed per-lane orders and xor butterflies; the k winners
+// come from k warp arg-max rounds under the total order (larger logit, then
+// lower expert index).
+template <int MAXJ>
+__global__ void __launch_bounds__(256)
+topk_softmax_kernel(const float *__restrict__ logits, int64_t T, int E, int k, int renorm, int32_t *__restrict__ ids,
+                    float *__restrict__ wout) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * 8 + warp;
+    if (t >= T) return;                       // whole warp leaves together
+    const float *l = logits + t * E;
+    float v[MAXJ];
+#pragma unroll
+    for (int j = 0; j < MAXJ; ++j) {
+        const int e = lane + 32 * j;
+        v[j] = e < E ? l[e] : -INFINITY;
+    }
+    float mx = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < MAXJ; ++j) mx = fmaxf(mx, v[j]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float s = 0.0f;
+#pragma unroll
+    for (int j = 0; j < MAXJ; ++j)
+        if (lane + 32 * j < E) s += expf(v[j] - mx);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+
+    uint32_t taken = 0;
+    float my_w = 0.0f, wsum = 0.0f;
+    for (int i = 0; i < k; ++i) {
+        float bv = -INFINITY;
+        int be = 0x7fffffff;
+#pragma unroll
+        for (int j = 0; j < MAXJ; ++j) {
+            const int e = lane + 32 * j;
+            if (e < E && !((taken >> j) & 1u) && (v[j] > bv || be == 0x7fffffff)) {
+                bv = v[j];
+                be = e;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+            if (ov > bv || (ov == bv && oe < be)) {
+                bv = ov;
+                be = oe;
+            }
+        }
+        if ((be & 31) == lane) taken |= 1u << (be >> 5);
+        const float wi = __fdiv_rn(expf(bv - mx), s);
+        wsum += wi;
+        if (lane == i) my_w = wi;
+        if (lane == 0) ids[t * k + i] = be;
+    }
+    if (lane < k) wout[t * k + lane] = renorm ? __fdiv_rn(my_w, wsum) : my_w;
+}
+
+// ------------------------------------------------------------- alignment
+// Step 1 (one block per expert): scan the (token, rank) pairs in order and
+// give each pair routed to this expert its rank among them; the expert's
+// count goes to offsets[e + 1].
+__global__ void __launch_bounds__(256)
+align_rank_kernel(const int32_t *__restrict__ ids, int64_t P, int32_t *__restrict__ pos, int32_t *__restrict__ offsets) {
+    __shared__ int warp_tot[8];
+    const int e = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int running = 0;
+    for (int64_t base = 0; base < P; base += 256) {
+        const int64_t p = base + threadIdx.x;
+        const bool f = p < P && ids[p] == e;
+        const unsigned ballot = __ballot_sync(0xffffffffu, f);
+        if (lane == 0) warp_tot[warp] = __popc(ballot);
+        __syncthreads();
+        int before = 0, chunk = 0;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            before += w < warp ? warp_tot[w] : 0;
+            chunk += warp_tot[w];
+        }
+        if (f) pos[p] = running + before + __popc(ballot & ((1u << lane) - 1u));
+        running += chunk;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        offsets[e + 1] = running;
+        if (e == 0) offsets[0] = 0;
+    }
+}
+
+// Step 2 (one block): offsets[1..E] counts -> inclusive prefix, in place.
+__global__ void __launch_bounds__(1024) align_scan_kernel(int32_t *offsets, int E) {
+    __shared__ int buf[1024];
+    const int i = threadIdx.x;
+    buf[i] = i < E ? offsets[i + 1] : 0;
+    __syncthreads();
+    for (int d = 1; d < 1024; d <<= 1) {      // Hillis-Steele: integer adds, order-free
+        const int add = i >= d ? buf[i - d] : 0;
+        __syncthreads();
+        buf[i] += add;
+        __syncthreads();
+    }
+    if (i < E) offsets[i + 1] = buf[i];
+}
+
+// Step 3: pos = offsets[expert] + rank; row_token[pos] = token.
+__global__ void __launch_bounds__(256)
+align_scatter_kernel(const int32_t *__restrict__ ids, int64_t P, int k, int E, const int32_t *__restrict__ offsets,
+                     int32_t *__restrict__ pos, int32_t *__restrict__ row_token, unsigned *status) {
+    for (int64_t p = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x; p < P;
+         p += static_cast<int64_t>(gridDim.x) * 256) {
+        const int e = ids[p];
+        if (e < 0 || e >= E) {
+            atomicOr(status, kDevBadOffsets);
+            continue;
+        }
+        const int r = offsets[e] + pos[p];
+        pos[p] = r;
+        row_token[r] = static_cast<int32_t>(p / k);
+    }
+}
+
+// ----------------------------------------------------------------- gather
+__global__ void __launch_bounds__(256)
+gather_kernel(const uint4 *__restrict__ hidden, int64_t T, int64_t hv, const int32_t *__restrict__ row_token,
+              int64_t rows, uint4 *__restrict__ out, unsigned *status) {
+    const int64_t total = rows * hv;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * 256) {
+        const int64_t r = i / hv, j = i - r * hv;
+        const int64_t t = row_token[r];
+        if (t < 0 || t >= T) {
+            atomicOr(status, kDevBadOffsets);
+            continue;
+        }
+        out[i] = __ldg(hidden + t * hv + j);
+    }
+}
+
+// --------------------------------------------------------------- SiLU-mul
+// act = bf16( silu(g) * u ), silu(g) = g / (1 + exp(-g)), fp32; rows are [gate | up].
+__global__ void __launch_bounds__(256)
+silu_mul_kernel(const uint4 *__restrict__ gu, int64_t rows, int64_t iv, uint4 *__restrict__ act) {
+    const int64_t total = rows * iv;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * 256) {
+        const int64_t r = i / iv, j = i - r * iv;
+        const uint4 g = __ldcs(gu + r * 2 * iv + j), u = __ldcs(gu + r * 2 * iv + iv + j);
+        const uint32_t gw[4] = {g.x, g.y, g.z, g.w}, uw[4] = {u.x, u.y, u.z, u.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float g0 = bf_lo(gw[q]), g1 = bf_hi(gw[q]);
+            const float a0 = __fmul_rn(__fdiv_rn(g0, 1.0f + expf(-g0)), bf_lo(uw[q]));
+            const float a1 = __fmul_rn(__fdiv_rn(g1, 1.0f + expf(-g1)), bf_hi(uw[q]));
+            o[q] = pack_bf16x2(__float_as_uint(a0), __float_as_uint(a1));
+        }
+        __stcs(act + i, make_uint4(o[0], o[1], o[2], o[3]));
+    }
+}
+
+// ---------------------------------------------------------------- combine
+// out[t] = bf16( sum_{i = 0..k-1} w[t][i] * Y[pos[t][i]] ), fp32 FMA in rank order.
+__global__ void __launch_bounds__(256)
+combine_kernel(const uint4 *__restrict__ Y, int64_t rows, const int32_t *__restrict__ pos,
+               const float *__restrict__ w, int k, int64_t hv, uint4 *__restrict__ out, unsigned *status) {
+    const int64_t t = blockIdx.x;
+    for (int64_t j = threadIdx.x; j < hv; j += 256) {
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        bool bad = false;
+        for (int i = 0; i < k; ++i) {
+            const int64_t r = pos[t * k + i];
+            if (r < 0 || r >= rows) {
+                bad = true;
+                continue;
+            }
+            const float wi = w[t * k + i];
+            const uint4 y = __ldg(Y + r * hv + j);
+            const uint32_t yw[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                acc[2 * q] = __fmaf_rn(wi, bf_lo(yw[q]), acc[2 * q]);
+                acc[2 * q + 1] = __fmaf_rn(wi, bf_hi(yw[q]), acc[2 * q + 1]);
+            }
+        }
+        if (bad) atomicOr(status, kDevBadOffsets);
+        uint32_t o[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) o[q] = pack_bf16x2(__float_as_uint(acc[2 * q]), __float_as_uint(acc[2 * q + 1]));
+        __stcs(out + t * hv + j, make_uint4(o[0], o[1], o[2], o[3]));
+    }
+}
+
+inline unsigned grid_for(int64_t items, const DeviceInfo *info) {
+    const int64_t g = (items + 255) / 256, cap = static_cast<int64_t>(info->sm_count) * 16;
+    return static_cast<unsigned>(g < 1 ? 1 : (g < cap ? g : cap));
+}
+
+}  // namespace
+
+bi_status launch_moe_topk_softmax(const float *logits, int64_t T, int32_t E, int32_t k, int32_t renorm, int32_t *ids,
+                                  float *w, cudaStream_t s) {
+    const unsigned grid = static_cast<unsigned>((T + 7) / 8);
+    if (E <= 32) topk_softmax_kernel<1><<<grid, 256, 0, s>>>(logits, T, E, k, renorm, ids, w);
+    else if (E <= 64) topk_softmax_kernel<2><<<grid, 256, 0, s>>>(logits, T, E, k, renorm, ids, w);
+    else if (E <= 128) topk_softmax_kernel<4><<<grid, 256, 0, s>>>(logits, T, E, k, renorm, ids, w);
+    else if (E <= 256) topk_softmax_kernel<8><<<grid, 256, 0, s>>>(logits, T, E, k, renorm, ids, w);
+    else if (E <= 512) topk_softmax_kernel<16><<<grid, 256, 0, s>>>(logits, T, E, k, renorm, ids, w);
+    else topk_softmax_kernel<32><<<grid, 256, 0, s>>>(logits, T, E, k, renorm, ids, w);
+    return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
+}
+
+bi_status launch_moe_align(const int32_t *ids, int64_t T, int32_t k, int32_t E, int32_t *offsets, int32_t *row_token,
+                           int32_t *pos, cudaStream_t s) {
+    int dev;
+    const DeviceInfo *info;
+    bi_status st = current_device(&dev, &info);
+    if (st != BI_OK) return st;
+    const int64_t P = T * k;
+    align_rank_kernel<<<E, 256, 0, s>>>(ids, P, pos, offsets);
+    align_scan_kernel<<<1, 1024, 0, s>>>(offsets, E);
+    align_scatter_kernel<<<grid_for(P, info), 256, 0, s>>>(ids, P, k, E, offsets, pos, row_token, device_status_word());
+    return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
+}
+
+bi_status launch_moe_gather(const void *hidden, int64_t T, int64_t H, const int32_t *row_token, int64_t rows,
+                            void *out, cudaStream_t s) {
+    int dev;
+    const DeviceInfo *info;
+    bi_status st = current_device(&dev, &info);
+    if (st != BI_OK) return st;
+    gather_kernel<<<grid_for(rows * (H / 8), info), 256, 0, s>>>(static_cast<const uint4 *>(hidden), T, H / 8,
+                                                                 row_token, rows, static_cast<uint4 *>(out),
+                                                                 device_status_word());
+    return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
+}
+
+bi_status launch_silu_mul(const void *gate_up, int64_t rows, int64_t I, void *act, cudaStream_t s) {
+    int dev;
+    const DeviceInfo *info;
+    bi_status st = current_device(&dev, &info);
+    if (st != BI_OK) return st;
+    silu_mul_kernel<<<grid_for(rows * (I / 8), info), 256, 0, s>>>(static_cast<const uint4 *>(gate_up), rows, I / 8,
+                                                                   static_cast<uint4 *>(act));
+    return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
+}
+
+bi_status launch_moe_combine(const void *Y, int64_t rows, const int32_t *pos, const float *w, int64_t T, int32_t k,
+                             int64_t H, void *out, cudaStream_t s) {
+    combine_kernel<<<static_cast<unsigned>(T), 256, 0, s>>>(static_cast<const uint4 *>(Y), rows, pos, w, k, H / 8,
+                                                            static_cast<uint4 *>(out), device_status_word());
+    return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
+}
+
+}  // namespace bi

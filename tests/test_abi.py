@@ -26,7 +26,7 @@ def declared_functions():
 
 def test_header_declares_the_calls():
     names = declared_functions()
-    for n in ["bi_gemm_bf16", "bi_grouped_gemm_bf16", "bi_gemm_nvfp4", "bi_rmsnorm", "bi_plan", "bi_quantize_nvfp4",
+    for n in ["bi_gemm_bf16", "bi_grouped_gemm_bf16", "bi_gemm_nvfp4", "bi_rmsnorm", "bi_plan", "bi_quantize_nvfp4", "bi_moe_topk_softmax", "bi_moe_align", "bi_moe_gather", "bi_silu_mul", "bi_moe_combine",
               "bi_device_status", "bi_status_string", "bi_version", "bi_check_wait_timeout"]:
         assert n in names
 
@@ -124,5 +124,13 @@ def test_other_calls_reject_bad_arguments(lib):
     assert so.bi_quantize_nvfp4(FAKE, 100, f(1.0), FAKE, FAKE, 4, 128, None) == 1          # ldx < K
     assert so.bi_quantize_nvfp4(FAKE, 136, f(1.0), FAKE + 8, FAKE, 4, 128, None) == 3      # Q align
     assert so.bi_quantize_nvfp4(FAKE, 128, f(1.0), FAKE, FAKE, 0, 128, None) == 0          # empty
+    assert so.bi_moe_topk_softmax(FAKE, 4, 128, 0, 1, FAKE, FAKE, None) == 1             # k < 1
+    assert so.bi_moe_topk_softmax(FAKE, 4, 2000, 8, 1, FAKE, FAKE, None) == 1            # E > 1024
+    assert so.bi_moe_topk_softmax(FAKE, 4, 4, 8, 1, FAKE, FAKE, None) == 1               # k > E
+    assert so.bi_moe_topk_softmax(FAKE, 0, 128, 8, 1, FAKE, FAKE, None) == 0             # empty
+    assert so.bi_moe_align(FAKE + 2, 4, 8, 128, FAKE, FAKE, FAKE, None) == 3
+    assert so.bi_moe_gather(FAKE, 4, 100, FAKE, 8, FAKE, None) == 2                      # H % 8
+    assert so.bi_silu_mul(FAKE, 4, 12, FAKE, None) == 2                                  # I % 8
+    assert so.bi_moe_combine(FAKE, 8, FAKE, FAKE, 4, 0, 64, FAKE, None) == 1              # k < 1
     assert so.bi_check_wait_timeout(0, None) == 1
     assert so.bi_plan(99, 1, 1, 1, 152, ctypes.byref(lib.Plan())) == 1
