@@ -478,6 +478,52 @@ def quant_sweep(bi, peaks):
     return rows
 
 
+MOE_LAYER_T = [1, 64, 512, 8192]
+
+
+def moe_layer_sweep(bi, peaks):
+    """The whole batch-invariant MoE layer (Qwen3-30B-A3B shapes): router top-8
+    softmax, alignment, gather, grouped gate_up, SiLU-mul, grouped down,
+    rank-order combine. Per-stage device time (CUDA-graph replays)."""
+    import torch
+    import bi_synth as syn
+    n1, k1 = MOE_LAYERS["gate_up"]
+    n2, k2 = MOE_LAYERS["down"]
+    W1 = bf16_dev(syn.moe_weights(MOE_E, n1, k1, seed=0, tensor_id=syn.TID_W1))
+    W2 = bf16_dev(syn.moe_weights(MOE_E, n2, k2, seed=0, tensor_id=syn.TID_W2))
+    out = []
+    for T in MOE_LAYER_T:
+        hidden = bf16_dev(syn.to_bf16_bits(syn.normal_rows(0, syn.TID_HIDDEN, T, k1)))
+        logits = torch.from_numpy(syn.normal_rows(0, syn.TID_LOGITS, T, MOE_E)).cuda()
+        ids, w = bi.moe_topk_softmax(logits, MOE_TOPK)
+        off, rt, pos = bi.moe_align(ids, MOE_E)
+        X = bi.moe_gather(hidden, rt)
+        gu = bi.grouped_gemm_bf16(X, W1, off)
+        act = bi.silu_mul(gu)
+        y = bi.grouped_gemm_bf16(act, W2, off)
+        o = bi.moe_combine(y, pos, w)
+        reps = 50 if T <= 512 else 10
+        stages = {
+            "topk_softmax": lambda: bi.moe_topk_softmax(logits, MOE_TOPK),
+            "align": lambda: bi.moe_align(ids, MOE_E),
+            "gather": lambda: bi.moe_gather(hidden, rt, out=X),
+            "grouped_gate_up": lambda: bi.grouped_gemm_bf16(X, W1, off, Y=gu),
+            "silu_mul": lambda: bi.silu_mul(gu, out=act),
+            "grouped_down": lambda: bi.grouped_gemm_bf16(act, W2, off, Y=y),
+            "combine": lambda: bi.moe_combine(y, pos, w, out=o),
+        }
+        times = {name: round(time_fn(fn, reps) * 1e3, 2) for name, fn in stages.items()}
+        total_us = sum(times.values())
+        flops = 2.0 * T * MOE_TOPK * (n1 * k1 + n2 * k2)
+        out.append({"T": T, "us_by_stage": times, "us_total": round(total_us, 2),
+                    "gemm_share": round((times["grouped_gate_up"] + times["grouped_down"]) / total_us, 3),
+                    "tflops_layer": round(flops / (total_us * 1e-6) / 1e12, 1)})
+        del hidden, logits, ids, w, off, rt, pos, X, gu, act, y, o
+    del W1, W2
+    torch.cuda.empty_cache()
+    return out
+
+
 def cpu_baseline(rows: int):
     """The fp64 oracle on a bounded sample of the step: `rows` rows of every
     GEMM of the step and of both RMSNorms, on the host's cores."""
@@ -585,6 +631,7 @@ def run_ours(args, dist):
         breakdown["grouped_gemm_bf16_moe"] = moe_sweep(bi, peaks)
         breakdown["gemm_nvfp4"] = nvfp4_sweep(bi, peaks)
         breakdown["quantize_nvfp4"] = quant_sweep(bi, peaks)
+        breakdown["moe_layer"] = moe_layer_sweep(bi, peaks)
         if bi.device_status() != bi.BI_OK:
             raise RuntimeError("device status after breakdown")
 
