@@ -226,6 +226,27 @@ BI_API bi_status bi_moe_combine(const void *Y_sorted, int64_t rows, const int32_
 BI_API bi_status bi_rmsnorm(const void *x, void *residual, const void *w, void *out,
                      int64_t M, int64_t H, float eps, bi_stream stream);
 
+/*
+ * bi_rank_sum_rmsnorm -- deterministic tensor-parallel all-reduce + RMSNorm.
+ *
+ * vLLM PR #51292 disables its fused all-reduce + RMSNorm under batch
+ * invariance because that kernel reduces in an order that varies from run to
+ * run ("a fixed-order reduction ... is bitwise-stable"). Here the R ranks'
+ * partial rows, all readable from the current GPU (gathered there, or peer
+ * memory), are summed in rank order 0, 1, ..., R-1 in fp32 and rounded once:
+ *   a   = bf16( x_0 + x_1 + ... + x_{R-1} )   (written to sum_out if given)
+ *   h   = residual ? bf16(a + residual) : a    (written back to residual)
+ *   out = bf16( h / sqrt(sum(h^2)/H + eps) * w ), the bi_rmsnorm tree
+ * Every rank that runs this on the same R inputs gets the same bits.
+ *
+ *   parts     HOST array of R DEVICE pointers, each bf16 [M][H] (dense)
+ *   residual  bf16 [M][H] NULLABLE, updated in place; sum_out bf16 [M][H] NULLABLE
+ *   w bf16 [H]; out bf16 [M][H]
+ * Requirements: 1 <= R <= 16; H % 8 == 0, 8 <= H <= 65536; eps >= 0.
+ */
+BI_API bi_status bi_rank_sum_rmsnorm(const void *const *parts, int32_t R, void *residual, const void *w,
+                                     void *sum_out, void *out, int64_t M, int64_t H, float eps, bi_stream stream);
+
 /* Operation ids for bi_plan. */
 enum { BI_OP_GEMM_BF16 = 0, BI_OP_GROUPED_GEMM_BF16 = 1, BI_OP_GEMM_NVFP4 = 2, BI_OP_RMSNORM = 3,
        BI_OP_QUANTIZE_NVFP4 = 4 };

@@ -67,6 +67,7 @@ def load() -> ctypes.CDLL:
             "bi_moe_gather": [P, I64, I64, P, I64, P, P],
             "bi_silu_mul": [P, I64, I64, P, P],
             "bi_moe_combine": [P, I64, P, P, I64, I32, I64, P, P],
+            "bi_rank_sum_rmsnorm": [P, I32, P, P, P, P, I64, I64, F, P],
             "bi_plan": [I32, I64, I64, I64, I32, ctypes.POINTER(Plan)],
             "bi_device_status": [P],
             "bi_check_wait_timeout": [ctypes.c_uint32, P],
@@ -292,6 +293,28 @@ def rmsnorm(x, w, eps: float, residual=None, out=None, stream=None):
         raise ValueError("out must be contiguous [M, H]")
     _check(load().bi_rmsnorm(_ptr(x), _ptr(residual) if residual is not None else None, _ptr(w), _ptr(out), M, H,
                              float(eps), _stream(stream)), "bi_rmsnorm")
+    return out
+
+
+def rank_sum_rmsnorm(parts, w, eps: float, residual=None, sum_out=None, out=None, stream=None):
+    """Deterministic all-reduce + RMSNorm over a list of R ranks' partial rows
+    (bf16 [M, H] CUDA tensors on this GPU), summed in list (rank) order."""
+    import torch
+    R = len(parts)
+    if R < 1:
+        raise ValueError("need at least one rank")
+    for r, t in enumerate(parts):
+        _dev(t, torch.bfloat16, f"parts[{r}]")
+        if t.shape != parts[0].shape or not t.is_contiguous():
+            raise ValueError("all parts must be contiguous and the same shape")
+    M, H = parts[0].shape
+    _dev(w, torch.bfloat16, "w")
+    if out is None:
+        out = torch.empty_like(parts[0])
+    ptrs = (ctypes.c_void_p * R)(*[t.data_ptr() for t in parts])
+    _check(load().bi_rank_sum_rmsnorm(ptrs, R, _ptr(residual) if residual is not None else None, _ptr(w),
+                                      _ptr(sum_out) if sum_out is not None else None, _ptr(out), M, H, float(eps),
+                                      _stream(stream)), "bi_rank_sum_rmsnorm")
     return out
 
 

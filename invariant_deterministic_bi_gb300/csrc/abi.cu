@@ -236,6 +236,23 @@ bi_status bi_rmsnorm(const void *x, void *residual, const void *w, void *out, in
     return launch_rmsnorm(x, residual, w, out, M, H, eps, as_stream(stream));
 }
 
+bi_status bi_rank_sum_rmsnorm(const void *const *parts, int32_t R, void *residual, const void *w, void *sum_out,
+                              void *out, int64_t M, int64_t H, float eps, bi_stream stream) {
+    if (R < 1 || R > 16 || M < 0 || M >= kI32Max || H < 8 || H > 65536 || !(eps >= 0.0f)) return BI_ERR_INVALID_ARG;
+    if (M == 0) return BI_OK;
+    if (!parts || !w || !out) return BI_ERR_INVALID_ARG;
+    for (int r = 0; r < R; ++r) {
+        if (!parts[r]) return BI_ERR_INVALID_ARG;
+        if (!aligned16(parts[r])) return BI_ERR_MISALIGNED;
+    }
+    if (H % 8 != 0) return BI_ERR_UNSUPPORTED;
+    if (!aligned16(w) || !aligned16(out) || (residual && !aligned16(residual)) || (sum_out && !aligned16(sum_out)))
+        return BI_ERR_MISALIGNED;
+    bi_status st = require_device();
+    if (st != BI_OK) return st;
+    return launch_rank_sum_rmsnorm(parts, R, residual, w, sum_out, out, M, H, eps, as_stream(stream));
+}
+
 bi_status bi_plan(int32_t op, int64_t M, int64_t N, int64_t K, int32_t num_sms, bi_plan_t *out) {
     if (!out || M < 0 || N < 0 || K < 0 || num_sms < 0) return BI_ERR_INVALID_ARG;
     int sms = num_sms;

@@ -57,6 +57,8 @@ bi_status launch_moe_combine(const void *Y, int64_t rows, const int32_t *pos, co
                              int64_t H, void *out, cudaStream_t s);
 bi_status launch_rmsnorm(const void *x, void *residual, const void *w, void *out, int64_t M, int64_t H,
                          float eps, cudaStream_t s);
+bi_status launch_rank_sum_rmsnorm(const void *const *parts, int32_t R, void *residual, const void *w, void *sum_out,
+                                  void *out, int64_t M, int64_t H, float eps, cudaStream_t s);
 bi_status launch_wait_timeout_check(uint32_t limit_us, cudaStream_t s);
 
 // Plans (M-independent except tiles_m and grid).

@@ -122,6 +122,68 @@ rmsnorm_kernel(const uint4 *x, uint4 *residual, const uint4 *__restrict__ w, uin
     }
 }
 
+// ---- Deterministic tensor-parallel all-reduce + RMSNorm: R ranks' partial
+// rows (all readable from this GPU) are summed in rank order 0, 1, ..., R-1 in
+// fp32 and rounded once to bf16 (the all-reduced row), then the residual add
+// and the RMSNorm above follow with the same tree. vLLM PR #51292 turns off
+// its fused all-reduce + RMSNorm under batch invariance because that kernel's
+// reduction order varies between runs; here the order is the rank index.
+constexpr int kMaxRanks = 16;
+struct RankParts {
+    const uint4 *p[kMaxRanks];
+};
+
+template <int T, int VPT, bool RESIDUAL>
+__global__ void __launch_bounds__(T)
+rank_sum_rmsnorm_kernel(const RankParts parts, int R, uint4 *residual, const uint4 *__restrict__ w, uint4 *sum_out,
+                        uint4 *out, int H, float eps) {
+    __shared__ float red[T / 32 + 1];
+    const int64_t row = blockIdx.x;
+    const int nvec = H >> 3;
+    const int t = threadIdx.x;
+    uint4 *rr = RESIDUAL ? residual + row * nvec : nullptr;
+    uint4 h[VPT];
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        const int j = t + T * i;
+        if (j < nvec) {
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int r = 0; r < R; ++r) {
+                const uint4 v = __ldcs(parts.p[r] + row * nvec + j);
+                const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    acc[2 * q] = __fadd_rn(acc[2 * q], bf_lo(vw[q]));
+                    acc[2 * q + 1] = __fadd_rn(acc[2 * q + 1], bf_hi(vw[q]));
+                }
+            }
+            uint4 a;
+            a.x = pack_bf16x2(__float_as_uint(acc[0]), __float_as_uint(acc[1]));
+            a.y = pack_bf16x2(__float_as_uint(acc[2]), __float_as_uint(acc[3]));
+            a.z = pack_bf16x2(__float_as_uint(acc[4]), __float_as_uint(acc[5]));
+            a.w = pack_bf16x2(__float_as_uint(acc[6]), __float_as_uint(acc[7]));
+            if (sum_out) __stcs(sum_out + row * nvec + j, a);
+            h[i] = RESIDUAL ? add_round(a, __ldcs(rr + j)) : a;
+        }
+    }
+    float ss = 0.0f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        const int j = t + T * i;
+        if (j < nvec) {
+            if (RESIDUAL) __stcs(rr + j, h[i]);
+            ss = sum_squares(h[i], ss);
+        }
+    }
+    const float r = row_scale<T>(ss, H, eps, red);
+    uint4 *orow = out + row * nvec;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        const int j = t + T * i;
+        if (j < nvec) __stcs(orow + j, scale(h[i], __ldg(w + j), r));
+    }
+}
+
 // Threads per row and vectors per thread, chosen from H alone.
 struct RowShape {
     int threads, vpt;
@@ -169,6 +231,37 @@ bi_status launch_res(const void *x, void *residual, const void *w, void *out, in
     }
 }
 
+template <int T, int VPT, bool RES>
+bi_status launch_rank_one(const RankParts &parts, int R, void *residual, const void *w, void *sum_out, void *out,
+                          int64_t M, int64_t H, float eps, cudaStream_t s) {
+    rank_sum_rmsnorm_kernel<T, VPT, RES><<<static_cast<unsigned>(M), T, 0, s>>>(
+        parts, R, static_cast<uint4 *>(residual), static_cast<const uint4 *>(w), static_cast<uint4 *>(sum_out),
+        static_cast<uint4 *>(out), static_cast<int>(H), eps);
+    return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
+}
+
+template <bool RES>
+bi_status launch_rank_res(const RankParts &parts, int R, void *residual, const void *w, void *sum_out, void *out,
+                          int64_t M, int64_t H, float eps, cudaStream_t s) {
+    const RowShape rs = row_shape(H);
+    if (rs.threads == 128) {
+        switch (rs.vpt) {
+            case 1: return launch_rank_one<128, 1, RES>(parts, R, residual, w, sum_out, out, M, H, eps, s);
+            case 2: return launch_rank_one<128, 2, RES>(parts, R, residual, w, sum_out, out, M, H, eps, s);
+            case 4: return launch_rank_one<128, 4, RES>(parts, R, residual, w, sum_out, out, M, H, eps, s);
+            case 8: return launch_rank_one<128, 8, RES>(parts, R, residual, w, sum_out, out, M, H, eps, s);
+            default: return launch_rank_one<128, 16, RES>(parts, R, residual, w, sum_out, out, M, H, eps, s);
+        }
+    }
+    switch (rs.vpt) {
+        case 1: return launch_rank_one<512, 1, RES>(parts, R, residual, w, sum_out, out, M, H, eps, s);
+        case 2: return launch_rank_one<512, 2, RES>(parts, R, residual, w, sum_out, out, M, H, eps, s);
+        case 4: return launch_rank_one<512, 4, RES>(parts, R, residual, w, sum_out, out, M, H, eps, s);
+        case 8: return launch_rank_one<512, 8, RES>(parts, R, residual, w, sum_out, out, M, H, eps, s);
+        default: return launch_rank_one<512, 16, RES>(parts, R, residual, w, sum_out, out, M, H, eps, s);
+    }
+}
+
 __global__ void wait_timeout_check_kernel(unsigned *status, unsigned long long limit_ns) {
     __shared__ uint64_t bar;
     if (threadIdx.x == 0) {
@@ -203,6 +296,14 @@ bi_status launch_rmsnorm(const void *x, void *residual, const void *w, void *out
                          cudaStream_t s) {
     return residual ? launch_res<true>(x, residual, w, out, M, H, eps, s)
                     : launch_res<false>(x, residual, w, out, M, H, eps, s);
+}
+
+bi_status launch_rank_sum_rmsnorm(const void *const *parts, int32_t R, void *residual, const void *w, void *sum_out,
+                                  void *out, int64_t M, int64_t H, float eps, cudaStream_t s) {
+    RankParts rp{};
+    for (int r = 0; r < R; ++r) rp.p[r] = static_cast<const uint4 *>(parts[r]);
+    return residual ? launch_rank_res<true>(rp, R, residual, w, sum_out, out, M, H, eps, s)
+                    : launch_rank_res<false>(rp, R, residual, w, sum_out, out, M, H, eps, s);
 }
 
 bi_status launch_wait_timeout_check(uint32_t limit_us, cudaStream_t s) {

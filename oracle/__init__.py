@@ -71,6 +71,7 @@ def _load():
             lib.oracle_moe_align.argtypes = [I64, ctypes.c_int32, ctypes.c_int32, P, P, P, P]
             lib.oracle_silu_mul.argtypes = [I64, I64, P, P]
             lib.oracle_moe_combine.argtypes = [I64, ctypes.c_int32, I64, P, P, P, P]
+            lib.oracle_rank_sum_rmsnorm.argtypes = [ctypes.c_int32, I64, I64, P, P, P, D, P, P, P]
             lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
             lib.oracle_e4m3_encode.restype = ctypes.c_uint
             lib.oracle_e2m1_encode.argtypes = [ctypes.c_float]
@@ -216,6 +217,26 @@ def e4m3_encode(v: float) -> int:
 
 def e2m1_encode(v: float) -> int:
     return int(_load().oracle_e2m1_encode(float(v)))
+
+
+def rank_sum_rmsnorm(parts, w, eps: float, residual=None):
+    """All-reduce of R ranks' bf16 partial rows (exact sum, one bf16 rounding),
+    then RMSNorm with optional residual add. parts: bf16 bits [R, M, H].
+    Returns (y fp64 [M, H], a_bits [M, H] all-reduced rows, h_bits or None)."""
+    parts, w = _c(parts, np.uint16), _c(w, np.uint16)
+    R, M, H = parts.shape
+    y = np.zeros((M, H), dtype=np.float64)
+    a = np.zeros((M, H), dtype=np.uint16)
+    h = None
+    rp = None
+    if residual is not None:
+        residual = _c(residual, np.uint16)
+        h = np.zeros((M, H), dtype=np.uint16)
+        rp = _p(residual)
+    if M:
+        _load().oracle_rank_sum_rmsnorm(R, M, H, _p(parts), rp, _p(w), float(eps), _p(y), _p(a),
+                                        _p(h) if h is not None else None)
+    return y, a, h
 
 
 def e2m1_value(code: int) -> float:

@@ -328,6 +328,43 @@ void oracle_moe_combine(int64_t T, int32_t k, int64_t H, const uint16_t *Y, cons
         }
 }
 
+/* ---- Deterministic tensor-parallel all-reduce followed by RMSNorm (the pair
+ * vLLM PR #51292 stops fusing under batch invariance: "a fixed-order reduction
+ * is bitwise-stable"). R ranks hold partial rows x_r; the all-reduced row is
+ *   a = bf16( x_0 + x_1 + ... + x_{R-1} )     (exact sum, one rounding)
+ * and then, as in oracle_rmsnorm: h = residual ? bf16(a + residual) : a,
+ *   y = h / sqrt(mean(h^2) + eps) * w.
+ * parts: bf16 [R][M][H]; a_out, h_out (nullable): bf16 bits; y: fp64 [M][H]. */
+void oracle_rank_sum_rmsnorm(int32_t R, int64_t M, int64_t H, const uint16_t *parts, const uint16_t *residual,
+                             const uint16_t *w, double eps, double *y, uint16_t *a_out, uint16_t *h_out)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < M; ++i) {
+        double ss = 0.0;
+        for (int64_t k = 0; k < H; ++k) {
+            double s = 0.0;
+            for (int32_t r = 0; r < R; ++r) s += bf16_to_double(parts[((int64_t)r * M + i) * H + k]);
+            uint16_t ab = double_to_bf16(s);
+            if (a_out) a_out[i * H + k] = ab;
+            double h = bf16_to_double(ab);
+            if (residual) {
+                uint16_t hb = double_to_bf16(h + bf16_to_double(residual[i * H + k]));
+                if (h_out) h_out[i * H + k] = hb;
+                h = bf16_to_double(hb);
+            }
+            ss += h * h;
+        }
+        double rinv = 1.0 / sqrt(ss / (double)H + eps);
+        for (int64_t k = 0; k < H; ++k) {
+            double s = 0.0;
+            for (int32_t r = 0; r < R; ++r) s += bf16_to_double(parts[((int64_t)r * M + i) * H + k]);
+            double h = bf16_to_double(double_to_bf16(s));
+            if (residual) h = bf16_to_double(double_to_bf16(h + bf16_to_double(residual[i * H + k])));
+            y[i * H + k] = h * rinv * bf16_to_double(w[k]);
+        }
+    }
+}
+
 /* RMSNorm with optional residual add, per row i:
  *   h = residual ? bf16(x + residual) : x         (the stored, rounded sum)
  *   y = h / sqrt( (1/H) sum_k h_k^2 + eps ) * w

@@ -26,7 +26,7 @@ def declared_functions():
 
 def test_header_declares_the_calls():
     names = declared_functions()
-    for n in ["bi_gemm_bf16", "bi_grouped_gemm_bf16", "bi_gemm_nvfp4", "bi_rmsnorm", "bi_plan", "bi_quantize_nvfp4", "bi_moe_topk_softmax", "bi_moe_align", "bi_moe_gather", "bi_silu_mul", "bi_moe_combine",
+    for n in ["bi_gemm_bf16", "bi_grouped_gemm_bf16", "bi_gemm_nvfp4", "bi_rmsnorm", "bi_plan", "bi_quantize_nvfp4", "bi_moe_topk_softmax", "bi_moe_align", "bi_moe_gather", "bi_silu_mul", "bi_moe_combine", "bi_rank_sum_rmsnorm",
               "bi_device_status", "bi_status_string", "bi_version", "bi_check_wait_timeout"]:
         assert n in names
 
@@ -132,5 +132,9 @@ def test_other_calls_reject_bad_arguments(lib):
     assert so.bi_moe_gather(FAKE, 4, 100, FAKE, 8, FAKE, None) == 2                      # H % 8
     assert so.bi_silu_mul(FAKE, 4, 12, FAKE, None) == 2                                  # I % 8
     assert so.bi_moe_combine(FAKE, 8, FAKE, FAKE, 4, 0, 64, FAKE, None) == 1              # k < 1
+    ptrs2 = (ctypes.c_void_p * 2)(FAKE, FAKE + 8)
+    assert so.bi_rank_sum_rmsnorm(ptrs2, 2, None, FAKE, None, FAKE, 4, 4096, f(1e-6), None) == 3  # part align
+    assert so.bi_rank_sum_rmsnorm(ptrs2, 0, None, FAKE, None, FAKE, 4, 4096, f(1e-6), None) == 1  # R < 1
+    assert so.bi_rank_sum_rmsnorm(ptrs2, 17, None, FAKE, None, FAKE, 4, 4096, f(1e-6), None) == 1  # R > 16
     assert so.bi_check_wait_timeout(0, None) == 1
     assert so.bi_plan(99, 1, 1, 1, 152, ctypes.byref(lib.Plan())) == 1

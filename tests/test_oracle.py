@@ -392,6 +392,28 @@ def test_rmsnorm_residual_is_rounded_sum():
     assert np.allclose(y[0], want, rtol=1e-14)
 
 
+def test_rank_sum_rmsnorm_reduces_to_rmsnorm_and_sums_exactly():
+    x, res, w, _ = syn.rmsnorm_inputs(6, 256, seed=11)
+    # one rank: exactly RMSNorm
+    y1, a1, h1 = oracle.rank_sum_rmsnorm(x[None], w, 1e-6, residual=res)
+    y0, h0 = oracle.rmsnorm(x, w, 1e-6, residual=res)
+    assert np.array_equal(a1, x) and np.array_equal(h1, h0) and np.array_equal(y1, y0)
+    # x and -x cancel exactly: the all-reduced rows are zero, the output is zero
+    neg = x ^ np.uint16(0x8000)
+    y2, a2, _ = oracle.rank_sum_rmsnorm(np.stack([x, neg]), w, 1e-6)
+    assert np.all(syn.bf16_bits_to_f32(a2) == 0) and np.all(y2 == 0)
+    # small integers: the all-reduced value is the integer sum (exact in bf16 below 256)
+    parts = syn.integer_bf16(3, 0, (4, 5, 64), lo=-30, hi=30)
+    _, a3, _ = oracle.rank_sum_rmsnorm(parts, w[:64], 1e-6)
+    assert np.array_equal(syn.bf16_bits_to_f32(a3), syn.bf16_bits_to_f32(parts).sum(axis=0))
+    # the all-reduce rounds once: 1 + 2^-8 + 2^-8 = 1 + 2^-7 exactly (two partial
+    # roundings would give 1.0)
+    one = syn.to_bf16_bits(np.array([[[1.0] * 8]], dtype=np.float32))
+    tiny = syn.to_bf16_bits(np.array([[[2.0 ** -8] * 8]], dtype=np.float32))
+    _, a4, _ = oracle.rank_sum_rmsnorm(np.concatenate([one, tiny, tiny]), w[:8], 1e-6)
+    assert np.all(a4 == 0x3F81)
+
+
 def test_rmsnorm_rows_independent():
     x, res, w, _ = syn.rmsnorm_inputs(7, 128, seed=10)
     full, hfull = oracle.rmsnorm(x, w, 1e-6, residual=res)

@@ -1,0 +1,59 @@
+"""bi_rank_sum_rmsnorm on one GPU with R emulated ranks (all partials in this
+GPU's memory, reduced by one kernel): parity with the oracle, R = 1 equals
+bi_rmsnorm bit for bit, rows are independent, repeated runs agree."""
+import numpy as np
+import pytest
+
+import bi_synth as syn
+import oracle
+from util import assert_close_rel, bits_of, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+EPS = 1e-6
+
+
+def parts_for(R, M, H, seed=0):
+    return np.stack([syn.to_bf16_bits(syn.normal_rows(seed + r, syn.TID_X, M, H)) for r in range(R)])
+
+
+@pytest.mark.parametrize("R", [1, 2, 4, 8])
+@pytest.mark.parametrize("M", [1, 4097])
+def test_parity(bi, R, M):
+    import torch
+    H = 4096
+    P = parts_for(R, M, H)
+    _, res, w, _ = syn.rmsnorm_inputs(M, H, seed=1)
+    pd = [to_dev_bf16(P[r]) for r in range(R)]
+    rd = to_dev_bf16(res)
+    a_out = torch.empty_like(pd[0])
+    out = bi.rank_sum_rmsnorm(pd, to_dev_bf16(w), EPS, residual=rd, sum_out=a_out)
+    y, a, h = oracle.rank_sum_rmsnorm(P, w, EPS, residual=res)
+    ga = syn.bf16_bits_to_f32(bits_of(a_out)).astype(np.float64)
+    # one fp32 rounding of the rank-ordered sum, then bf16: within one bf16 step of the exact rounding
+    assert_close_rel(ga, syn.bf16_bits_to_f32(a).astype(np.float64), 2.0 ** -7, 1e-30, "all-reduced rows")
+    exact = np.mean(bits_of(a_out) == a)
+    assert exact > 0.999, f"only {exact:.4f} of all-reduced values are bit-exact"
+    assert_close_rel(syn.bf16_bits_to_f32(bits_of(out)).astype(np.float64), y, 1.6e-2, 1e-6, "out")
+    assert bi.device_status() == bi.BI_OK
+
+
+def test_one_rank_is_rmsnorm(bi):
+    M, H = 300, 4096
+    x, res, w, _ = syn.rmsnorm_inputs(M, H, seed=2)
+    a = bits_of(bi.rank_sum_rmsnorm([to_dev_bf16(x)], to_dev_bf16(w), EPS, residual=to_dev_bf16(res)))
+    b = bits_of(bi.rmsnorm(to_dev_bf16(x), to_dev_bf16(w), EPS, residual=to_dev_bf16(res)))
+    assert np.array_equal(a, b)
+
+
+def test_rows_independent_and_repeatable(bi):
+    R, M, H = 4, 200, 2048
+    P = parts_for(R, M, H, seed=5)
+    _, _, w, _ = syn.rmsnorm_inputs(M, H, seed=6)
+    wd = to_dev_bf16(w)
+    full = bits_of(bi.rank_sum_rmsnorm([to_dev_bf16(P[r]) for r in range(R)], wd, EPS))
+    for i in (0, 99, 199):
+        one = bits_of(bi.rank_sum_rmsnorm([to_dev_bf16(P[r][i:i + 1]) for r in range(R)], wd, EPS))
+        assert np.array_equal(one[0], full[i])
+    outs = {bits_of(bi.rank_sum_rmsnorm([to_dev_bf16(P[r]) for r in range(R)], wd, EPS)).tobytes()
+            for _ in range(8)}
+    assert len(outs) == 1
