@@ -206,9 +206,10 @@ def nvfp4_global_scale(x: np.ndarray) -> np.float32:
 def nvfp4_quantize(x: np.ndarray, gs: np.float32):
     """Quantise fp32 [R, K] (K % 16 == 0) with global scale gs.
 
-    Per 16-element block: s = e4m3(amax_block / 6 * gs); q = e2m1(x * gs / s),
-    q = 0 where s decodes to 0. Returns (packed codes u8 [R, K/2] with the even k
-    in the low nibble, block scales u8 [R, K/16] row-major)."""
+    Per 16-element block: s = e4m3(amax_block / 6 * gs); q = e2m1(x * (gs / s)),
+    q = 0 where s decodes to 0 (fp32: one division per block, one multiply per
+    element). Returns (packed codes u8 [R, K/2] with the even k in the low
+    nibble, block scales u8 [R, K/16] row-major)."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     R, K = x.shape
     assert K % 16 == 0
@@ -217,7 +218,8 @@ def nvfp4_quantize(x: np.ndarray, gs: np.float32):
     s_code = e4m3_encode_pos((amax / np.float32(6.0)) * gs)
     s_val = _E4M3[s_code].astype(np.float32)
     with np.errstate(divide="ignore", invalid="ignore"):
-        scaled = (blocks * gs) / s_val[:, :, None]
+        inv = np.float32(gs) / s_val
+        scaled = blocks * inv[:, :, None]
     scaled = np.where(s_val[:, :, None] == 0, np.float32(0), scaled)
     scaled = np.clip(scaled, -6.0, 6.0)
     q = e2m1_encode(scaled).reshape(R, K)

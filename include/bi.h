@@ -131,7 +131,7 @@ BI_API bi_status bi_gemm_nvfp4(const uint8_t *A, const uint8_t *A_sf, const uint
  * The activation quantiser of vLLM PR #39912's test (scaled_fp4_quant with
  * the tensor's global scale). Per row and 16-element block, with gs = global_scale:
  *   s = e4m3( (amax / 6) * gs )       fp32 arithmetic, round to nearest even, saturating at 448
- *   q = e2m1( (x * gs) / value(s) )   round to nearest even, saturating at 6; q = 0 where value(s) = 0
+ *   q = e2m1( x * (gs / value(s)) )   round to nearest even, saturating at 6; q = 0 where value(s) = 0
  * A zero magnitude is stored as code 0 (never code 8). Row-local: a row's
  * codes and scales do not depend on the other rows (the global scale is an
  * input, computed once for the whole tensor as in the page's test).

@@ -270,12 +270,12 @@ bi_status bi_plan(int32_t op, int64_t M, int64_t N, int64_t K, int32_t num_sms, 
         case BI_OP_GEMM_NVFP4: plan_gemm_nvfp4(M, N, K, sms, out); return BI_OK;
         case BI_OP_QUANTIZE_NVFP4:
             out->op = BI_OP_QUANTIZE_NVFP4;
-            out->block_m = 1; out->block_n = 64; out->block_k = 16;   /* 64 elements (4 scale blocks) per thread */
-            out->k_steps = static_cast<int32_t>(K / 64);
+            out->block_m = 1; out->block_n = 16; out->block_k = 16;   /* one 16-element scale block per thread */
+            out->k_steps = static_cast<int32_t>(K / 16);
             out->split_k = 1; out->stages = 1; out->threads = 256;
-            out->tiles_m = M; out->tiles_n = K / 64;
+            out->tiles_m = M; out->tiles_n = K / 16;
             {
-                const int64_t g = (M * (K / 64) + 255) / 256, cap = static_cast<int64_t>(sms) * 8;
+                const int64_t g = (M * (K / 16) + 255) / 256, cap = static_cast<int64_t>(sms) * 16;
                 out->grid = static_cast<int32_t>(g < cap ? g : cap);
             }
             return BI_OK;   /* N unused, K = columns */

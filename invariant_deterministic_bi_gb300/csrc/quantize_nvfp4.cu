@@ -4,14 +4,15 @@
 // ("NVFP4 CUTLASS batch invariant mode", test code: scaled_fp4_quant with the
 // tensor's global scale). Per row and 16-element block, with global scale gs:
 //   s = e4m3( (amax / 6) * gs )        round to nearest even, saturating at 448
-//   q = e2m1( (x * gs) / value(s) )    round to nearest even, saturating at 6; q = 0 if value(s) = 0
+//   q = e2m1( x * (gs / value(s)) )    round to nearest even, saturating at 6; q = 0 if value(s) = 0
 // Every output depends only on its own row and gs, so a row quantises to the
 // same bytes whatever the batch. Zero magnitudes are stored as code 0 (never
 // the negative-zero code 8).
 //
-// One thread per 64 elements (four blocks): 128-byte coalesced loads, 32 bytes
-// of packed codes and one 32-bit word of four scales, written straight into
-// the interleaved 128x4 scale layout bi_gemm_nvfp4 reads.
+// One thread per 16-element block: a warp reads 1 KB of consecutive elements
+// (two 16-byte loads per thread) and writes 256 consecutive bytes of packed
+// codes; each thread stores its scale byte straight into the interleaved
+// 128x4 scale layout bi_gemm_nvfp4 reads.
 #include <cuda_bf16.h>
 
 #include "bi_internal.h"
@@ -61,49 +62,39 @@ __device__ __forceinline__ uint32_t to_e2m1x8(const float (&y)[8]) {
 __global__ void __launch_bounds__(kThreads)
 quantize_nvfp4_kernel(const uint4 *__restrict__ X, int64_t ldx_vec, uint8_t *__restrict__ Q, uint8_t *__restrict__ SF,
                       int64_t M, int K, float gs) {
-    const int groups = K / 64;                       // 64-element groups per row = scale words per row
-    const int64_t total = M * groups;
+    const int blocks = K / 16;                       // 16-element scale blocks per row
+    const int atoms = K / 64;                        // 512-byte scale atoms per 128-row group
+    const int64_t total = M * blocks;
     for (int64_t gid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; gid < total;
          gid += static_cast<int64_t>(gridDim.x) * kThreads) {
-        const int64_t r = gid / groups;
-        const int g = static_cast<int>(gid - r * groups);
-        const uint4 *src = X + r * ldx_vec + g * 8;
-        uint4 v[8];
+        const int64_t r = gid / blocks;
+        const int c = static_cast<int>(gid - r * blocks);
+        const uint4 *src = X + r * ldx_vec + c * 2;
+        const uint4 v0 = __ldcs(src), v1 = __ldcs(src + 1);
+        const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        float x[16];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = __ldcs(src + i);
-        uint32_t codes[8];
-        uint32_t scale_word = 0;
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            float x[16];
-            const uint32_t w[8] = {v[2 * b].x, v[2 * b].y, v[2 * b].z, v[2 * b].w,
-                                   v[2 * b + 1].x, v[2 * b + 1].y, v[2 * b + 1].z, v[2 * b + 1].w};
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                x[2 * i] = bf_lo(w[i]);
-                x[2 * i + 1] = bf_hi(w[i]);
-            }
-            float amax = 0.0f;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
-            const uint32_t s = to_e4m3(__fmul_rn(__fdiv_rn(amax, 6.0f), gs));
-            const float sv = from_e4m3(s);
-            scale_word |= s << (8 * b);
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                float y[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    y[i] = sv == 0.0f ? 0.0f : __fdiv_rn(__fmul_rn(x[8 * h + i], gs), sv);
-                codes[2 * b + h] = to_e2m1x8(y);
-            }
+        for (int i = 0; i < 8; ++i) {
+            x[2 * i] = bf_lo(w[i]);
+            x[2 * i + 1] = bf_hi(w[i]);
         }
-        uint4 *dst = reinterpret_cast<uint4 *>(Q + r * (K / 2) + g * 32);
-        __stcs(dst, make_uint4(codes[0], codes[1], codes[2], codes[3]));
-        __stcs(dst + 1, make_uint4(codes[4], codes[5], codes[6], codes[7]));
-        const int64_t atom = (r / 128) * groups + g;
-        const int64_t off = atom * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4;
-        *reinterpret_cast<uint32_t *>(SF + off) = scale_word;
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+        const uint32_t s = to_e4m3(__fmul_rn(__fdiv_rn(amax, 6.0f), gs));
+        const float sv = from_e4m3(s);
+        const float inv = sv == 0.0f ? 0.0f : __fdiv_rn(gs, sv);    // one division per block
+        uint32_t codes[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float y[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) y[i] = __fmul_rn(x[8 * h + i], inv);
+            codes[h] = to_e2m1x8(y);
+        }
+        *reinterpret_cast<uint2 *>(Q + r * (K / 2) + c * 8) = make_uint2(codes[0], codes[1]);
+        const int64_t atom = (r / 128) * atoms + c / 4;
+        SF[atom * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4 + c % 4] = static_cast<uint8_t>(s);
     }
 }
 
@@ -115,9 +106,9 @@ bi_status launch_quantize_nvfp4(const void *X, int64_t ldx, float gs, uint8_t *Q
     const DeviceInfo *info;
     bi_status st = current_device(&dev, &info);
     if (st != BI_OK) return st;
-    const int64_t threads = M * (K / 64);
+    const int64_t threads = M * (K / 16);
     int64_t grid = (threads + kThreads - 1) / kThreads;
-    const int64_t cap = static_cast<int64_t>(info->sm_count) * 8;
+    const int64_t cap = static_cast<int64_t>(info->sm_count) * 16;
     if (grid > cap) grid = cap;
     quantize_nvfp4_kernel<<<static_cast<unsigned>(grid), kThreads, 0, s>>>(
         static_cast<const uint4 *>(X), ldx / 8, Q, Q_sf, M, static_cast<int>(K), gs);

@@ -171,7 +171,7 @@ void oracle_gemm_nvfp4(int64_t M, int64_t N, int64_t K,
  * Per row r and 16-element block b, with the per-tensor global scale gs:
  *   amax = max |x| over the block                          (exact)
  *   s    = e4m3_rne_satfinite( (amax / 6) * gs )           (fp32 ops, then encode)
- *   q_k  = e2m1_rne( clamp( (x_k * gs) / value(s), -6, 6 ) )   (fp32 ops), q = 0 if value(s) == 0
+ *   q_k  = e2m1_rne( clamp( x_k * (gs / value(s)), -6, 6 ) )   (fp32 ops), q = 0 if value(s) == 0
  * Floating point decides integer codes here, so the arithmetic is binary32
  * (the precision the kernel uses), one rounding per operation (-ffp-contract=off).
  * Encoders are written from the format definitions: round to the nearest
@@ -225,13 +225,13 @@ void oracle_quantize_nvfp4(int64_t M, int64_t K, const uint16_t *X, float gs, ui
             unsigned s = e4m3_encode_satfinite(t * gs);
             float sv = (float)e4m3_to_double(s);
             S[i * (K / 16) + b] = (uint8_t)s;
+            volatile float inv = (sv == 0.0f) ? 0.0f : gs / sv;
             for (int k = 0; k < 16; k += 2) {
                 unsigned c[2];
                 for (int h = 0; h < 2; ++h) {
                     float x = (float)bf16_to_double(X[i * K + b * 16 + k + h]);
                     if (sv == 0.0f) { c[h] = 0u; continue; }
-                    volatile float xs = x * gs;
-                    float y = xs / sv;
+                    float y = x * inv;
                     y = fminf(fmaxf(y, -6.0f), 6.0f);
                     c[h] = oracle_e2m1_encode(y);
                 }
