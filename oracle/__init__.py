@@ -72,6 +72,8 @@ def _load():
             lib.oracle_silu_mul.argtypes = [I64, I64, P, P]
             lib.oracle_moe_combine.argtypes = [I64, ctypes.c_int32, I64, P, P, P, P]
             lib.oracle_rank_sum_rmsnorm.argtypes = [ctypes.c_int32, I64, I64, P, P, P, D, P, P, P]
+            lib.oracle_attention_decode.argtypes = [I64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                                    ctypes.c_int32, ctypes.c_int32, P, P, P, P, P, D, P]
             lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
             lib.oracle_e4m3_encode.restype = ctypes.c_uint
             lib.oracle_e2m1_encode.argtypes = [ctypes.c_float]
@@ -237,6 +239,23 @@ def rank_sum_rmsnorm(parts, w, eps: float, residual=None):
         _load().oracle_rank_sum_rmsnorm(R, M, H, _p(parts), rp, _p(w), float(eps), _p(y), _p(a),
                                         _p(h) if h is not None else None)
     return y, a, h
+
+
+def attention_decode(Q, K, V, table, lens, scale: float):
+    """Softmax attention of one query token per sequence over a paged KV cache (fp64).
+
+    Q bf16 [B, Hq, D]; K, V bf16 [blocks, bs, Hkv, D]; table int32 [B, max_blocks];
+    lens int32 [B]. Returns O fp64 [B, Hq, D]."""
+    Q, K, V = _c(Q, np.uint16), _c(K, np.uint16), _c(V, np.uint16)
+    table, lens = _c(table, np.int32), _c(lens, np.int32)
+    B, Hq, D = Q.shape
+    _, bs, Hkv, D2 = K.shape
+    assert D2 == D and V.shape == K.shape and Hq % Hkv == 0 and table.shape[0] == B and np.all(lens >= 1)
+    O = np.zeros((B, Hq, D), dtype=np.float64)
+    if B:
+        _load().oracle_attention_decode(B, Hq, Hkv, D, bs, table.shape[1], _p(Q), _p(K), _p(V), _p(table),
+                                        _p(lens), float(scale), _p(O))
+    return O
 
 
 def e2m1_value(code: int) -> float:

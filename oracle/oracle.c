@@ -365,6 +365,51 @@ void oracle_rank_sum_rmsnorm(int32_t R, int64_t M, int64_t H, const uint16_t *pa
     }
 }
 
+/* ---- Decode attention over a paged KV cache (batch-invariant attention is on
+ * the tracking issue's TODO list: FlashInfer, TRITON_MLA, FLASHINFER_MLA; the
+ * vllm-ascend guide's batch-invariant attention operators).
+ * For sequence b, query head h (KV head g = h / (Hq / Hkv)) and its L_b
+ * cached tokens j (token j of sequence b lives in block table[b][j / bs] at
+ * offset j % bs):
+ *   s_j = scale * sum_d q[b][h][d] * k_j[g][d]
+ *   o[b][h][d] = sum_j softmax(s)_j * v_j[g][d]          (fp64, exact softmax)
+ * Q: bf16 [B][Hq][D]; K, V: bf16 [blocks][bs][Hkv][D]; table: int32 [B][max_blocks];
+ * lens: int32 [B] (>= 1); O: fp64 [B][Hq][D]. */
+void oracle_attention_decode(int64_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t bs, int32_t max_blocks,
+                             const uint16_t *Q, const uint16_t *K, const uint16_t *V, const int32_t *table,
+                             const int32_t *lens, double scale, double *O)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t bh = 0; bh < B * Hq; ++bh) {
+        const int64_t b = bh / Hq;
+        const int32_t h = (int32_t)(bh % Hq), g = h / (Hq / Hkv);
+        const int32_t L = lens[b];
+        double mx = -INFINITY;
+        for (int32_t j = 0; j < L; ++j) {
+            const int64_t blk = table[b * max_blocks + j / bs];
+            const uint16_t *k = K + ((blk * bs + j % bs) * (int64_t)Hkv + g) * D;
+            double s = 0.0;
+            for (int32_t d = 0; d < D; ++d) s += bf16_to_double(Q[(b * Hq + h) * D + d]) * bf16_to_double(k[d]);
+            s *= scale;
+            if (s > mx) mx = s;
+        }
+        double den = 0.0;
+        double *o = O + (b * Hq + h) * D;
+        for (int32_t d = 0; d < D; ++d) o[d] = 0.0;
+        for (int32_t j = 0; j < L; ++j) {
+            const int64_t blk = table[b * max_blocks + j / bs];
+            const uint16_t *k = K + ((blk * bs + j % bs) * (int64_t)Hkv + g) * D;
+            const uint16_t *v = V + ((blk * bs + j % bs) * (int64_t)Hkv + g) * D;
+            double s = 0.0;
+            for (int32_t d = 0; d < D; ++d) s += bf16_to_double(Q[(b * Hq + h) * D + d]) * bf16_to_double(k[d]);
+            const double p = exp(s * scale - mx);
+            den += p;
+            for (int32_t d = 0; d < D; ++d) o[d] += p * bf16_to_double(v[d]);
+        }
+        for (int32_t d = 0; d < D; ++d) o[d] /= den;
+    }
+}
+
 /* RMSNorm with optional residual add, per row i:
  *   h = residual ? bf16(x + residual) : x         (the stored, rounded sum)
  *   y = h / sqrt( (1/H) sum_k h_k^2 + eps ) * w

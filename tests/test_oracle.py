@@ -346,6 +346,71 @@ def test_combine_bruteforce():
         assert [Fraction(v) for v in out[t]] == list(ref)
 
 
+# ------------------------------------------------------------ attention
+
+def _paged(B, L, Hkv, D, bs, seed, lens=None):
+    """Random contiguous K/V per sequence, stored in shuffled physical blocks."""
+    lens = np.full(B, L, dtype=np.int32) if lens is None else np.asarray(lens, dtype=np.int32)
+    nb = -(-lens.max() // bs)
+    blocks = B * nb
+    K = syn.to_bf16_bits(syn.normal_rows(seed, 0, blocks * bs, Hkv * D)).reshape(blocks, bs, Hkv, D)
+    V = syn.to_bf16_bits(syn.normal_rows(seed, 1, blocks * bs, Hkv * D)).reshape(blocks, bs, Hkv, D)
+    table = syn.rng(seed, 2).permutation(blocks).astype(np.int32).reshape(B, nb)
+    return K, V, table, lens
+
+
+def _dense(K, V, table, lens, b):
+    bs = K.shape[1]
+    L = lens[b]
+    idx = [(table[b, j // bs], j % bs) for j in range(L)]
+    return (np.stack([K[p, o] for p, o in idx]), np.stack([V[p, o] for p, o in idx]))   # [L, Hkv, D]
+
+
+def test_attention_single_token_and_uniform_keys():
+    B, Hq, Hkv, D, bs = 1, 4, 2, 16, 4
+    Q = syn.to_bf16_bits(syn.normal_rows(1, 0, B * Hq, D)).reshape(B, Hq, D)
+    K, V, table, lens = _paged(B, 1, Hkv, D, bs, seed=2)
+    O = oracle.attention_decode(Q, K, V, table, lens, 0.125)
+    k0, v0 = _dense(K, V, table, lens, 0)
+    for h in range(Hq):
+        assert np.array_equal(O[0, h], syn.bf16_bits_to_f32(v0[0, h // 2]).astype(np.float64))
+    # identical keys: uniform weights, output = mean of the values (integers, L = 4: exact)
+    K4 = np.zeros((1, 4, Hkv, D), dtype=np.uint16) + syn.to_bf16_bits(np.float32(0.5))
+    V4 = syn.integer_bf16(3, 0, (1, 4, Hkv, D))
+    O4 = oracle.attention_decode(Q, K4, V4, np.zeros((1, 1), np.int32), np.array([4], np.int32), 1.0)
+    for h in range(Hq):
+        assert np.array_equal(O4[0, h], syn.bf16_bits_to_f32(V4[0, :, h // 2]).astype(np.float64).mean(axis=0))
+
+
+def test_attention_matches_dense_numpy():
+    scipy = pytest.importorskip("scipy.special")
+    B, Hq, Hkv, D, bs = 3, 8, 2, 64, 16
+    lens = [37, 1, 100]
+    Q = syn.to_bf16_bits(syn.normal_rows(4, 0, B * Hq, D)).reshape(B, Hq, D)
+    K, V, table, lens = _paged(B, 0, Hkv, D, bs, seed=5, lens=lens)
+    scale = 1 / np.sqrt(D)
+    O = oracle.attention_decode(Q, K, V, table, lens, scale)
+    for b in range(B):
+        kd, vd = _dense(K, V, table, lens, b)
+        kf = syn.bf16_bits_to_f32(kd).astype(np.float64)
+        vf = syn.bf16_bits_to_f32(vd).astype(np.float64)
+        for h in range(Hq):
+            q = syn.bf16_bits_to_f32(Q[b, h]).astype(np.float64)
+            p = scipy.softmax(kf[:, h // 4] @ q * scale)
+            assert np.allclose(O[b, h], p @ vf[:, h // 4], rtol=1e-12, atol=1e-14)
+
+
+def test_attention_block_placement_does_not_matter():
+    B, Hq, Hkv, D, bs = 2, 4, 1, 32, 8
+    Q = syn.to_bf16_bits(syn.normal_rows(6, 0, B * Hq, D)).reshape(B, Hq, D)
+    K, V, table, lens = _paged(B, 50, Hkv, D, bs, seed=7)
+    O = oracle.attention_decode(Q, K, V, table, lens, 0.2)
+    perm = syn.rng(8, 0).permutation(K.shape[0])
+    inv = np.argsort(perm)
+    O2 = oracle.attention_decode(Q, K[perm], V[perm], inv[table].astype(np.int32), lens, 0.2)
+    assert np.array_equal(O, O2)
+
+
 # ----------------------------------------------------------------- RMSNorm
 
 def test_rmsnorm_golden_cases():
