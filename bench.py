@@ -524,6 +524,38 @@ def moe_layer_sweep(bi, peaks):
     return out
 
 
+ATTN_B = [1, 8, 64]
+ATTN_L = 4096
+
+
+def attention_sweep(bi, peaks):
+    """Decode attention, Qwen3-8B heads (32 q, 8 kv, dim 128), paged KV (block 16),
+    every sequence 4096 tokens: KV GB/s against HBM (KV bytes dominate)."""
+    import torch
+    Hq, Hkv, D, bs = 32, 8, 128, 16
+    rows = []
+    g = torch.Generator(device="cuda").manual_seed(0)
+    for B in ATTN_B:
+        nb = ATTN_L // bs
+        blocks = B * nb
+        K = torch.randn((blocks, bs, Hkv, D), device="cuda", generator=g).to(torch.bfloat16)
+        V = torch.randn((blocks, bs, Hkv, D), device="cuda", generator=g).to(torch.bfloat16)
+        table = torch.randperm(blocks, device="cuda", generator=g).to(torch.int32).view(B, nb)
+        lens = torch.full((B,), ATTN_L, dtype=torch.int32, device="cuda")
+        Q = torch.randn((B, Hq, D), device="cuda", generator=g).to(torch.bfloat16)
+        ws = torch.empty(bi.attention_decode_workspace_size(B, Hq, ATTN_L), dtype=torch.uint8, device="cuda")
+        O = torch.empty_like(Q)
+        t = time_fn(lambda: bi.attention_decode(Q, K, V, table, lens, ATTN_L, D ** -0.5, workspace=ws, O=O),
+                    50 if B <= 8 else 10)
+        kv_bytes = 2.0 * B * ATTN_L * Hkv * D * 2
+        gbs = kv_bytes / (t * 1e-3) / 1e9
+        rows.append({"B": B, "L": ATTN_L, "us": round(t * 1e3, 2), "kv_gbs": round(gbs, 0),
+                     "frac_hbm_measured": round(gbs / peaks["hbm_gbs"], 3)})
+        del K, V, table, lens, Q, ws, O
+    torch.cuda.empty_cache()
+    return rows
+
+
 def cpu_baseline(rows: int):
     """The fp64 oracle on a bounded sample of the step: `rows` rows of every
     GEMM of the step and of both RMSNorms, on the host's cores."""
@@ -632,6 +664,7 @@ def run_ours(args, dist):
         breakdown["gemm_nvfp4"] = nvfp4_sweep(bi, peaks)
         breakdown["quantize_nvfp4"] = quant_sweep(bi, peaks)
         breakdown["moe_layer"] = moe_layer_sweep(bi, peaks)
+        breakdown["attention_decode"] = attention_sweep(bi, peaks)
         if bi.device_status() != bi.BI_OK:
             raise RuntimeError("device status after breakdown")
 

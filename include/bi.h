@@ -247,6 +247,40 @@ BI_API bi_status bi_rmsnorm(const void *x, void *residual, const void *w, void *
 BI_API bi_status bi_rank_sum_rmsnorm(const void *const *parts, int32_t R, void *residual, const void *w,
                                      void *sum_out, void *out, int64_t M, int64_t H, float eps, bi_stream stream);
 
+/*
+ * bi_attention_decode -- batch-invariant decode attention over a paged KV cache.
+ *
+ * Batch-invariant attention is on the vLLM tracking issue's TODO list
+ * (FlashInfer, TRITON_MLA, FLASHINFER_MLA) and the vllm-ascend guide ships
+ * batch-invariant attention operators. One query token per sequence b and
+ * query head h (KV head g = h / (Hq/Hkv)), over the sequence's seq_lens[b]
+ * cached tokens; token j of sequence b sits in physical block
+ * block_table[b][j / block_size] at offset j % block_size:
+ *   O[b][h] = sum_j softmax_j(scale * q.k_j) v_j
+ * The KV range is split into fixed 256-token chunks by position alone (never
+ * by batch size); each chunk is reduced in a fixed order and the chunks are
+ * merged in chunk order, so a sequence's output does not depend on the batch.
+ *
+ *   Q         bf16 [B][Hq][128]
+ *   K_cache   bf16 [num_blocks][block_size][Hkv][128]; V_cache likewise
+ *   block_table int32 [B][max_blocks_per_seq]; seq_lens int32 [B] (device)
+ *   workspace caller-owned device scratch of at least
+ *             bi_attention_decode_workspace_size(B, Hq, max_seq_len) bytes
+ *             (fp32 per-chunk partial results); contents need not be initialised
+ *   O         bf16 [B][Hq][128]
+ * A sequence with seq_lens outside [1, max_seq_len] (or longer than its table)
+ * is skipped, a block index outside [0, num_blocks) is ignored, and the device
+ * status becomes BI_ERR_INVALID_ARG.
+ * Requirements: head_dim == 128; Hq % Hkv == 0 and Hq / Hkv in {1, 2, 4, 8};
+ * 1 <= B <= 65535; block_size >= 1; max_seq_len >= 1.
+ */
+BI_API int64_t bi_attention_decode_workspace_size(int64_t B, int32_t Hq, int32_t max_seq_len);
+BI_API bi_status bi_attention_decode(const void *Q, const void *K_cache, const void *V_cache,
+                                     const int32_t *block_table, int32_t max_blocks_per_seq, int64_t num_blocks,
+                                     const int32_t *seq_lens, int64_t B, int32_t Hq, int32_t Hkv,
+                                     int32_t head_dim, int32_t block_size, int32_t max_seq_len, float scale,
+                                     void *workspace, int64_t workspace_bytes, void *O, bi_stream stream);
+
 /* Operation ids for bi_plan. */
 enum { BI_OP_GEMM_BF16 = 0, BI_OP_GROUPED_GEMM_BF16 = 1, BI_OP_GEMM_NVFP4 = 2, BI_OP_RMSNORM = 3,
        BI_OP_QUANTIZE_NVFP4 = 4 };

@@ -68,6 +68,8 @@ def load() -> ctypes.CDLL:
             "bi_silu_mul": [P, I64, I64, P, P],
             "bi_moe_combine": [P, I64, P, P, I64, I32, I64, P, P],
             "bi_rank_sum_rmsnorm": [P, I32, P, P, P, P, I64, I64, F, P],
+            "bi_attention_decode": [P, P, P, P, I32, I64, P, I64, I32, I32, I32, I32, I32, F, P, I64, P, P],
+            "bi_attention_decode_workspace_size": [I64, I32, I32],
             "bi_plan": [I32, I64, I64, I64, I32, ctypes.POINTER(Plan)],
             "bi_device_status": [P],
             "bi_check_wait_timeout": [ctypes.c_uint32, P],
@@ -79,6 +81,7 @@ def load() -> ctypes.CDLL:
             fn.argtypes = args
             fn.restype = ctypes.c_int
         lib.bi_status_string.restype = ctypes.c_char_p
+        lib.bi_attention_decode_workspace_size.restype = ctypes.c_int64
         _lib = lib
         return lib
 
@@ -316,6 +319,39 @@ def rank_sum_rmsnorm(parts, w, eps: float, residual=None, sum_out=None, out=None
                                       _ptr(sum_out) if sum_out is not None else None, _ptr(out), M, H, float(eps),
                                       _stream(stream)), "bi_rank_sum_rmsnorm")
     return out
+
+
+def attention_decode_workspace_size(B: int, Hq: int, max_seq_len: int) -> int:
+    return int(load().bi_attention_decode_workspace_size(B, Hq, max_seq_len))
+
+
+def attention_decode(Q, K_cache, V_cache, block_table, seq_lens, max_seq_len: int, scale: float,
+                     workspace=None, O=None, stream=None):
+    """Batch-invariant decode attention over a paged KV cache (see bi.h).
+
+    Q bf16 [B, Hq, 128]; K_cache, V_cache bf16 [blocks, block_size, Hkv, 128];
+    block_table int32 [B, max_blocks]; seq_lens int32 [B]. The workspace
+    (uint8, device) is allocated with torch if not given."""
+    import torch
+    _dev(Q, torch.bfloat16, "Q"), _dev(K_cache, torch.bfloat16, "K_cache"), _dev(V_cache, torch.bfloat16, "V_cache")
+    _dev(block_table, torch.int32, "block_table"), _dev(seq_lens, torch.int32, "seq_lens")
+    for t, n in ((Q, "Q"), (K_cache, "K_cache"), (V_cache, "V_cache"), (block_table, "block_table")):
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    B, Hq, D = Q.shape
+    nblk, bs, Hkv, D2 = K_cache.shape
+    if D2 != D or V_cache.shape != K_cache.shape or block_table.shape[0] != B or seq_lens.numel() != B:
+        raise ValueError("shape mismatch")
+    need = attention_decode_workspace_size(B, Hq, max_seq_len)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=Q.device)
+    if O is None:
+        O = torch.empty_like(Q)
+    _check(load().bi_attention_decode(_ptr(Q), _ptr(K_cache), _ptr(V_cache), _ptr(block_table), block_table.shape[1],
+                                      nblk, _ptr(seq_lens), B, Hq, Hkv, D, bs, max_seq_len, float(scale),
+                                      _ptr(workspace), workspace.numel(), _ptr(O), _stream(stream)),
+           "bi_attention_decode")
+    return O
 
 
 def plan(op: int, M: int, N: int, K: int, num_sms: int = 0) -> dict:

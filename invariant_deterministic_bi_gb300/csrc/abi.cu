@@ -253,6 +253,33 @@ bi_status bi_rank_sum_rmsnorm(const void *const *parts, int32_t R, void *residua
     return launch_rank_sum_rmsnorm(parts, R, residual, w, sum_out, out, M, H, eps, as_stream(stream));
 }
 
+int64_t bi_attention_decode_workspace_size(int64_t B, int32_t Hq, int32_t max_seq_len) {
+    if (B < 0 || Hq < 1 || max_seq_len < 1) return -1;
+    return attention_decode_workspace_bytes(B, Hq, max_seq_len);
+}
+
+bi_status bi_attention_decode(const void *Q, const void *K_cache, const void *V_cache, const int32_t *block_table,
+                              int32_t max_blocks_per_seq, int64_t num_blocks, const int32_t *seq_lens, int64_t B,
+                              int32_t Hq, int32_t Hkv, int32_t head_dim, int32_t block_size, int32_t max_seq_len,
+                              float scale, void *workspace, int64_t workspace_bytes, void *O, bi_stream stream) {
+    if (B < 0 || B > 65535 || Hq < 1 || Hkv < 1 || block_size < 1 || max_seq_len < 1 || max_blocks_per_seq < 1 ||
+        num_blocks < 1 || !(scale == scale))
+        return BI_ERR_INVALID_ARG;
+    if (B == 0) return BI_OK;
+    if (!Q || !K_cache || !V_cache || !block_table || !seq_lens || !workspace || !O) return BI_ERR_INVALID_ARG;
+    if (head_dim != 128 || Hq % Hkv != 0) return BI_ERR_UNSUPPORTED;
+    const int32_t G = Hq / Hkv;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return BI_ERR_UNSUPPORTED;
+    if (workspace_bytes < attention_decode_workspace_bytes(B, Hq, max_seq_len)) return BI_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(K_cache) || !aligned16(V_cache) || !aligned16(O) || !aligned16(workspace) ||
+        !aligned4(block_table) || !aligned4(seq_lens))
+        return BI_ERR_MISALIGNED;
+    bi_status st = require_device();
+    if (st != BI_OK) return st;
+    return launch_attention_decode(Q, K_cache, V_cache, block_table, max_blocks_per_seq, num_blocks, seq_lens, B, Hq,
+                                   Hkv, head_dim, block_size, max_seq_len, scale, workspace, O, as_stream(stream));
+}
+
 bi_status bi_plan(int32_t op, int64_t M, int64_t N, int64_t K, int32_t num_sms, bi_plan_t *out) {
     if (!out || M < 0 || N < 0 || K < 0 || num_sms < 0) return BI_ERR_INVALID_ARG;
     int sms = num_sms;

@@ -59,6 +59,11 @@ bi_status launch_rmsnorm(const void *x, void *residual, const void *w, void *out
                          float eps, cudaStream_t s);
 bi_status launch_rank_sum_rmsnorm(const void *const *parts, int32_t R, void *residual, const void *w, void *sum_out,
                                   void *out, int64_t M, int64_t H, float eps, cudaStream_t s);
+int64_t attention_decode_workspace_bytes(int64_t B, int32_t Hq, int32_t max_len);
+bi_status launch_attention_decode(const void *Q, const void *K, const void *V, const int32_t *table,
+                                  int32_t max_blocks, int64_t num_blocks, const int32_t *lens, int64_t B, int32_t Hq,
+                                  int32_t Hkv, int32_t D, int32_t bs, int32_t max_len, float scale, void *workspace,
+                                  void *O, cudaStream_t s);
 bi_status launch_wait_timeout_check(uint32_t limit_us, cudaStream_t s);
 
 // Plans (M-independent except tiles_m and grid).

@@ -21,12 +21,12 @@ def lib():
 
 def declared_functions():
     text = open(HEADER).read()
-    return sorted(set(re.findall(r"^\s*(?:BI_API\s+)?(?:bi_status|const char \*|int32_t)\s*(bi_\w+)\s*\(", text, re.M)))
+    return sorted(set(re.findall(r"^\s*(?:BI_API\s+)?(?:bi_status|const char \*|int32_t|int64_t)\s*(bi_\w+)\s*\(", text, re.M)))
 
 
 def test_header_declares_the_calls():
     names = declared_functions()
-    for n in ["bi_gemm_bf16", "bi_grouped_gemm_bf16", "bi_gemm_nvfp4", "bi_rmsnorm", "bi_plan", "bi_quantize_nvfp4", "bi_moe_topk_softmax", "bi_moe_align", "bi_moe_gather", "bi_silu_mul", "bi_moe_combine", "bi_rank_sum_rmsnorm",
+    for n in ["bi_gemm_bf16", "bi_grouped_gemm_bf16", "bi_gemm_nvfp4", "bi_rmsnorm", "bi_plan", "bi_quantize_nvfp4", "bi_moe_topk_softmax", "bi_moe_align", "bi_moe_gather", "bi_silu_mul", "bi_moe_combine", "bi_rank_sum_rmsnorm", "bi_attention_decode", "bi_attention_decode_workspace_size",
               "bi_device_status", "bi_status_string", "bi_version", "bi_check_wait_timeout"]:
         assert n in names
 
@@ -136,5 +136,17 @@ def test_other_calls_reject_bad_arguments(lib):
     assert so.bi_rank_sum_rmsnorm(ptrs2, 2, None, FAKE, None, FAKE, 4, 4096, f(1e-6), None) == 3  # part align
     assert so.bi_rank_sum_rmsnorm(ptrs2, 0, None, FAKE, None, FAKE, 4, 4096, f(1e-6), None) == 1  # R < 1
     assert so.bi_rank_sum_rmsnorm(ptrs2, 17, None, FAKE, None, FAKE, 4, 4096, f(1e-6), None) == 1  # R > 16
+    A = so.bi_attention_decode
+    ok_args = lambda **kw: dict(dict(Q=FAKE, K=FAKE, V=FAKE, table=FAKE, mb=8, nb=64, lens=FAKE, B=4, Hq=32, Hkv=8,
+                                     D=128, bs=16, L=128, scale=f(0.1), ws=FAKE, wsb=1 << 30, O=FAKE), **kw)
+    call = lambda a: A(a["Q"], a["K"], a["V"], a["table"], a["mb"], a["nb"], a["lens"], a["B"], a["Hq"], a["Hkv"],
+                       a["D"], a["bs"], a["L"], a["scale"], a["ws"], a["wsb"], a["O"], None)
+    assert call(ok_args(D=64)) == 2                 # head_dim != 128
+    assert call(ok_args(Hkv=3)) == 2                # Hq % Hkv
+    assert call(ok_args(Hq=48, Hkv=4)) == 2         # group of 12
+    assert call(ok_args(wsb=100)) == 1              # workspace too small
+    assert call(ok_args(Q=FAKE + 8)) == 3
+    assert call(ok_args(B=0)) == 0
+    assert so.bi_attention_decode_workspace_size(4, 32, 300) == 4 * 32 * 2 * 130 * 4
     assert so.bi_check_wait_timeout(0, None) == 1
     assert so.bi_plan(99, 1, 1, 1, 152, ctypes.byref(lib.Plan())) == 1

@@ -1,0 +1,81 @@
+"""bi_attention_decode on the GPU: parity with the fp64 oracle and bit-exact
+batch invariance of decode attention over a paged KV cache (Qwen3-8B heads:
+32 query heads, 8 KV heads, head_dim 128). Batch-invariant attention is on the
+vLLM batch-invariance tracking issue's TODO list."""
+import numpy as np
+import pytest
+
+import bi_synth as syn
+import oracle
+from util import assert_close_rel, bits_of, to_dev, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+HQ, HKV, D, BS = 32, 8, 128, 16
+SCALE = 1.0 / np.sqrt(D)
+
+
+def make_cache(lens, seed=0, spare_blocks=3):
+    lens = np.asarray(lens, dtype=np.int32)
+    nb = int(-(-lens.max() // BS))
+    blocks = len(lens) * nb + spare_blocks
+    K = syn.to_bf16_bits(syn.normal_rows(seed, 0, blocks * BS, HKV * D)).reshape(blocks, BS, HKV, D)
+    V = syn.to_bf16_bits(syn.normal_rows(seed, 1, blocks * BS, HKV * D)).reshape(blocks, BS, HKV, D)
+    perm = syn.rng(seed, 2).permutation(blocks)[: len(lens) * nb].astype(np.int32)
+    return K, V, perm.reshape(len(lens), nb), lens
+
+
+def run(bi, Q, K, V, table, lens, max_len):
+    return bits_of(bi.attention_decode(to_dev_bf16(Q), to_dev_bf16(K), to_dev_bf16(V), to_dev(table),
+                                       to_dev(lens), max_len, SCALE))
+
+
+@pytest.mark.parametrize("lens", [[1, 300, 1000], [256, 257, 512, 513], [4096, 7]])
+def test_parity(bi, lens):
+    K, V, table, lens = make_cache(lens, seed=len(lens))
+    B = len(lens)
+    Q = syn.to_bf16_bits(syn.normal_rows(9, 0, B * HQ, D)).reshape(B, HQ, D)
+    got = syn.bf16_bits_to_f32(run(bi, Q, K, V, table, lens, int(lens.max()))).astype(np.float64)
+    ref = oracle.attention_decode(Q, K, V, table, lens, SCALE)
+    assert_close_rel(got, ref, 1e-2, 2e-3, f"lens={list(lens)}")
+    assert bi.device_status() == bi.BI_OK
+
+
+def test_single_token_sequences_return_values(bi):
+    """One cached token: softmax weight 1, the output is v itself (bf16 exact)."""
+    K, V, table, lens = make_cache([1, 1, 1], seed=11)
+    Q = syn.to_bf16_bits(syn.normal_rows(12, 0, 3 * HQ, D)).reshape(3, HQ, D)
+    got = run(bi, Q, K, V, table, lens, 64)
+    for b in range(3):
+        v = V[table[b, 0], 0]
+        for h in range(HQ):
+            assert np.array_equal(got[b, h], v[h // (HQ // HKV)])
+
+
+def test_batch_invariance(bi):
+    """A sequence's output is the same bits alone, in this batch, in another
+    batch and after reordering; 8 identical runs give one output."""
+    lens = [700, 33, 4000, 256, 1]
+    K, V, table, lens = make_cache(lens, seed=21)
+    B = len(lens)
+    Q = syn.to_bf16_bits(syn.normal_rows(22, 0, B * HQ, D)).reshape(B, HQ, D)
+    full = run(bi, Q, K, V, table, lens, 4096)
+    for b in range(B):
+        one = run(bi, Q[b:b + 1], K, V, table[b:b + 1], lens[b:b + 1], 4096)
+        assert np.array_equal(one[0], full[b]), f"sequence {b} alone differs"
+        other = run(bi, Q[b:b + 1], K, V, table[b:b + 1], lens[b:b + 1], int(lens[b]))
+        assert np.array_equal(other[0], full[b]), f"sequence {b}: max_seq_len changed its bits"
+    perm = np.array([3, 0, 4, 2, 1])
+    pr = run(bi, Q[perm], K, V, table[perm], lens[perm], 4096)
+    assert np.array_equal(pr, full[perm])
+    outs = {run(bi, Q, K, V, table, lens, 4096).tobytes() for _ in range(8)}
+    assert len(outs) == 1
+
+
+def test_bad_lengths_reported(bi):
+    import torch
+    K, V, table, lens = make_cache([10, 10], seed=31)
+    Q = syn.to_bf16_bits(syn.normal_rows(32, 0, 2 * HQ, D)).reshape(2, HQ, D)
+    bad = np.array([10, 0], dtype=np.int32)
+    bi.attention_decode(to_dev_bf16(Q), to_dev_bf16(K), to_dev_bf16(V), to_dev(table), to_dev(bad), 16, SCALE)
+    torch.cuda.synchronize()
+    assert bi.device_status() == bi.BI_ERR_INVALID_ARG
