@@ -281,6 +281,37 @@ BI_API bi_status bi_attention_decode(const void *Q, const void *K_cache, const v
                                      int32_t head_dim, int32_t block_size, int32_t max_seq_len, float scale,
                                      void *workspace, int64_t workspace_bytes, void *O, bi_stream stream);
 
+/*
+ * bi_attention_decode_noalloc -- bi_attention_decode for callers that cannot
+ * allocate device memory. (The pages have no counterpart: this is a library
+ * convenience, not part of the method.)
+ *
+ * Some callers cannot call cudaMalloc or hand over a workspace: code linked
+ * into a host program whose allocator has already reserved all device memory,
+ * or code on a latency-critical path that must not risk the device-wide
+ * synchronisation an allocation can cause. This entry point takes the same
+ * arguments as bi_attention_decode minus the workspace and computes the same
+ * result. Its per-chunk partial results go to one fixed array of
+ * BI_ATTENTION_NOALLOC_SCRATCH_BYTES (16 MiB) that the library keeps in device
+ * memory, on every GPU that loads it, until the process exits.
+ *  - A problem whose partial results need more than that
+ *    (bi_attention_decode_workspace_size(B, Hq, max_seq_len) > 16 MiB) is
+ *    refused with BI_ERR_UNSUPPORTED before anything is launched.
+ *  - The first call on a device looks up the array's device address (once
+ *    per device, with that device current); make that first call before any
+ *    stream capture.
+ *  - All calls share the array and it keeps what the last call left in it;
+ *    nothing in it needs to start at zero. Calls whose kernels overlap on the
+ *    GPU (for example on two streams) race on it: serialise them.
+ * Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ */
+#define BI_ATTENTION_NOALLOC_SCRATCH_BYTES (16u << 20)
+BI_API bi_status bi_attention_decode_noalloc(const void *Q, const void *K_cache, const void *V_cache,
+                                             const int32_t *block_table, int32_t max_blocks_per_seq,
+                                             int64_t num_blocks, const int32_t *seq_lens, int64_t B, int32_t Hq,
+                                             int32_t Hkv, int32_t head_dim, int32_t block_size, int32_t max_seq_len,
+                                             float scale, void *O, bi_stream stream);
+
 /* Operation ids for bi_plan. */
 enum { BI_OP_GEMM_BF16 = 0, BI_OP_GROUPED_GEMM_BF16 = 1, BI_OP_GEMM_NVFP4 = 2, BI_OP_RMSNORM = 3,
        BI_OP_QUANTIZE_NVFP4 = 4 };

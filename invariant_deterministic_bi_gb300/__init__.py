@@ -70,6 +70,7 @@ def load() -> ctypes.CDLL:
             "bi_rank_sum_rmsnorm": [P, I32, P, P, P, P, I64, I64, F, P],
             "bi_attention_decode": [P, P, P, P, I32, I64, P, I64, I32, I32, I32, I32, I32, F, P, I64, P, P],
             "bi_attention_decode_workspace_size": [I64, I32, I32],
+            "bi_attention_decode_noalloc": [P, P, P, P, I32, I64, P, I64, I32, I32, I32, I32, I32, F, P, P],
             "bi_plan": [I32, I64, I64, I64, I32, ctypes.POINTER(Plan)],
             "bi_device_status": [P],
             "bi_check_wait_timeout": [ctypes.c_uint32, P],

@@ -24,6 +24,8 @@
 //   sum_c e^{m_c - M} o_c / sum_c e^{m_c - M} l_c, chunks in order, rounded to bf16.
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 #include "bi_internal.h"
 #include "bi_ptx.cuh"
 
@@ -220,3 +222,82 @@ bi_status launch_attention_decode(const void *Q, const void *K, const void *V, c
 }
 
 }  // namespace bi
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of bi_attention_decode.
+//
+// Some callers cannot call cudaMalloc: for example code linked into a host
+// program whose allocator has already reserved all device memory up front, or
+// code on a latency-critical path that must not risk the device-wide
+// synchronisation an allocation can cause. bi_attention_decode_noalloc gives
+// them the same decode attention without a workspace argument: the per-chunk
+// partial results go to the fixed array below instead. The array lives in
+// device memory for as long as the library is loaded, on every GPU that loads
+// it, so its size is kept modest and larger problems are refused.
+//
+// Every call shares the one array, and nothing in it needs to start at zero:
+// the split kernel writes every entry the combine kernel later reads. The
+// array keeps whatever the last call left in it. Two calls whose kernels
+// overlap on the GPU (for example on different streams) race on it.
+// ---------------------------------------------------------------------------
+namespace bi {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = BI_ATTENTION_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchBytes / sizeof(float)];
+
+constexpr int kMaxScratchDevices = 64;
+std::once_flag g_scratch_once[kMaxScratchDevices];
+void *g_scratch_ptr[kMaxScratchDevices];
+cudaError_t g_scratch_err[kMaxScratchDevices];
+
+// Device address of the array for the current device, looked up once per
+// device (with that device current) on the first call made on it.
+bi_status noalloc_scratch(void **ptr) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxScratchDevices) return BI_ERR_CUDA;
+    std::call_once(g_scratch_once[dev], [dev] {
+        void *p = nullptr;
+        g_scratch_err[dev] = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        g_scratch_ptr[dev] = p;
+    });
+    if (g_scratch_err[dev] != cudaSuccess || !g_scratch_ptr[dev]) return BI_ERR_CUDA;
+    *ptr = g_scratch_ptr[dev];
+    return BI_OK;
+}
+
+}  // namespace
+}  // namespace bi
+
+extern "C" bi_status bi_attention_decode_noalloc(const void *Q, const void *K_cache, const void *V_cache,
+                                                 const int32_t *block_table, int32_t max_blocks_per_seq,
+                                                 int64_t num_blocks, const int32_t *seq_lens, int64_t B, int32_t Hq,
+                                                 int32_t Hkv, int32_t head_dim, int32_t block_size,
+                                                 int32_t max_seq_len, float scale, void *O, bi_stream stream) {
+    using namespace bi;
+    if (B < 0 || B > 65535 || Hq < 1 || Hkv < 1 || block_size < 1 || max_seq_len < 1 || max_blocks_per_seq < 1 ||
+        num_blocks < 1 || !(scale == scale))
+        return BI_ERR_INVALID_ARG;
+    if (B == 0) return BI_OK;
+    if (!Q || !K_cache || !V_cache || !block_table || !seq_lens || !O) return BI_ERR_INVALID_ARG;
+    if (head_dim != 128 || Hq % Hkv != 0) return BI_ERR_UNSUPPORTED;
+    const int32_t G = Hq / Hkv;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return BI_ERR_UNSUPPORTED;
+    // the problem's partial results must fit in the fixed array
+    if (attention_decode_workspace_bytes(B, Hq, max_seq_len) > static_cast<int64_t>(kNoAllocScratchBytes))
+        return BI_ERR_UNSUPPORTED;
+    const auto a16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    const auto a4 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; };
+    if (!a16(Q) || !a16(K_cache) || !a16(V_cache) || !a16(O) || !a4(block_table) || !a4(seq_lens))
+        return BI_ERR_MISALIGNED;
+    int dev;
+    const DeviceInfo *info;
+    bi_status st = current_device(&dev, &info);
+    if (st != BI_OK) return st;
+    void *scratch = nullptr;
+    st = noalloc_scratch(&scratch);
+    if (st != BI_OK) return st;
+    return launch_attention_decode(Q, K_cache, V_cache, block_table, max_blocks_per_seq, num_blocks, seq_lens, B, Hq,
+                                   Hkv, head_dim, block_size, max_seq_len, scale, scratch, O,
+                                   static_cast<cudaStream_t>(stream));
+}
