@@ -81,9 +81,7 @@ bi_status ensure_smem_attr(const void *kernel, int bytes, unsigned long long *do
     return BI_OK;
 }
 
-bi_status make_tmap_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, uint64_t inner,
-                       uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
-                       CUtensorMapSwizzle swizzle) {
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
     std::call_once(g_encode_once, [] {
         void *fn = nullptr;
         cudaDriverEntryPointQueryResult q;
@@ -92,14 +90,33 @@ bi_status make_tmap_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *
             q == cudaDriverEntryPointSuccess)
             g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     });
-    if (!g_encode) return BI_ERR_CUDA;
+    return g_encode;
+}
+
+bi_status make_tmap_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, uint64_t inner,
+                       uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
+                       CUtensorMapSwizzle swizzle) {
+    auto enc = encoder();
+    if (!enc) return BI_ERR_CUDA;
     const cuuint64_t dims[2] = {inner, outer};
     const cuuint64_t strides[1] = {row_stride_bytes};
     const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(map, dtype, 2, const_cast<void *>(base), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = enc(map, dtype, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? BI_OK : BI_ERR_CUDA;
+}
+
+bi_status make_tmap_3d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, const uint64_t dims[3],
+                       const uint64_t strides_bytes[2], const uint32_t box[3], CUtensorMapSwizzle swizzle) {
+    auto enc = encoder();
+    if (!enc) return BI_ERR_CUDA;
+    const cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+    const cuuint64_t s[2] = {strides_bytes[0], strides_bytes[1]};
+    const cuuint32_t b[3] = {box[0], box[1], box[2]};
+    const cuuint32_t e[3] = {1, 1, 1};
+    CUresult r = enc(map, dtype, 3, const_cast<void *>(base), d, s, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? BI_OK : BI_ERR_CUDA;
 }
 

@@ -237,6 +237,35 @@ __device__ __forceinline__ void tc_commit_pair(uint64_t *bar, uint16_t cta_mask)
         ::"r"(smem_u32(bar)), "h"(cta_mask) : "memory");
 }
 
+// Block-scaled e2m1 MMA on a CTA pair (256 x N x 64): each CTA's scale
+// factors are read from its own tensor memory at the given addresses.
+__device__ __forceinline__ void mma_nvf4_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Shared -> tensor memory copy issued for a CTA pair: in each CTA of the pair,
+// 32 lanes x 128 bits of that CTA's shared memory land replicated in its four
+// lane quarters.
+__device__ __forceinline__ void tmem_cp_32x128b_x4_pair(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// TMA 3-D load into this CTA's shared memory counted on a pair-leader barrier.
+__device__ __forceinline__ void tma_load_3d_pair_bar(void *dst, const CUtensorMap *m, uint32_t bar_cluster,
+                                                     int32_t c0, int32_t c1, int32_t c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
 // Arrive on an mbarrier once all prior tcgen05 async operations of this thread complete.
 __device__ __forceinline__ void tc_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"

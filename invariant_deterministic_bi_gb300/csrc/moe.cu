@@ -85,18 +85,34 @@ topk_softmax_kernel(const float *__restrict__ logits, int64_t T, int E, int k, i
 // ------------------------------------------------------------- alignment
 // Step 1 (one block per expert): scan the (token, rank) pairs in order and
 // give each pair routed to this expert its rank among them; the expert's
-// count goes to offsets[e + 1].
+// count goes to offsets[e + 1]. Each pass covers 1024 pairs: thread t holds
+// pairs 4t..4t+3 of the pass, an inclusive shuffle scan gives the thread's
+// offset in its warp, and the warp totals are added in warp order.
 __global__ void __launch_bounds__(256)
 align_rank_kernel(const int32_t *__restrict__ ids, int64_t P, int32_t *__restrict__ pos, int32_t *__restrict__ offsets) {
     __shared__ int warp_tot[8];
     const int e = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool vec_ok = (reinterpret_cast<uintptr_t>(ids) & 15u) == 0;   // 16-byte loads only when aligned
     int running = 0;
-    for (int64_t base = 0; base < P; base += 256) {
-        const int64_t p = base + threadIdx.x;
-        const bool f = p < P && ids[p] == e;
-        const unsigned ballot = __ballot_sync(0xffffffffu, f);
-        if (lane == 0) warp_tot[warp] = __popc(ballot);
+    for (int64_t base = 0; base < P; base += 1024) {
+        const int64_t p0 = base + 4 * static_cast<int64_t>(threadIdx.x);
+        int f[4];
+        if (vec_ok && p0 + 3 < P) {
+            const int4 v = *reinterpret_cast<const int4 *>(ids + p0);
+            f[0] = v.x == e; f[1] = v.y == e; f[2] = v.z == e; f[3] = v.w == e;
+        } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) f[q] = (p0 + q < P) && ids[p0 + q] == e;
+        }
+        const int cnt = f[0] + f[1] + f[2] + f[3];
+        int incl = cnt;                                   // inclusive scan within the warp
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (lane == 31) warp_tot[warp] = incl;
         __syncthreads();
         int before = 0, chunk = 0;
 #pragma unroll
@@ -104,7 +120,10 @@ align_rank_kernel(const int32_t *__restrict__ ids, int64_t P, int32_t *__restric
             before += w < warp ? warp_tot[w] : 0;
             chunk += warp_tot[w];
         }
-        if (f) pos[p] = running + before + __popc(ballot & ((1u << lane) - 1u));
+        int r = running + before + incl - cnt;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (f[q]) pos[p0 + q] = r++;
         running += chunk;
         __syncthreads();
     }
