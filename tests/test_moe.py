@@ -48,6 +48,21 @@ def test_align_exact(bi, T):
     assert np.array_equal(pos.cpu().numpy(), o_pos)
 
 
+def test_align_with_unaligned_ids(bi):
+    """An id array that starts 4 bytes past a 16-byte boundary takes the scalar path: same result."""
+    import torch
+    T = 300
+    ids = oracle.moe_topk_softmax(logits_for(T, seed=3), TOPK)[0]
+    buf = torch.zeros(T * TOPK + 1, dtype=torch.int32, device="cuda")
+    buf[1:] = to_dev(ids).view(-1)
+    view = buf[1:].view(T, TOPK)
+    assert view.data_ptr() % 16 == 4
+    off, row_token, pos = bi.moe_align(view, E)
+    o_off, o_rt, o_pos = oracle.moe_align(ids, E)
+    assert np.array_equal(off.cpu().numpy(), o_off) and np.array_equal(pos.cpu().numpy(), o_pos)
+    assert np.array_equal(row_token.cpu().numpy(), o_rt)
+
+
 def test_align_rejects_bad_ids(bi):
     import torch
     ids = np.zeros((4, 2), dtype=np.int32)
