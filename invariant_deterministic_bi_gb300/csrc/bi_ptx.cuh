@@ -1,5 +1,5 @@
 // bi_ptx.cuh -- thin inline-PTX wrappers for sm_103a: mbarrier, TMA
-// (cp.async.bulk.tensor), tcgen05 (TMEM alloc, MMA, commit, load, copy).
+// (cp.async.bulk.tensor), tcgen05 (TMEM alloc, MMA, commit, load, store).
 // Written from the PTX ISA descriptions of these instructions.
 #pragma once
 #include <cstdint>
@@ -79,6 +79,34 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *m, uin
         : "memory");
 }
 
+// TMA 3-D load into this CTA's shared memory, counted on this CTA's barrier.
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *m, uint64_t *bar, int32_t c0, int32_t c1,
+                                            int32_t c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+// TMA 2-D store from this CTA's shared memory (bulk async-group completion).
+// Rows and columns outside the tensor map's extent are not written.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *m, const void *src, int32_t c0, int32_t c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];"
+                 ::"l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(src)), "r"(c0), "r"(c1) : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until every committed bulk store of this thread has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_group_read0() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Wait until every committed bulk store of this thread is complete.
+__device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Make this thread's generic-proxy shared-memory writes visible to the async proxy (TMA).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Untiled bulk copy global -> shared (16-byte aligned addresses, size % 16 == 0).
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
     asm volatile(
@@ -106,9 +134,13 @@ __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
 
-// Arrive on an mbarrier given by its shared::cluster address (possibly in a peer CTA).
+// Arrive on an mbarrier given by its shared::cluster address (possibly in a
+// peer CTA), with the default release semantics at CTA scope. Callers first
+// complete what the arrival announces (tcgen05.wait::ld / wait::st, then
+// tcgen05.fence::before_thread_sync). A cluster-scope release here costs the
+// arriving warp most of a microsecond on a busy SM.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // TMA 2-D load into this CTA's shared memory whose completion is counted on
@@ -154,13 +186,6 @@ __device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
            (static_cast<uint64_t>(2) << 61);
 }
 
-// Descriptor of a plain (unswizzled) stack of 8-row x 16-byte core matrices,
-// 128 bytes apart: the source shape tcgen05.cp reads for 32x128b copies.
-__device__ __forceinline__ uint64_t sdesc_plain_128(uint32_t saddr) {
-    return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(128 >> 4) << 16) |
-           (static_cast<uint64_t>(128 >> 4) << 32) | (static_cast<uint64_t>(1) << 46);
-}
-
 // Instruction descriptor, kind::f16 with bf16 A and B, fp32 D, both K-major:
 // D format [4,6) = 1 (f32), A format [7,10) = 1 (bf16), B format [10,13) = 1,
 // N >> 3 at [17,23), M >> 4 at [24,29).
@@ -199,12 +224,6 @@ __device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64
         "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
         ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
         : "memory");
-}
-
-// Copy 32 lanes x 128 bits from shared memory to tensor memory, replicated
-// into all four 32-lane quarters.
-__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 // ---- CTA-pair (cta_group::2) forms: one thread of the even CTA issues MMAs
@@ -249,23 +268,6 @@ __device__ __forceinline__ void mma_nvf4_pair(uint32_t d_tmem, uint64_t adesc, u
         : "memory");
 }
 
-// Shared -> tensor memory copy issued for a CTA pair: in each CTA of the pair,
-// 32 lanes x 128 bits of that CTA's shared memory land replicated in its four
-// lane quarters.
-__device__ __forceinline__ void tmem_cp_32x128b_x4_pair(uint32_t taddr, uint64_t sdesc) {
-    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-
-// TMA 3-D load into this CTA's shared memory counted on a pair-leader barrier.
-__device__ __forceinline__ void tma_load_3d_pair_bar(void *dst, const CUtensorMap *m, uint32_t bar_cluster,
-                                                     int32_t c0, int32_t c1, int32_t c2) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5}], [%2];"
-        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2)
-        : "memory");
-}
-
 // Arrive on an mbarrier once all prior tcgen05 async operations of this thread complete.
 __device__ __forceinline__ void tc_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
@@ -286,6 +288,28 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
           "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
 }
+// Store 16 consecutive 32-bit columns of this thread's TMEM lane (warp w
+// writes lanes 32*(w%4) .. 32*(w%4)+31), r[o] .. r[o+15].
+template <int N>
+__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[N], int o) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
+        ::"r"(taddr), "r"(r[o + 0]), "r"(r[o + 1]), "r"(r[o + 2]), "r"(r[o + 3]), "r"(r[o + 4]), "r"(r[o + 5]),
+          "r"(r[o + 6]), "r"(r[o + 7]), "r"(r[o + 8]), "r"(r[o + 9]), "r"(r[o + 10]), "r"(r[o + 11]),
+          "r"(r[o + 12]), "r"(r[o + 13]), "r"(r[o + 14]), "r"(r[o + 15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void st_shared_v4(uint32_t saddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+__device__ __forceinline__ void ld_shared_v4(uint32_t saddr, uint32_t &a, uint32_t &b, uint32_t &c, uint32_t &d) {
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "r"(saddr) : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Two fp32 -> packed bf16x2, round to nearest even (low half = a).

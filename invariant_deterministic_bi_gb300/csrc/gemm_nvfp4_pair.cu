@@ -4,22 +4,28 @@
 // NVFP4 linear layer of vLLM PR #39912 ("NVFP4 CUTLASS batch invariant mode").
 //
 // 256 x 256 output tiles on clusters of two CTAs (one per SM), K stages of 256
-// e2m1 values (128 bytes per row), 5 stages of 38 KB per CTA:
-//   - warp 0 of each CTA TMA-loads its own 128 rows of A, its half (128 rows)
-//     of B, the scale atoms of its own A rows (4 x 512 bytes) and the scale
-//     atoms of all 256 B rows (8 x 512 bytes; tiny, so both CTAs load them);
-//     every copy completes on the leader CTA's "full" barrier (cta_group::2);
-//   - one thread of the leader copies each stage's scale atoms from each CTA's
-//     shared memory into that CTA's tensor memory (tcgen05.cp.cta_group::2,
-//     32 lanes x 128 bits replicated to the four lane quarters: lane l,
-//     column c holds row 32c + l), then issues four
+// e2m1 values (128 bytes per row), 5 stages of 38 KB per CTA. Warp roles:
+//   - warp 0 (both CTAs): TMA-loads its own 128 rows of A and its half of B
+//     (completing on the leader CTA's "full" barrier, cta_group::2), and the
+//     stage's scale atoms -- its own 4 A atoms and all 8 B atoms, 512 bytes
+//     each -- on a barrier of its own CTA;
+//   - warps 2-5 (both CTAs): one per tensor-memory lane quarter, they move the
+//     stage's scale atoms from shared memory into the stage's scale slot in
+//     tensor memory with tcgen05.st (each quarter holds the same 48 columns:
+//     lane l, column c = row 32c + l of an atom), wait for the stores, and
+//     report to the leader;
+//   - warp 1 (leader only): one thread issues four
 //     tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X
-//     (256 x 256 x 64, fp32 accumulate): each SM's tensor core multiplies its
-//     128 A rows by both B halves;
-//   - both CTAs' epilogue warps read their own accumulator rows, scale by
-//     alpha, round to bf16, hand the accumulator back to the leader, then store.
-// Per FLOP this issues half the scale-factor copies and loads half the operand
-// bytes of the single-CTA 128 x 256 tile.
+//     (256 x 256 x 64, fp32 accumulate) per stage once both CTAs' operands
+//     and scales are in place; each SM's tensor core multiplies its 128 A rows
+//     by both B halves;
+//   - warps 6-13 (both CTAs): two warps per lane quarter, 128 columns each,
+//     read the accumulator, scale by alpha, round to bf16, hand the
+//     accumulator back to the leader, then store.
+// Writing the scales with tcgen05.st from registers instead of tcgen05.cp
+// keeps them off the tensor pipe: 48 columns x 128 lanes per stage take a few
+// dozen cycles of the writer warps, while the equivalent twelve 32x128b
+// copies cost more tensor-pipe time than the stage's four MMAs.
 //
 // TMEM per CTA: one 256-column accumulator + a 5 x 48-column scale ring.
 // Invariance: tile shape, MMA shape and K order (ascending 64-wide steps from
@@ -40,7 +46,9 @@ constexpr int kBK = 2 * kBKBytes;
 constexpr int kMmaK = 64;
 constexpr int kMmasPerStage = kBK / kMmaK;
 constexpr int kStages = 5;
-constexpr int kThreads = 192;
+constexpr int kSfWarps = 4;              // scale writers, one per TMEM lane quarter
+constexpr int kEpiWarps = 8;             // two per lane quarter
+constexpr int kThreads = 32 * (2 + kSfWarps + kEpiWarps);
 constexpr int kGroupM = 8;
 constexpr int kAtom = 512;
 
@@ -50,13 +58,15 @@ constexpr int kSfaBytes = kMmasPerStage * kAtom;            // 2 KB
 constexpr int kSfbBytes = 2 * kMmasPerStage * kAtom;        // 4 KB (both B row blocks)
 constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
 static_assert(kStageBytes % 1024 == 0, "stage must keep 1024-byte alignment");
+constexpr int kOutCols = 64;                                // bf16 columns per output box (128 bytes)
+constexpr int kOutBytes = 32 * kOutCols * 2;                // one epilogue warp's staging box: 32 rows
 constexpr int kBarBytes = 256;
-constexpr int kSmem = 1024 + kStages * kStageBytes + kBarBytes;
+constexpr int kSmem = 1024 + kStages * kStageBytes + kEpiWarps * kOutBytes + kBarBytes;
 
 constexpr int kTmemCols = 512;
 constexpr int kAccCol = 0;
 constexpr int kSfCol = 256;
-constexpr int kSfColsPerMma = 4 + 8;
+constexpr int kSfColsPerMma = 4 + 8;     // SFA (128 rows) + SFB (256 rows) per 64-wide K step
 constexpr int kSfColsPerStage = kMmasPerStage * kSfColsPerMma;
 static_assert(kSfCol + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
 
@@ -71,13 +81,16 @@ struct Params {
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
-                       const Params p) {
+                       const __grid_constant__ CUtensorMap tmY, const Params p) {
     constexpr uint32_t kIdesc = idesc_nvf4(kBM, kBN);
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes);
+    uint8_t *out_stage = smem + kStages * kStageBytes;   // kEpiWarps staging boxes of kOutBytes
+    uint64_t *full = reinterpret_cast<uint64_t *>(out_stage + kEpiWarps * kOutBytes);
     uint64_t *empty = full + kStages;
-    uint64_t *tfull = empty + kStages;
+    uint64_t *sf_full = empty + kStages;     // this CTA's scale atoms landed in shared memory
+    uint64_t *sf_ready = sf_full + kStages;  // (leader) both CTAs' scales are in tensor memory
+    uint64_t *tfull = sf_ready + kStages;
     uint64_t *tempty = tfull + 1;
     uint64_t *drain = tempty + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
@@ -100,9 +113,11 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
+            mbar_init(&sf_full[s], 1);
+            mbar_init(&sf_ready[s], 2 * kSfWarps);   // scale writer warps of both CTAs
         }
         mbar_init(tfull, 1);
-        mbar_init(tempty, 8);            // 4 epilogue warps in each CTA
+        mbar_init(tempty, 2 * kEpiWarps);            // epilogue warps of both CTAs
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -132,6 +147,10 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
         nb = local / gm;
     };
     auto mmas_in = [&](int ks) { return min(kMmasPerStage, (p.K - ks * kBK) / kMmaK); };
+    auto give_up = [&]() {
+        *abort_flag = 1;
+        atomicOr(p.status, kDevTimeout);
+    };
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer (both CTAs)
@@ -149,15 +168,16 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
                 const int rb_b = nb * 2;                                 // the tile's two B scale blocks
                 for (int ks = 0; ks < k_stages; ++ks) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
-                    if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes);
+                    if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * (kABytes + kBBytes));
                     const uint32_t bar = full_leader + stage * 8;
-                    const int atom = ks * kMmasPerStage;
                     tma_load_2d_pair_bar(stage_a(stage), &tmA, bar, ks * kBKBytes, a_row);
                     tma_load_2d_pair_bar(stage_b(stage), &tmB, bar, ks * kBKBytes, b_row);
-                    tma_load_3d_pair_bar(stage_sfa(stage), &tmSFA, bar, 0, 0, rb_a * p.atoms_per_rowblock + atom);
-                    tma_load_3d_pair_bar(stage_sfb(stage), &tmSFB, bar, 0, 0, rb_b * p.atoms_per_rowblock + atom);
-                    tma_load_3d_pair_bar(stage_sfb(stage) + kMmasPerStage * kAtom, &tmSFB, bar, 0, 0,
-                                         (rb_b + 1) * p.atoms_per_rowblock + atom);
+                    const int atom = ks * kMmasPerStage;
+                    mbar_arrive_expect_tx(&sf_full[stage], kSfaBytes + kSfbBytes);
+                    tma_load_3d(stage_sfa(stage), &tmSFA, &sf_full[stage], 0, 0, rb_a * p.atoms_per_rowblock + atom);
+                    tma_load_3d(stage_sfb(stage), &tmSFB, &sf_full[stage], 0, 0, rb_b * p.atoms_per_rowblock + atom);
+                    tma_load_3d(stage_sfb(stage) + kMmasPerStage * kAtom, &tmSFB, &sf_full[stage], 0, 0,
+                                (rb_b + 1) * p.atoms_per_rowblock + atom);
                     issued |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -168,11 +188,13 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
                 if (++stage == kStages) { stage = 0; phase ^= 1u; }
             }
             if (!ok) {
-                *abort_flag = 1;
-                atomicOr(p.status, kDevTimeout);
-                if (rank == 0)   // the leader's full barriers count both CTAs' bytes
-                    for (int s = 0; s < kStages; ++s)
-                        if ((issued >> s) & 1u) mbar_wait(&full[s], (issued_phase >> s) & 1u, nullptr);
+                give_up();
+                // let this CTA's copies in flight land before the CTA exits
+                for (int s = 0; s < kStages; ++s)
+                    if ((issued >> s) & 1u) {
+                        mbar_wait(&sf_full[s], (issued_phase >> s) & 1u, nullptr);
+                        if (rank == 0) mbar_wait(&full[s], (issued_phase >> s) & 1u, nullptr);
+                    }
             }
         }
         __syncwarp();
@@ -187,17 +209,11 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
                 if (!mbar_wait(tempty, (it & 1) ^ 1u, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 for (int ks = 0; ks < k_stages; ++ks) {
-                    if (!mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
+                    if (!mbar_wait(&full[stage], phase, abort_flag) ||
+                        !mbar_wait(&sf_ready[stage], phase, abort_flag)) { ok = false; break; }
                     tc_fence_after();
                     const int nk = mmas_in(ks);
                     const uint32_t sf = tmem_base + kSfCol + stage * kSfColsPerStage;
-                    const uint32_t sa = smem_u32(stage_sfa(stage)), sb = smem_u32(stage_sfb(stage));
-                    for (int j = 0; j < nk; ++j) {
-                        tmem_cp_32x128b_x4_pair(sf + j * kSfColsPerMma, sdesc_plain_128(sa + j * kAtom));
-                        tmem_cp_32x128b_x4_pair(sf + j * kSfColsPerMma + 4, sdesc_plain_128(sb + j * kAtom));
-                        tmem_cp_32x128b_x4_pair(sf + j * kSfColsPerMma + 8,
-                                                sdesc_plain_128(sb + (kMmasPerStage + j) * kAtom));
-                    }
                     const uint32_t a0 = smem_u32(stage_a(stage)), b0 = smem_u32(stage_b(stage));
                     for (int j = 0; j < nk; ++j)
                         mma_nvf4_pair(d, sdesc_k_sw128(a0 + j * (kMmaK / 2)), sdesc_k_sw128(b0 + j * (kMmaK / 2)),
@@ -209,37 +225,79 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
                 tc_commit_pair(tfull, 0x3);
             }
             if (!ok) {
-                *abort_flag = 1;
-                atomicOr(p.status, kDevTimeout);
+                give_up();
                 tc_commit_pair(drain, 0x1);
                 mbar_wait(drain, 0, nullptr);
             }
         }
         __syncwarp();
+    } else if (warp < 2 + kSfWarps) {
+        // ------------------------------------------------ scale writers (both CTAs)
+        // Lane l moves 16 bytes per atom: atom bytes l*16 .. l*16+15 are rows
+        // l, 32+l, 64+l, 96+l of its 128-row block (4 scales each), i.e. the
+        // four 32-bit columns of lane l for that atom.
+        const int q = warp & 3;
+        const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kSfCol;
+        const uint32_t ready_leader = mapa_shared(smem_u32(sf_ready), 0);
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int t = pair; t < total && ok; t += npairs) {
+            for (int ks = 0; ks < k_stages; ++ks) {
+                int w = 1;
+                if (lane == 0) w = mbar_wait(&sf_full[stage], phase, abort_flag) ? 1 : 0;
+                if (!__shfl_sync(0xffffffffu, w, 0)) {
+                    if (lane == 0) give_up();
+                    ok = false;
+                    break;
+                }
+                uint32_t r[kSfColsPerStage];
+                const uint32_t sa = smem_u32(stage_sfa(stage)) + lane * 16, sb = smem_u32(stage_sfb(stage)) + lane * 16;
+#pragma unroll
+                for (int j = 0; j < kMmasPerStage; ++j) {
+                    uint32_t *c = r + j * kSfColsPerMma;
+                    ld_shared_v4(sa + j * kAtom, c[0], c[1], c[2], c[3]);
+                    ld_shared_v4(sb + j * kAtom, c[4], c[5], c[6], c[7]);
+                    ld_shared_v4(sb + (kMmasPerStage + j) * kAtom, c[8], c[9], c[10], c[11]);
+                }
+                const uint32_t dst = lane_base + stage * kSfColsPerStage;
+#pragma unroll
+                for (int o = 0; o < kSfColsPerStage; o += 16) tmem_st_32x32b_x16(dst + o, r, o);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(ready_leader + stage * 8);
+                if (++stage == kStages) { stage = 0; phase ^= 1u; }
+            }
+        }
     } else {
         // ------------------------------------------------ epilogue (both CTAs)
+        // Each warp owns 32 accumulator rows (its lane quarter) x 128 columns.
+        // After handing the accumulator back it writes the rounded rows in two
+        // 32 x 64 boxes through its own 4 KB staging buffer (128-byte swizzle:
+        // 16-byte chunk c of row r sits at chunk c ^ (r % 8)), stored by TMA
+        // as whole 128-byte lines; rows past M and columns past N are clipped.
+        const int e = warp - 2 - kSfWarps;
         const int q = warp & 3;
-        const int r_in_tile = static_cast<int>(rank) * kHalf + q * 32 + lane;
+        const int half = e / 4;                               // which 128 columns of the tile
         const uint32_t tempty_leader = mapa_shared(smem_u32(tempty), 0);
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kAccCol + half * (kBN / 2);
+        const uint32_t box = smem_u32(out_stage + e * kOutBytes);
+        if (lane == 0) tma_prefetch_desc(&tmY);
         int it = 0;
         for (int t = pair; t < total; t += npairs, ++it) {
             int mb, nb;
             tile_of(t, mb, nb);
             int ok = 1;
             if (lane == 0) ok = mbar_wait(tfull, it & 1, abort_flag) ? 1 : 0;
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) {
-                if (lane == 0) {
-                    *abort_flag = 1;
-                    atomicOr(p.status, kDevTimeout);
-                }
+            if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                if (lane == 0) give_up();
                 break;
             }
             tc_fence_after();
-            uint32_t packed[kBN / 2];
-            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kAccCol;
+            uint32_t packed[kBN / 4];
 #pragma unroll
-            for (int c = 0; c < kBN / 32; ++c) {
+            for (int c = 0; c < kBN / 64; ++c) {
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(taddr + c * 32, r);
                 tmem_wait_ld();
@@ -251,17 +309,28 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(tempty_leader);   // accumulator may be overwritten now
-            const int64_t row = static_cast<int64_t>(mb) * kBM + r_in_tile;
-            if (row < p.M) {
-                const int n0 = nb * kBN;
-                uint8_t *yrow = p.Y + (row * p.N + n0) * 2;
+            const int row0 = mb * kBM + static_cast<int>(rank) * kHalf + q * 32;
+            const int col0 = nb * kBN + half * (kBN / 2);
+            if (row0 >= p.M || col0 >= p.N) continue;
 #pragma unroll
-                for (int g = 0; g < kBN / 8; ++g)
-                    if (n0 + g * 8 < p.N)
-                        st_global_v4(yrow + g * 16, packed[4 * g], packed[4 * g + 1], packed[4 * g + 2],
-                                     packed[4 * g + 3]);
+            for (int rd = 0; rd < 2; ++rd) {
+                if (lane == 0) bulk_wait_group_read0();       // the previous box has left the buffer
+                __syncwarp();
+#pragma unroll
+                for (int c = 0; c < kOutCols / 8; ++c) {
+                    const uint32_t *w = packed + rd * (kOutCols / 2) + c * 4;
+                    st_shared_v4(box + lane * 128 + ((c ^ (lane & 7)) << 4), w[0], w[1], w[2], w[3]);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&tmY, out_stage + e * kOutBytes, col0 + rd * kOutCols, row0);
+                    bulk_commit_group();
+                }
             }
         }
+        if (lane == 0) bulk_wait_group0();
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -311,6 +380,9 @@ bi_status launch_gemm_nvfp4(const uint8_t *A, const uint8_t *A_sf, const uint8_t
     if (st != BI_OK) return st;
     st = make_tmap_3d(&tsb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B_sf, sfb_dims, sf_strides, sf_box, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (st != BI_OK) return st;
+    CUtensorMap ty;
+    st = make_tmap_2d(&ty, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Y, N, M, N * 2, kOutCols, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != BI_OK) return st;
     bi_plan_t pl;
     plan_gemm_nvfp4(M, N, K, info->sm_count, &pl);
     Params p{};
@@ -324,7 +396,7 @@ bi_status launch_gemm_nvfp4(const uint8_t *A, const uint8_t *A_sf, const uint8_t
     static unsigned long long configured = 0;
     if (ensure_smem_attr(reinterpret_cast<const void *>(gemm_nvfp4_pair_kernel), kSmem, &configured) != BI_OK)
         return BI_ERR_CUDA;
-    gemm_nvfp4_pair_kernel<<<pl.grid, kThreads, kSmem, s>>>(ta, tb, tsa, tsb, p);
+    gemm_nvfp4_pair_kernel<<<pl.grid, kThreads, kSmem, s>>>(ta, tb, tsa, tsb, ty, p);
     return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
 }
 
