@@ -11,8 +11,10 @@
 //     tensor memory (two accumulators of 256 columns, so the epilogue of one
 //     tile overlaps the main loop of the next);
 //   - the leader's commits are multicast to both CTAs' barriers (stage free,
-//     accumulator ready); both CTAs' epilogue warps read their own rows and
-//     report back to the leader's "accumulator empty" barrier.
+//     accumulator ready); both CTAs' epilogue warps read their own rows,
+//     report back to the leader's "accumulator empty" barrier, and write
+//     32 x 64 output boxes through two swizzled 4 KB staging buffers per warp
+//     with TMA stores (whole 128-byte lines instead of 16-byte pieces).
 // Against the single-CTA 128 x 256 tile this halves the B bytes each SM loads
 // and reads from shared memory per MMA (64 instead of 96 bytes per clock at
 // full rate) and cuts L2-to-SM traffic per output by a third.
@@ -39,26 +41,28 @@ constexpr int kGroupM = 8;     // 8 pair tiles (2048 rows) per raster band
 constexpr int kABytes = kHalf * kBK * 2;
 constexpr int kBBytes = kHalf * kBK * 2;
 constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kOutCols = 64;                    // bf16 columns per output box (128 bytes)
+constexpr int kOutBytes = 32 * kOutCols * 2;    // one 32-row box
+constexpr int kEpiWarps = 4;
 constexpr int kBarBytes = 256;
-constexpr int kSmem = 1024 + kStages * kStageBytes + kBarBytes;
+constexpr int kSmem = 1024 + kStages * kStageBytes + kEpiWarps * 2 * kOutBytes + kBarBytes;
 constexpr int kTmemCols = 512;
 
 struct Params {
-    uint8_t *Y;
-    int64_t ldy;
     int32_t M, N, K;
     unsigned *status;
 };
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                      const Params p) {
+                      const __grid_constant__ CUtensorMap tmY, const Params p) {
     constexpr uint32_t kIdesc = idesc_bf16(kBM, kBN);
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sA = smem;
     uint8_t *sB = smem + kStages * kABytes;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes);
+    uint8_t *out_stage = smem + kStages * kStageBytes;   // 2 staging boxes per epilogue warp
+    uint64_t *full = reinterpret_cast<uint64_t *>(out_stage + kEpiWarps * 2 * kOutBytes);
     uint64_t *empty = full + kStages;
     uint64_t *tfull = empty + kStages;
     uint64_t *tempty = tfull + 2;
@@ -185,9 +189,15 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         __syncwarp();
     } else {
         // ------------------------------------------------ epilogue (both CTAs)
+        // Warp q owns accumulator rows 32q .. 32q+31 of its CTA. Per 64-column
+        // box: two 32-column TMEM loads, bf16 rounding, then the box goes into
+        // one of the warp's two staging buffers (128-byte swizzle: 16-byte
+        // chunk c of row r at chunk c ^ (r % 8)) and out by TMA; rows past M
+        // and columns past N are clipped by the tensor map.
         const int q = warp & 3;
-        const int r_in_tile = static_cast<int>(rank) * kHalf + q * 32 + lane;
         const uint32_t tempty_leader = mapa_shared(smem_u32(tempty), 0);
+        uint8_t *boxes = out_stage + q * 2 * kOutBytes;
+        if (lane == 0) tma_prefetch_desc(&tmY);
         int it = 0;
         for (int t = pair; t < total; t += npairs, ++it) {
             const int acc = it & 1;
@@ -205,24 +215,33 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                 break;
             }
             tc_fence_after();
-            const int64_t row = static_cast<int64_t>(mb) * kBM + r_in_tile;
+            const int row0 = mb * kBM + static_cast<int>(rank) * kHalf + q * 32;
             const int n0 = nb * kBN;
-            const bool valid = row < p.M;
-            uint8_t *yrow = p.Y + (row * p.ldy + n0) * 2;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
+            if (row0 < p.M) {
 #pragma unroll 1
-            for (int c = 0; c < kBN / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(taddr + c * 32, r);
-                tmem_wait_ld();
-                if (valid) {
+                for (int bx = 0; bx < kBN / kOutCols && n0 + bx * kOutCols < p.N; ++bx) {
+                    uint32_t r[32], w[32];
+                    tmem_ld_32x32b_x32(taddr + bx * kOutCols, r);
+                    tmem_wait_ld();
 #pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        if (n0 + c * 32 + g * 8 < p.N)
-                            st_global_v4(yrow + (c * 32 + g * 8) * 2, pack_bf16x2(r[8 * g + 0], r[8 * g + 1]),
-                                         pack_bf16x2(r[8 * g + 2], r[8 * g + 3]),
-                                         pack_bf16x2(r[8 * g + 4], r[8 * g + 5]),
-                                         pack_bf16x2(r[8 * g + 6], r[8 * g + 7]));
+                    for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(r[2 * i], r[2 * i + 1]);
+                    tmem_ld_32x32b_x32(taddr + bx * kOutCols + 32, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) w[16 + i] = pack_bf16x2(r[2 * i], r[2 * i + 1]);
+                    uint8_t *buf = boxes + (bx & 1) * kOutBytes;
+                    if (lane == 0) bulk_wait_group_read1();   // the box stored from this buffer two rounds ago has left
+                    __syncwarp();
+                    const uint32_t sb = smem_u32(buf) + lane * 128;
+#pragma unroll
+                    for (int c = 0; c < kOutCols / 8; ++c)
+                        st_shared_v4(sb + ((c ^ (lane & 7)) << 4), w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmY, buf, n0 + bx * kOutCols, row0);
+                        bulk_commit_group();
                     }
                 }
             }
@@ -230,6 +249,8 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(tempty_leader + acc * 8);
         }
+        if (lane == 0) bulk_wait_group0();
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -270,11 +291,12 @@ bi_status launch_gemm_bf16(const void *X, int64_t ldx, const void *W, int64_t ld
     if (st != BI_OK) return st;
     st = make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, K, N, ldw * 2, kBK, kHalf, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != BI_OK) return st;
+    CUtensorMap ty;
+    st = make_tmap_2d(&ty, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Y, N, M, ldy * 2, kOutCols, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != BI_OK) return st;
     bi_plan_t pl;
     plan_gemm_bf16(M, N, K, info->sm_count, &pl);
     Params p{};
-    p.Y = static_cast<uint8_t *>(Y);
-    p.ldy = ldy;
     p.M = static_cast<int32_t>(M);
     p.N = static_cast<int32_t>(N);
     p.K = static_cast<int32_t>(K);
@@ -282,7 +304,7 @@ bi_status launch_gemm_bf16(const void *X, int64_t ldx, const void *W, int64_t ld
     static unsigned long long configured = 0;
     if (ensure_smem_attr(reinterpret_cast<const void *>(gemm_bf16_pair_kernel), kSmem, &configured) != BI_OK)
         return BI_ERR_CUDA;
-    gemm_bf16_pair_kernel<<<pl.grid, kThreads, kSmem, s>>>(ta, tb, p);
+    gemm_bf16_pair_kernel<<<pl.grid, kThreads, kSmem, s>>>(ta, tb, ty, p);
     return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
 }
 
