@@ -12,7 +12,6 @@
 namespace bi {
 namespace {
 
-constexpr int kMaxDevices = 64;
 
 // One status word per device; kernels or codes into it, bi_device_status
 // reads and clears it.
@@ -311,7 +310,7 @@ bi_status bi_plan(int32_t op, int64_t M, int64_t N, int64_t K, int32_t num_sms, 
     switch (op) {
         case BI_OP_GEMM_BF16: plan_gemm_bf16(M, N, K, sms, out); return BI_OK;
         case BI_OP_GROUPED_GEMM_BF16: plan_grouped_gemm_bf16(M, N, K, sms, out); return BI_OK;
-        case BI_OP_GEMM_NVFP4: plan_gemm_nvfp4(M, N, K, sms, out); return BI_OK;
+        case BI_OP_GEMM_NVFP4: plan_gemm_nvfp4(M, N, K, nvfp4_clusters(sms), out); return BI_OK;
         case BI_OP_QUANTIZE_NVFP4:
             out->op = BI_OP_QUANTIZE_NVFP4;
             out->block_m = 1; out->block_n = 16; out->block_k = 16;   /* one 16-element scale block per thread */

@@ -9,6 +9,8 @@
 
 namespace bi {
 
+constexpr int kMaxDevices = 64;      // devices the library keeps per-device state for
+
 // Device status codes (or-ed into the per-device status word by kernels).
 constexpr unsigned kDevTimeout = 1u;      // a bounded wait ran out
 constexpr unsigned kDevBadOffsets = 2u;   // MoE expert offsets were not 0 <= ... <= rows
@@ -73,7 +75,9 @@ bi_status launch_wait_timeout_check(uint32_t limit_us, cudaStream_t s);
 // Plans (M-independent except tiles_m and grid).
 void plan_gemm_bf16(int64_t M, int64_t N, int64_t K, int sms, bi_plan_t *p);
 void plan_grouped_gemm_bf16(int64_t rows, int64_t N, int64_t K, int sms, bi_plan_t *p);
-void plan_gemm_nvfp4(int64_t M, int64_t N, int64_t K, int sms, bi_plan_t *p);
+void plan_gemm_nvfp4(int64_t M, int64_t N, int64_t K, int clusters, bi_plan_t *p);
+// Clusters of the NVFP4 kernel resident at once on the current device (sms / 4 if the query fails).
+int nvfp4_clusters(int sms);
 void plan_rmsnorm(int64_t M, int64_t H, bi_plan_t *p);
 
 }  // namespace bi

@@ -1,36 +1,44 @@
-// gemm_nvfp4_pair.cu -- batch-invariant block-scaled NVFP4 linear layer on CTA pairs.
+// gemm_nvfp4.cu -- batch-invariant block-scaled NVFP4 linear layer.
 //
 // Y[i][j] = bf16( alpha * sum_k (a[i][k] sa[i][k/16]) (b[j][k] sb[j][k/16]) ), the
 // NVFP4 linear layer of vLLM PR #39912 ("NVFP4 CUTLASS batch invariant mode").
 //
-// 256 x 256 output tiles on clusters of two CTAs (one per SM), K stages of 256
-// e2m1 values (128 bytes per row), 5 stages of 38 KB per CTA. Warp roles:
-//   - warp 0 (both CTAs): TMA-loads its own 128 rows of A and its half of B
-//     (completing on the leader CTA's "full" barrier, cta_group::2), and the
-//     stage's scale atoms -- its own 4 A atoms and all 8 B atoms, 512 bytes
-//     each -- on a barrier of its own CTA;
-//   - warps 2-5 (both CTAs): one per tensor-memory lane quarter, they move the
-//     stage's scale atoms from shared memory into the stage's scale slot in
-//     tensor memory with tcgen05.st (each quarter holds the same 48 columns:
-//     lane l, column c = row 32c + l of an atom), wait for the stores, and
-//     report to the leader;
-//   - warp 1 (leader only): one thread issues four
+// Output tiles are 256 x 256, each computed by a CTA pair (cta_group::2, one
+// CTA per SM, 128 accumulator rows each). Clusters hold two pairs that work on
+// the same 256 A rows and on two neighbouring 256-column tiles, so every A
+// byte is read from L2 once per cluster: the CTA with lane-half h of pair p
+// loads A rows [128h + 64p, +64) of the tile and multicasts them to CTA h of
+// both pairs. K advances in stages of 256 e2m1 values (128 bytes per row),
+// 5 stages of 38 KB per CTA. Warp roles:
+//   - warp 0 (every CTA): per stage, its 64-row A multicast, its own 128 B
+//     rows, and the stage's scale atoms (its 4 A atoms, all 8 B atoms of the
+//     pair's tile, 512 bytes each), all counted on its own "full" barrier;
+//   - warps 2-5 (every CTA): one per tensor-memory lane quarter; once "full"
+//     completes they move the scale atoms from shared memory into the
+//     stage's scale slot in tensor memory with tcgen05.st (each quarter holds
+//     the same 48 columns: lane l, column c = row 32c + l of an atom), wait
+//     for the stores and report to the pair leader's "ready" barrier -- so
+//     "ready" also means both CTAs' operands have landed;
+//   - warp 1 (pair leaders): one thread issues four
 //     tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X
-//     (256 x 256 x 64, fp32 accumulate) per stage once both CTAs' operands
-//     and scales are in place; each SM's tensor core multiplies its 128 A rows
-//     by both B halves;
-//   - warps 6-13 (both CTAs): two warps per lane quarter, 128 columns each,
+//     (256 x 256 x 64, fp32 accumulate) per stage, then commits the stage
+//     to all four CTAs: a stage slot is refilled only when both pairs'
+//     MMAs have read it, since each CTA's A multicast lands in both pairs;
+//   - warps 6-13 (every CTA): two warps per lane quarter, 128 columns each:
 //     read the accumulator, scale by alpha, round to bf16, hand the
-//     accumulator back to the leader, then store.
-// Writing the scales with tcgen05.st from registers instead of tcgen05.cp
-// keeps them off the tensor pipe: 48 columns x 128 lanes per stage take a few
-// dozen cycles of the writer warps, while the equivalent twelve 32x128b
-// copies cost more tensor-pipe time than the stage's four MMAs.
+//     accumulator back, then write 32 x 64 boxes through a swizzled staging
+//     buffer with TMA stores (rows past M, columns past N are clipped).
+// Writing the scales with tcgen05.st keeps them off the tensor pipe: the
+// equivalent twelve tcgen05.cp 32x128b copies per stage cost more tensor-pipe
+// time than the stage's four MMAs.
 //
 // TMEM per CTA: one 256-column accumulator + a 5 x 48-column scale ring.
 // Invariance: tile shape, MMA shape and K order (ascending 64-wide steps from
-// zero) are the same for every M; rows never interact.
+// zero) are the same for every M; rows never interact; which cluster computes
+// which tile does not change any result.
 #include <cuda_bf16.h>
+
+#include <mutex>
 
 #include "bi_internal.h"
 #include "bi_ptx.cuh"
@@ -38,8 +46,10 @@
 namespace bi {
 namespace {
 
+constexpr int kClusterCtas = 4;          // two CTA pairs
 constexpr int kBM = 256;                 // pair tile rows (128 per CTA)
 constexpr int kHalf = 128;
+constexpr int kAPart = 64;               // A rows each CTA loads and multicasts per stage
 constexpr int kBN = 256;
 constexpr int kBKBytes = 128;            // K bytes per stage (256 e2m1 values)
 constexpr int kBK = 2 * kBKBytes;
@@ -52,8 +62,8 @@ constexpr int kThreads = 32 * (2 + kSfWarps + kEpiWarps);
 constexpr int kGroupM = 8;
 constexpr int kAtom = 512;
 
-constexpr int kABytes = kHalf * kBKBytes;                   // 16 KB
-constexpr int kBBytes = kHalf * kBKBytes;                   // 16 KB (this CTA's half)
+constexpr int kABytes = kHalf * kBKBytes;                   // 16 KB (two multicast parts of 8 KB)
+constexpr int kBBytes = kHalf * kBKBytes;                   // 16 KB (this CTA's half of the pair's B)
 constexpr int kSfaBytes = kMmasPerStage * kAtom;            // 2 KB
 constexpr int kSfbBytes = 2 * kMmasPerStage * kAtom;        // 4 KB (both B row blocks)
 constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
@@ -71,30 +81,29 @@ constexpr int kSfColsPerStage = kMmasPerStage * kSfColsPerMma;
 static_assert(kSfCol + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
 
 struct Params {
-    uint8_t *Y;
     float alpha;
     int32_t M, N, K;
     int32_t atoms_per_rowblock;   // K / 64
     unsigned *status;
 };
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                       const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
-                       const __grid_constant__ CUtensorMap tmY, const Params p) {
+__global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kThreads, 1)
+gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                  const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
+                  const __grid_constant__ CUtensorMap tmY, const Params p) {
     constexpr uint32_t kIdesc = idesc_nvf4(kBM, kBN);
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *out_stage = smem + kStages * kStageBytes;   // kEpiWarps staging boxes of kOutBytes
     uint64_t *full = reinterpret_cast<uint64_t *>(out_stage + kEpiWarps * kOutBytes);
-    uint64_t *empty = full + kStages;
-    uint64_t *sf_full = empty + kStages;     // this CTA's scale atoms landed in shared memory
-    uint64_t *sf_ready = sf_full + kStages;  // (leader) both CTAs' scales are in tensor memory
-    uint64_t *tfull = sf_ready + kStages;
+    uint64_t *empty = full + kStages;        // [2][kStages]: one barrier per pair leader
+    uint64_t *ready = empty + 2 * kStages;   // (pair leader) both CTAs' operands and scales in place
+    uint64_t *tfull = ready + kStages;
     uint64_t *tempty = tfull + 1;
     uint64_t *drain = tempty + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    static_assert((5 * kStages + 3) * 8 + 8 <= kBarBytes, "barrier area");
 
     auto stage_a = [&](int s) { return smem + s * kStageBytes; };
     auto stage_b = [&](int s) { return smem + s * kStageBytes + kABytes; };
@@ -103,21 +112,26 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
-    const int pair = static_cast<int>(blockIdx.x >> 1), npairs = static_cast<int>(gridDim.x >> 1);
+    const int h = static_cast<int>(rank & 1u);          // lane half of the pair's tile
+    const int pc = static_cast<int>(rank >> 1);         // which pair of the cluster
+    const uint32_t lead = rank & ~1u;                   // this pair's leader
+    const int cl = static_cast<int>(blockIdx.x) / kClusterCtas;
+    const int ncl = static_cast<int>(gridDim.x) / kClusterCtas;
     const int num_m = (p.M + kBM - 1) / kBM;
     const int num_n = (p.N + kBN - 1) / kBN;
-    const int total = num_m * num_n;
+    const int num_sn = (num_n + 1) / 2;                  // column-tile pairs
+    const int total = num_m * num_sn;
     const int k_stages = (p.K + kBK - 1) / kBK;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
-            mbar_init(&sf_full[s], 1);
-            mbar_init(&sf_ready[s], 2 * kSfWarps);   // scale writer warps of both CTAs
+            mbar_init(&empty[kStages + s], 1);
+            mbar_init(&ready[s], 2 * kSfWarps);      // scale writer warps of both CTAs of the pair
         }
         mbar_init(tfull, 1);
-        mbar_init(tempty, 2 * kEpiWarps);            // epilogue warps of both CTAs
+        mbar_init(tempty, 2 * kEpiWarps);            // epilogue warps of both CTAs of the pair
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -137,14 +151,15 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    auto tile_of = [&](int t, int &mb, int &nb) {
-        const int per_group = kGroupM * num_n;
+    // Supertile t -> (row tile mb, column-tile pair sn); pair pc takes column tile 2*sn + pc.
+    auto tile_of = [&](int t, int &mb, int &sn) {
+        const int per_group = kGroupM * num_sn;
         const int g = t / per_group;
         const int first = g * kGroupM;
         const int gm = min(kGroupM, num_m - first);
         const int local = t - g * per_group;
         mb = first + local % gm;
-        nb = local / gm;
+        sn = local / gm;
     };
     auto mmas_in = [&](int ks) { return min(kMmasPerStage, (p.K - ks * kBK) / kMmaK); };
     auto give_up = [&]() {
@@ -153,30 +168,32 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
     };
 
     if (warp == 0) {
-        // ------------------------------------------------ TMA producer (both CTAs)
+        // ------------------------------------------------ TMA producer (every CTA)
         if (lane == 0) {
-            const uint32_t full_leader = mapa_shared(smem_u32(full), 0);
+            const uint16_t a_dest = static_cast<uint16_t>(0x5u << h);   // CTA h of both pairs
             int stage = 0;
             uint32_t phase = 0, issued = 0, issued_phase = 0;
             bool ok = true;
-            for (int t = pair; t < total && ok; t += npairs) {
-                int mb, nb;
-                tile_of(t, mb, nb);
-                const int a_row = mb * kBM + static_cast<int>(rank) * kHalf;
-                const int b_row = nb * kBN + static_cast<int>(rank) * kHalf;
-                const int rb_a = mb * 2 + static_cast<int>(rank);       // this CTA's 128-row scale block
-                const int rb_b = nb * 2;                                 // the tile's two B scale blocks
+            for (int t = cl; t < total && ok; t += ncl) {
+                int mb, sn;
+                tile_of(t, mb, sn);
+                const int nb = 2 * sn + pc;
+                const int a_row = mb * kBM + h * kHalf + pc * kAPart;
+                const int b_row = nb * kBN + h * kHalf;
+                const int rb_a = mb * 2 + h;               // this CTA's 128-row scale block of A
+                const int rb_b = nb * 2;                   // the tile's two B scale blocks
                 for (int ks = 0; ks < k_stages; ++ks) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
-                    if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * (kABytes + kBBytes));
-                    const uint32_t bar = full_leader + stage * 8;
-                    tma_load_2d_pair_bar(stage_a(stage), &tmA, bar, ks * kBKBytes, a_row);
-                    tma_load_2d_pair_bar(stage_b(stage), &tmB, bar, ks * kBKBytes, b_row);
+                    // the slot is free once both pairs' MMAs have read it
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag) ||
+                        !mbar_wait(&empty[kStages + stage], phase ^ 1u, abort_flag)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&full[stage], kStageBytes);
+                    tma_load_2d_multicast(stage_a(stage) + pc * (kAPart * kBKBytes), &tmA, &full[stage],
+                                          ks * kBKBytes, a_row, a_dest);
+                    tma_load_2d(stage_b(stage), &tmB, &full[stage], ks * kBKBytes, b_row);
                     const int atom = ks * kMmasPerStage;
-                    mbar_arrive_expect_tx(&sf_full[stage], kSfaBytes + kSfbBytes);
-                    tma_load_3d(stage_sfa(stage), &tmSFA, &sf_full[stage], 0, 0, rb_a * p.atoms_per_rowblock + atom);
-                    tma_load_3d(stage_sfb(stage), &tmSFB, &sf_full[stage], 0, 0, rb_b * p.atoms_per_rowblock + atom);
-                    tma_load_3d(stage_sfb(stage) + kMmasPerStage * kAtom, &tmSFB, &sf_full[stage], 0, 0,
+                    tma_load_3d(stage_sfa(stage), &tmSFA, &full[stage], 0, 0, rb_a * p.atoms_per_rowblock + atom);
+                    tma_load_3d(stage_sfb(stage), &tmSFB, &full[stage], 0, 0, rb_b * p.atoms_per_rowblock + atom);
+                    tma_load_3d(stage_sfb(stage) + kMmasPerStage * kAtom, &tmSFB, &full[stage], 0, 0,
                                 (rb_b + 1) * p.atoms_per_rowblock + atom);
                     issued |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
@@ -184,33 +201,31 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
                 }
             }
             for (int i = 0; i < kStages && ok; ++i) {
-                if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) ok = false;
+                if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag) ||
+                    !mbar_wait(&empty[kStages + stage], phase ^ 1u, abort_flag)) ok = false;
                 if (++stage == kStages) { stage = 0; phase ^= 1u; }
             }
             if (!ok) {
                 give_up();
-                // let this CTA's copies in flight land before the CTA exits
+                // let the copies this CTA is waiting for land before it exits
                 for (int s = 0; s < kStages; ++s)
-                    if ((issued >> s) & 1u) {
-                        mbar_wait(&sf_full[s], (issued_phase >> s) & 1u, nullptr);
-                        if (rank == 0) mbar_wait(&full[s], (issued_phase >> s) & 1u, nullptr);
-                    }
+                    if ((issued >> s) & 1u) mbar_wait(&full[s], (issued_phase >> s) & 1u, nullptr);
             }
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer (leader only)
-        if (lane == 0 && rank == 0) {
+        // ------------------------------------------------ MMA issuer (pair leaders)
+        if (lane == 0 && h == 0) {
             int stage = 0, it = 0;
             uint32_t phase = 0;
             bool ok = true;
             const uint32_t d = tmem_base + kAccCol;
-            for (int t = pair; t < total && ok; t += npairs, ++it) {
+            uint64_t *my_empty = empty + pc * kStages;
+            for (int t = cl; t < total && ok; t += ncl, ++it) {
                 if (!mbar_wait(tempty, (it & 1) ^ 1u, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 for (int ks = 0; ks < k_stages; ++ks) {
-                    if (!mbar_wait(&full[stage], phase, abort_flag) ||
-                        !mbar_wait(&sf_ready[stage], phase, abort_flag)) { ok = false; break; }
+                    if (!mbar_wait(&ready[stage], phase, abort_flag)) { ok = false; break; }
                     tc_fence_after();
                     const int nk = mmas_in(ks);
                     const uint32_t sf = tmem_base + kSfCol + stage * kSfColsPerStage;
@@ -218,34 +233,34 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
                     for (int j = 0; j < nk; ++j)
                         mma_nvf4_pair(d, sdesc_k_sw128(a0 + j * (kMmaK / 2)), sdesc_k_sw128(b0 + j * (kMmaK / 2)),
                                       kIdesc, sf + j * kSfColsPerMma, sf + j * kSfColsPerMma + 4, (ks | j) != 0);
-                    tc_commit_pair(&empty[stage], 0x3);
+                    tc_commit_pair(&my_empty[stage], 0xF);
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                tc_commit_pair(tfull, 0x3);
+                tc_commit_pair(tfull, static_cast<uint16_t>(0x3u << lead));
             }
             if (!ok) {
                 give_up();
-                tc_commit_pair(drain, 0x1);
+                tc_commit_pair(drain, static_cast<uint16_t>(1u << lead));
                 mbar_wait(drain, 0, nullptr);
             }
         }
         __syncwarp();
     } else if (warp < 2 + kSfWarps) {
-        // ------------------------------------------------ scale writers (both CTAs)
+        // ------------------------------------------------ scale writers (every CTA)
         // Lane l moves 16 bytes per atom: atom bytes l*16 .. l*16+15 are rows
         // l, 32+l, 64+l, 96+l of its 128-row block (4 scales each), i.e. the
         // four 32-bit columns of lane l for that atom.
         const int q = warp & 3;
         const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kSfCol;
-        const uint32_t ready_leader = mapa_shared(smem_u32(sf_ready), 0);
+        const uint32_t ready_leader = mapa_shared(smem_u32(ready), lead);
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
-        for (int t = pair; t < total && ok; t += npairs) {
+        for (int t = cl; t < total && ok; t += ncl) {
             for (int ks = 0; ks < k_stages; ++ks) {
                 int w = 1;
-                if (lane == 0) w = mbar_wait(&sf_full[stage], phase, abort_flag) ? 1 : 0;
+                if (lane == 0) w = mbar_wait(&full[stage], phase, abort_flag) ? 1 : 0;
                 if (!__shfl_sync(0xffffffffu, w, 0)) {
                     if (lane == 0) give_up();
                     ok = false;
@@ -271,23 +286,24 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
             }
         }
     } else {
-        // ------------------------------------------------ epilogue (both CTAs)
+        // ------------------------------------------------ epilogue (every CTA)
         // Each warp owns 32 accumulator rows (its lane quarter) x 128 columns.
         // After handing the accumulator back it writes the rounded rows in two
         // 32 x 64 boxes through its own 4 KB staging buffer (128-byte swizzle:
         // 16-byte chunk c of row r sits at chunk c ^ (r % 8)), stored by TMA
-        // as whole 128-byte lines; rows past M and columns past N are clipped.
+        // as whole 128-byte lines.
         const int e = warp - 2 - kSfWarps;
         const int q = warp & 3;
         const int half = e / 4;                               // which 128 columns of the tile
-        const uint32_t tempty_leader = mapa_shared(smem_u32(tempty), 0);
+        const uint32_t tempty_leader = mapa_shared(smem_u32(tempty), lead);
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kAccCol + half * (kBN / 2);
         const uint32_t box = smem_u32(out_stage + e * kOutBytes);
         if (lane == 0) tma_prefetch_desc(&tmY);
         int it = 0;
-        for (int t = pair; t < total; t += npairs, ++it) {
-            int mb, nb;
-            tile_of(t, mb, nb);
+        for (int t = cl; t < total; t += ncl, ++it) {
+            int mb, sn;
+            tile_of(t, mb, sn);
+            const int nb = 2 * sn + pc;
             int ok = 1;
             if (lane == 0) ok = mbar_wait(tfull, it & 1, abort_flag) ? 1 : 0;
             if (!__shfl_sync(0xffffffffu, ok, 0)) {
@@ -309,7 +325,7 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(tempty_leader);   // accumulator may be overwritten now
-            const int row0 = mb * kBM + static_cast<int>(rank) * kHalf + q * 32;
+            const int row0 = mb * kBM + h * kHalf + q * 32;
             const int col0 = nb * kBN + half * (kBN / 2);
             if (row0 >= p.M || col0 >= p.N) continue;
 #pragma unroll
@@ -334,16 +350,36 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
     }
 
     tc_fence_before();
-    cluster_sync();
+    cluster_sync();                      // no CTA leaves while a peer may still write or signal it
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc_pair(tmem_base, kTmemCols);
     }
 }
 
+// Clusters of this kernel that fit on the device at once (queried once per device).
+int resident_clusters(int dev, int sms) {
+    static std::once_flag once[kMaxDevices];
+    static int count[kMaxDevices];
+    std::call_once(once[dev], [&] {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(sms / kClusterCtas * kClusterCtas), 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = kSmem;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void *>(gemm_nvfp4_kernel), &cfg) !=
+                cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            n = sms / kClusterCtas;
+        }
+        count[dev] = n;
+    });
+    return count[dev];
+}
+
 }  // namespace
 
-void plan_gemm_nvfp4(int64_t M, int64_t N, int64_t K, int sms, bi_plan_t *pl) {
+void plan_gemm_nvfp4(int64_t M, int64_t N, int64_t K, int clusters, bi_plan_t *pl) {
     pl->op = BI_OP_GEMM_NVFP4;
     pl->block_m = kBM; pl->block_n = kBN; pl->block_k = kBK;
     pl->mma_m = kBM; pl->mma_n = kBN; pl->mma_k = kMmaK;
@@ -354,9 +390,18 @@ void plan_gemm_nvfp4(int64_t M, int64_t N, int64_t K, int sms, bi_plan_t *pl) {
     pl->smem_bytes = kSmem;
     pl->tiles_m = (M + kBM - 1) / kBM;
     pl->tiles_n = (N + kBN - 1) / kBN;
-    const int64_t tiles = pl->tiles_m * pl->tiles_n, pairs = sms / 2;
-    pl->grid = static_cast<int32_t>(2 * (tiles < pairs ? tiles : pairs));
+    const int64_t supertiles = pl->tiles_m * ((pl->tiles_n + 1) / 2);
+    pl->grid = static_cast<int32_t>(kClusterCtas * (supertiles < clusters ? supertiles : clusters));
     pl->reduce_tree = 0;
+}
+
+int nvfp4_clusters(int sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return sms / kClusterCtas;
+    static unsigned long long configured = 0;
+    if (ensure_smem_attr(reinterpret_cast<const void *>(gemm_nvfp4_kernel), kSmem, &configured) != BI_OK)
+        return sms / kClusterCtas;
+    return resident_clusters(dev, sms);
 }
 
 bi_status launch_gemm_nvfp4(const uint8_t *A, const uint8_t *A_sf, const uint8_t *B, const uint8_t *B_sf,
@@ -365,8 +410,9 @@ bi_status launch_gemm_nvfp4(const uint8_t *A, const uint8_t *A_sf, const uint8_t
     const DeviceInfo *info;
     bi_status st = current_device(&dev, &info);
     if (st != BI_OK) return st;
-    CUtensorMap ta, tb, tsa, tsb;
-    st = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K / 2, M, K / 2, kBKBytes, kHalf, CU_TENSOR_MAP_SWIZZLE_128B);
+    CUtensorMap ta, tb, tsa, tsb, ty;
+    st = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K / 2, M, K / 2, kBKBytes, kAPart,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != BI_OK) return st;
     st = make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K / 2, N, K / 2, kBKBytes, kHalf, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != BI_OK) return st;
@@ -380,23 +426,18 @@ bi_status launch_gemm_nvfp4(const uint8_t *A, const uint8_t *A_sf, const uint8_t
     if (st != BI_OK) return st;
     st = make_tmap_3d(&tsb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B_sf, sfb_dims, sf_strides, sf_box, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (st != BI_OK) return st;
-    CUtensorMap ty;
     st = make_tmap_2d(&ty, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Y, N, M, N * 2, kOutCols, 32, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != BI_OK) return st;
     bi_plan_t pl;
-    plan_gemm_nvfp4(M, N, K, info->sm_count, &pl);
+    plan_gemm_nvfp4(M, N, K, nvfp4_clusters(info->sm_count), &pl);
     Params p{};
-    p.Y = static_cast<uint8_t *>(Y);
     p.alpha = alpha;
     p.M = static_cast<int32_t>(M);
     p.N = static_cast<int32_t>(N);
     p.K = static_cast<int32_t>(K);
     p.atoms_per_rowblock = static_cast<int32_t>(K / 64);
     p.status = device_status_word();
-    static unsigned long long configured = 0;
-    if (ensure_smem_attr(reinterpret_cast<const void *>(gemm_nvfp4_pair_kernel), kSmem, &configured) != BI_OK)
-        return BI_ERR_CUDA;
-    gemm_nvfp4_pair_kernel<<<pl.grid, kThreads, kSmem, s>>>(ta, tb, tsa, tsb, ty, p);
+    gemm_nvfp4_kernel<<<pl.grid, kThreads, kSmem, s>>>(ta, tb, tsa, tsb, ty, p);
     return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
 }
 
