@@ -541,13 +541,14 @@ def moe_layer_sweep(bi, peaks):
 
 ATTN_B = [1, 8, 64]
 ATTN_L = 4096
+ATTN_HEADS = (32, 8, 128, 16)     # Qwen3-8B: query heads, KV heads, head_dim; KV block size
 
 
 def attention_sweep(bi, peaks):
     """Decode attention, Qwen3-8B heads (32 q, 8 kv, dim 128), paged KV (block 16),
     every sequence 4096 tokens: KV GB/s against HBM (KV bytes dominate)."""
     import torch
-    Hq, Hkv, D, bs = 32, 8, 128, 16
+    Hq, Hkv, D, bs = ATTN_HEADS
     rows = []
     g = torch.Generator(device="cuda").manual_seed(0)
     for B in ATTN_B:
@@ -740,7 +741,8 @@ def run_reference(args, dist):
 
 def profile_case(spec: str, reps: int):
     """Run one kernel configuration `reps` times (for ncu captures); no output line.
-    spec: gemm:<qkv|gate_up|down>:<M> | rmsnorm:<M>:<0|1 residual> | grouped:<gate_up|down>:<T>"""
+    spec: gemm:<qkv|gate_up|down>:<M> | rmsnorm:<M>:<0|1 residual> | grouped:<gate_up|down>:<T> |
+          nvfp4:<M> | quant:<M> | attention:<B> (decode, 4096 cached tokens per sequence)"""
     import torch
     import bi_synth as syn
     import invariant_deterministic_bi_gb300 as bi
@@ -776,6 +778,18 @@ def profile_case(spec: str, reps: int):
         X, W, off, _ = moe_inputs(rest[0], int(rest[1]))
         Y = torch.empty((X.shape[0], W.shape[1]), dtype=torch.bfloat16, device="cuda")
         fn = lambda: bi.grouped_gemm_bf16(X, W, off, Y=Y)
+    elif kind == "attention":
+        B, (Hq, Hkv, D, bs) = int(rest[0]), ATTN_HEADS
+        nb = ATTN_L // bs
+        g = torch.Generator(device="cuda").manual_seed(0)
+        K = torch.randn((B * nb, bs, Hkv, D), device="cuda", generator=g).to(torch.bfloat16)
+        V = torch.randn((B * nb, bs, Hkv, D), device="cuda", generator=g).to(torch.bfloat16)
+        table = torch.randperm(B * nb, device="cuda", generator=g).to(torch.int32).view(B, nb)
+        lens = torch.full((B,), ATTN_L, dtype=torch.int32, device="cuda")
+        Q = torch.randn((B, Hq, D), device="cuda", generator=g).to(torch.bfloat16)
+        ws = torch.empty(bi.attention_decode_workspace_size(B, Hq, ATTN_L), dtype=torch.uint8, device="cuda")
+        O = torch.empty_like(Q)
+        fn = lambda: bi.attention_decode(Q, K, V, table, lens, ATTN_L, D ** -0.5, workspace=ws, O=O)
     else:
         raise SystemExit(f"unknown profile case {spec}")
     ms = time_fn(fn, reps, warm=1)

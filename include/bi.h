@@ -257,7 +257,7 @@ BI_API bi_status bi_rank_sum_rmsnorm(const void *const *parts, int32_t R, void *
  * cached tokens; token j of sequence b sits in physical block
  * block_table[b][j / block_size] at offset j % block_size:
  *   O[b][h] = sum_j softmax_j(scale * q.k_j) v_j
- * The KV range is split into fixed 256-token chunks by position alone (never
+ * The KV range is split into fixed 128-token chunks by position alone (never
  * by batch size); each chunk is reduced in a fixed order and the chunks are
  * merged in chunk order, so a sequence's output does not depend on the batch.
  *

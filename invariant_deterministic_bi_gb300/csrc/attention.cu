@@ -10,15 +10,20 @@
 // chunk results are merged in chunk order. Nothing a sequence sees depends on
 // the other sequences in the batch.
 //
-// Step 1, one CTA per (sequence, KV head, chunk), 128 threads, head_dim 128,
-//   the G = Hq/Hkv query heads of the KV head together (GQA):
-//   - scores: warp w takes tokens w, w+4, ...; lane l holds dims 4l..4l+3;
-//     per head, the 4 products are added in order and the 32 lane sums by a
-//     fixed xor butterfly; s = scale * q.k;
-//   - per head (one warp each): m = max s (exact), p = exp(s - m), l = sum p
-//     (lane-sequential, then butterfly);
-//   - values: thread t owns dimension t and adds p_j v_j[t] over the chunk's
-//     tokens in increasing order, for every head;
+// Step 1, one CTA per (sequence, KV head, chunk of kChunk = 128 tokens),
+//   256 threads, head_dim 128, the G = Hq/Hkv query heads of the KV head
+//   together (GQA):
+//   - every thread issues its share of the chunk's K rows, then V rows, as
+//     16-byte cp.async copies into shared memory (32 KB each; rows past the
+//     sequence or in an invalid block are zero-filled), so the whole chunk is
+//     in flight at once and three CTAs share an SM;
+//   - scores, once K has landed: warp w takes tokens w, w+8, ...; lane l holds
+//     dims 4l..4l+3; per head the 4 products are added in order and the 32
+//     lane sums by a fixed xor butterfly; s = scale * q.k;
+//   - per head (warp h): m = max s (exact), p = exp(s - m), l = sum p
+//     (lane-strided, then butterfly);
+//   - values, once V has landed: thread (pair of dims, head group) adds
+//     p_t v_t over the chunk's tokens in increasing order;
 //   - writes fp32 (m, l, o[0..127]) per head and chunk to the workspace.
 // Step 2, one CTA per (sequence, query head): M = max_c m_c; the output is
 //   sum_c e^{m_c - M} o_c / sum_c e^{m_c - M} l_c, chunks in order, rounded to bf16.
@@ -33,9 +38,29 @@ namespace bi {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kChunk = 256;
-constexpr int kThreads = 128;
-constexpr int kMaxGroup = 8;
+constexpr int kChunk = 128;                    // tokens per chunk: fixed, by position
+constexpr int kThreads = 256;                  // split kernel
+constexpr int kWarps = kThreads / 32;
+constexpr int kCombineThreads = 128;           // one thread per output dimension
+constexpr int kRowBytes = kD * 2;              // one token's K (or V) row of one KV head
+constexpr int kTileBytes = kChunk * kRowBytes; // 32 KB
+
+// K and V tiles, then q (G x kD fp32), scores (G x kChunk fp32), (m, l) per
+// head and the K-row offset of every token of the chunk. The value phase's
+// partial sums (kThreads x G x 8 fp32) reuse the K and V tiles.
+template <int G>
+constexpr int split_smem_bytes() {
+    return 2 * kTileBytes + (G * kD + G * kChunk + 2 * G) * 4 + kChunk * 8;
+}
+static_assert(kThreads * 8 * 8 * 4 <= 2 * kTileBytes, "value partials must fit in the K and V tiles");
+
+// 16-byte global -> shared copy; src_bytes = 0 writes 16 zero bytes and reads nothing.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 __device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
@@ -63,116 +88,219 @@ __device__ __forceinline__ bool seq_ok(const AttnParams &p, int64_t b, int &L) {
 template <int G>
 __global__ void __launch_bounds__(kThreads)
 attn_split_kernel(const AttnParams p) {
-    __shared__ float qs[G][kD];
-    __shared__ float S[G][kChunk];
-    __shared__ float ml[G][2];
+    extern __shared__ __align__(16) uint8_t smem[];
+    uint8_t *Ks = smem;                                            // [kChunk][kD] bf16, 16-byte chunks swizzled
+    uint8_t *Vs = smem + kTileBytes;                               // [kChunk][kD] bf16
+    float *qs = reinterpret_cast<float *>(smem + 2 * kTileBytes);  // [G][kD]
+    float *S = qs + G * kD;                                        // [G][kChunk]
+    float *ml = S + G * kChunk;                                    // [G][2]
+    int64_t *rowoff = reinterpret_cast<int64_t *>(ml + 2 * G);     // [kChunk], -1: no row
+    float *part = reinterpret_cast<float *>(smem);                 // value partials, after the tiles are read
     const int c = blockIdx.x, g = blockIdx.y;
     const int64_t b = blockIdx.z;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int L;
     if (!seq_ok(p, b, L)) {
-        if (threadIdx.x == 0 && c == 0 && g == 0) atomicOr(p.status, kDevBadOffsets);
+        if (tid == 0 && c == 0 && g == 0) atomicOr(p.status, kDevBadOffsets);
         return;
     }
     const int j0 = c * kChunk;
     if (j0 >= L) return;                                  // this sequence has fewer chunks
     const int n = min(kChunk, L - j0);
 
-    for (int i = threadIdx.x; i < G * kD; i += kThreads) {
-        const int h = i / kD, d = i % kD;
-        qs[h][d] = bf_at(p.Q + (b * p.Hq + g * G + h) * kD, d);
+    // element offset of each token's K (and V) row for KV head g
+    if (tid < kChunk) {
+        int64_t off = -1;
+        if (tid < n) {
+            const int j = j0 + tid;
+            const int64_t blk = p.table[b * p.max_blocks + j / p.bs];
+            if (blk >= 0 && blk < p.num_blocks)
+                off = ((blk * p.bs + j % p.bs) * p.Hkv + g) * kD;
+            else
+                atomicOr(p.status, kDevBadOffsets);
+        }
+        rowoff[tid] = off;
+    }
+    for (int i = tid; i < G * kD; i += kThreads) qs[i] = bf_at(p.Q + (b * p.Hq + g * G) * kD, i);
+    __syncthreads();
+
+    // K rows (chunk x of row t at chunk x ^ (t % 8)), then V rows; missing rows are zero-filled
+#pragma unroll
+    for (int which = 0; which < 2; ++which) {
+        const uint16_t *base = which == 0 ? p.K : p.V;
+        const uint32_t dst0 = smem_u32(which == 0 ? Ks : Vs);
+#pragma unroll
+        for (int r = 0; r < kChunk * 16 / kThreads; ++r) {
+            const int i = tid + r * kThreads;
+            const int t = i >> 4, x = i & 15;
+            const int64_t off = rowoff[t];
+            const int xs = which == 0 ? (x ^ (t & 7)) : x;
+            cp_async_16(dst0 + t * kRowBytes + xs * 16, off >= 0 ? base + off + x * 8 : base, off >= 0 ? 16u : 0u);
+        }
+        cp_async_commit();
+    }
+    cp_async_wait<1>();                                   // this thread's K copies
+    __syncthreads();                                      // everyone's
+
+    // scores: lane = token (t = 32*(warp%4) + lane), warp/4 picks every other head;
+    // q.k adds the 128 products in dimension order
+    {
+        const int t = (warp & 3) * 32 + lane;
+        const int h0 = warp >> 2;
+        if (G > 1 || h0 == 0) {
+            constexpr int NH = G > 1 ? G / 2 : 1;
+            float acc[NH];
+#pragma unroll
+            for (int i = 0; i < NH; ++i) acc[i] = 0.0f;
+            const uint8_t *krow = Ks + t * kRowBytes;
+#pragma unroll 4
+            for (int x = 0; x < 16; ++x) {
+                const uint4 kv = *reinterpret_cast<const uint4 *>(krow + ((x ^ (t & 7)) << 4));
+                const float k[8] = {bf_lo(kv.x), bf_hi(kv.x), bf_lo(kv.y), bf_hi(kv.y),
+                                    bf_lo(kv.z), bf_hi(kv.z), bf_lo(kv.w), bf_hi(kv.w)};
+#pragma unroll
+                for (int i = 0; i < NH; ++i) {
+                    const float *q = qs + (h0 + (G > 1 ? 2 * i : 0)) * kD + x * 8;
+                    const float4 qa = *reinterpret_cast<const float4 *>(q);
+                    const float4 qb = *reinterpret_cast<const float4 *>(q + 4);
+                    float sc = acc[i];
+                    sc = __fmaf_rn(qa.x, k[0], sc);
+                    sc = __fmaf_rn(qa.y, k[1], sc);
+                    sc = __fmaf_rn(qa.z, k[2], sc);
+                    sc = __fmaf_rn(qa.w, k[3], sc);
+                    sc = __fmaf_rn(qb.x, k[4], sc);
+                    sc = __fmaf_rn(qb.y, k[5], sc);
+                    sc = __fmaf_rn(qb.z, k[6], sc);
+                    sc = __fmaf_rn(qb.w, k[7], sc);
+                    acc[i] = sc;
+                }
+            }
+            if (t < n) {
+                const bool valid = rowoff[t] >= 0;
+#pragma unroll
+                for (int i = 0; i < NH; ++i)
+                    S[(h0 + (G > 1 ? 2 * i : 0)) * kChunk + t] = valid ? __fmul_rn(acc[i], p.scale) : -INFINITY;
+            }
+        }
     }
     __syncthreads();
 
-    // scores
-    bool bad = false;
-    for (int t = warp; t < n; t += kThreads / 32) {
-        const int j = j0 + t;
-        const int64_t blk = p.table[b * p.max_blocks + j / p.bs];
-        if (blk < 0 || blk >= p.num_blocks) {
-            bad = true;
-            if (lane == 0)
-                for (int h = 0; h < G; ++h) S[h][t] = -INFINITY;
-            continue;
-        }
-        const uint16_t *k = p.K + ((blk * p.bs + j % p.bs) * p.Hkv + g) * kD;
-        const uint2 kv = *reinterpret_cast<const uint2 *>(k + 4 * lane);
-        const float k0 = bf_lo(kv.x), k1 = bf_hi(kv.x), k2 = bf_lo(kv.y), k3 = bf_hi(kv.y);
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-            float s = qs[h][4 * lane] * k0;
-            s = __fmaf_rn(qs[h][4 * lane + 1], k1, s);
-            s = __fmaf_rn(qs[h][4 * lane + 2], k2, s);
-            s = __fmaf_rn(qs[h][4 * lane + 3], k3, s);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-            if (lane == 0) S[h][t] = __fmul_rn(s, p.scale);
-        }
-    }
-    if (bad && lane == 0) atomicOr(p.status, kDevBadOffsets);
-    __syncthreads();
-
-    // per head: max, exponentials, sum (head h on warp h % 4)
-    for (int h = warp; h < G; h += kThreads / 32) {
+    // per head: max, exponentials, sum (head h on warp h)
+    if (warp < G) {
+        const int h = warp;
         float m = -INFINITY;
-        for (int t = lane; t < n; t += 32) m = fmaxf(m, S[h][t]);
+        for (int t = lane; t < n; t += 32) m = fmaxf(m, S[h * kChunk + t]);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         float l = 0.0f;
         for (int t = lane; t < n; t += 32) {
-            const float e = expf(S[h][t] - m);
-            S[h][t] = e;
+            const float e = expf(S[h * kChunk + t] - m);
+            S[h * kChunk + t] = e;
             l += e;
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
         if (lane == 0) {
-            ml[h][0] = m;
-            ml[h][1] = l;
+            ml[2 * h] = m;
+            ml[2 * h + 1] = l;
         }
     }
+    cp_async_wait<0>();                                   // this thread's V copies
     __syncthreads();
 
-    // values: thread t owns dimension t
-    const int d = threadIdx.x;
-    float acc[G];
+    // values: thread (dims 8*dg .. 8*dg+7, token group tg) adds p_t v_t over
+    // tokens tg, tg+16, ... in order, for every head; the 16 token groups'
+    // partial sums are then added in group order
+    const int dg = tid & 15, tg = tid >> 4;
+    float acc[G][8];
 #pragma unroll
-    for (int h = 0; h < G; ++h) acc[h] = 0.0f;
-    for (int t = 0; t < n; ++t) {
-        const int j = j0 + t;
-        const int64_t blk = p.table[b * p.max_blocks + j / p.bs];
-        if (blk < 0 || blk >= p.num_blocks) continue;
-        const float v = bf_at(p.V + ((blk * p.bs + j % p.bs) * p.Hkv + g) * kD, d);
+    for (int h = 0; h < G; ++h)
 #pragma unroll
-        for (int h = 0; h < G; ++h) acc[h] = __fmaf_rn(S[h][t], v, acc[h]);
+        for (int k = 0; k < 8; ++k) acc[h][k] = 0.0f;
+#pragma unroll 2
+    for (int t = tg; t < n; t += 16) {
+        const uint4 vv = *reinterpret_cast<const uint4 *>(Vs + t * kRowBytes + dg * 16);
+        const float v[8] = {bf_lo(vv.x), bf_hi(vv.x), bf_lo(vv.y), bf_hi(vv.y),
+                            bf_lo(vv.z), bf_hi(vv.z), bf_lo(vv.w), bf_hi(vv.w)};
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            const float e = S[h * kChunk + t];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) acc[h][k] = __fmaf_rn(e, v[k], acc[h][k]);
+        }
     }
+    __syncthreads();                                      // tiles no longer read: reuse them
 #pragma unroll
     for (int h = 0; h < G; ++h) {
+        float4 *dst = reinterpret_cast<float4 *>(part + (tg * G + h) * kD + dg * 8);
+        dst[0] = make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
+        dst[1] = make_float4(acc[h][4], acc[h][5], acc[h][6], acc[h][7]);
+    }
+    __syncthreads();
+    for (int o = tid; o < G * kD; o += kThreads) {
+        const int h = o / kD, d = o % kD;
+        float sum = part[h * kD + d];
+#pragma unroll
+        for (int gg = 1; gg < 16; ++gg) sum += part[(gg * G + h) * kD + d];
         float *w = p.ws + (((b * p.Hq + g * G + h) * p.chunks) + c) * (kD + 2);
-        w[2 + d] = acc[h];
+        w[2 + d] = sum;
         if (d == 0) {
-            w[0] = ml[h][0];
-            w[1] = ml[h][1];
+            w[0] = ml[2 * h];
+            w[1] = ml[2 * h + 1];
         }
     }
 }
 
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kCombineThreads)
 attn_combine_kernel(const AttnParams p) {
+    // Chunk statistics go through shared memory in tiles of kCombineThreads
+    // chunks, loaded in parallel; the arithmetic is the sequential chunk-order
+    // merge described at the top of the file (the maximum is exact in any order).
+    __shared__ float red[kCombineThreads / 32];
+    __shared__ float fw[kCombineThreads];     // e^{m_c - M} for the tile's chunks
+    __shared__ float fl[kCombineThreads];     // l_c
     const int h = blockIdx.x;
     const int64_t b = blockIdx.y;
-    const int d = threadIdx.x;
+    const int d = threadIdx.x, lane = d & 31, warp = d >> 5;
     int L;
     if (!seq_ok(p, b, L)) return;
     const int nc = (L + kChunk - 1) / kChunk;
     const float *w = p.ws + (b * p.Hq + h) * p.chunks * (kD + 2);
-    float M = -INFINITY;
-    for (int c = 0; c < nc; ++c) M = fmaxf(M, w[c * (kD + 2)]);
+    float m = -INFINITY;
+    for (int c = d; c < nc; c += kCombineThreads) m = fmaxf(m, w[static_cast<int64_t>(c) * (kD + 2)]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    float M = red[0];
+#pragma unroll
+    for (int i = 1; i < kCombineThreads / 32; ++i) M = fmaxf(M, red[i]);
     float num = 0.0f, den = 0.0f;
-    for (int c = 0; c < nc; ++c) {
-        const float f = expf(w[c * (kD + 2)] - M);
-        num = __fmaf_rn(f, w[c * (kD + 2) + 2 + d], num);
-        den = __fmaf_rn(f, w[c * (kD + 2) + 1], den);
+    for (int c0 = 0; c0 < nc; c0 += kCombineThreads) {
+        const int nt = min(kCombineThreads, nc - c0);
+        __syncthreads();                                   // previous tile fully consumed
+        if (d < nt) {
+            const float *wc = w + static_cast<int64_t>(c0 + d) * (kD + 2);
+            fw[d] = expf(wc[0] - M);
+            fl[d] = wc[1];
+        }
+        __syncthreads();
+        const float *oc = w + static_cast<int64_t>(c0) * (kD + 2) + 2 + d;
+        int c = 0;
+        for (; c + 8 <= nt; c += 8) {                      // 8 independent loads in flight
+            float o8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) o8[i] = oc[static_cast<int64_t>(c + i) * (kD + 2)];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                num = __fmaf_rn(fw[c + i], o8[i], num);
+                den = __fmaf_rn(fw[c + i], fl[c + i], den);
+            }
+        }
+        for (; c < nt; ++c) {
+            num = __fmaf_rn(fw[c], oc[static_cast<int64_t>(c) * (kD + 2)], num);
+            den = __fmaf_rn(fw[c], fl[c], den);
+        }
     }
     const float o = __fdiv_rn(num, den);
     const uint32_t packed = pack_bf16x2(__float_as_uint(o), 0u);
@@ -185,6 +313,21 @@ int64_t attention_decode_workspace_bytes(int64_t B, int32_t Hq, int32_t max_len)
     const int64_t chunks = (max_len + kChunk - 1) / kChunk;
     return B * Hq * chunks * (kD + 2) * static_cast<int64_t>(sizeof(float));
 }
+
+template <int G>
+bi_status launch_split(const dim3 &grid, const AttnParams &p, cudaStream_t s) {
+    static unsigned long long configured = 0;
+    if (ensure_smem_attr(reinterpret_cast<const void *>(attn_split_kernel<G>), split_smem_bytes<G>(), &configured) !=
+        BI_OK)
+        return BI_ERR_CUDA;
+    attn_split_kernel<G><<<grid, kThreads, split_smem_bytes<G>(), s>>>(p);
+    return BI_OK;
+}
+#define SPLIT_LAUNCH(G)                                    \
+    do {                                                   \
+        const bi_status st_ = launch_split<G>(grid1, p, s); \
+        if (st_ != BI_OK) return st_;                      \
+    } while (0)
 
 bi_status launch_attention_decode(const void *Q, const void *K, const void *V, const int32_t *table,
                                   int32_t max_blocks, int64_t num_blocks, const int32_t *lens, int64_t B, int32_t Hq,
@@ -211,13 +354,13 @@ bi_status launch_attention_decode(const void *Q, const void *K, const void *V, c
     const int G = Hq / Hkv;
     const dim3 grid1(p.chunks, Hkv, static_cast<unsigned>(B));
     switch (G) {
-        case 1: attn_split_kernel<1><<<grid1, kThreads, 0, s>>>(p); break;
-        case 2: attn_split_kernel<2><<<grid1, kThreads, 0, s>>>(p); break;
-        case 4: attn_split_kernel<4><<<grid1, kThreads, 0, s>>>(p); break;
-        case 8: attn_split_kernel<8><<<grid1, kThreads, 0, s>>>(p); break;
+        case 1: SPLIT_LAUNCH(1); break;
+        case 2: SPLIT_LAUNCH(2); break;
+        case 4: SPLIT_LAUNCH(4); break;
+        case 8: SPLIT_LAUNCH(8); break;
         default: return BI_ERR_UNSUPPORTED;
     }
-    attn_combine_kernel<<<dim3(Hq, static_cast<unsigned>(B)), kThreads, 0, s>>>(p);
+    attn_combine_kernel<<<dim3(Hq, static_cast<unsigned>(B)), kCombineThreads, 0, s>>>(p);
     return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
 }
 

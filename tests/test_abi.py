@@ -147,6 +147,6 @@ def test_other_calls_reject_bad_arguments(lib):
     assert call(ok_args(wsb=100)) == 1              # workspace too small
     assert call(ok_args(Q=FAKE + 8)) == 3
     assert call(ok_args(B=0)) == 0
-    assert so.bi_attention_decode_workspace_size(4, 32, 300) == 4 * 32 * 2 * 130 * 4
+    assert so.bi_attention_decode_workspace_size(4, 32, 300) == 4 * 32 * 3 * 130 * 4   # ceil(300 / 128) chunks
     assert so.bi_check_wait_timeout(0, None) == 1
     assert so.bi_plan(99, 1, 1, 1, 152, ctypes.byref(lib.Plan())) == 1
