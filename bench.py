@@ -424,7 +424,8 @@ def nvfp4_sweep(bi, peaks):
     Bd, SBd = torch.from_numpy(d["B"]).cuda(), torch.from_numpy(d["SB_il"]).cuda()
     rows, fp4_peak, peak_note = [], None, "unmeasured"
     # dense fp4 peak on this GPU: cuBLASLt NVFP4 at 8192^3, if torch exposes it
-    if os.environ.get("BI_BENCH_CUBLASLT_FP4", "0") == "1":
+    use_lt = os.environ.get("BI_BENCH_CUBLASLT_FP4", "1") == "1"
+    if use_lt:
         g = torch.Generator(device="cuda").manual_seed(0)
         big = torch.randint(0, 256, (8192, 4096), dtype=torch.uint8, device="cuda", generator=g)
         sc = torch.full((8192 * 512,), 0x38, dtype=torch.uint8, device="cuda")
@@ -449,7 +450,7 @@ def nvfp4_sweep(bi, peaks):
              "frac_fp4_peak": round(flops / (t * 1e-3) / 1e12 / fp4_peak, 3),
              "gbs": round(nbytes / (t * 1e-3) / 1e9, 0),
              "frac_hbm_measured": round(nbytes / (t * 1e-3) / 1e9 / peaks["hbm_gbs"], 3)}
-        f = torch_nvfp4_mm(A, SA, Bd, SBd, M, NVFP4_N, NVFP4_K) if os.environ.get("BI_BENCH_CUBLASLT_FP4") == "1" \
+        f = torch_nvfp4_mm(A, SA, Bd, SBd, M, NVFP4_N, NVFP4_K) if use_lt \
             else None
         if f is not None:
             t2 = time_fn(f, 50 if M <= 256 else 10)
