@@ -1,7 +1,8 @@
-// gemm_bf16_pair.cu -- batch-invariant dense bf16 linear layer on CTA pairs (tcgen05 cta_group::2).
+// gemm_bf16_pair.cu -- batch-invariant bf16 linear layers on CTA pairs (tcgen05 cta_group::2):
+// the dense layer Y = X W^T, and the MoE-grouped layer (for each expert e with
+// rows [off[e], off[e+1]) of the expert-sorted X: Y_rows = X_rows W[e]^T).
 //
-// Y = X W^T with 256 x 256 output tiles, each computed by a cluster of two CTAs
-// on two SMs:
+// 256 x 256 output tiles, each computed by a cluster of two CTAs on two SMs:
 //   - each CTA's warp 0 TMA-loads its own 128 rows of the A tile and its own
 //     half (128 rows) of the B tile per 64-wide K step into a 6-stage ring;
 //     both CTAs' copies complete on the even (leader) CTA's "full" barrier;
@@ -19,9 +20,19 @@
 // and reads from shared memory per MMA (64 instead of 96 bytes per clock at
 // full rate) and cuts L2-to-SM traffic per output by a third.
 //
+// Grouped: a tile never spans two experts -- each expert's rows are cut into
+// 256-row tiles of their own (the last one partial), experts in order, M-tiles
+// fastest inside an expert so that pairs working at the same time share the
+// expert's weight panel in L2; the tile map is built on the device from the
+// offsets (prefix of tile counts in shared memory + binary search), with no
+// host synchronisation. An epilogue warp whose 32 rows all belong to the
+// expert stores them by TMA; one straddling the expert's last row stores the
+// rows that exist with 16-byte stores (rows past it belong to the next expert).
+//
 // Batch invariance: the tile shape, MMA instruction and K order (64-wide K
 // steps, four 16-wide MMA steps each, ascending, from zero) are the same for
-// every M; rows never interact; only which pair computes which tile depends on M.
+// every M and every routing, and the same in both modes; rows never interact;
+// only which pair computes which tile depends on M (or on the routing).
 #include <cuda_bf16.h>
 
 #include "bi_internal.h"
@@ -45,37 +56,61 @@ constexpr int kOutCols = 64;                    // bf16 columns per output box (
 constexpr int kOutBytes = 32 * kOutCols * 2;    // one 32-row box
 constexpr int kEpiWarps = 4;
 constexpr int kBarBytes = 256;
-constexpr int kSmem = 1024 + kStages * kStageBytes + kEpiWarps * 2 * kOutBytes + kBarBytes;
+constexpr int kMaxExperts = 1024;
+constexpr int kSchedBytes = 2 * (kMaxExperts + 1) * 4;
+// dense: two staging boxes per epilogue warp; grouped: one, plus the tile map
+template <bool GROUPED>
+__host__ __device__ constexpr int out_boxes() { return GROUPED ? 1 : 2; }
+template <bool GROUPED>
+__host__ __device__ constexpr int smem_bytes() {
+    return 1024 + kStages * kStageBytes + kEpiWarps * out_boxes<GROUPED>() * kOutBytes + kBarBytes +
+           (GROUPED ? kSchedBytes : 0);
+}
+static_assert(smem_bytes<true>() <= 232448 && smem_bytes<false>() <= 232448, "shared memory per CTA");
 constexpr int kTmemCols = 512;
 
 struct Params {
-    int32_t M, N, K;
+    int32_t M, N, K;           // dense: M rows; grouped: M = offsets[E] (all rows)
+    const int32_t *offsets;    // grouped: device offsets [E+1]
+    int32_t E;                 // grouped: experts
+    uint8_t *Yg;               // grouped: Y (dense N-strided rows), for rows stored without TMA
     unsigned *status;
 };
 
+struct Tile {
+    int32_t a_row;     // first row of the pair's 256-row A tile
+    int32_t row_end;   // rows >= row_end are not stored
+    int32_t n0;        // first output column
+    int32_t b_row;     // first row of the pair's 256-row B tile
+};
+
+template <bool GROUPED>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmY, const Params p) {
     constexpr uint32_t kIdesc = idesc_bf16(kBM, kBN);
+    constexpr int kBoxes = out_boxes<GROUPED>();
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sA = smem;
     uint8_t *sB = smem + kStages * kABytes;
-    uint8_t *out_stage = smem + kStages * kStageBytes;   // 2 staging boxes per epilogue warp
-    uint64_t *full = reinterpret_cast<uint64_t *>(out_stage + kEpiWarps * 2 * kOutBytes);
+    uint8_t *out_stage = smem + kStages * kStageBytes;   // kBoxes staging boxes per epilogue warp
+    uint64_t *full = reinterpret_cast<uint64_t *>(out_stage + kEpiWarps * kBoxes * kOutBytes);
     uint64_t *empty = full + kStages;
     uint64_t *tfull = empty + kStages;
     uint64_t *tempty = tfull + 2;
     uint64_t *drain = tempty + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    int *total_s = reinterpret_cast<int *>(tmem_slot + 2);
+    int *off_s = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(full) + kBarBytes);   // grouped only
+    int *pre_s = off_s + (kMaxExperts + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();          // 0: leader (issues the MMAs)
     const int pair = static_cast<int>(blockIdx.x >> 1), npairs = static_cast<int>(gridDim.x >> 1);
     const int num_m = (p.M + kBM - 1) / kBM;
     const int num_n = (p.N + kBN - 1) / kBN;
-    const int total = num_m * num_n;
     const int k_steps = (p.K + kBK - 1) / kBK;
 
     if (threadIdx.x == 0) {
@@ -99,19 +134,53 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         tmem_alloc_pair(tmem_slot, kTmemCols);
         tmem_relinquish_pair();
     }
+    if constexpr (GROUPED) {
+        for (int i = threadIdx.x; i <= p.E; i += kThreads) off_s[i] = p.offsets[i];
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            bool ok = off_s[0] == 0 && off_s[p.E] == p.M;
+            int acc = 0;
+            pre_s[0] = 0;
+            for (int e = 0; e < p.E; ++e) {
+                const long long c = static_cast<long long>(off_s[e + 1]) - off_s[e];
+                if (c < 0) ok = false;
+                acc += ok ? static_cast<int>((c + kBM - 1) / kBM) : 0;
+                pre_s[e + 1] = acc;
+            }
+            *total_s = ok ? acc * num_n : 0;
+            if (!ok && blockIdx.x == 0) atomicOr(p.status, kDevBadOffsets);
+        }
+    } else {
+        if (threadIdx.x == 0) *total_s = num_m * num_n;
+    }
     tc_fence_before();
     cluster_sync();                      // both CTAs' barriers exist, TMEM allocated
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    const int total = *total_s;
 
-    auto tile_of = [&](int t, int &mb, int &nb) {
-        const int per_group = kGroupM * num_n;
-        const int g = t / per_group;
-        const int first = g * kGroupM;
-        const int gm = min(kGroupM, num_m - first);
-        const int local = t - g * per_group;
-        mb = first + local % gm;
-        nb = local / gm;
+    auto tile_of = [&](int t) -> Tile {
+        if constexpr (GROUPED) {
+            const int x = t / num_n;
+            int lo = 0, hi = p.E - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (pre_s[mid] <= x) lo = mid; else hi = mid - 1;
+            }
+            const int e = lo;
+            const int mt = pre_s[e + 1] - pre_s[e];
+            const int local = t - pre_s[e] * num_n;
+            const int mb = local % mt, nb = local / mt;
+            return Tile{off_s[e] + mb * kBM, off_s[e + 1], nb * kBN, e * p.N + nb * kBN};
+        } else {
+            const int per_group = kGroupM * num_n;
+            const int g = t / per_group;
+            const int first = g * kGroupM;
+            const int gm = min(kGroupM, num_m - first);
+            const int local = t - g * per_group;
+            const int mb = first + local % gm, nb = local / gm;
+            return Tile{mb * kBM, p.M, nb * kBN, nb * kBN};
+        }
     };
 
     if (warp == 0) {
@@ -122,10 +191,9 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
             uint32_t phase = 0, issued = 0, issued_phase = 0;
             bool ok = true;
             for (int t = pair; t < total && ok; t += npairs) {
-                int mb, nb;
-                tile_of(t, mb, nb);
-                const int a_row = mb * kBM + static_cast<int>(rank) * kHalf;
-                const int b_row = nb * kBN + static_cast<int>(rank) * kHalf;
+                const Tile tl = tile_of(t);
+                const int a_row = tl.a_row + static_cast<int>(rank) * kHalf;
+                const int b_row = tl.b_row + static_cast<int>(rank) * kHalf;
                 for (int kb = 0; kb < k_steps; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
                     if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes);
@@ -191,19 +259,19 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         // ------------------------------------------------ epilogue (both CTAs)
         // Warp q owns accumulator rows 32q .. 32q+31 of its CTA. Per 64-column
         // box: two 32-column TMEM loads, bf16 rounding, then the box goes into
-        // one of the warp's two staging buffers (128-byte swizzle: 16-byte
-        // chunk c of row r at chunk c ^ (r % 8)) and out by TMA; rows past M
-        // and columns past N are clipped by the tensor map.
+        // one of the warp's staging buffers (128-byte swizzle: 16-byte chunk c
+        // of row r at chunk c ^ (r % 8)) and out by TMA; rows past M and
+        // columns past N are clipped by the tensor map. Grouped: a warp whose
+        // rows cross the end of the expert stores its rows that exist directly.
         const int q = warp & 3;
         const uint32_t tempty_leader = mapa_shared(smem_u32(tempty), 0);
-        uint8_t *boxes = out_stage + q * 2 * kOutBytes;
+        uint8_t *boxes = out_stage + q * kBoxes * kOutBytes;
         if (lane == 0) tma_prefetch_desc(&tmY);
         int it = 0;
         for (int t = pair; t < total; t += npairs, ++it) {
             const int acc = it & 1;
             const uint32_t acc_phase = (it >> 1) & 1;
-            int mb, nb;
-            tile_of(t, mb, nb);
+            const Tile tl = tile_of(t);
             int ok = 1;
             if (lane == 0) ok = mbar_wait(&tfull[acc], acc_phase, abort_flag) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -215,10 +283,12 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                 break;
             }
             tc_fence_after();
-            const int row0 = mb * kBM + static_cast<int>(rank) * kHalf + q * 32;
-            const int n0 = nb * kBN;
+            const int row0 = tl.a_row + static_cast<int>(rank) * kHalf + q * 32;
+            const int n0 = tl.n0;
+            const bool whole = !GROUPED || row0 + 32 <= tl.row_end;     // warp-uniform
+            const int64_t row = static_cast<int64_t>(row0) + lane;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
-            if (row0 < p.M) {
+            if (row0 < tl.row_end) {
 #pragma unroll 1
                 for (int bx = 0; bx < kBN / kOutCols && n0 + bx * kOutCols < p.N; ++bx) {
                     uint32_t r[32], w[32];
@@ -230,18 +300,29 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 16; ++i) w[16 + i] = pack_bf16x2(r[2 * i], r[2 * i + 1]);
-                    uint8_t *buf = boxes + (bx & 1) * kOutBytes;
-                    if (lane == 0) bulk_wait_group_read1();   // the box stored from this buffer two rounds ago has left
-                    __syncwarp();
-                    const uint32_t sb = smem_u32(buf) + lane * 128;
+                    if (whole) {
+                        uint8_t *buf = boxes + (bx % kBoxes) * kOutBytes;
+                        if (lane == 0) {      // the box last stored from this buffer has left it
+                            if constexpr (kBoxes == 2) bulk_wait_group_read1(); else bulk_wait_group_read0();
+                        }
+                        __syncwarp();
+                        const uint32_t sb = smem_u32(buf) + lane * 128;
 #pragma unroll
-                    for (int c = 0; c < kOutCols / 8; ++c)
-                        st_shared_v4(sb + ((c ^ (lane & 7)) << 4), w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_store_2d(&tmY, buf, n0 + bx * kOutCols, row0);
-                        bulk_commit_group();
+                        for (int c = 0; c < kOutCols / 8; ++c)
+                            st_shared_v4(sb + ((c ^ (lane & 7)) << 4), w[4 * c], w[4 * c + 1], w[4 * c + 2],
+                                         w[4 * c + 3]);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tmY, buf, n0 + bx * kOutCols, row0);
+                            bulk_commit_group();
+                        }
+                    } else if (row < tl.row_end) {
+                        uint8_t *yrow = p.Yg + (row * p.N + n0 + bx * kOutCols) * 2;
+#pragma unroll
+                        for (int c = 0; c < kOutCols / 8; ++c)
+                            if (n0 + bx * kOutCols + c * 8 < p.N)
+                                st_global_v4(yrow + c * 16, w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
                     }
                 }
             }
@@ -271,7 +352,7 @@ void plan_gemm_bf16(int64_t M, int64_t N, int64_t K, int sms, bi_plan_t *pl) {
     pl->split_k = 1;
     pl->stages = kStages;
     pl->threads = kThreads;
-    pl->smem_bytes = kSmem;
+    pl->smem_bytes = smem_bytes<false>();
     pl->tiles_m = (M + kBM - 1) / kBM;
     pl->tiles_n = (N + kBN - 1) / kBN;
     const int64_t tiles = pl->tiles_m * pl->tiles_n;
@@ -280,18 +361,43 @@ void plan_gemm_bf16(int64_t M, int64_t N, int64_t K, int sms, bi_plan_t *pl) {
     pl->reduce_tree = 0;
 }
 
+void plan_grouped_gemm_bf16(int64_t rows, int64_t N, int64_t K, int sms, bi_plan_t *pl) {
+    pl->op = BI_OP_GROUPED_GEMM_BF16;
+    pl->block_m = kBM; pl->block_n = kBN; pl->block_k = kBK;
+    pl->mma_m = kBM; pl->mma_n = kBN; pl->mma_k = kMmaK;
+    pl->k_steps = static_cast<int32_t>((K + kBK - 1) / kBK);
+    pl->split_k = 1;
+    pl->stages = kStages;
+    pl->threads = kThreads;
+    pl->smem_bytes = smem_bytes<true>();
+    pl->tiles_m = (rows + kBM - 1) / kBM;   // without the per-expert partial tiles
+    pl->tiles_n = (N + kBN - 1) / kBN;
+    pl->grid = sms / 2 * 2;                 // the tile count is only known on the device
+    pl->reduce_tree = 0;
+}
+
+template <bool GROUPED>
+bi_status launch_pair(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ty, const Params &p, int grid,
+                      cudaStream_t s) {
+    static unsigned long long configured = 0;
+    auto kern = gemm_bf16_pair_kernel<GROUPED>;
+    if (ensure_smem_attr(reinterpret_cast<const void *>(kern), smem_bytes<GROUPED>(), &configured) != BI_OK)
+        return BI_ERR_CUDA;
+    kern<<<grid, kThreads, smem_bytes<GROUPED>(), s>>>(ta, tb, ty, p);
+    return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
+}
+
 bi_status launch_gemm_bf16(const void *X, int64_t ldx, const void *W, int64_t ldw, void *Y, int64_t ldy,
                            int64_t M, int64_t N, int64_t K, cudaStream_t s) {
     int dev;
     const DeviceInfo *info;
     bi_status st = current_device(&dev, &info);
     if (st != BI_OK) return st;
-    CUtensorMap ta, tb;
+    CUtensorMap ta, tb, ty;
     st = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, K, M, ldx * 2, kBK, kHalf, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != BI_OK) return st;
     st = make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, K, N, ldw * 2, kBK, kHalf, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != BI_OK) return st;
-    CUtensorMap ty;
     st = make_tmap_2d(&ty, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Y, N, M, ldy * 2, kOutCols, 32, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != BI_OK) return st;
     bi_plan_t pl;
@@ -301,11 +407,38 @@ bi_status launch_gemm_bf16(const void *X, int64_t ldx, const void *W, int64_t ld
     p.N = static_cast<int32_t>(N);
     p.K = static_cast<int32_t>(K);
     p.status = device_status_word();
-    static unsigned long long configured = 0;
-    if (ensure_smem_attr(reinterpret_cast<const void *>(gemm_bf16_pair_kernel), kSmem, &configured) != BI_OK)
-        return BI_ERR_CUDA;
-    gemm_bf16_pair_kernel<<<pl.grid, kThreads, kSmem, s>>>(ta, tb, ty, p);
-    return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
+    return launch_pair<false>(ta, tb, ty, p, pl.grid, s);
+}
+
+bi_status launch_grouped_gemm_bf16(const void *X, const void *W, void *Y, const int32_t *offsets, int32_t E,
+                                   int64_t rows, int64_t N, int64_t K, cudaStream_t s) {
+    int dev;
+    const DeviceInfo *info;
+    bi_status st = current_device(&dev, &info);
+    if (st != BI_OK) return st;
+    if (E > kMaxExperts) return BI_ERR_INVALID_ARG;
+    CUtensorMap ta, tb, ty;
+    st = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, K, rows, K * 2, kBK, kHalf, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != BI_OK) return st;
+    st = make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, K, static_cast<uint64_t>(E) * N, K * 2, kBK, kHalf,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != BI_OK) return st;
+    st = make_tmap_2d(&ty, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Y, N, rows, N * 2, kOutCols, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != BI_OK) return st;
+    Params p{};
+    p.M = static_cast<int32_t>(rows);
+    p.N = static_cast<int32_t>(N);
+    p.K = static_cast<int32_t>(K);
+    p.offsets = offsets;
+    p.E = E;
+    p.Yg = static_cast<uint8_t *>(Y);
+    p.status = device_status_word();
+    // Upper bound on tiles: every expert adds at most one partial 256-row tile.
+    const int64_t tiles_n = (N + kBN - 1) / kBN;
+    const int64_t max_tiles = ((rows + kBM - 1) / kBM + E) * tiles_n;
+    const int64_t pairs = info->sm_count / 2;
+    const int grid = static_cast<int>(2 * (max_tiles < pairs ? max_tiles : pairs));
+    return launch_pair<true>(ta, tb, ty, p, grid, s);
 }
 
 }  // namespace bi
