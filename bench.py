@@ -250,6 +250,14 @@ def time_fn(fn, reps: int, warm: int = 3, graph: bool = True) -> float:
     return a.elapsed_time(b) / reps
 
 
+def l2_sets(nbytes: float, cap: int = 16) -> int:
+    """Input sets to cycle through so that consecutive calls touch more than
+    twice the L2 (a call's reads hit L2 only if it ran within the last sets)."""
+    import torch
+    l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+    return max(1, min(cap, int(2 * l2 // max(1.0, nbytes)) + 1))
+
+
 def rotate(inputs_list):
     """Cycle through several input sets so consecutive calls miss in L2."""
     state = {"i": 0}
@@ -267,7 +275,8 @@ def gemm_sweep(bi, peaks):
     import bi_synth as syn
     rows = []
     for name, (n, k) in LAYERS.items():
-        Ws = [bf16_dev(syn.to_bf16_bits(syn.normal_rows(20 + j, syn.TID_W, n, k, std=0.02))) for j in range(2)]
+        W0 = bf16_dev(syn.to_bf16_bits(syn.normal_rows(20, syn.TID_W, n, k, std=0.02)))
+        Ws = [W0] + [W0.clone() for _ in range(l2_sets(2.0 * n * k) - 1)]   # weights rotate past L2
         Xmax = bf16_dev(syn.to_bf16_bits(syn.normal_rows(0, syn.TID_X, max(M_SWEEP), k)))
         for M in M_SWEEP:
             X = Xmax[:M]
@@ -302,7 +311,7 @@ def rmsnorm_sweep(bi, peaks):
     for with_res in (True, False):
         for M in RMS_SWEEP:
             sets = []
-            nsets = max(1, min(4, (512 << 20) // max(1, 8 * M * H)))
+            nsets = l2_sets((8 if with_res else 4) * M * H)
             for j in range(nsets):
                 x, res, w, _ = syn.rmsnorm_inputs(M, H, seed=j)
                 sets.append((bf16_dev(x), bf16_dev(res) if with_res else None, bf16_dev(w),
@@ -365,9 +374,12 @@ def moe_sweep(bi, peaks):
         for T in MOE_T:
             X, W, off, exp = moe_inputs(layer, T, W=W)
             Y = torch.empty((X.shape[0], n), dtype=torch.bfloat16, device="cuda")
-            t = time_fn(lambda: bi.grouped_gemm_bf16(X, W, off, Y=Y), 20 if T <= 512 else 5)
-            flops = 2.0 * X.shape[0] * n * k
             touched = len(set(exp.tolist()))
+            # copies of the expert weights so the touched experts' weights rotate past L2
+            Wsets = [W] + [W.clone() for _ in range(l2_sets(2.0 * touched * n * k, cap=6) - 1)]
+            wsel = rotate(Wsets)
+            t = time_fn(lambda: bi.grouped_gemm_bf16(X, wsel(), off, Y=Y), 20 if T <= 512 else 5)
+            flops = 2.0 * X.shape[0] * n * k
             nbytes = 2.0 * (touched * n * k + X.shape[0] * (k + n))
             r = {"layer": layer, "T": T, "rows": int(X.shape[0]), "experts_touched": touched, "us": round(t * 1e3, 2),
                  "tflops": round(flops / (t * 1e-3) / 1e12, 1),
@@ -378,13 +390,18 @@ def moe_sweep(bi, peaks):
             offh = off.cpu().tolist()
             segs = [(e, offh[e], offh[e + 1]) for e in range(MOE_E) if offh[e + 1] > offh[e]]
 
+            wsel2 = rotate(Wsets)
+
             def per_expert():
+                Wc = wsel2()
                 for e, a, b in segs:
-                    torch.matmul(X[a:b], W[e].t(), out=Y[a:b])
+                    torch.matmul(X[a:b], Wc[e].t(), out=Y[a:b])
             t2 = time_fn(per_expert, 20 if T <= 512 else 5)
             r["cublas_per_expert_us"] = round(t2 * 1e3, 2)
             r["cost_vs_cublas_per_expert"] = round(t / t2, 3)
+            r["weight_sets"] = len(Wsets)
             rows.append(r)
+            del Wsets
         del W
         torch.cuda.empty_cache()
     return rows
@@ -422,6 +439,8 @@ def nvfp4_sweep(bi, peaks):
     import bi_synth as syn
     d = syn.nvfp4_inputs(max(NVFP4_M), NVFP4_N, NVFP4_K, seed=0)
     Bd, SBd = torch.from_numpy(d["B"]).cuda(), torch.from_numpy(d["SB_il"]).cuda()
+    bsets = [(Bd, SBd)] + [(Bd.clone(), SBd.clone())
+                           for _ in range(l2_sets(Bd.numel() + SBd.numel()) - 1)]   # weights rotate past L2
     rows, fp4_peak, peak_note = [], None, "unmeasured"
     # dense fp4 peak on this GPU: cuBLASLt NVFP4 at 8192^3, if torch exposes it
     use_lt = os.environ.get("BI_BENCH_CUBLASLT_FP4", "1") == "1"
@@ -442,7 +461,8 @@ def nvfp4_sweep(bi, peaks):
         A = torch.from_numpy(d["A"][:M].copy()).cuda()
         SA = torch.from_numpy(syn.swizzle_block_scales(d["SA"][:M])).cuda()
         Y = torch.empty((M, NVFP4_N), dtype=torch.bfloat16, device="cuda")
-        t = time_fn(lambda: bi.gemm_nvfp4(A, SA, Bd, SBd, float(d["alpha"]), Y=Y), 50 if M <= 256 else 10)
+        bsel = rotate(bsets)
+        t = time_fn(lambda: bi.gemm_nvfp4(A, SA, *bsel(), float(d["alpha"]), Y=Y), 50 if M <= 256 else 10)
         flops = 2.0 * M * NVFP4_N * NVFP4_K
         nbytes = (M + NVFP4_N) * NVFP4_K * (0.5 + 1 / 16) + 2 * M * NVFP4_N
         r = {"M": M, "N": NVFP4_N, "K": NVFP4_K, "us": round(t * 1e3, 2),
@@ -473,7 +493,7 @@ def quant_sweep(bi, peaks):
     K = NVFP4_K
     rows = []
     for M in QUANT_M:
-        nsets = max(1, min(4, (512 << 20) // (2 * M * K)))
+        nsets = l2_sets(M * K * (2 + 0.5 + 1 / 16))
         sets = []
         for j in range(nsets):
             X = bf16_dev(syn.to_bf16_bits(syn.normal_rows(j, syn.TID_FP4_A, M, K)))
@@ -562,13 +582,18 @@ def attention_sweep(bi, peaks):
         Q = torch.randn((B, Hq, D), device="cuda", generator=g).to(torch.bfloat16)
         ws = torch.empty(bi.attention_decode_workspace_size(B, Hq, ATTN_L), dtype=torch.uint8, device="cuda")
         O = torch.empty_like(Q)
-        t = time_fn(lambda: bi.attention_decode(Q, K, V, table, lens, ATTN_L, D ** -0.5, workspace=ws, O=O),
-                    50 if B <= 8 else 10)
+        kvsets = [(K, V)] + [(K.clone(), V.clone()) for _ in range(l2_sets(2.0 * K.numel() * 2) - 1)]
+        kvsel = rotate(kvsets)             # the KV cache rotates past L2
+
+        def call():
+            Kc, Vc = kvsel()
+            bi.attention_decode(Q, Kc, Vc, table, lens, ATTN_L, D ** -0.5, workspace=ws, O=O)
+        t = time_fn(call, 50 if B <= 8 else 10)
         kv_bytes = 2.0 * B * ATTN_L * Hkv * D * 2
         gbs = kv_bytes / (t * 1e-3) / 1e9
         rows.append({"B": B, "L": ATTN_L, "us": round(t * 1e3, 2), "kv_gbs": round(gbs, 0),
                      "frac_hbm_measured": round(gbs / peaks["hbm_gbs"], 3)})
-        del K, V, table, lens, Q, ws, O
+        del K, V, kvsets, table, lens, Q, ws, O
     torch.cuda.empty_cache()
     return rows
 
