@@ -520,7 +520,8 @@ MOE_LAYER_T = [1, 64, 512, 8192]
 def moe_layer_sweep(bi, peaks):
     """The whole batch-invariant MoE layer (Qwen3-30B-A3B shapes): router top-8
     softmax, alignment, gather, grouped gate_up, SiLU-mul, grouped down,
-    rank-order combine. Per-stage device time (CUDA-graph replays)."""
+    rank-order combine. Per-stage device time (CUDA-graph replays), and the
+    layer with gate_up and SiLU-mul fused (checked bit-equal to the pair)."""
     import torch
     import bi_synth as syn
     n1, k1 = MOE_LAYERS["gate_up"]
@@ -538,6 +539,9 @@ def moe_layer_sweep(bi, peaks):
         act = bi.silu_mul(gu)
         y = bi.grouped_gemm_bf16(act, W2, off)
         o = bi.moe_combine(y, pos, w)
+        act_f = bi.grouped_gemm_silu_bf16(X, W1, off)
+        if not torch.equal(act_f.view(torch.int16), act.view(torch.int16)):
+            raise RuntimeError(f"fused gate_up + SiLU-mul differs from the unfused pair at T={T}")
         reps = 50 if T <= 512 else 10
         stages = {
             "topk_softmax": lambda: bi.moe_topk_softmax(logits, MOE_TOPK),
@@ -549,12 +553,16 @@ def moe_layer_sweep(bi, peaks):
             "combine": lambda: bi.moe_combine(y, pos, w, out=o),
         }
         times = {name: round(time_fn(fn, reps) * 1e3, 2) for name, fn in stages.items()}
+        fused_us = round(time_fn(lambda: bi.grouped_gemm_silu_bf16(X, W1, off, act=act_f), reps) * 1e3, 2)
         total_us = sum(times.values())
+        total_fused = total_us - times["grouped_gate_up"] - times["silu_mul"] + fused_us
         flops = 2.0 * T * MOE_TOPK * (n1 * k1 + n2 * k2)
         out.append({"T": T, "us_by_stage": times, "us_total": round(total_us, 2),
                     "gemm_share": round((times["grouped_gate_up"] + times["grouped_down"]) / total_us, 3),
-                    "tflops_layer": round(flops / (total_us * 1e-6) / 1e12, 1)})
-        del hidden, logits, ids, w, off, rt, pos, X, gu, act, y, o
+                    "tflops_layer": round(flops / (total_us * 1e-6) / 1e12, 1),
+                    "fused_gate_up_silu_us": fused_us, "us_total_fused": round(total_fused, 2),
+                    "tflops_layer_fused": round(flops / (total_fused * 1e-6) / 1e12, 1)})
+        del hidden, logits, ids, w, off, rt, pos, X, gu, act, act_f, y, o
     del W1, W2
     torch.cuda.empty_cache()
     return out

@@ -101,6 +101,28 @@ BI_API bi_status bi_grouped_gemm_bf16(const void *X, const void *W, void *Y,
                                int64_t N, int64_t K, bi_stream stream);
 
 /*
+ * bi_grouped_gemm_silu_bf16 -- the MoE gate_up expert linear with the SiLU-mul
+ * of the layer (bi_silu_mul) applied in its epilogue.
+ *
+ * For row r of expert e:  g = bf16(X[r] W[e][j]^T), u = bf16(X[r] W[e][I + j]^T)
+ * (each exactly as bi_grouped_gemm_bf16 computes it) and
+ *   act[r][j] = bf16( silu(g) * u ),  silu(g) computed as bi_silu_mul does,
+ * so the result equals bi_grouped_gemm_bf16 (N = 2I) followed by bi_silu_mul,
+ * bit for bit, without writing and re-reading the [rows][2I] intermediate.
+ * The pages' MoE layers (vllm-ascend guide, Tested Models) have no fused
+ * counterpart; this is the same layer with one pass over memory fewer.
+ *
+ *   X        bf16 [rows][K]     expert-sorted activations (dense, ld = K)
+ *   W        bf16 [E][2I][K]    per expert: I gate rows, then I up rows (dense)
+ *   act      bf16 [rows][I]     output (dense, ld = I)
+ *   expert_offsets  as for bi_grouped_gemm_bf16 (same checks, same status)
+ * Requirements: 1 <= E <= 1024; K % 8 == 0; I % 128 == 0; 2*E*I < 2^31.
+ */
+BI_API bi_status bi_grouped_gemm_silu_bf16(const void *X, const void *W, void *act,
+                                           const int32_t *expert_offsets, int32_t E, int64_t rows,
+                                           int64_t I, int64_t K, bi_stream stream);
+
+/*
  * bi_gemm_nvfp4 -- batch-invariant block-scaled NVFP4 linear layer.
  *
  * vLLM PR #39912 ("NVFP4 CUTLASS batch invariant mode"): e2m1 values packed two
@@ -190,7 +212,8 @@ BI_API bi_status bi_moe_gather(const void *hidden, int64_t T, int64_t H, const i
 
 /*
  * bi_silu_mul -- act[r][j] = bf16( silu(g) * u ), g = gate_up[r][j],
- * u = gate_up[r][I + j], silu(g) = g / (1 + exp(-g)), fp32 arithmetic.
+ * u = gate_up[r][I + j], silu(g) = g / (1 + exp(-g)) in fp32 with the hardware
+ * exponential and fast division (a few ulp of fp32 before the bf16 rounding).
  *   gate_up bf16 [rows][2I] ([gate | up]), act bf16 [rows][I]; I % 8 == 0.
  */
 BI_API bi_status bi_silu_mul(const void *gate_up, int64_t rows, int64_t I, void *act, bi_stream stream);
@@ -314,7 +337,7 @@ BI_API bi_status bi_attention_decode_noalloc(const void *Q, const void *K_cache,
 
 /* Operation ids for bi_plan. */
 enum { BI_OP_GEMM_BF16 = 0, BI_OP_GROUPED_GEMM_BF16 = 1, BI_OP_GEMM_NVFP4 = 2, BI_OP_RMSNORM = 3,
-       BI_OP_QUANTIZE_NVFP4 = 4 };
+       BI_OP_QUANTIZE_NVFP4 = 4, BI_OP_GROUPED_GEMM_SILU_BF16 = 5 /* N carries I */ };
 
 /*
  * bi_plan -- the launch plan a call with these sizes uses (host only, no GPU needed).

@@ -59,6 +59,7 @@ def load() -> ctypes.CDLL:
         sig = {
             "bi_gemm_bf16": [P, I64, P, I64, P, I64, I64, I64, I64, P],
             "bi_grouped_gemm_bf16": [P, P, P, P, I32, I64, I64, I64, P],
+            "bi_grouped_gemm_silu_bf16": [P, P, P, P, I32, I64, I64, I64, P],
             "bi_gemm_nvfp4": [P, P, P, P, F, P, I64, I64, I64, P],
             "bi_rmsnorm": [P, P, P, P, I64, I64, F, P],
             "bi_quantize_nvfp4": [P, I64, F, P, P, I64, I64, P],
@@ -161,6 +162,29 @@ def grouped_gemm_bf16(X, W, offsets, Y=None, stream=None):
     _check(load().bi_grouped_gemm_bf16(_ptr(X), _ptr(W), _ptr(Y), _ptr(offsets), E, rows, N, K, _stream(stream)),
            "bi_grouped_gemm_bf16")
     return Y
+
+
+def grouped_gemm_silu_bf16(X, W, offsets, act=None, stream=None):
+    """MoE gate_up with SiLU-mul fused: act[r] = silu(X[r] Wg[e]^T) * (X[r] Wu[e]^T),
+    gate and up rounded to bf16 first, for rows r in [offsets[e], offsets[e+1]).
+
+    X [rows,K], W [E,2I,K] bf16 (gate rows then up rows; contiguous); offsets int32 [E+1]."""
+    import torch
+    _dev(X, torch.bfloat16, "X"), _dev(W, torch.bfloat16, "W"), _dev(offsets, torch.int32, "offsets")
+    if not (X.is_contiguous() and W.is_contiguous() and offsets.is_contiguous()):
+        raise ValueError("X, W and offsets must be contiguous")
+    E, N2, K = W.shape
+    rows, I = X.shape[0], N2 // 2
+    if X.shape[1] != K or offsets.numel() != E + 1 or N2 % 2:
+        raise ValueError("shape mismatch")
+    if act is None:
+        act = torch.empty((rows, I), dtype=torch.bfloat16, device=X.device)
+    _dev(act, torch.bfloat16, "act")
+    if act.shape != (rows, I) or not act.is_contiguous():
+        raise ValueError("act must be contiguous [rows, I]")
+    _check(load().bi_grouped_gemm_silu_bf16(_ptr(X), _ptr(W), _ptr(act), _ptr(offsets), E, rows, I, K,
+                                            _stream(stream)), "bi_grouped_gemm_silu_bf16")
+    return act
 
 
 def gemm_nvfp4(A, A_sf, B, B_sf, alpha: float, Y=None, stream=None):

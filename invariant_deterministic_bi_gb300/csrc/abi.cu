@@ -155,6 +155,19 @@ bi_status bi_grouped_gemm_bf16(const void *X, const void *W, void *Y, const int3
     return launch_grouped_gemm_bf16(X, W, Y, expert_offsets, E, rows, N, K, as_stream(stream));
 }
 
+bi_status bi_grouped_gemm_silu_bf16(const void *X, const void *W, void *act, const int32_t *expert_offsets, int32_t E,
+                                    int64_t rows, int64_t I, int64_t K, bi_stream stream) {
+    if (E < 1 || E > 1024 || rows < 0 || I < 0 || K <= 0 || rows >= kI32Max || K >= kI32Max ||
+        2 * static_cast<int64_t>(E) * I >= kI32Max)
+        return BI_ERR_INVALID_ARG;
+    if (rows == 0 || I == 0) return BI_OK;
+    if (!X || !W || !act || !expert_offsets) return BI_ERR_INVALID_ARG;
+    if (K % 8 != 0 || I % 128 != 0) return BI_ERR_UNSUPPORTED;
+    if (!aligned16(X) || !aligned16(W) || !aligned16(act) || (reinterpret_cast<uintptr_t>(expert_offsets) & 3u))
+        return BI_ERR_MISALIGNED;
+    return launch_grouped_gemm_silu_bf16(X, W, act, expert_offsets, E, rows, I, K, as_stream(stream));
+}
+
 bi_status bi_gemm_nvfp4(const uint8_t *A, const uint8_t *A_sf, const uint8_t *B, const uint8_t *B_sf, float alpha,
                         void *Y, int64_t M, int64_t N, int64_t K, bi_stream stream) {
     if (M < 0 || N < 0 || K <= 0 || M >= kI32Max || N >= kI32Max || K >= kI32Max) return BI_ERR_INVALID_ARG;
@@ -310,6 +323,10 @@ bi_status bi_plan(int32_t op, int64_t M, int64_t N, int64_t K, int32_t num_sms, 
     switch (op) {
         case BI_OP_GEMM_BF16: plan_gemm_bf16(M, N, K, sms, out); return BI_OK;
         case BI_OP_GROUPED_GEMM_BF16: plan_grouped_gemm_bf16(M, N, K, sms, out); return BI_OK;
+        case BI_OP_GROUPED_GEMM_SILU_BF16:
+            plan_grouped_gemm_bf16(M, 2 * N, K, sms, out);   /* the tiles of the 2I-wide gate_up product */
+            out->op = BI_OP_GROUPED_GEMM_SILU_BF16;
+            return BI_OK;
         case BI_OP_GEMM_NVFP4: plan_gemm_nvfp4(M, N, K, nvfp4_clusters(sms), out); return BI_OK;
         case BI_OP_QUANTIZE_NVFP4:
             out->op = BI_OP_QUANTIZE_NVFP4;

@@ -48,6 +48,8 @@ bi_status launch_gemm_bf16(const void *X, int64_t ldx, const void *W, int64_t ld
                            int64_t M, int64_t N, int64_t K, cudaStream_t s);
 bi_status launch_grouped_gemm_bf16(const void *X, const void *W, void *Y, const int32_t *offsets, int32_t E,
                                    int64_t rows, int64_t N, int64_t K, cudaStream_t s);
+bi_status launch_grouped_gemm_silu_bf16(const void *X, const void *W, void *act, const int32_t *offsets, int32_t E,
+                                        int64_t rows, int64_t I, int64_t K, cudaStream_t s);
 bi_status launch_gemm_nvfp4(const uint8_t *A, const uint8_t *A_sf, const uint8_t *B, const uint8_t *B_sf,
                             float alpha, void *Y, int64_t M, int64_t N, int64_t K, cudaStream_t s);
 bi_status launch_quantize_nvfp4(const void *X, int64_t ldx, float gs, uint8_t *Q, uint8_t *Q_sf, int64_t M, int64_t K,

@@ -328,6 +328,13 @@ __device__ __forceinline__ void ld_shared_v4(uint32_t saddr, uint32_t &a, uint32
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// silu(g) * u = g / (1 + e^-g) * u in fp32, with the hardware exponential and
+// the fast division: the SiLU-mul kernel and the fused gate_up epilogue both
+// use this one definition, so the two give the same bits.
+__device__ __forceinline__ float silu_mul_f32(float g, float u) {
+    return __fmul_rn(__fdividef(g, 1.0f + __expf(-g)), u);
+}
+
 // Two fp32 -> packed bf16x2, round to nearest even (low half = a).
 __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t a_bits, uint32_t b_bits) {
     uint32_t out;

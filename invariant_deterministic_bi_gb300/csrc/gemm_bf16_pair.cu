@@ -58,15 +58,26 @@ constexpr int kEpiWarps = 4;
 constexpr int kBarBytes = 256;
 constexpr int kMaxExperts = 1024;
 constexpr int kSchedBytes = 2 * (kMaxExperts + 1) * 4;
+// Modes of the kernel: the dense layer, the grouped layer, and the grouped
+// gate_up layer with SiLU-mul applied in the epilogue.
+constexpr int kDense = 0, kGrouped = 1, kGroupedSilu = 2;
 // dense: two staging boxes per epilogue warp; grouped: one, plus the tile map
-template <bool GROUPED>
-__host__ __device__ constexpr int out_boxes() { return GROUPED ? 1 : 2; }
-template <bool GROUPED>
+template <int MODE>
+__host__ __device__ constexpr int out_boxes() { return MODE == kDense ? 2 : 1; }
+template <int MODE>
 __host__ __device__ constexpr int smem_bytes() {
-    return 1024 + kStages * kStageBytes + kEpiWarps * out_boxes<GROUPED>() * kOutBytes + kBarBytes +
-           (GROUPED ? kSchedBytes : 0);
+    return 1024 + kStages * kStageBytes + kEpiWarps * out_boxes<MODE>() * kOutBytes + kBarBytes +
+           (MODE != kDense ? kSchedBytes : 0);
 }
-static_assert(smem_bytes<true>() <= 232448 && smem_bytes<false>() <= 232448, "shared memory per CTA");
+static_assert(smem_bytes<kGrouped>() <= 232448 && smem_bytes<kDense>() <= 232448, "shared memory per CTA");
+
+// act = bf16(silu(g) * u) on bf16 g and u: the arithmetic of bi_silu_mul
+// (silu_mul_f32), so the fused layer gives the same bits.
+__device__ __forceinline__ uint32_t silu_mul_bf16x2(uint32_t g2, uint32_t u2) {
+    const float g0 = __uint_as_float(g2 << 16), g1 = __uint_as_float(g2 & 0xFFFF0000u);
+    const float u0 = __uint_as_float(u2 << 16), u1 = __uint_as_float(u2 & 0xFFFF0000u);
+    return pack_bf16x2(__float_as_uint(silu_mul_f32(g0, u0)), __float_as_uint(silu_mul_f32(g1, u1)));
+}
 constexpr int kTmemCols = 512;
 
 struct Params {
@@ -84,12 +95,18 @@ struct Tile {
     int32_t b_row;     // first row of the pair's 256-row B tile
 };
 
-template <bool GROUPED>
+template <int MODE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmY, const Params p) {
     constexpr uint32_t kIdesc = idesc_bf16(kBM, kBN);
-    constexpr int kBoxes = out_boxes<GROUPED>();
+    constexpr bool GROUPED = MODE != kDense;
+    constexpr bool SILU = MODE == kGroupedSilu;
+    // SILU: a tile's 256 accumulator columns are 128 gate columns (B rows from
+    // the first half of the expert's weight) and the matching 128 up columns
+    // (B rows from the second half); it yields 128 output columns.
+    constexpr int kOutTile = SILU ? kBN / 2 : kBN;
+    constexpr int kBoxes = out_boxes<MODE>();
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sA = smem;
@@ -110,7 +127,7 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
     const uint32_t rank = cluster_ctarank();          // 0: leader (issues the MMAs)
     const int pair = static_cast<int>(blockIdx.x >> 1), npairs = static_cast<int>(gridDim.x >> 1);
     const int num_m = (p.M + kBM - 1) / kBM;
-    const int num_n = (p.N + kBN - 1) / kBN;
+    const int num_n = (p.N + kOutTile - 1) / kOutTile;
     const int k_steps = (p.K + kBK - 1) / kBK;
 
     if (threadIdx.x == 0) {
@@ -171,7 +188,10 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
             const int mt = pre_s[e + 1] - pre_s[e];
             const int local = t - pre_s[e] * num_n;
             const int mb = local % mt, nb = local / mt;
-            return Tile{off_s[e] + mb * kBM, off_s[e + 1], nb * kBN, e * p.N + nb * kBN};
+            if constexpr (SILU)   // gate rows [nb*128, +128) of W[e] in CTA 0, up rows [N + nb*128, +128) in CTA 1
+                return Tile{off_s[e] + mb * kBM, off_s[e + 1], nb * kOutTile, 2 * e * p.N + nb * kOutTile};
+            else
+                return Tile{off_s[e] + mb * kBM, off_s[e + 1], nb * kBN, e * p.N + nb * kBN};
         } else {
             const int per_group = kGroupM * num_n;
             const int g = t / per_group;
@@ -193,7 +213,7 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
             for (int t = pair; t < total && ok; t += npairs) {
                 const Tile tl = tile_of(t);
                 const int a_row = tl.a_row + static_cast<int>(rank) * kHalf;
-                const int b_row = tl.b_row + static_cast<int>(rank) * kHalf;
+                const int b_row = tl.b_row + static_cast<int>(rank) * (SILU ? p.N : kHalf);
                 for (int kb = 0; kb < k_steps; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
                     if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes);
@@ -290,16 +310,22 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
             if (row0 < tl.row_end) {
 #pragma unroll 1
-                for (int bx = 0; bx < kBN / kOutCols && n0 + bx * kOutCols < p.N; ++bx) {
+                for (int bx = 0; bx < kOutTile / kOutCols && n0 + bx * kOutCols < p.N; ++bx) {
                     uint32_t r[32], w[32];
-                    tmem_ld_32x32b_x32(taddr + bx * kOutCols, r);
-                    tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(r[2 * i], r[2 * i + 1]);
-                    tmem_ld_32x32b_x32(taddr + bx * kOutCols + 32, r);
-                    tmem_wait_ld();
+                    for (int hf = 0; hf < 2; ++hf) {
+                        tmem_ld_32x32b_x32(taddr + bx * kOutCols + hf * 32, r);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) w[16 + i] = pack_bf16x2(r[2 * i], r[2 * i + 1]);
+                        for (int i = 0; i < 16; ++i) w[16 * hf + i] = pack_bf16x2(r[2 * i], r[2 * i + 1]);
+                        if constexpr (SILU) {   // the matching up columns sit kOutTile columns further
+                            tmem_ld_32x32b_x32(taddr + kOutTile + bx * kOutCols + hf * 32, r);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                w[16 * hf + i] = silu_mul_bf16x2(w[16 * hf + i], pack_bf16x2(r[2 * i], r[2 * i + 1]));
+                        }
+                    }
                     if (whole) {
                         uint8_t *buf = boxes + (bx % kBoxes) * kOutBytes;
                         if (lane == 0) {      // the box last stored from this buffer has left it
@@ -352,7 +378,7 @@ void plan_gemm_bf16(int64_t M, int64_t N, int64_t K, int sms, bi_plan_t *pl) {
     pl->split_k = 1;
     pl->stages = kStages;
     pl->threads = kThreads;
-    pl->smem_bytes = smem_bytes<false>();
+    pl->smem_bytes = smem_bytes<kDense>();
     pl->tiles_m = (M + kBM - 1) / kBM;
     pl->tiles_n = (N + kBN - 1) / kBN;
     const int64_t tiles = pl->tiles_m * pl->tiles_n;
@@ -369,21 +395,21 @@ void plan_grouped_gemm_bf16(int64_t rows, int64_t N, int64_t K, int sms, bi_plan
     pl->split_k = 1;
     pl->stages = kStages;
     pl->threads = kThreads;
-    pl->smem_bytes = smem_bytes<true>();
+    pl->smem_bytes = smem_bytes<kGrouped>();
     pl->tiles_m = (rows + kBM - 1) / kBM;   // without the per-expert partial tiles
     pl->tiles_n = (N + kBN - 1) / kBN;
     pl->grid = sms / 2 * 2;                 // the tile count is only known on the device
     pl->reduce_tree = 0;
 }
 
-template <bool GROUPED>
+template <int MODE>
 bi_status launch_pair(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ty, const Params &p, int grid,
                       cudaStream_t s) {
     static unsigned long long configured = 0;
-    auto kern = gemm_bf16_pair_kernel<GROUPED>;
-    if (ensure_smem_attr(reinterpret_cast<const void *>(kern), smem_bytes<GROUPED>(), &configured) != BI_OK)
+    auto kern = gemm_bf16_pair_kernel<MODE>;
+    if (ensure_smem_attr(reinterpret_cast<const void *>(kern), smem_bytes<MODE>(), &configured) != BI_OK)
         return BI_ERR_CUDA;
-    kern<<<grid, kThreads, smem_bytes<GROUPED>(), s>>>(ta, tb, ty, p);
+    kern<<<grid, kThreads, smem_bytes<MODE>(), s>>>(ta, tb, ty, p);
     return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
 }
 
@@ -407,11 +433,14 @@ bi_status launch_gemm_bf16(const void *X, int64_t ldx, const void *W, int64_t ld
     p.N = static_cast<int32_t>(N);
     p.K = static_cast<int32_t>(K);
     p.status = device_status_word();
-    return launch_pair<false>(ta, tb, ty, p, pl.grid, s);
+    return launch_pair<kDense>(ta, tb, ty, p, pl.grid, s);
 }
 
-bi_status launch_grouped_gemm_bf16(const void *X, const void *W, void *Y, const int32_t *offsets, int32_t E,
-                                   int64_t rows, int64_t N, int64_t K, cudaStream_t s) {
+// Grouped launch. silu == false: Y [rows][N] = X W[e]^T with W [E][N][K].
+// silu == true: W [E][2N][K] holds each expert's gate rows then its up rows,
+// and Y [rows][N] = bf16(silu(gate) * up) with gate and up rounded to bf16.
+bi_status launch_grouped(const void *X, const void *W, void *Y, const int32_t *offsets, int32_t E, int64_t rows,
+                         int64_t N, int64_t K, bool silu, cudaStream_t s) {
     int dev;
     const DeviceInfo *info;
     bi_status st = current_device(&dev, &info);
@@ -420,8 +449,8 @@ bi_status launch_grouped_gemm_bf16(const void *X, const void *W, void *Y, const 
     CUtensorMap ta, tb, ty;
     st = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, K, rows, K * 2, kBK, kHalf, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != BI_OK) return st;
-    st = make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, K, static_cast<uint64_t>(E) * N, K * 2, kBK, kHalf,
-                      CU_TENSOR_MAP_SWIZZLE_128B);
+    st = make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, K, static_cast<uint64_t>(E) * N * (silu ? 2 : 1), K * 2,
+                      kBK, kHalf, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != BI_OK) return st;
     st = make_tmap_2d(&ty, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Y, N, rows, N * 2, kOutCols, 32, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != BI_OK) return st;
@@ -434,11 +463,22 @@ bi_status launch_grouped_gemm_bf16(const void *X, const void *W, void *Y, const 
     p.Yg = static_cast<uint8_t *>(Y);
     p.status = device_status_word();
     // Upper bound on tiles: every expert adds at most one partial 256-row tile.
-    const int64_t tiles_n = (N + kBN - 1) / kBN;
+    const int64_t out_tile = silu ? kBN / 2 : kBN;
+    const int64_t tiles_n = (N + out_tile - 1) / out_tile;
     const int64_t max_tiles = ((rows + kBM - 1) / kBM + E) * tiles_n;
     const int64_t pairs = info->sm_count / 2;
     const int grid = static_cast<int>(2 * (max_tiles < pairs ? max_tiles : pairs));
-    return launch_pair<true>(ta, tb, ty, p, grid, s);
+    return silu ? launch_pair<kGroupedSilu>(ta, tb, ty, p, grid, s) : launch_pair<kGrouped>(ta, tb, ty, p, grid, s);
+}
+
+bi_status launch_grouped_gemm_bf16(const void *X, const void *W, void *Y, const int32_t *offsets, int32_t E,
+                                   int64_t rows, int64_t N, int64_t K, cudaStream_t s) {
+    return launch_grouped(X, W, Y, offsets, E, rows, N, K, false, s);
+}
+
+bi_status launch_grouped_gemm_silu_bf16(const void *X, const void *W, void *act, const int32_t *offsets, int32_t E,
+                                        int64_t rows, int64_t I, int64_t K, cudaStream_t s) {
+    return launch_grouped(X, W, act, offsets, E, rows, I, K, true, s);
 }
 
 }  // namespace bi

@@ -183,7 +183,7 @@ gather_kernel(const uint4 *__restrict__ hidden, int64_t T, int64_t hv, const int
 }
 
 // --------------------------------------------------------------- SiLU-mul
-// act = bf16( silu(g) * u ), silu(g) = g / (1 + exp(-g)), fp32; rows are [gate | up].
+// act = bf16( silu(g) * u ), silu(g) = g / (1 + exp(-g)), fp32 (silu_mul_f32); rows are [gate | up].
 __global__ void __launch_bounds__(256)
 silu_mul_kernel(const uint4 *__restrict__ gu, int64_t rows, int64_t iv, uint4 *__restrict__ act) {
     const int64_t total = rows * iv;
@@ -196,8 +196,8 @@ silu_mul_kernel(const uint4 *__restrict__ gu, int64_t rows, int64_t iv, uint4 *_
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const float g0 = bf_lo(gw[q]), g1 = bf_hi(gw[q]);
-            const float a0 = __fmul_rn(__fdiv_rn(g0, 1.0f + expf(-g0)), bf_lo(uw[q]));
-            const float a1 = __fmul_rn(__fdiv_rn(g1, 1.0f + expf(-g1)), bf_hi(uw[q]));
+            const float a0 = silu_mul_f32(g0, bf_lo(uw[q]));
+            const float a1 = silu_mul_f32(g1, bf_hi(uw[q]));
             o[q] = pack_bf16x2(__float_as_uint(a0), __float_as_uint(a1));
         }
         __stcs(act + i, make_uint4(o[0], o[1], o[2], o[3]));

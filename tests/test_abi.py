@@ -26,7 +26,7 @@ def declared_functions():
 
 def test_header_declares_the_calls():
     names = declared_functions()
-    for n in ["bi_gemm_bf16", "bi_grouped_gemm_bf16", "bi_gemm_nvfp4", "bi_rmsnorm", "bi_plan", "bi_quantize_nvfp4", "bi_moe_topk_softmax", "bi_moe_align", "bi_moe_gather", "bi_silu_mul", "bi_moe_combine", "bi_rank_sum_rmsnorm", "bi_attention_decode", "bi_attention_decode_workspace_size",
+    for n in ["bi_gemm_bf16", "bi_grouped_gemm_bf16", "bi_grouped_gemm_silu_bf16", "bi_gemm_nvfp4", "bi_rmsnorm", "bi_plan", "bi_quantize_nvfp4", "bi_moe_topk_softmax", "bi_moe_align", "bi_moe_gather", "bi_silu_mul", "bi_moe_combine", "bi_rank_sum_rmsnorm", "bi_attention_decode", "bi_attention_decode_workspace_size",
               "bi_device_status", "bi_status_string", "bi_version", "bi_check_wait_timeout"]:
         assert n in names
 
@@ -113,6 +113,11 @@ def test_other_calls_reject_bad_arguments(lib):
     assert so.bi_grouped_gemm_bf16(FAKE, FAKE, FAKE, FAKE, 0, 8, 64, 64, None) == 1        # E < 1
     assert so.bi_grouped_gemm_bf16(FAKE, FAKE, FAKE, FAKE, 2000, 8, 64, 64, None) == 1     # E > 1024
     assert so.bi_grouped_gemm_bf16(FAKE, FAKE, FAKE, FAKE + 2, 4, 8, 64, 64, None) == 3    # offsets align
+    assert so.bi_grouped_gemm_silu_bf16(FAKE, FAKE, FAKE, FAKE, 0, 8, 768, 64, None) == 1   # E < 1
+    assert so.bi_grouped_gemm_silu_bf16(FAKE, FAKE, FAKE, FAKE, 4, 8, 96, 64, None) == 2    # I % 128
+    assert so.bi_grouped_gemm_silu_bf16(FAKE, FAKE, FAKE, FAKE, 4, 8, 768, 60, None) == 2   # K % 8
+    assert so.bi_grouped_gemm_silu_bf16(FAKE, FAKE, FAKE + 8, FAKE, 4, 8, 768, 64, None) == 3   # act align
+    assert so.bi_grouped_gemm_silu_bf16(FAKE, FAKE, FAKE, FAKE, 4, 0, 768, 64, None) == 0   # no rows
     assert so.bi_gemm_nvfp4(FAKE, FAKE, FAKE, FAKE, f(1.0), FAKE, 4, 64, 96, None) == 2    # K % 64
     assert so.bi_gemm_nvfp4(FAKE, FAKE + 4, FAKE, FAKE, f(1.0), FAKE, 4, 64, 128, None) == 3
     assert so.bi_rmsnorm(FAKE, None, FAKE, FAKE, 4, 4, f(1e-6), None) == 1                 # H < 8

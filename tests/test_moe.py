@@ -105,15 +105,19 @@ def layer_weights():
     return W1, W2, to_dev_bf16(W1), to_dev_bf16(W2)
 
 
-def gpu_layer(bi, hidden_bits, logits, W1d, W2d):
+def gpu_layer(bi, hidden_bits, logits, W1d, W2d, fused=False):
     hd, ld = to_dev_bf16(hidden_bits), to_dev(logits)
     ids, w = bi.moe_topk_softmax(ld, TOPK)
     off, rt, pos = bi.moe_align(ids, E)
     X = bi.moe_gather(hd, rt)
-    gu = bi.grouped_gemm_bf16(X, W1d, off)
-    act = bi.silu_mul(gu)
+    if fused:
+        gu = None
+        act = bi.grouped_gemm_silu_bf16(X, W1d, off)
+    else:
+        gu = bi.grouped_gemm_bf16(X, W1d, off)
+        act = bi.silu_mul(gu)
     y = bi.grouped_gemm_bf16(act, W2d, off)
-    return bits_of(bi.moe_combine(y, pos, w)), bits_of(gu)
+    return bits_of(bi.moe_combine(y, pos, w)), (bits_of(gu) if gu is not None else None)
 
 
 def test_full_layer_against_oracle_and_token_invariance(bi, layer_weights):
@@ -148,3 +152,38 @@ def test_full_layer_against_oracle_and_token_invariance(bi, layer_weights):
     for j, t in enumerate(rows[:6]):
         assert np.array_equal(o2[j], out[t]), f"token {t}: changes with co-routed tokens"
     assert bi.device_status() == bi.BI_OK
+
+
+@pytest.mark.parametrize("T", [1, 7, 64, 512, 8192])
+def test_fused_gate_up_silu_equals_unfused(bi, layer_weights, T):
+    """bi_grouped_gemm_silu_bf16 gives the bits of bi_grouped_gemm_bf16 followed by
+    bi_silu_mul, for every routed row, including partial 256-row expert tiles."""
+    _, _, W1d, _ = layer_weights
+    tok, exp, off, _ = syn.moe_routing(T, E, TOPK, seed=T)
+    X = to_dev_bf16(syn.to_bf16_bits(syn.normal_rows(T, syn.TID_HIDDEN, T, HID))[tok])
+    offd = to_dev(off)
+    ref = bits_of(bi.silu_mul(bi.grouped_gemm_bf16(X, W1d, offd)))
+    got = bits_of(bi.grouped_gemm_silu_bf16(X, W1d, offd))
+    assert np.array_equal(got, ref)
+    assert bi.device_status() == bi.BI_OK
+
+
+def test_fused_layer_equals_unfused_layer(bi, layer_weights):
+    W1, W2, W1d, W2d = layer_weights
+    T = 300
+    hidden = syn.to_bf16_bits(syn.normal_rows(7, syn.TID_HIDDEN, T, HID))
+    logits = logits_for(T, seed=7)
+    a, _ = gpu_layer(bi, hidden, logits, W1d, W2d)
+    b, _ = gpu_layer(bi, hidden, logits, W1d, W2d, fused=True)
+    assert np.array_equal(a, b)
+
+
+def test_fused_rejects_bad_offsets(bi, layer_weights):
+    import torch
+    _, _, W1d, _ = layer_weights
+    X = torch.zeros((16, HID), dtype=torch.bfloat16, device="cuda")
+    off = np.zeros(E + 1, dtype=np.int32)
+    off[5:] = 20                         # ends past the 16 rows
+    bi.grouped_gemm_silu_bf16(X, W1d, to_dev(off))
+    torch.cuda.synchronize()
+    assert bi.device_status() == bi.BI_ERR_INVALID_ARG
