@@ -17,9 +17,9 @@
 //     16-byte cp.async copies into shared memory (32 KB each; rows past the
 //     sequence or in an invalid block are zero-filled), so the whole chunk is
 //     in flight at once and three CTAs share an SM;
-//   - scores, once K has landed: warp w takes tokens w, w+8, ...; lane l holds
-//     dims 4l..4l+3; per head the 4 products are added in order and the 32
-//     lane sums by a fixed xor butterfly; s = scale * q.k;
+//   - scores, once K has landed: one lane per token, the 128 bf16 products
+//     q[d] k[d] added in dimension order by fp32 FMAs on the bf16 operands
+//     (each warp group of 4 takes every other head); s = scale * q.k;
 //   - per head (warp h): m = max s (exact), p = exp(s - m), l = sum p
 //     (lane-strided, then butterfly);
 //   - values, once V has landed: thread (pair of dims, head group) adds
@@ -53,6 +53,19 @@ constexpr int split_smem_bytes() {
     return 2 * kTileBytes + (G * kD + G * kChunk + 2 * G) * 4 + kChunk * 8;
 }
 static_assert(kThreads * 8 * 8 * 4 <= 2 * kTileBytes, "value partials must fit in the K and V tiles");
+
+// acc + a.lo * b.lo, then + a.hi * b.hi, each one fp32 FMA on bf16 operands
+// (the product of two bf16 values is exact in fp32, so this is the same as
+// widening both to fp32 first).
+__device__ __forceinline__ float fma_bf16x2(uint32_t a, uint32_t b, float acc) {
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
+        "mov.b32 {al, ah}, %1;\n\t"
+        "mov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, al, bl, %0;\n\t"
+        "fma.rn.f32.bf16 %0, ah, bh, %0;\n\t}"
+        : "+f"(acc) : "r"(a), "r"(b));
+    return acc;
+}
 
 // 16-byte global -> shared copy; src_bytes = 0 writes 16 zero bytes and reads nothing.
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes) {
@@ -91,8 +104,9 @@ attn_split_kernel(const AttnParams p) {
     extern __shared__ __align__(16) uint8_t smem[];
     uint8_t *Ks = smem;                                            // [kChunk][kD] bf16, 16-byte chunks swizzled
     uint8_t *Vs = smem + kTileBytes;                               // [kChunk][kD] bf16
-    float *qs = reinterpret_cast<float *>(smem + 2 * kTileBytes);  // [G][kD]
-    float *S = qs + G * kD;                                        // [G][kChunk]
+    float *qs = reinterpret_cast<float *>(smem + 2 * kTileBytes);  // [G][kD] bf16 (first half used)
+    uint16_t *qb = reinterpret_cast<uint16_t *>(qs);
+    float *S = qs + G * kD;                                        // [kChunk][G]
     float *ml = S + G * kChunk;                                    // [G][2]
     int64_t *rowoff = reinterpret_cast<int64_t *>(ml + 2 * G);     // [kChunk], -1: no row
     float *part = reinterpret_cast<float *>(smem);                 // value partials, after the tiles are read
@@ -121,7 +135,7 @@ attn_split_kernel(const AttnParams p) {
         }
         rowoff[tid] = off;
     }
-    for (int i = tid; i < G * kD; i += kThreads) qs[i] = bf_at(p.Q + (b * p.Hq + g * G) * kD, i);
+    for (int i = tid; i < G * kD; i += kThreads) qb[i] = p.Q[(b * p.Hq + g * G) * kD + i];
     __syncthreads();
 
     // K rows (chunk x of row t at chunk x ^ (t % 8)), then V rows; missing rows are zero-filled
@@ -156,22 +170,14 @@ attn_split_kernel(const AttnParams p) {
 #pragma unroll 4
             for (int x = 0; x < 16; ++x) {
                 const uint4 kv = *reinterpret_cast<const uint4 *>(krow + ((x ^ (t & 7)) << 4));
-                const float k[8] = {bf_lo(kv.x), bf_hi(kv.x), bf_lo(kv.y), bf_hi(kv.y),
-                                    bf_lo(kv.z), bf_hi(kv.z), bf_lo(kv.w), bf_hi(kv.w)};
 #pragma unroll
                 for (int i = 0; i < NH; ++i) {
-                    const float *q = qs + (h0 + (G > 1 ? 2 * i : 0)) * kD + x * 8;
-                    const float4 qa = *reinterpret_cast<const float4 *>(q);
-                    const float4 qb = *reinterpret_cast<const float4 *>(q + 4);
+                    const uint4 qv = *reinterpret_cast<const uint4 *>(qb + (h0 + (G > 1 ? 2 * i : 0)) * kD + x * 8);
                     float sc = acc[i];
-                    sc = __fmaf_rn(qa.x, k[0], sc);
-                    sc = __fmaf_rn(qa.y, k[1], sc);
-                    sc = __fmaf_rn(qa.z, k[2], sc);
-                    sc = __fmaf_rn(qa.w, k[3], sc);
-                    sc = __fmaf_rn(qb.x, k[4], sc);
-                    sc = __fmaf_rn(qb.y, k[5], sc);
-                    sc = __fmaf_rn(qb.z, k[6], sc);
-                    sc = __fmaf_rn(qb.w, k[7], sc);
+                    sc = fma_bf16x2(qv.x, kv.x, sc);
+                    sc = fma_bf16x2(qv.y, kv.y, sc);
+                    sc = fma_bf16x2(qv.z, kv.z, sc);
+                    sc = fma_bf16x2(qv.w, kv.w, sc);
                     acc[i] = sc;
                 }
             }
@@ -179,7 +185,7 @@ attn_split_kernel(const AttnParams p) {
                 const bool valid = rowoff[t] >= 0;
 #pragma unroll
                 for (int i = 0; i < NH; ++i)
-                    S[(h0 + (G > 1 ? 2 * i : 0)) * kChunk + t] = valid ? __fmul_rn(acc[i], p.scale) : -INFINITY;
+                    S[t * G + h0 + (G > 1 ? 2 * i : 0)] = valid ? __fmul_rn(acc[i], p.scale) : -INFINITY;
             }
         }
     }
@@ -189,13 +195,13 @@ attn_split_kernel(const AttnParams p) {
     if (warp < G) {
         const int h = warp;
         float m = -INFINITY;
-        for (int t = lane; t < n; t += 32) m = fmaxf(m, S[h * kChunk + t]);
+        for (int t = lane; t < n; t += 32) m = fmaxf(m, S[t * G + h]);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         float l = 0.0f;
         for (int t = lane; t < n; t += 32) {
-            const float e = expf(S[h * kChunk + t] - m);
-            S[h * kChunk + t] = e;
+            const float e = expf(S[t * G + h] - m);
+            S[t * G + h] = e;
             l += e;
         }
 #pragma unroll
@@ -222,12 +228,21 @@ attn_split_kernel(const AttnParams p) {
         const uint4 vv = *reinterpret_cast<const uint4 *>(Vs + t * kRowBytes + dg * 16);
         const float v[8] = {bf_lo(vv.x), bf_hi(vv.x), bf_lo(vv.y), bf_hi(vv.y),
                             bf_lo(vv.z), bf_hi(vv.z), bf_lo(vv.w), bf_hi(vv.w)};
+        float e[G];
+        if constexpr (G % 4 == 0) {
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-            const float e = S[h * kChunk + t];
+            for (int h = 0; h < G; h += 4) {
+                const float4 e4 = *reinterpret_cast<const float4 *>(S + t * G + h);
+                e[h] = e4.x, e[h + 1] = e4.y, e[h + 2] = e4.z, e[h + 3] = e4.w;
+            }
+        } else {
 #pragma unroll
-            for (int k = 0; k < 8; ++k) acc[h][k] = __fmaf_rn(e, v[k], acc[h][k]);
+            for (int h = 0; h < G; ++h) e[h] = S[t * G + h];
         }
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) acc[h][k] = __fmaf_rn(e[h], v[k], acc[h][k]);
     }
     __syncthreads();                                      // tiles no longer read: reuse them
 #pragma unroll
