@@ -82,6 +82,7 @@ constexpr int kTmemCols = 512;
 
 struct Params {
     int32_t M, N, K;           // dense: M rows; grouped: M = offsets[E] (all rows)
+    int32_t a_bytes;           // A bytes each CTA loads per K step (fewer rows when M < 128)
     const int32_t *offsets;    // grouped: device offsets [E+1]
     int32_t E;                 // grouped: experts
     uint8_t *Yg;               // grouped: Y (dense N-strided rows), for rows stored without TMA
@@ -216,7 +217,7 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                 const int b_row = tl.b_row + static_cast<int>(rank) * (SILU ? p.N : kHalf);
                 for (int kb = 0; kb < k_steps; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
-                    if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes);
+                    if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * (p.a_bytes + kBBytes));
                     const uint32_t bar = full_leader + stage * 8;
                     tma_load_2d_pair_bar(sA + stage * kABytes, &tmA, bar, kb * kBK, a_row);
                     tma_load_2d_pair_bar(sB + stage * kBBytes, &tmB, bar, kb * kBK, b_row);
@@ -419,8 +420,14 @@ bi_status launch_gemm_bf16(const void *X, int64_t ldx, const void *W, int64_t ld
     const DeviceInfo *info;
     bi_status st = current_device(&dev, &info);
     if (st != BI_OK) return st;
+    // With fewer than 128 rows, each CTA copies only the A rows that can hold
+    // data (rounded up to 16); the MMA still multiplies 128 rows, and the
+    // accumulator rows past M -- computed from whatever the rest of the tile
+    // holds -- are never stored. Rows never interact, so this changes no bit
+    // of any stored row; it only spares the copy engine the zero rows.
+    const int a_rows = M >= kHalf ? kHalf : static_cast<int>((M + 15) / 16 * 16);
     CUtensorMap ta, tb, ty;
-    st = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, K, M, ldx * 2, kBK, kHalf, CU_TENSOR_MAP_SWIZZLE_128B);
+    st = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, K, M, ldx * 2, kBK, a_rows, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != BI_OK) return st;
     st = make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, K, N, ldw * 2, kBK, kHalf, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != BI_OK) return st;
@@ -429,6 +436,7 @@ bi_status launch_gemm_bf16(const void *X, int64_t ldx, const void *W, int64_t ld
     bi_plan_t pl;
     plan_gemm_bf16(M, N, K, info->sm_count, &pl);
     Params p{};
+    p.a_bytes = a_rows * kBK * 2;
     p.M = static_cast<int32_t>(M);
     p.N = static_cast<int32_t>(N);
     p.K = static_cast<int32_t>(K);
@@ -455,6 +463,7 @@ bi_status launch_grouped(const void *X, const void *W, void *Y, const int32_t *o
     st = make_tmap_2d(&ty, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Y, N, rows, N * 2, kOutCols, 32, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != BI_OK) return st;
     Params p{};
+    p.a_bytes = kABytes;
     p.M = static_cast<int32_t>(rows);
     p.N = static_cast<int32_t>(N);
     p.K = static_cast<int32_t>(K);

@@ -84,6 +84,7 @@ struct Params {
     float alpha;
     int32_t M, N, K;
     int32_t atoms_per_rowblock;   // K / 64
+    int32_t stage_tx;             // bytes landing in a CTA per stage (fewer A rows when M < 64)
     unsigned *status;
 };
 
@@ -186,7 +187,7 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     // the slot is free once both pairs' MMAs have read it
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag) ||
                         !mbar_wait(&empty[kStages + stage], phase ^ 1u, abort_flag)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&full[stage], kStageBytes);
+                    mbar_arrive_expect_tx(&full[stage], p.stage_tx);
                     tma_load_2d_multicast(stage_a(stage) + pc * (kAPart * kBKBytes), &tmA, &full[stage],
                                           ks * kBKBytes, a_row, a_dest);
                     tma_load_2d(stage_b(stage), &tmB, &full[stage], ks * kBKBytes, b_row);
@@ -411,7 +412,12 @@ bi_status launch_gemm_nvfp4(const uint8_t *A, const uint8_t *A_sf, const uint8_t
     bi_status st = current_device(&dev, &info);
     if (st != BI_OK) return st;
     CUtensorMap ta, tb, tsa, tsb, ty;
-    st = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K / 2, M, K / 2, kBKBytes, kAPart,
+    // With fewer than 64 rows, each CTA copies only the A rows that can hold
+    // data (rounded up to 16) of its 64-row part; the MMA still multiplies the
+    // whole tile and the accumulator rows past M are never stored. Rows never
+    // interact, so no stored bit changes.
+    const int a_rows = M >= kAPart ? kAPart : static_cast<int>((M + 15) / 16 * 16);
+    st = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K / 2, M, K / 2, kBKBytes, a_rows,
                       CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != BI_OK) return st;
     st = make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K / 2, N, K / 2, kBKBytes, kHalf, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -436,6 +442,7 @@ bi_status launch_gemm_nvfp4(const uint8_t *A, const uint8_t *A_sf, const uint8_t
     p.N = static_cast<int32_t>(N);
     p.K = static_cast<int32_t>(K);
     p.atoms_per_rowblock = static_cast<int32_t>(K / 64);
+    p.stage_tx = kStageBytes - 2 * (kAPart - a_rows) * kBKBytes;   // both A parts it receives are a_rows high
     p.status = device_status_word();
     gemm_nvfp4_kernel<<<pl.grid, kThreads, kSmem, s>>>(ta, tb, tsa, tsb, ty, p);
     return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
