@@ -83,28 +83,67 @@ topk_softmax_kernel(const float *__restrict__ logits, int64_t T, int E, int k, i
 }
 
 // ------------------------------------------------------------- alignment
-// Step 1 (one block per expert): scan the (token, rank) pairs in order and
-// give each pair routed to this expert its rank among them; the expert's
-// count goes to offsets[e + 1]. Each pass covers 1024 pairs: thread t holds
-// pairs 4t..4t+3 of the pass, an inclusive shuffle scan gives the thread's
-// offset in its warp, and the warp totals are added in warp order.
+// The (token, rank) pairs are cut into S segments of consecutive pairs.
+// Step 0 (one block per (expert, segment)): count the segment's pairs routed
+// to the expert; the counts go to row_token[e * S + s] (row_token is written
+// for real only in step 3, and E * S <= T * k is kept).
+// Step 1 (one block per (expert, segment)): give each of the segment's pairs
+// routed to the expert its rank among all of the expert's pairs: the counts
+// of the expert's earlier segments plus its rank inside the segment. Each
+// pass covers 1024 pairs: thread t holds pairs 4t..4t+3 of the pass, an
+// inclusive shuffle scan gives the thread's offset in its warp, and the warp
+// totals are added in warp order. The last segment's block writes the
+// expert's count to offsets[e + 1]. All integer: the result is the unique
+// stable order, whatever the segmentation.
+__device__ __forceinline__ void match4(const int32_t *ids, int64_t p0, int64_t end, int e, bool vec_ok, int (&f)[4]) {
+    if (vec_ok && p0 + 3 < end) {
+        const int4 v = *reinterpret_cast<const int4 *>(ids + p0);
+        f[0] = v.x == e; f[1] = v.y == e; f[2] = v.z == e; f[3] = v.w == e;
+    } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) f[q] = (p0 + q < end) && ids[p0 + q] == e;
+    }
+}
+
 __global__ void __launch_bounds__(256)
-align_rank_kernel(const int32_t *__restrict__ ids, int64_t P, int32_t *__restrict__ pos, int32_t *__restrict__ offsets) {
+align_count_kernel(const int32_t *__restrict__ ids, int64_t P, int64_t seg, int S, int32_t *__restrict__ counts) {
     __shared__ int warp_tot[8];
-    const int e = blockIdx.x;
+    const int e = blockIdx.x / S, sgi = blockIdx.x - e * S;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const bool vec_ok = (reinterpret_cast<uintptr_t>(ids) & 15u) == 0;   // 16-byte loads only when aligned
+    const int64_t begin = sgi * seg, end = min(P, begin + seg);
+    int c = 0;
+    for (int64_t p0 = begin + 4 * static_cast<int64_t>(threadIdx.x); p0 < end; p0 += 1024) {
+        int f[4];
+        match4(ids, p0, end, e, vec_ok, f);
+        c += f[0] + f[1] + f[2] + f[3];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+    if (lane == 0) warp_tot[warp] = c;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int tot = 0;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) tot += warp_tot[w];
+        counts[e * S + sgi] = tot;
+    }
+}
+
+__global__ void __launch_bounds__(256)
+align_rank_kernel(const int32_t *__restrict__ ids, int64_t P, int64_t seg, int S, const int32_t *__restrict__ counts,
+                  int32_t *__restrict__ pos, int32_t *__restrict__ offsets) {
+    __shared__ int warp_tot[8];
+    const int e = blockIdx.x / S, sgi = blockIdx.x - e * S;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool vec_ok = (reinterpret_cast<uintptr_t>(ids) & 15u) == 0;
+    const int64_t begin = sgi * seg, end = min(P, begin + seg);
     int running = 0;
-    for (int64_t base = 0; base < P; base += 1024) {
+    for (int i = 0; i < sgi; ++i) running += counts[e * S + i];       // the expert's earlier segments
+    for (int64_t base = begin; base < end; base += 1024) {
         const int64_t p0 = base + 4 * static_cast<int64_t>(threadIdx.x);
         int f[4];
-        if (vec_ok && p0 + 3 < P) {
-            const int4 v = *reinterpret_cast<const int4 *>(ids + p0);
-            f[0] = v.x == e; f[1] = v.y == e; f[2] = v.z == e; f[3] = v.w == e;
-        } else {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) f[q] = (p0 + q < P) && ids[p0 + q] == e;
-        }
+        match4(ids, p0, end, e, vec_ok, f);
         const int cnt = f[0] + f[1] + f[2] + f[3];
         int incl = cnt;                                   // inclusive scan within the warp
 #pragma unroll
@@ -127,7 +166,7 @@ align_rank_kernel(const int32_t *__restrict__ ids, int64_t P, int32_t *__restric
         running += chunk;
         __syncthreads();
     }
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0 && sgi == S - 1) {
         offsets[e + 1] = running;
         if (e == 0) offsets[0] = 0;
     }
@@ -262,7 +301,13 @@ bi_status launch_moe_align(const int32_t *ids, int64_t T, int32_t k, int32_t E, 
     bi_status st = current_device(&dev, &info);
     if (st != BI_OK) return st;
     const int64_t P = T * k;
-    align_rank_kernel<<<E, 256, 0, s>>>(ids, P, pos, offsets);
+    // segments of whole 1024-pair passes, at most 32 per expert, E * S <= P;
+    // below 16384 pairs one segment (no counting pass) is quicker
+    int S = 1;
+    while (P >= 16384 && S < 32 && static_cast<int64_t>(E) * (2 * S) <= P && P / (2 * S) >= 1024) S *= 2;
+    const int64_t seg = ((P + S - 1) / S + 1023) / 1024 * 1024;   // whole passes: 16-byte aligned pair groups
+    if (S > 1) align_count_kernel<<<E * S, 256, 0, s>>>(ids, P, seg, S, row_token);
+    align_rank_kernel<<<E * S, 256, 0, s>>>(ids, P, seg, S, row_token, pos, offsets);
     align_scan_kernel<<<1, 1024, 0, s>>>(offsets, E);
     align_scatter_kernel<<<grid_for(P, info), 256, 0, s>>>(ids, P, k, E, offsets, pos, row_token, device_status_word());
     return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
