@@ -19,7 +19,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libbi.so")
 
 BI_OK, BI_ERR_INVALID_ARG, BI_ERR_UNSUPPORTED, BI_ERR_MISALIGNED, BI_ERR_ARCH, BI_ERR_CUDA, BI_ERR_TIMEOUT = range(7)
-OP_GEMM_BF16, OP_GROUPED_GEMM_BF16, OP_GEMM_NVFP4, OP_RMSNORM, OP_QUANTIZE_NVFP4 = range(5)
+OP_GEMM_BF16, OP_GROUPED_GEMM_BF16, OP_GEMM_NVFP4, OP_RMSNORM, OP_QUANTIZE_NVFP4, OP_GROUPED_GEMM_SILU_BF16 = range(6)
 
 _lock = threading.Lock()
 _lib = None

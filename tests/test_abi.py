@@ -68,11 +68,20 @@ def test_gemm_plan_independent_of_M(lib, N, K):
 
 def test_grouped_and_nvfp4_and_rmsnorm_plans_independent_of_M(lib):
     for op, N, K in [(lib.OP_GROUPED_GEMM_BF16, 1536, 2048), (lib.OP_GROUPED_GEMM_BF16, 2048, 768),
+                     (lib.OP_GROUPED_GEMM_SILU_BF16, 768, 2048),
                      (lib.OP_GEMM_NVFP4, 14336, 4096), (lib.OP_RMSNORM, 4096, 0)]:
         ps = [_plan(lib, op, M, N, K) for M in [1, 3, 128, 4097, 16384]]
         for p in ps:
             for k in ["block_n", "block_k", "mma_m", "mma_n", "mma_k", "k_steps", "split_k", "reduce_tree"]:
                 assert p[k] == ps[0][k], (op, k)
+
+
+def test_fused_silu_plan_matches_gate_up_plan(lib):
+    """The fused gate_up + SiLU-mul runs the gate_up product's tiles: same plan as N = 2I."""
+    p = _plan(lib, lib.OP_GROUPED_GEMM_SILU_BF16, 4096, 768, 2048)
+    q = _plan(lib, lib.OP_GROUPED_GEMM_BF16, 4096, 1536, 2048)
+    assert p["op"] == lib.OP_GROUPED_GEMM_SILU_BF16
+    assert {k: p[k] for k in p if k != "op"} == {k: q[k] for k in q if k != "op"}
 
 
 def test_rmsnorm_plan_tree(lib):
