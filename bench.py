@@ -480,7 +480,20 @@ def nvfp4_sweep(bi, peaks):
             theirs = f().float() * float(d["alpha"])
             r["max_rel_diff_vs_cublaslt"] = float(((ours - theirs).abs() / (theirs.abs() + 1)).max())
         rows.append(r)
-    return {"fp4_peak_tflops": round(fp4_peak, 1), "fp4_peak_source": peak_note, "rows": rows}
+    # is cuBLASLt's NVFP4 GEMM itself batch-invariant here? (informational)
+    lt_inv = None
+    if use_lt:
+        Mx = max(NVFP4_M)
+        A = torch.from_numpy(d["A"][:Mx].copy()).cuda()
+        SA = torch.from_numpy(syn.swizzle_block_scales(d["SA"][:Mx])).cuda()
+        A1 = torch.from_numpy(d["A"][:1].copy()).cuda()
+        SA1 = torch.from_numpy(syn.swizzle_block_scales(d["SA"][:1])).cuda()
+        f_full = torch_nvfp4_mm(A, SA, Bd, SBd, Mx, NVFP4_N, NVFP4_K)
+        f_one = torch_nvfp4_mm(A1, SA1, Bd, SBd, 1, NVFP4_N, NVFP4_K)
+        if f_full is not None and f_one is not None:
+            lt_inv = bool(torch.equal(f_full()[0], f_one()[0]))
+    return {"fp4_peak_tflops": round(fp4_peak, 1), "fp4_peak_source": peak_note, "rows": rows,
+            "cublaslt_row0_equal_M1_vs_M4096": lt_inv}
 
 
 QUANT_M = [1, 16, 256, 4096, 16384]
