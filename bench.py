@@ -826,7 +826,8 @@ def run_reference(args, dist):
 def profile_case(spec: str, reps: int):
     """Run one kernel configuration `reps` times (for ncu captures); no output line.
     spec: gemm:<qkv|gate_up|down>:<M> | rmsnorm:<M>:<0|1 residual> | grouped:<gate_up|down>:<T> |
-          nvfp4:<M> | quant:<M> | attention:<B> (decode, 4096 cached tokens per sequence)"""
+          nvfp4:<M> | quant:<M> | attention:<B> (decode, 4096 cached tokens per sequence) |
+          moe_layer:<T> (the whole MoE layer, gate_up with SiLU-mul fused)"""
     import torch
     import bi_synth as syn
     import invariant_deterministic_bi_gb300 as bi
@@ -862,6 +863,22 @@ def profile_case(spec: str, reps: int):
         X, W, off, _ = moe_inputs(rest[0], int(rest[1]))
         Y = torch.empty((X.shape[0], W.shape[1]), dtype=torch.bfloat16, device="cuda")
         fn = lambda: bi.grouped_gemm_bf16(X, W, off, Y=Y)
+    elif kind == "moe_layer":
+        T = int(rest[0])
+        n1, k1 = MOE_LAYERS["gate_up"]
+        n2, k2 = MOE_LAYERS["down"]
+        W1 = bf16_dev(syn.moe_weights(MOE_E, n1, k1, seed=0, tensor_id=syn.TID_W1))
+        W2 = bf16_dev(syn.moe_weights(MOE_E, n2, k2, seed=0, tensor_id=syn.TID_W2))
+        hidden = bf16_dev(syn.to_bf16_bits(syn.normal_rows(0, syn.TID_HIDDEN, T, k1)))
+        logits = torch.from_numpy(syn.normal_rows(0, syn.TID_LOGITS, T, MOE_E)).cuda()
+
+        def fn():
+            ids, w = bi.moe_topk_softmax(logits, MOE_TOPK)
+            off, rt, pos = bi.moe_align(ids, MOE_E)
+            X = bi.moe_gather(hidden, rt)
+            act = bi.grouped_gemm_silu_bf16(X, W1, off)
+            y = bi.grouped_gemm_bf16(act, W2, off)
+            return bi.moe_combine(y, pos, w)
     elif kind == "attention":
         B, (Hq, Hkv, D, bs) = int(rest[0]), ATTN_HEADS
         nb = ATTN_L // bs
