@@ -205,19 +205,32 @@ align_scatter_kernel(const int32_t *__restrict__ ids, int64_t P, int k, int E, c
 }
 
 // ----------------------------------------------------------------- gather
+// One warp per destination row at a time (grid-stride over rows): the source
+// token index is read once, and each lane moves up to 8 of the row's 16-byte
+// pieces with all its loads in flight before its stores.
 __global__ void __launch_bounds__(256)
 gather_kernel(const uint4 *__restrict__ hidden, int64_t T, int64_t hv, const int32_t *__restrict__ row_token,
               int64_t rows, uint4 *__restrict__ out, unsigned *status) {
-    const int64_t total = rows * hv;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x; i < total;
-         i += static_cast<int64_t>(gridDim.x) * 256) {
-        const int64_t r = i / hv, j = i - r * hv;
+    constexpr int kPer = 8;
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * 8;
+    for (int64_t r = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5); r < rows; r += warps) {
         const int64_t t = row_token[r];
         if (t < 0 || t >= T) {
-            atomicOr(status, kDevBadOffsets);
+            if (lane == 0) atomicOr(status, kDevBadOffsets);
             continue;
         }
-        out[i] = __ldg(hidden + t * hv + j);
+        const uint4 *src = hidden + t * hv;
+        uint4 *dst = out + r * hv;
+        for (int64_t j0 = lane; j0 < hv; j0 += 32 * kPer) {
+            uint4 v[kPer];
+#pragma unroll
+            for (int u = 0; u < kPer; ++u)
+                if (j0 + 32 * u < hv) v[u] = __ldg(src + j0 + 32 * u);
+#pragma unroll
+            for (int u = 0; u < kPer; ++u)
+                if (j0 + 32 * u < hv) dst[j0 + 32 * u] = v[u];
+        }
     }
 }
 
@@ -319,7 +332,7 @@ bi_status launch_moe_gather(const void *hidden, int64_t T, int64_t H, const int3
     const DeviceInfo *info;
     bi_status st = current_device(&dev, &info);
     if (st != BI_OK) return st;
-    gather_kernel<<<grid_for(rows * (H / 8), info), 256, 0, s>>>(static_cast<const uint4 *>(hidden), T, H / 8,
+    gather_kernel<<<grid_for(rows * 32, info), 256, 0, s>>>(static_cast<const uint4 *>(hidden), T, H / 8,
                                                                  row_token, rows, static_cast<uint4 *>(out),
                                                                  device_status_word());
     return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
