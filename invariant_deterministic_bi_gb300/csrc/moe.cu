@@ -265,19 +265,33 @@ combine_kernel(const uint4 *__restrict__ Y, int64_t rows, const int32_t *__restr
     for (int64_t j = threadIdx.x; j < hv; j += 256) {
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         bool bad = false;
-        for (int i = 0; i < k; ++i) {
-            const int64_t r = pos[t * k + i];
-            if (r < 0 || r >= rows) {
-                bad = true;
-                continue;
-            }
-            const float wi = w[t * k + i];
-            const uint4 y = __ldg(Y + r * hv + j);
-            const uint32_t yw[4] = {y.x, y.y, y.z, y.w};
+        for (int i0 = 0; i0 < k; i0 += 8) {          // up to 8 rows' loads in flight, then the FMAs in rank order
+            uint4 y[8];
+            float wi[8];
+            bool ok[8];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                acc[2 * q] = __fmaf_rn(wi, bf_lo(yw[q]), acc[2 * q]);
-                acc[2 * q + 1] = __fmaf_rn(wi, bf_hi(yw[q]), acc[2 * q + 1]);
+            for (int u = 0; u < 8; ++u) {
+                ok[u] = false;
+                if (i0 + u < k) {
+                    const int64_t r = pos[t * k + i0 + u];
+                    if (r < 0 || r >= rows) {
+                        bad = true;
+                    } else {
+                        wi[u] = w[t * k + i0 + u];
+                        y[u] = __ldg(Y + r * hv + j);
+                        ok[u] = true;
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (!ok[u]) continue;
+                const uint32_t yw[4] = {y[u].x, y[u].y, y[u].z, y[u].w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    acc[2 * q] = __fmaf_rn(wi[u], bf_lo(yw[q]), acc[2 * q]);
+                    acc[2 * q + 1] = __fmaf_rn(wi[u], bf_hi(yw[q]), acc[2 * q + 1]);
+                }
             }
         }
         if (bad) atomicOr(status, kDevBadOffsets);
