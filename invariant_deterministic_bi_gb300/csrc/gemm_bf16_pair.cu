@@ -155,18 +155,36 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
     if constexpr (GROUPED) {
         for (int i = threadIdx.x; i <= p.E; i += kThreads) off_s[i] = p.offsets[i];
         __syncthreads();
-        if (threadIdx.x == 0) {
-            bool ok = off_s[0] == 0 && off_s[p.E] == p.M;
-            int acc = 0;
-            pre_s[0] = 0;
-            for (int e = 0; e < p.E; ++e) {
+        if (warp == 2) {
+            // Row-tile prefix over the experts: lane l takes a contiguous block
+            // of experts, the block sums are scanned across the warp.
+            const int per = (p.E + 31) >> 5;
+            const int lo = min(lane * per, p.E), hi = min(lo + per, p.E);
+            auto tiles_of = [&](int e) {
                 const long long c = static_cast<long long>(off_s[e + 1]) - off_s[e];
-                if (c < 0) ok = false;
-                acc += ok ? static_cast<int>((c + kBM - 1) / kBM) : 0;
+                return c > 0 ? static_cast<int>((c + kBM - 1) / kBM) : 0;
+            };
+            bool ok = true;
+            int sum = 0;
+            for (int e = lo; e < hi; ++e) {
+                if (off_s[e + 1] < off_s[e]) ok = false;
+                sum += tiles_of(e);
+            }
+            int incl = sum;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, d);
+                if (lane >= d) incl += v;
+            }
+            ok = __all_sync(0xffffffffu, ok) && off_s[0] == 0 && off_s[p.E] == p.M;
+            int acc = incl - sum;
+            for (int e = lo; e < hi; ++e) {
+                acc += tiles_of(e);
                 pre_s[e + 1] = acc;
             }
-            *total_s = ok ? acc * num_n : 0;
-            if (!ok && blockIdx.x == 0) atomicOr(p.status, kDevBadOffsets);
+            if (lane == 0) pre_s[0] = 0;
+            if (lane == 31) *total_s = ok ? incl * num_n : 0;
+            if (lane == 0 && !ok && blockIdx.x == 0) atomicOr(p.status, kDevBadOffsets);
         }
     } else {
         if (threadIdx.x == 0) *total_s = num_m * num_n;
