@@ -21,7 +21,11 @@
  *    dimensions are in elements and must keep every row 16-byte aligned.
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream). Calls are
  *    asynchronous on it; argument errors are returned synchronously before
- *    anything is launched; a failed launch returns BI_ERR_CUDA.
+ *    anything is launched; a failed launch returns BI_ERR_CUDA. Kernels are
+ *    launched with programmatic stream serialization: one may begin its
+ *    set-up while the previous kernel of the stream finishes, but touches no
+ *    global memory before that kernel has completed, so stream order holds
+ *    for all data (also inside CUDA graphs captured from the stream).
  *  - libbi allocates no device memory per call and never synchronises inside
  *    a compute call. It owns one status word per device, set by kernels whose
  *    bounded waits ran out or that found invalid device-side data

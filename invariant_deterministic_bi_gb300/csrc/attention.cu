@@ -101,6 +101,8 @@ __device__ __forceinline__ bool seq_ok(const AttnParams &p, int64_t b, int &L) {
 template <int G>
 __global__ void __launch_bounds__(kThreads)
 attn_split_kernel(const AttnParams p) {
+    grid_dep_wait();      // earlier work of the stream is complete and visible
+    grid_dep_launch();
     extern __shared__ __align__(16) uint8_t smem[];
     uint8_t *Ks = smem;                                            // [kChunk][kD] bf16, 16-byte chunks swizzled
     uint8_t *Vs = smem + kTileBytes;                               // [kChunk][kD] bf16
@@ -268,6 +270,8 @@ attn_split_kernel(const AttnParams p) {
 
 __global__ void __launch_bounds__(kCombineThreads)
 attn_combine_kernel(const AttnParams p) {
+    grid_dep_wait();      // earlier work of the stream is complete and visible
+    grid_dep_launch();
     // Chunk statistics go through shared memory in tiles of kCombineThreads
     // chunks, loaded in parallel; the arithmetic is the sequential chunk-order
     // merge described at the top of the file (the maximum is exact in any order).
@@ -335,8 +339,7 @@ bi_status launch_split(const dim3 &grid, const AttnParams &p, cudaStream_t s) {
     if (ensure_smem_attr(reinterpret_cast<const void *>(attn_split_kernel<G>), split_smem_bytes<G>(), &configured) !=
         BI_OK)
         return BI_ERR_CUDA;
-    attn_split_kernel<G><<<grid, kThreads, split_smem_bytes<G>(), s>>>(p);
-    return BI_OK;
+    return launch_pdl(attn_split_kernel<G>, grid, dim3(kThreads), split_smem_bytes<G>(), s, p);
 }
 #define SPLIT_LAUNCH(G)                                    \
     do {                                                   \
@@ -375,8 +378,7 @@ bi_status launch_attention_decode(const void *Q, const void *K, const void *V, c
         case 8: SPLIT_LAUNCH(8); break;
         default: return BI_ERR_UNSUPPORTED;
     }
-    attn_combine_kernel<<<dim3(Hq, static_cast<unsigned>(B)), kCombineThreads, 0, s>>>(p);
-    return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
+    return launch_pdl(attn_combine_kernel, dim3(Hq, static_cast<unsigned>(B)), dim3(kCombineThreads), 0, s, p);
 }
 
 }  // namespace bi

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <utility>
 
 #include "../../include/bi.h"
 
@@ -42,6 +43,26 @@ inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 // Raise a kernel's dynamic shared-memory limit once per device. `done` is a
 // per-kernel bitmask of devices already configured.
 bi_status ensure_smem_attr(const void *kernel, int bytes, unsigned long long *done);
+
+// Launch `kernel` with programmatic stream serialization: it may begin while
+// the previous kernel of the stream finishes (its launch and set-up overlap
+// that kernel's tail). Every libbi kernel calls grid_dep_wait() before it
+// touches global memory, so stream order is kept for all data.
+template <typename... KArgs, typename... Args>
+inline bi_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                            Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...) == cudaSuccess ? BI_OK : BI_ERR_CUDA;
+}
 
 // Kernel launchers (defined in the .cu files); arguments already validated.
 bi_status launch_gemm_bf16(const void *X, int64_t ldx, const void *W, int64_t ldw, void *Y, int64_t ldy,

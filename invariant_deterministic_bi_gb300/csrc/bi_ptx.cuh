@@ -131,6 +131,18 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
         : "memory");
 }
 
+// ------------------------------------------ programmatic dependent launch ---
+// Every libbi kernel is launched with programmatic stream serialization, so
+// it may start while the previous kernel of the stream is still running.
+// grid_dep_wait() returns once the grids this one depends on have completed
+// and their memory operations are visible; a kernel calls it before its first
+// access to global memory that other work of the stream reads or writes (only
+// set-up of barriers, tensor memory and descriptor prefetches comes before).
+// It returns at once when there is no such dependency.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next programmatically serialized grid of the stream begin
+// launching; it still waits for this grid's completion in grid_dep_wait().
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 // -------------------------------------------------------------- cluster ---
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {

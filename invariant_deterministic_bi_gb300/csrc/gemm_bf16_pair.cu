@@ -152,6 +152,7 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         tmem_alloc_pair(tmem_slot, kTmemCols);
         tmem_relinquish_pair();
     }
+    grid_dep_wait();      // the set-up above overlaps the previous kernel; global memory only from here
     if constexpr (GROUPED) {
         for (int i = threadIdx.x; i <= p.E; i += kThreads) off_s[i] = p.offsets[i];
         __syncthreads();
@@ -379,6 +380,7 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
         __syncwarp();
     }
 
+    grid_dep_launch();                   // the next kernel may start launching on SMs as they free up
     tc_fence_before();
     cluster_sync();                      // no CTA leaves while its peer may still signal it
     if (warp == 1) {
@@ -428,8 +430,7 @@ bi_status launch_pair(const CUtensorMap &ta, const CUtensorMap &tb, const CUtens
     auto kern = gemm_bf16_pair_kernel<MODE>;
     if (ensure_smem_attr(reinterpret_cast<const void *>(kern), smem_bytes<MODE>(), &configured) != BI_OK)
         return BI_ERR_CUDA;
-    kern<<<grid, kThreads, smem_bytes<MODE>(), s>>>(ta, tb, ty, p);
-    return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
+    return launch_pdl(kern, dim3(grid), dim3(kThreads), smem_bytes<MODE>(), s, ta, tb, ty, p);
 }
 
 bi_status launch_gemm_bf16(const void *X, int64_t ldx, const void *W, int64_t ldw, void *Y, int64_t ldy,

@@ -147,6 +147,7 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         tmem_alloc_pair(tmem_slot, kTmemCols);
         tmem_relinquish_pair();
     }
+    grid_dep_wait();      // the set-up above overlaps the previous kernel; global memory only from here
     tc_fence_before();
     cluster_sync();
     tc_fence_after();
@@ -350,6 +351,7 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         __syncwarp();
     }
 
+    grid_dep_launch();                   // the next kernel may start launching on SMs as they free up
     tc_fence_before();
     cluster_sync();                      // no CTA leaves while a peer may still write or signal it
     if (warp == 1) {
@@ -444,8 +446,7 @@ bi_status launch_gemm_nvfp4(const uint8_t *A, const uint8_t *A_sf, const uint8_t
     p.atoms_per_rowblock = static_cast<int32_t>(K / 64);
     p.stage_tx = kStageBytes - 2 * (kAPart - a_rows) * kBKBytes;   // both A parts it receives are a_rows high
     p.status = device_status_word();
-    gemm_nvfp4_kernel<<<pl.grid, kThreads, kSmem, s>>>(ta, tb, tsa, tsb, ty, p);
-    return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
+    return launch_pdl(gemm_nvfp4_kernel, dim3(pl.grid), dim3(kThreads), kSmem, s, ta, tb, tsa, tsb, ty, p);
 }
 
 }  // namespace bi

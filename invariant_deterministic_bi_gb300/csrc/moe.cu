@@ -29,6 +29,8 @@ template <int MAXJ>
 __global__ void __launch_bounds__(256)
 topk_softmax_kernel(const float *__restrict__ logits, int64_t T, int E, int k, int renorm, int32_t *__restrict__ ids,
                     float *__restrict__ wout) {
+    grid_dep_wait();      // earlier work of the stream is complete and visible
+    grid_dep_launch();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t t = static_cast<int64_t>(blockIdx.x) * 8 + warp;
     if (t >= T) return;                       // whole warp leaves together
@@ -107,6 +109,8 @@ __device__ __forceinline__ void match4(const int32_t *ids, int64_t p0, int64_t e
 
 __global__ void __launch_bounds__(256)
 align_count_kernel(const int32_t *__restrict__ ids, int64_t P, int64_t seg, int S, int32_t *__restrict__ counts) {
+    grid_dep_wait();      // earlier work of the stream is complete and visible
+    grid_dep_launch();
     __shared__ int warp_tot[8];
     const int e = blockIdx.x / S, sgi = blockIdx.x - e * S;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -133,6 +137,8 @@ align_count_kernel(const int32_t *__restrict__ ids, int64_t P, int64_t seg, int 
 __global__ void __launch_bounds__(256)
 align_rank_kernel(const int32_t *__restrict__ ids, int64_t P, int64_t seg, int S, const int32_t *__restrict__ counts,
                   int32_t *__restrict__ pos, int32_t *__restrict__ offsets) {
+    grid_dep_wait();      // earlier work of the stream is complete and visible
+    grid_dep_launch();
     __shared__ int warp_tot[8];
     const int e = blockIdx.x / S, sgi = blockIdx.x - e * S;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -174,6 +180,8 @@ align_rank_kernel(const int32_t *__restrict__ ids, int64_t P, int64_t seg, int S
 
 // Step 2 (one block): offsets[1..E] counts -> inclusive prefix, in place.
 __global__ void __launch_bounds__(1024) align_scan_kernel(int32_t *offsets, int E) {
+    grid_dep_wait();      // earlier work of the stream is complete and visible
+    grid_dep_launch();
     __shared__ int buf[1024];
     const int i = threadIdx.x;
     buf[i] = i < E ? offsets[i + 1] : 0;
@@ -191,6 +199,8 @@ __global__ void __launch_bounds__(1024) align_scan_kernel(int32_t *offsets, int 
 __global__ void __launch_bounds__(256)
 align_scatter_kernel(const int32_t *__restrict__ ids, int64_t P, int k, int E, const int32_t *__restrict__ offsets,
                      int32_t *__restrict__ pos, int32_t *__restrict__ row_token, unsigned *status) {
+    grid_dep_wait();      // earlier work of the stream is complete and visible
+    grid_dep_launch();
     for (int64_t p = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x; p < P;
          p += static_cast<int64_t>(gridDim.x) * 256) {
         const int e = ids[p];
@@ -211,6 +221,8 @@ align_scatter_kernel(const int32_t *__restrict__ ids, int64_t P, int k, int E, c
 __global__ void __launch_bounds__(256)
 gather_kernel(const uint4 *__restrict__ hidden, int64_t T, int64_t hv, const int32_t *__restrict__ row_token,
               int64_t rows, uint4 *__restrict__ out, unsigned *status) {
+    grid_dep_wait();      // earlier work of the stream is complete and visible
+    grid_dep_launch();
     constexpr int kPer = 8;
     const int lane = threadIdx.x & 31;
     const int64_t warps = static_cast<int64_t>(gridDim.x) * 8;
@@ -238,6 +250,8 @@ gather_kernel(const uint4 *__restrict__ hidden, int64_t T, int64_t hv, const int
 // act = bf16( silu(g) * u ), silu(g) = g / (1 + exp(-g)), fp32 (silu_mul_f32); rows are [gate | up].
 __global__ void __launch_bounds__(256)
 silu_mul_kernel(const uint4 *__restrict__ gu, int64_t rows, int64_t iv, uint4 *__restrict__ act) {
+    grid_dep_wait();      // earlier work of the stream is complete and visible
+    grid_dep_launch();
     const int64_t total = rows * iv;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * 256) {
@@ -261,6 +275,8 @@ silu_mul_kernel(const uint4 *__restrict__ gu, int64_t rows, int64_t iv, uint4 *_
 __global__ void __launch_bounds__(256)
 combine_kernel(const uint4 *__restrict__ Y, int64_t rows, const int32_t *__restrict__ pos,
                const float *__restrict__ w, int k, int64_t hv, uint4 *__restrict__ out, unsigned *status) {
+    grid_dep_wait();      // earlier work of the stream is complete and visible
+    grid_dep_launch();
     const int64_t t = blockIdx.x;
     for (int64_t j = threadIdx.x; j < hv; j += 256) {
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -311,14 +327,14 @@ inline unsigned grid_for(int64_t items, const DeviceInfo *info) {
 
 bi_status launch_moe_topk_softmax(const float *logits, int64_t T, int32_t E, int32_t k, int32_t renorm, int32_t *ids,
                                   float *w, cudaStream_t s) {
-    const unsigned grid = static_cast<unsigned>((T + 7) / 8);
-    if (E <= 32) topk_softmax_kernel<1><<<grid, 256, 0, s>>>(logits, T, E, k, renorm, ids, w);
-    else if (E <= 64) topk_softmax_kernel<2><<<grid, 256, 0, s>>>(logits, T, E, k, renorm, ids, w);
-    else if (E <= 128) topk_softmax_kernel<4><<<grid, 256, 0, s>>>(logits, T, E, k, renorm, ids, w);
-    else if (E <= 256) topk_softmax_kernel<8><<<grid, 256, 0, s>>>(logits, T, E, k, renorm, ids, w);
-    else if (E <= 512) topk_softmax_kernel<16><<<grid, 256, 0, s>>>(logits, T, E, k, renorm, ids, w);
-    else topk_softmax_kernel<32><<<grid, 256, 0, s>>>(logits, T, E, k, renorm, ids, w);
-    return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
+    const dim3 grid(static_cast<unsigned>((T + 7) / 8));
+    auto go = [&](auto kernel) { return launch_pdl(kernel, grid, dim3(256), 0, s, logits, T, E, k, renorm, ids, w); };
+    if (E <= 32) return go(topk_softmax_kernel<1>);
+    if (E <= 64) return go(topk_softmax_kernel<2>);
+    if (E <= 128) return go(topk_softmax_kernel<4>);
+    if (E <= 256) return go(topk_softmax_kernel<8>);
+    if (E <= 512) return go(topk_softmax_kernel<16>);
+    return go(topk_softmax_kernel<32>);
 }
 
 bi_status launch_moe_align(const int32_t *ids, int64_t T, int32_t k, int32_t E, int32_t *offsets, int32_t *row_token,
@@ -333,11 +349,14 @@ bi_status launch_moe_align(const int32_t *ids, int64_t T, int32_t k, int32_t E, 
     int S = 1;
     while (P >= 16384 && S < 32 && static_cast<int64_t>(E) * (2 * S) <= P && P / (2 * S) >= 1024) S *= 2;
     const int64_t seg = ((P + S - 1) / S + 1023) / 1024 * 1024;   // whole passes: 16-byte aligned pair groups
-    if (S > 1) align_count_kernel<<<E * S, 256, 0, s>>>(ids, P, seg, S, row_token);
-    align_rank_kernel<<<E * S, 256, 0, s>>>(ids, P, seg, S, row_token, pos, offsets);
-    align_scan_kernel<<<1, 1024, 0, s>>>(offsets, E);
-    align_scatter_kernel<<<grid_for(P, info), 256, 0, s>>>(ids, P, k, E, offsets, pos, row_token, device_status_word());
-    return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
+    const dim3 blocks(static_cast<unsigned>(E * S));
+    if (S > 1 && (st = launch_pdl(align_count_kernel, blocks, dim3(256), 0, s, ids, P, seg, S, row_token)) != BI_OK)
+        return st;
+    if ((st = launch_pdl(align_rank_kernel, blocks, dim3(256), 0, s, ids, P, seg, S, row_token, pos, offsets)) != BI_OK)
+        return st;
+    if ((st = launch_pdl(align_scan_kernel, dim3(1), dim3(1024), 0, s, offsets, E)) != BI_OK) return st;
+    return launch_pdl(align_scatter_kernel, dim3(grid_for(P, info)), dim3(256), 0, s, ids, P, k, E, offsets, pos,
+                      row_token, device_status_word());
 }
 
 bi_status launch_moe_gather(const void *hidden, int64_t T, int64_t H, const int32_t *row_token, int64_t rows,
@@ -346,10 +365,9 @@ bi_status launch_moe_gather(const void *hidden, int64_t T, int64_t H, const int3
     const DeviceInfo *info;
     bi_status st = current_device(&dev, &info);
     if (st != BI_OK) return st;
-    gather_kernel<<<grid_for(rows * 32, info), 256, 0, s>>>(static_cast<const uint4 *>(hidden), T, H / 8,
-                                                                 row_token, rows, static_cast<uint4 *>(out),
-                                                                 device_status_word());
-    return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
+    return launch_pdl(gather_kernel, dim3(grid_for(rows * 32, info)), dim3(256), 0, s,
+                      static_cast<const uint4 *>(hidden), T, H / 8, row_token, rows, static_cast<uint4 *>(out),
+                      device_status_word());
 }
 
 bi_status launch_silu_mul(const void *gate_up, int64_t rows, int64_t I, void *act, cudaStream_t s) {
@@ -357,16 +375,14 @@ bi_status launch_silu_mul(const void *gate_up, int64_t rows, int64_t I, void *ac
     const DeviceInfo *info;
     bi_status st = current_device(&dev, &info);
     if (st != BI_OK) return st;
-    silu_mul_kernel<<<grid_for(rows * (I / 8), info), 256, 0, s>>>(static_cast<const uint4 *>(gate_up), rows, I / 8,
-                                                                   static_cast<uint4 *>(act));
-    return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
+    return launch_pdl(silu_mul_kernel, dim3(grid_for(rows * (I / 8), info)), dim3(256), 0, s,
+                      static_cast<const uint4 *>(gate_up), rows, I / 8, static_cast<uint4 *>(act));
 }
 
 bi_status launch_moe_combine(const void *Y, int64_t rows, const int32_t *pos, const float *w, int64_t T, int32_t k,
                              int64_t H, void *out, cudaStream_t s) {
-    combine_kernel<<<static_cast<unsigned>(T), 256, 0, s>>>(static_cast<const uint4 *>(Y), rows, pos, w, k, H / 8,
-                                                            static_cast<uint4 *>(out), device_status_word());
-    return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
+    return launch_pdl(combine_kernel, dim3(static_cast<unsigned>(T)), dim3(256), 0, s, static_cast<const uint4 *>(Y),
+                      rows, pos, w, k, H / 8, static_cast<uint4 *>(out), device_status_word());
 }
 
 }  // namespace bi

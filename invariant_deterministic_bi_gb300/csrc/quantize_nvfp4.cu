@@ -62,6 +62,8 @@ __device__ __forceinline__ uint32_t to_e2m1x8(const float (&y)[8]) {
 __global__ void __launch_bounds__(kThreads)
 quantize_nvfp4_kernel(const uint4 *__restrict__ X, int64_t ldx_vec, uint8_t *__restrict__ Q, uint8_t *__restrict__ SF,
                       int64_t M, int K, float gs) {
+    grid_dep_wait();      // earlier work of the stream is complete and visible
+    grid_dep_launch();
     const int blocks = K / 16;                       // 16-element scale blocks per row
     const int atoms = K / 64;                        // 512-byte scale atoms per 128-row group
     const int64_t total = M * blocks;
@@ -110,9 +112,8 @@ bi_status launch_quantize_nvfp4(const void *X, int64_t ldx, float gs, uint8_t *Q
     int64_t grid = (threads + kThreads - 1) / kThreads;
     const int64_t cap = static_cast<int64_t>(info->sm_count) * 16;
     if (grid > cap) grid = cap;
-    quantize_nvfp4_kernel<<<static_cast<unsigned>(grid), kThreads, 0, s>>>(
-        static_cast<const uint4 *>(X), ldx / 8, Q, Q_sf, M, static_cast<int>(K), gs);
-    return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
+    return launch_pdl(quantize_nvfp4_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, s,
+                      static_cast<const uint4 *>(X), ldx / 8, Q, Q_sf, M, static_cast<int>(K), gs);
 }
 
 }  // namespace bi

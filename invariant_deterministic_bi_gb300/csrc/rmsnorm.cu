@@ -89,6 +89,8 @@ __device__ __forceinline__ float row_scale(float ss, int H, float eps, float *re
 template <int T, int VPT, bool RESIDUAL>
 __global__ void __launch_bounds__(T)
 rmsnorm_kernel(const uint4 *x, uint4 *residual, const uint4 *__restrict__ w, uint4 *out, int H, float eps) {
+    grid_dep_wait();      // earlier work of the stream is complete and visible
+    grid_dep_launch();
     __shared__ float red[T / 32 + 1];
     const int64_t row = blockIdx.x;
     const int nvec = H >> 3;
@@ -137,6 +139,8 @@ template <int T, int VPT, bool RESIDUAL>
 __global__ void __launch_bounds__(T)
 rank_sum_rmsnorm_kernel(const RankParts parts, int R, uint4 *residual, const uint4 *__restrict__ w, uint4 *sum_out,
                         uint4 *out, int H, float eps) {
+    grid_dep_wait();      // earlier work of the stream is complete and visible
+    grid_dep_launch();
     __shared__ float red[T / 32 + 1];
     const int64_t row = blockIdx.x;
     const int nvec = H >> 3;
@@ -203,10 +207,9 @@ RowShape row_shape(int64_t H) {
 template <int T, int VPT, bool RES>
 bi_status launch_one(const void *x, void *residual, const void *w, void *out, int64_t M, int64_t H, float eps,
                      cudaStream_t s) {
-    rmsnorm_kernel<T, VPT, RES><<<static_cast<unsigned>(M), T, 0, s>>>(
-        static_cast<const uint4 *>(x), static_cast<uint4 *>(residual), static_cast<const uint4 *>(w),
-        static_cast<uint4 *>(out), static_cast<int>(H), eps);
-    return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
+    return launch_pdl(rmsnorm_kernel<T, VPT, RES>, dim3(static_cast<unsigned>(M)), dim3(T), 0, s,
+                      static_cast<const uint4 *>(x), static_cast<uint4 *>(residual), static_cast<const uint4 *>(w),
+                      static_cast<uint4 *>(out), static_cast<int>(H), eps);
 }
 
 template <bool RES>
@@ -234,10 +237,9 @@ bi_status launch_res(const void *x, void *residual, const void *w, void *out, in
 template <int T, int VPT, bool RES>
 bi_status launch_rank_one(const RankParts &parts, int R, void *residual, const void *w, void *sum_out, void *out,
                           int64_t M, int64_t H, float eps, cudaStream_t s) {
-    rank_sum_rmsnorm_kernel<T, VPT, RES><<<static_cast<unsigned>(M), T, 0, s>>>(
-        parts, R, static_cast<uint4 *>(residual), static_cast<const uint4 *>(w), static_cast<uint4 *>(sum_out),
-        static_cast<uint4 *>(out), static_cast<int>(H), eps);
-    return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
+    return launch_pdl(rank_sum_rmsnorm_kernel<T, VPT, RES>, dim3(static_cast<unsigned>(M)), dim3(T), 0, s, parts, R,
+                      static_cast<uint4 *>(residual), static_cast<const uint4 *>(w), static_cast<uint4 *>(sum_out),
+                      static_cast<uint4 *>(out), static_cast<int>(H), eps);
 }
 
 template <bool RES>
