@@ -45,7 +45,7 @@ NOMINAL_HBM_GBS = 8000.0
 # DRAM bytes (read + write) of one gate_up launch at M=8192 from the ncu capture
 # summarised in profiles/gemm_bf16_pair_gate_up_M8192.md, valid only for the
 # kernel source it was taken on (checked by hash at run time).
-GATE_UP_TRAFFIC = {"source_sha256_16": "ffd940cd23203b5b", "bytes": 896564480 + 386728960}
+GATE_UP_TRAFFIC = {"source_sha256_16": "3a434c5bd9eca660", "bytes": 901581056 + 384537088}
 
 
 def gate_up_traffic():
