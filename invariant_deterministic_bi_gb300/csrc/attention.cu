@@ -5,7 +5,7 @@
 // lists batch-invariant attention operators. Split-KV ("flash decoding")
 // kernels usually pick the number of KV splits from the batch size to fill the
 // GPU; that makes a sequence's reduction order depend on the batch. Here the
-// split is fixed: a sequence's KV is cut into chunks of kChunk = 256 tokens by
+// split is fixed: a sequence's KV is cut into chunks of kChunk = 128 tokens by
 // position alone, every chunk is reduced by one CTA in a fixed order, and the
 // chunk results are merged in chunk order. Nothing a sequence sees depends on
 // the other sequences in the batch.
@@ -14,17 +14,22 @@
 //   256 threads, head_dim 128, the G = Hq/Hkv query heads of the KV head
 //   together (GQA):
 //   - every thread issues its share of the chunk's K rows, then V rows, as
-//     16-byte cp.async copies into shared memory (32 KB each; rows past the
-//     sequence or in an invalid block are zero-filled), so the whole chunk is
-//     in flight at once and three CTAs share an SM;
-//   - scores, once K has landed: one lane per token, the 128 bf16 products
-//     q[d] k[d] added in dimension order by fp32 FMAs on the bf16 operands
-//     (each warp group of 4 takes every other head); s = scale * q.k;
+//     16-byte cp.async copies into shared memory (32 KB each, 16-byte chunks
+//     XOR-swizzled by row; rows past the sequence or in an invalid block are
+//     zero-filled), so the whole chunk is in flight at once and three CTAs
+//     share an SM;
+//   - scores, once K has landed, on the tensor cores (mma.sync m16n8k16, bf16
+//     operands, fp32 accumulation): the G q rows (zero rows up to 16) times
+//     K^T, warp w taking tokens 16w..16w+15, dimensions ascending in steps of
+//     16; s = scale * q.k;
 //   - per head (warp h): m = max s (exact), p = exp(s - m), l = sum p
 //     (lane-strided, then butterfly);
-//   - values, once V has landed: thread (pair of dims, head group) adds
-//     p_t v_t over the chunk's tokens in increasing order;
+//   - values, once V has landed, on the tensor cores: p (as bf16 hi + lo,
+//     two MMAs per step, 16 significant bits) times V, warp w taking
+//     dimensions 16w..16w+15, tokens ascending in steps of 16;
 //   - writes fp32 (m, l, o[0..127]) per head and chunk to the workspace.
+//   The MMA shapes and step orders are the same for every chunk of every
+//   batch, so the per-chunk results do not depend on the batch either.
 // Step 2, one CTA per (sequence, query head): M = max_c m_c; the output is
 //   sum_c e^{m_c - M} o_c / sum_c e^{m_c - M} l_c, chunks in order, rounded to bf16.
 #include <cuda_bf16.h>
@@ -40,31 +45,15 @@ namespace {
 constexpr int kD = 128;
 constexpr int kChunk = 128;                    // tokens per chunk: fixed, by position
 constexpr int kThreads = 256;                  // split kernel
-constexpr int kWarps = kThreads / 32;
 constexpr int kCombineThreads = 128;           // one thread per output dimension
 constexpr int kRowBytes = kD * 2;              // one token's K (or V) row of one KV head
 constexpr int kTileBytes = kChunk * kRowBytes; // 32 KB
 
-// K and V tiles, then q (G x kD fp32), scores (G x kChunk fp32), (m, l) per
-// head and the K-row offset of every token of the chunk. The value phase's
-// partial sums (kThreads x G x 8 fp32) reuse the K and V tiles.
+// K and V tiles, then q (G x kD fp32 of space, bf16 used), scores
+// (G x kChunk fp32) and the K/V row offset of every token of the chunk.
 template <int G>
 constexpr int split_smem_bytes() {
-    return 2 * kTileBytes + (G * kD + G * kChunk + 2 * G) * 4 + kChunk * 8;
-}
-static_assert(kThreads * 8 * 8 * 4 <= 2 * kTileBytes, "value partials must fit in the K and V tiles");
-
-// acc + a.lo * b.lo, then + a.hi * b.hi, each one fp32 FMA on bf16 operands
-// (the product of two bf16 values is exact in fp32, so this is the same as
-// widening both to fp32 first).
-__device__ __forceinline__ float fma_bf16x2(uint32_t a, uint32_t b, float acc) {
-    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
-        "mov.b32 {al, ah}, %1;\n\t"
-        "mov.b32 {bl, bh}, %2;\n\t"
-        "fma.rn.f32.bf16 %0, al, bl, %0;\n\t"
-        "fma.rn.f32.bf16 %0, ah, bh, %0;\n\t}"
-        : "+f"(acc) : "r"(a), "r"(b));
-    return acc;
+    return 2 * kTileBytes + (G * kD + G * kChunk) * 4 + kChunk * 8;
 }
 
 // 16-byte global -> shared copy; src_bytes = 0 writes 16 zero bytes and reads nothing.
@@ -75,9 +64,29 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-__device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
-__device__ __forceinline__ float bf_at(const uint16_t *p, int i) { return __uint_as_float(static_cast<uint32_t>(p[i]) << 16); }
+// D += A B on the tensor cores, one warp: A 16x16 bf16 (row-major fragment
+// a0..a3), B 16x8 bf16 (column fragment b0, b1), D 16x8 fp32.
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+                 "{%8, %9}, {%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// Four 8x8 bf16 matrices from shared memory, transposed (lanes 8i..8i+7 give
+// the 16-byte rows of matrix i).
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3,
+                                                  uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+// (p0, p1) = hi + lo, hi and lo packed bf16 pairs (round to nearest even);
+// hi + lo carries 16 significant bits of each p.
+__device__ __forceinline__ void split_bf16x2(float p0, float p1, uint32_t &hi, uint32_t &lo) {
+    hi = pack_bf16x2(__float_as_uint(p0), __float_as_uint(p1));
+    const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xFFFF0000u);
+    lo = pack_bf16x2(__float_as_uint(p0 - h0), __float_as_uint(p1 - h1));
+}
 
 struct AttnParams {
     const uint16_t *Q;       // [B][Hq][D]
@@ -105,13 +114,11 @@ attn_split_kernel(const AttnParams p) {
     grid_dep_launch();
     extern __shared__ __align__(16) uint8_t smem[];
     uint8_t *Ks = smem;                                            // [kChunk][kD] bf16, 16-byte chunks swizzled
-    uint8_t *Vs = smem + kTileBytes;                               // [kChunk][kD] bf16
+    uint8_t *Vs = smem + kTileBytes;                               // [kChunk][kD] bf16, the same swizzle
     float *qs = reinterpret_cast<float *>(smem + 2 * kTileBytes);  // [G][kD] bf16 (first half used)
     uint16_t *qb = reinterpret_cast<uint16_t *>(qs);
     float *S = qs + G * kD;                                        // [kChunk][G]
-    float *ml = S + G * kChunk;                                    // [G][2]
-    int64_t *rowoff = reinterpret_cast<int64_t *>(ml + 2 * G);     // [kChunk], -1: no row
-    float *part = reinterpret_cast<float *>(smem);                 // value partials, after the tiles are read
+    int64_t *rowoff = reinterpret_cast<int64_t *>(S + G * kChunk); // [kChunk], -1: no row
     const int c = blockIdx.x, g = blockIdx.y;
     const int64_t b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -140,7 +147,8 @@ attn_split_kernel(const AttnParams p) {
     for (int i = tid; i < G * kD; i += kThreads) qb[i] = p.Q[(b * p.Hq + g * G) * kD + i];
     __syncthreads();
 
-    // K rows (chunk x of row t at chunk x ^ (t % 8)), then V rows; missing rows are zero-filled
+    // K rows, then V rows (16-byte chunk x of row t at chunk x ^ (t % 8));
+    // missing rows are zero-filled
 #pragma unroll
     for (int which = 0; which < 2; ++which) {
         const uint16_t *base = which == 0 ? p.K : p.V;
@@ -150,50 +158,51 @@ attn_split_kernel(const AttnParams p) {
             const int i = tid + r * kThreads;
             const int t = i >> 4, x = i & 15;
             const int64_t off = rowoff[t];
-            const int xs = which == 0 ? (x ^ (t & 7)) : x;
-            cp_async_16(dst0 + t * kRowBytes + xs * 16, off >= 0 ? base + off + x * 8 : base, off >= 0 ? 16u : 0u);
+            cp_async_16(dst0 + t * kRowBytes + ((x ^ (t & 7)) << 4), off >= 0 ? base + off + x * 8 : base,
+                        off >= 0 ? 16u : 0u);
         }
         cp_async_commit();
     }
+    const int gq = lane >> 2, cq = lane & 3;              // fragment row group, column pair
+    float *wsh = p.ws + ((b * p.Hq + g * G) * p.chunks + c) * static_cast<int64_t>(kD + 2);
+    const int64_t ws_head = static_cast<int64_t>(p.chunks) * (kD + 2);   // next query head's record
     cp_async_wait<1>();                                   // this thread's K copies
     __syncthreads();                                      // everyone's
 
-    // scores: lane = token (t = 32*(warp%4) + lane), warp/4 picks every other head;
-    // q.k adds the 128 products in dimension order
+    // scores S[h][t] = q_h . k_t on the tensor cores: A = q (rows = the G heads,
+    // zero beyond), B = K^T; warp w takes tokens 16w .. 16w+15, K ascending
+    // in 16-dimension steps
     {
-        const int t = (warp & 3) * 32 + lane;
-        const int h0 = warp >> 2;
-        if (G > 1 || h0 == 0) {
-            constexpr int NH = G > 1 ? G / 2 : 1;
-            float acc[NH];
+        uint32_t qa[kD / 16][2];
 #pragma unroll
-            for (int i = 0; i < NH; ++i) acc[i] = 0.0f;
-            const uint8_t *krow = Ks + t * kRowBytes;
-#pragma unroll 4
-            for (int x = 0; x < 16; ++x) {
-                const uint4 kv = *reinterpret_cast<const uint4 *>(krow + ((x ^ (t & 7)) << 4));
+        for (int ks = 0; ks < kD / 16; ++ks) {
+            qa[ks][0] = gq < G ? *reinterpret_cast<const uint32_t *>(qb + gq * kD + 16 * ks + 2 * cq) : 0u;
+            qa[ks][1] = gq < G ? *reinterpret_cast<const uint32_t *>(qb + gq * kD + 16 * ks + 8 + 2 * cq) : 0u;
+        }
 #pragma unroll
-                for (int i = 0; i < NH; ++i) {
-                    const uint4 qv = *reinterpret_cast<const uint4 *>(qb + (h0 + (G > 1 ? 2 * i : 0)) * kD + x * 8);
-                    float sc = acc[i];
-                    sc = fma_bf16x2(qv.x, kv.x, sc);
-                    sc = fma_bf16x2(qv.y, kv.y, sc);
-                    sc = fma_bf16x2(qv.z, kv.z, sc);
-                    sc = fma_bf16x2(qv.w, kv.w, sc);
-                    acc[i] = sc;
-                }
+        for (int nb = 0; nb < 2; ++nb) {
+            const int n0 = warp * 16 + nb * 8;
+            const int t = n0 + gq;                        // the K row of this lane's B fragment
+            const uint8_t *krow = Ks + t * kRowBytes + cq * 4;
+            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+            for (int ks = 0; ks < kD / 16; ++ks) {
+                const uint32_t b0 = *reinterpret_cast<const uint32_t *>(krow + (((2 * ks) ^ (t & 7)) << 4));
+                const uint32_t b1 = *reinterpret_cast<const uint32_t *>(krow + (((2 * ks + 1) ^ (t & 7)) << 4));
+                mma_16816(acc, qa[ks][0], 0u, qa[ks][1], 0u, b0, b1);
             }
-            if (t < n) {
-                const bool valid = rowoff[t] >= 0;
+            if (gq < G) {
 #pragma unroll
-                for (int i = 0; i < NH; ++i)
-                    S[t * G + h0 + (G > 1 ? 2 * i : 0)] = valid ? __fmul_rn(acc[i], p.scale) : -INFINITY;
+                for (int e = 0; e < 2; ++e) {
+                    const int tt = n0 + 2 * cq + e;
+                    if (tt < n) S[tt * G + gq] = rowoff[tt] >= 0 ? __fmul_rn(acc[e], p.scale) : -INFINITY;
+                }
             }
         }
     }
     __syncthreads();
 
-    // per head: max, exponentials, sum (head h on warp h)
+    // per head: max, exponentials, sum (head h on warp h); (m, l) to the workspace
     if (warp < G) {
         const int h = warp;
         float m = -INFINITY;
@@ -209,61 +218,48 @@ attn_split_kernel(const AttnParams p) {
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
         if (lane == 0) {
-            ml[2 * h] = m;
-            ml[2 * h + 1] = l;
+            wsh[h * ws_head] = m;
+            wsh[h * ws_head + 1] = l;
         }
     }
     cp_async_wait<0>();                                   // this thread's V copies
     __syncthreads();
 
-    // values: thread (dims 8*dg .. 8*dg+7, token group tg) adds p_t v_t over
-    // tokens tg, tg+16, ... in order, for every head; the 16 token groups'
-    // partial sums are then added in group order
-    const int dg = tid & 15, tg = tid >> 4;
-    float acc[G][8];
-#pragma unroll
-    for (int h = 0; h < G; ++h)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) acc[h][k] = 0.0f;
+    // values O[h][d] = sum_t p_t v_t[d] on the tensor cores: A = p (rows = the
+    // G heads; p = hi + lo, two bf16 MMAs per step; zero past the chunk's
+    // tokens), B = V read transposed by ldmatrix; warp w takes dimensions
+    // 16w .. 16w+15, tokens ascending in 16-token steps
+    {
+        const int d0 = warp * 16;
+        const int mi = lane >> 3, mr = lane & 7;          // ldmatrix: matrix, row
+        float acc[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
 #pragma unroll 2
-    for (int t = tg; t < n; t += 16) {
-        const uint4 vv = *reinterpret_cast<const uint4 *>(Vs + t * kRowBytes + dg * 16);
-        const float v[8] = {bf_lo(vv.x), bf_hi(vv.x), bf_lo(vv.y), bf_hi(vv.y),
-                            bf_lo(vv.z), bf_hi(vv.z), bf_lo(vv.w), bf_hi(vv.w)};
-        float e[G];
-        if constexpr (G % 4 == 0) {
-#pragma unroll
-            for (int h = 0; h < G; h += 4) {
-                const float4 e4 = *reinterpret_cast<const float4 *>(S + t * G + h);
-                e[h] = e4.x, e[h + 1] = e4.y, e[h + 2] = e4.z, e[h + 3] = e4.w;
+        for (int ks = 0; ks < kChunk / 16; ++ks) {
+            const int k0 = ks * 16;
+            uint32_t ph0 = 0u, pl0 = 0u, ph2 = 0u, pl2 = 0u;
+            if (gq < G) {
+                const int t0 = k0 + 2 * cq, t2 = t0 + 8;
+                const float p00 = t0 < n ? S[t0 * G + gq] : 0.0f;
+                const float p01 = t0 + 1 < n ? S[(t0 + 1) * G + gq] : 0.0f;
+                const float p20 = t2 < n ? S[t2 * G + gq] : 0.0f;
+                const float p21 = t2 + 1 < n ? S[(t2 + 1) * G + gq] : 0.0f;
+                split_bf16x2(p00, p01, ph0, pl0);
+                split_bf16x2(p20, p21, ph2, pl2);
             }
-        } else {
-#pragma unroll
-            for (int h = 0; h < G; ++h) e[h] = S[t * G + h];
+            const int tok = k0 + (mi & 1) * 8 + mr;
+            const int chunk = (d0 >> 3) + (mi >> 1);
+            uint32_t v0, v1, v2, v3;
+            ldmatrix_x4_trans(v0, v1, v2, v3, smem_u32(Vs + tok * kRowBytes + ((chunk ^ (tok & 7)) << 4)));
+            mma_16816(acc[0], ph0, 0u, ph2, 0u, v0, v1);
+            mma_16816(acc[0], pl0, 0u, pl2, 0u, v0, v1);
+            mma_16816(acc[1], ph0, 0u, ph2, 0u, v2, v3);
+            mma_16816(acc[1], pl0, 0u, pl2, 0u, v2, v3);
         }
+        if (gq < G) {
+            float *w = wsh + gq * ws_head + 2 + d0 + 2 * cq;
 #pragma unroll
-        for (int h = 0; h < G; ++h)
-#pragma unroll
-            for (int k = 0; k < 8; ++k) acc[h][k] = __fmaf_rn(e[h], v[k], acc[h][k]);
-    }
-    __syncthreads();                                      // tiles no longer read: reuse them
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-        float4 *dst = reinterpret_cast<float4 *>(part + (tg * G + h) * kD + dg * 8);
-        dst[0] = make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
-        dst[1] = make_float4(acc[h][4], acc[h][5], acc[h][6], acc[h][7]);
-    }
-    __syncthreads();
-    for (int o = tid; o < G * kD; o += kThreads) {
-        const int h = o / kD, d = o % kD;
-        float sum = part[h * kD + d];
-#pragma unroll
-        for (int gg = 1; gg < 16; ++gg) sum += part[(gg * G + h) * kD + d];
-        float *w = p.ws + (((b * p.Hq + g * G + h) * p.chunks) + c) * (kD + 2);
-        w[2 + d] = sum;
-        if (d == 0) {
-            w[0] = ml[2 * h];
-            w[1] = ml[2 * h + 1];
+            for (int nb = 0; nb < 2; ++nb)
+                *reinterpret_cast<float2 *>(w + nb * 8) = make_float2(acc[nb][0], acc[nb][1]);
         }
     }
 }
