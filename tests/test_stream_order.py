@@ -1,0 +1,115 @@
+"""Stream order with programmatic dependent launch (every libbi kernel may
+start while the previous kernel of the stream finishes, and waits for it
+before touching global memory). Chains of calls in which each launch reads
+what the previous one wrote, and overwrites what an earlier one read, must
+give the same bits back to back, inside a captured CUDA graph, and with the
+host synchronising after every call."""
+import numpy as np
+import pytest
+
+import bi_synth as syn
+from util import bits_of, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+M, H, STEPS, EPS = 64, 4096, 16, 1e-6
+
+
+def inputs():
+    x = to_dev_bf16(syn.to_bf16_bits(syn.normal_rows(70, syn.TID_X, M, H)))
+    r = to_dev_bf16(syn.to_bf16_bits(syn.normal_rows(71, syn.TID_X, M, H)))
+    w = to_dev_bf16(syn.to_bf16_bits(1.0 + 0.1 * syn.normal_rows(72, syn.TID_W, 1, H)[0]))
+    W = to_dev_bf16(syn.to_bf16_bits(syn.normal_rows(73, syn.TID_W, H, H, std=0.02)))
+    return x, r, w, W
+
+
+def bf16_chain(bi, x0, r0, w, W, sync: bool):
+    """rmsnorm (residual updated in place) -> GEMM, STEPS times; the GEMM writes
+    the buffer the rmsnorm before last read (ping-pong)."""
+    import torch
+    xs = [x0.clone(), torch.empty_like(x0)]
+    r = r0.clone()
+    y = torch.empty_like(x0)
+
+    def run():
+        for i in range(STEPS):
+            bi.rmsnorm(xs[i % 2], w, EPS, residual=r, out=y)
+            if sync:
+                torch.cuda.synchronize()
+            bi.gemm_bf16(y, W, Y=xs[(i + 1) % 2])
+            if sync:
+                torch.cuda.synchronize()
+    return xs, r, run
+
+
+def test_bf16_chain_back_to_back_equals_synchronised(bi):
+    import torch
+    x, r, w, W = inputs()
+    xs_a, r_a, run_a = bf16_chain(bi, x, r, w, W, sync=True)
+    run_a()
+    xs_b, r_b, run_b = bf16_chain(bi, x, r, w, W, sync=False)
+    run_b()
+    torch.cuda.synchronize()
+    assert np.array_equal(bits_of(xs_a[STEPS % 2]), bits_of(xs_b[STEPS % 2]))
+    assert np.array_equal(bits_of(r_a), bits_of(r_b))
+    assert bi.device_status() == bi.BI_OK
+
+
+def test_bf16_chain_in_a_graph_equals_synchronised(bi):
+    import torch
+    x, r, w, W = inputs()
+    xs_a, r_a, run_a = bf16_chain(bi, x, r, w, W, sync=True)
+    run_a()
+    xs_g, r_g, run_g = bf16_chain(bi, x, r, w, W, sync=False)
+    run_g()                                       # warm-up outside capture (loads the library)
+    torch.cuda.synchronize()
+    xs_g[0].copy_(x)
+    r_g.copy_(r)
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g):
+            run_g()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    xs_g[0].copy_(x)                              # capture does not run the work: start from the inputs
+    r_g.copy_(r)
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(bits_of(xs_a[STEPS % 2]), bits_of(xs_g[STEPS % 2]))
+    assert np.array_equal(bits_of(r_a), bits_of(r_g))
+
+
+def test_nvfp4_chain_back_to_back_equals_synchronised(bi):
+    """rmsnorm -> NVFP4 quantise (into the same Q buffers every step, which the
+    previous GEMM read) -> NVFP4 GEMM, STEPS times."""
+    import torch
+    x, _, w, W = inputs()
+    B, B_sf = bi.quantize_nvfp4(W, 1.0)
+    torch.cuda.synchronize()
+
+    def chain(sync: bool):
+        cur = x.clone()
+        y = torch.empty_like(x)
+        Q = torch.empty((M, H // 2), dtype=torch.uint8, device="cuda")
+        Q_sf = torch.zeros(128 * (H // 16), dtype=torch.uint8, device="cuda")
+        for _ in range(STEPS):
+            bi.rmsnorm(cur, w, EPS, out=y)
+            if sync:
+                torch.cuda.synchronize()
+            bi.quantize_nvfp4(y, 1.0, Q=Q, Q_sf=Q_sf)
+            if sync:
+                torch.cuda.synchronize()
+            bi.gemm_nvfp4(Q, Q_sf, B, B_sf, 1.0, Y=cur)
+            if sync:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        return bits_of(cur)
+
+    a = chain(True)
+    b = chain(False)
+    assert np.isfinite(syn.bf16_bits_to_f32(a)).all()
+    assert np.array_equal(a, b)
+    assert bi.device_status() == bi.BI_OK
