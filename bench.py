@@ -784,6 +784,15 @@ def run_ours(args, dist):
         cpu = {"value": round(v, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                "sample": f"{args.cpu_rows} rows of the step (2 RMSNorm rows + qkv/gate_up/down GEMM rows), "
                          f"fp64, {dt:.1f} s"}
+        # the same oracle on one core, on a 16-row slice of the step
+        import oracle
+        oracle.set_threads(1)
+        try:
+            v1, dt1, _ = cpu_baseline(16)
+        finally:
+            oracle.set_threads(cores)
+        cpu["one_core"] = {"value": round(v1, 6), "unit": "TFLOP/s", "cores": 1,
+                           "sample": f"16 rows of the step, fp64, {dt1:.1f} s"}
 
     line = {"metric": METRIC, "value": round(value, 1), "unit": "TFLOP/s", "n_gpus": dist.world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),

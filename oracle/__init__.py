@@ -66,6 +66,7 @@ def _load():
             lib.oracle_bf16_round.argtypes = [D]
             lib.oracle_bf16_round.restype = ctypes.c_uint16
             lib.oracle_bf16_round_array.argtypes = [I64, P, P]
+            lib.oracle_set_threads.argtypes = [ctypes.c_int]
             lib.oracle_quantize_nvfp4.argtypes = [I64, I64, P, ctypes.c_float, P, P]
             lib.oracle_moe_topk_softmax.argtypes = [I64, ctypes.c_int32, ctypes.c_int32, P, ctypes.c_int, P, P]
             lib.oracle_moe_align.argtypes = [I64, ctypes.c_int32, ctypes.c_int32, P, P, P, P]
@@ -94,6 +95,12 @@ def _c(a, dtype):
 def threads() -> int:
     """OpenMP threads the oracle's loops use."""
     return int(_load().oracle_threads())
+
+
+def set_threads(n: int) -> None:
+    """Use n OpenMP threads from now on (timing only: each output element is
+    one sequential sum, so results do not depend on the thread count)."""
+    _load().oracle_set_threads(int(n))
 
 
 def gemm_bf16(X: np.ndarray, W: np.ndarray) -> np.ndarray:

@@ -101,6 +101,18 @@ int oracle_threads(void)
 #endif
 }
 
+/* Threads for the parallel loops from now on (n >= 1); only for timing the
+   oracle on fewer cores: every output element is one sequential sum, so the
+   results do not depend on it. */
+void oracle_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /* Y[i][j] = sum_{k=0}^{K-1} X[i][k] * W[j][k]   (linear layer, Y = X W^T).
  * X: bf16 [M][ldx], W: bf16 [N][ldw] (nn.Linear layout), Y: fp64 [M][ldy]. */
 void oracle_gemm_bf16(int64_t M, int64_t N, int64_t K,
