@@ -343,6 +343,20 @@ def rmsnorm_sweep(bi, peaks):
     return rows
 
 
+def torch_rmsnorm_row0_equal() -> bool:
+    """Informational: is torch.nn.functional.rms_norm batch-invariant here, i.e.
+    does row 0 of an M=16384 call equal the same row normalised alone?"""
+    import torch
+    import bi_synth as syn
+    M = max(RMS_SWEEP)
+    x, _, w, _ = syn.rmsnorm_inputs(M, H, seed=0)
+    xd, wd = bf16_dev(x), bf16_dev(w)
+    full = torch.nn.functional.rms_norm(xd, (H,), wd, EPS)
+    one = torch.nn.functional.rms_norm(xd[:1].clone(), (H,), wd, EPS)
+    torch.cuda.synchronize()
+    return bool(torch.equal(full[:1].view(torch.int16), one.view(torch.int16)))
+
+
 MOE_E, MOE_TOPK = 128, 8
 MOE_LAYERS = {"gate_up": (1536, 2048), "down": (2048, 768)}
 MOE_T = [1, 64, 512, 8192]
@@ -770,6 +784,7 @@ def run_ours(args, dist):
         breakdown["gemm_bf16_vs_M"] = rows
         breakdown["cublas_row0_equal_M1_vs_M4096"] = cublas_inv
         breakdown["rmsnorm"] = rmsnorm_sweep(bi, peaks)
+        breakdown["torch_rms_norm_row0_equal_M1_vs_M16384"] = torch_rmsnorm_row0_equal()
         breakdown["grouped_gemm_bf16_moe"] = moe_sweep(bi, peaks)
         breakdown["gemm_nvfp4"] = nvfp4_sweep(bi, peaks)
         breakdown["quantize_nvfp4"] = quant_sweep(bi, peaks)

@@ -61,7 +61,9 @@ inline bi_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, siz
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...) == cudaSuccess ? BI_OK : BI_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...) == cudaSuccess) return BI_OK;
+    cudaGetLastError();   // reported here; do not leave it for a later, unrelated check
+    return BI_ERR_CUDA;
 }
 
 // Kernel launchers (defined in the .cu files); arguments already validated.
