@@ -79,3 +79,24 @@ def test_bad_lengths_reported(bi):
     bi.attention_decode(to_dev_bf16(Q), to_dev_bf16(K), to_dev_bf16(V), to_dev(table), to_dev(bad), 16, SCALE)
     torch.cuda.synchronize()
     assert bi.device_status() == bi.BI_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (16, 8), (32, 4)])
+def test_group_sizes(bi, hq, hkv):
+    """GQA groups G = 1, 2, 8 (the shapes above use G = 4): parity with the
+    oracle, and a sequence alone gives the same bits as in the batch."""
+    lens = np.asarray([1, 129, 300], dtype=np.int32)
+    nb = int(-(-lens.max() // BS))
+    blocks = len(lens) * nb + 2
+    K = syn.to_bf16_bits(syn.normal_rows(40 + hq, 0, blocks * BS, hkv * D)).reshape(blocks, BS, hkv, D)
+    V = syn.to_bf16_bits(syn.normal_rows(40 + hq, 1, blocks * BS, hkv * D)).reshape(blocks, BS, hkv, D)
+    table = syn.rng(40 + hq, 2).permutation(blocks)[: len(lens) * nb].astype(np.int32).reshape(len(lens), nb)
+    Q = syn.to_bf16_bits(syn.normal_rows(41 + hq, 0, len(lens) * hq, D)).reshape(len(lens), hq, D)
+    full = run(bi, Q, K, V, table, lens, 512)
+    got = syn.bf16_bits_to_f32(full).astype(np.float64)
+    ref = oracle.attention_decode(Q, K, V, table, lens, SCALE)
+    assert_close_rel(got, ref, 1e-2, 2e-3, f"Hq={hq} Hkv={hkv}")
+    for b in range(len(lens)):
+        one = run(bi, Q[b:b + 1], K, V, table[b:b + 1], lens[b:b + 1], 512)
+        assert np.array_equal(one[0], full[b]), f"Hq={hq} Hkv={hkv}: sequence {b} alone differs"
+    assert bi.device_status() == bi.BI_OK
