@@ -109,3 +109,23 @@ def test_repeat_and_permuted_groups(bi, weights):
         perm[a:b] = a + g.permutation(b - a)
     Y = bits_of(bi.grouped_gemm_bf16(to_dev_bf16(X[perm]), Wd, od))
     assert np.array_equal(Y, base[perm])
+
+
+@pytest.mark.parametrize("Ee", [1, 33, 100, 1024])
+def test_expert_counts_exact(bi, Ee):
+    """Expert counts from 1 to the maximum (1024): the device-side tile map
+    (a prefix over the experts, split into one block per lane of a warp)
+    covers every expert; random group sizes with empty experts and integer
+    inputs, so outputs are bf16(exact sum) bit for bit."""
+    counts = syn.rng(50 + Ee, 0).integers(0, 6 if Ee > 1 else 300, size=Ee)
+    if Ee > 1:
+        counts[::7] = 0
+    N, K = 264, 136
+    off = syn.offsets_from_counts(counts)
+    rows = int(off[-1])
+    X = syn.integer_bf16(5, 0, (rows, K))
+    W = syn.integer_bf16(5, 1, (Ee, N, K))
+    Y = bits_of(bi.grouped_gemm_bf16(to_dev_bf16(X), to_dev_bf16(W), to_dev(off)))
+    ref = oracle.grouped_gemm_bf16(X, W, off)
+    assert np.array_equal(Y, oracle.bf16_round_array(ref))
+    assert bi.device_status() == bi.BI_OK
