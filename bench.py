@@ -642,6 +642,18 @@ def attention_sweep(bi, peaks):
     return rows
 
 
+_STEP_WEIGHTS = {}
+
+
+def step_weights():
+    """The step's three weight matrices as bf16 bits (seeded; generated once)."""
+    import bi_synth as syn
+    if not _STEP_WEIGHTS:
+        for i, (name, (n, k)) in enumerate(LAYERS.items()):
+            _STEP_WEIGHTS[name] = syn.to_bf16_bits(syn.normal_rows(10 + i, syn.TID_W, n, k, std=0.02))
+    return _STEP_WEIGHTS
+
+
 def cpu_baseline(rows: int):
     """The fp64 oracle on a bounded sample of the step: `rows` rows of every
     GEMM of the step and of both RMSNorms, on the host's cores."""
@@ -649,8 +661,7 @@ def cpu_baseline(rows: int):
     import bi_synth as syn
     import oracle
     x, res, w, _ = syn.rmsnorm_inputs(rows, H, seed=0, outlier_frac=0.0)
-    Ws = {name: syn.to_bf16_bits(syn.normal_rows(10 + i, syn.TID_W, n, k, std=0.02))
-          for i, (name, (n, k)) in enumerate(LAYERS.items())}
+    Ws = step_weights()
     Xd = syn.to_bf16_bits(syn.normal_rows(0, syn.TID_X, rows, LAYERS["down"][1]))
     t0 = time.perf_counter()
     y1, h = oracle.rmsnorm(x, w, EPS, residual=res)
