@@ -287,6 +287,10 @@ BI_API bi_status bi_rank_sum_rmsnorm(const void *const *parts, int32_t R, void *
  * The KV range is split into fixed 128-token chunks by position alone (never
  * by batch size); each chunk is reduced in a fixed order and the chunks are
  * merged in chunk order, so a sequence's output does not depend on the batch.
+ * Arithmetic: q.k and p.v are bf16 tensor-core products with fp32
+ * accumulation; the probabilities enter p.v as a bf16 high part plus a bf16
+ * low part (16 significant bits); softmax statistics and the chunk merge are
+ * fp32.
  *
  *   Q         bf16 [B][Hq][128]
  *   K_cache   bf16 [num_blocks][block_size][Hkv][128]; V_cache likewise
