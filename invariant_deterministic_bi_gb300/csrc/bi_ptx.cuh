@@ -79,18 +79,6 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *m, uin
         : "memory");
 }
 
-// TMA 2-D load multicast to the CTAs of the cluster in cta_mask: the box lands
-// at the same shared-memory offset in each of them and is counted on the
-// barrier at the same offset in each.
-__device__ __forceinline__ void tma_load_2d_multicast(void *dst, const CUtensorMap *m, uint64_t *bar, int32_t c0,
-                                                      int32_t c1, uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4}], [%2], %5;"
-        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "h"(cta_mask)
-        : "memory");
-}
-
 // TMA 3-D load into this CTA's shared memory, counted on this CTA's barrier.
 __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *m, uint64_t *bar, int32_t c0, int32_t c1,
                                             int32_t c2) {

@@ -3,28 +3,26 @@
 // Y[i][j] = bf16( alpha * sum_k (a[i][k] sa[i][k/16]) (b[j][k] sb[j][k/16]) ), the
 // NVFP4 linear layer of vLLM PR #39912 ("NVFP4 CUTLASS batch invariant mode").
 //
-// Output tiles are 256 x 256, each computed by a CTA pair (cta_group::2, one
-// CTA per SM, 128 accumulator rows each). Clusters hold two pairs that work on
-// the same 256 A rows and on two neighbouring 256-column tiles, so every A
-// byte is read from L2 once per cluster: the CTA with lane-half h of pair p
-// loads A rows [128h + 64p, +64) of the tile and multicasts them to CTA h of
-// both pairs. K advances in stages of 256 e2m1 values (128 bytes per row),
-// 5 stages of 38 KB per CTA. Warp roles:
-//   - warp 0 (every CTA): per stage, its 64-row A multicast, its own 128 B
-//     rows, and the stage's scale atoms (its 4 A atoms, all 8 B atoms of the
-//     pair's tile, 512 bytes each), all counted on its own "full" barrier;
-//   - warps 2-5 (every CTA): one per tensor-memory lane quarter; once "full"
+// Output tiles are 256 x 256, each computed by a CTA pair (a cluster of two
+// CTAs, cta_group::2, one CTA per SM, 128 accumulator rows each). Every CTA
+// loads its own operands with plain TMA copies into its own shared memory:
+// the 128 A rows of its lane half and its 128-row half of the B tile. K
+// advances in stages of 256 e2m1 values (128 bytes per row), 5 stages of
+// 38 KB per CTA. Warp roles:
+//   - warp 0 (both CTAs): per stage, its 128 A rows, its 128 B rows and the
+//     stage's scale atoms (its 4 A atoms, all 8 B atoms of the pair's tile,
+//     512 bytes each), all counted on its own "full" barrier;
+//   - warps 2-5 (both CTAs): one per tensor-memory lane quarter; once "full"
 //     completes they move the scale atoms from shared memory into the
 //     stage's scale slot in tensor memory with tcgen05.st (each quarter holds
 //     the same 48 columns: lane l, column c = row 32c + l of an atom), wait
 //     for the stores and report to the pair leader's "ready" barrier -- so
 //     "ready" also means both CTAs' operands have landed;
-//   - warp 1 (pair leaders): one thread issues four
+//   - warp 1 (pair leader): one thread issues four
 //     tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X
-//     (256 x 256 x 64, fp32 accumulate) per stage, then commits the stage
-//     to all four CTAs: a stage slot is refilled only when both pairs'
-//     MMAs have read it, since each CTA's A multicast lands in both pairs;
-//   - warps 6-13 (every CTA): two warps per lane quarter, 128 columns each:
+//     (256 x 256 x 64, fp32 accumulate) per stage, then commits the stage to
+//     both CTAs' "empty" barriers;
+//   - warps 6-13 (both CTAs): two warps per lane quarter, 128 columns each:
 //     read the accumulator, scale by alpha, round to bf16, hand the
 //     accumulator back, then write 32 x 64 boxes through a swizzled staging
 //     buffer with TMA stores (rows past M, columns past N are clipped).
@@ -34,7 +32,7 @@
 //
 // TMEM per CTA: one 256-column accumulator + a 5 x 48-column scale ring.
 // Invariance: tile shape, MMA shape and K order (ascending 64-wide steps from
-// zero) are the same for every M; rows never interact; which cluster computes
+// zero) are the same for every M; rows never interact; which pair computes
 // which tile does not change any result.
 #include <cuda_bf16.h>
 
@@ -46,10 +44,9 @@
 namespace bi {
 namespace {
 
-constexpr int kClusterCtas = 4;          // two CTA pairs
+constexpr int kClusterCtas = 2;          // one CTA pair
 constexpr int kBM = 256;                 // pair tile rows (128 per CTA)
-constexpr int kHalf = 128;
-constexpr int kAPart = 64;               // A rows each CTA loads and multicasts per stage
+constexpr int kHalf = 128;               // A rows and B rows each CTA loads per stage
 constexpr int kBN = 256;
 constexpr int kBKBytes = 128;            // K bytes per stage (256 e2m1 values)
 constexpr int kBK = 2 * kBKBytes;
@@ -62,7 +59,7 @@ constexpr int kThreads = 32 * (2 + kSfWarps + kEpiWarps);
 constexpr int kGroupM = 8;
 constexpr int kAtom = 512;
 
-constexpr int kABytes = kHalf * kBKBytes;                   // 16 KB (two multicast parts of 8 KB)
+constexpr int kABytes = kHalf * kBKBytes;                   // 16 KB (this CTA's 128 A rows)
 constexpr int kBBytes = kHalf * kBKBytes;                   // 16 KB (this CTA's half of the pair's B)
 constexpr int kSfaBytes = kMmasPerStage * kAtom;            // 2 KB
 constexpr int kSfbBytes = 2 * kMmasPerStage * kAtom;        // 4 KB (both B row blocks)
@@ -84,7 +81,7 @@ struct Params {
     float alpha;
     int32_t M, N, K;
     int32_t atoms_per_rowblock;   // K / 64
-    int32_t stage_tx;             // bytes landing in a CTA per stage (fewer A rows when M < 64)
+    int32_t stage_tx;             // bytes landing in a CTA per stage (fewer A rows when M < 128)
     unsigned *status;
 };
 
@@ -97,14 +94,14 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *out_stage = smem + kStages * kStageBytes;   // kEpiWarps staging boxes of kOutBytes
     uint64_t *full = reinterpret_cast<uint64_t *>(out_stage + kEpiWarps * kOutBytes);
-    uint64_t *empty = full + kStages;        // [2][kStages]: one barrier per pair leader
-    uint64_t *ready = empty + 2 * kStages;   // (pair leader) both CTAs' operands and scales in place
+    uint64_t *empty = full + kStages;        // stage read by the pair's MMAs
+    uint64_t *ready = empty + kStages;       // (pair leader) both CTAs' operands and scales in place
     uint64_t *tfull = ready + kStages;
     uint64_t *tempty = tfull + 1;
     uint64_t *drain = tempty + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    static_assert((5 * kStages + 3) * 8 + 8 <= kBarBytes, "barrier area");
+    static_assert((3 * kStages + 3) * 8 + 8 <= kBarBytes, "barrier area");
 
     auto stage_a = [&](int s) { return smem + s * kStageBytes; };
     auto stage_b = [&](int s) { return smem + s * kStageBytes + kABytes; };
@@ -113,22 +110,18 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
-    const int h = static_cast<int>(rank & 1u);          // lane half of the pair's tile
-    const int pc = static_cast<int>(rank >> 1);         // which pair of the cluster
-    const uint32_t lead = rank & ~1u;                   // this pair's leader
+    const int h = static_cast<int>(rank);               // lane half of the pair's tile (0: leader)
     const int cl = static_cast<int>(blockIdx.x) / kClusterCtas;
     const int ncl = static_cast<int>(gridDim.x) / kClusterCtas;
     const int num_m = (p.M + kBM - 1) / kBM;
     const int num_n = (p.N + kBN - 1) / kBN;
-    const int num_sn = (num_n + 1) / 2;                  // column-tile pairs
-    const int total = num_m * num_sn;
+    const int total = num_m * num_n;
     const int k_stages = (p.K + kBK - 1) / kBK;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
-            mbar_init(&empty[kStages + s], 1);
             mbar_init(&ready[s], 2 * kSfWarps);      // scale writer warps of both CTAs of the pair
         }
         mbar_init(tfull, 1);
@@ -153,15 +146,17 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    // Supertile t -> (row tile mb, column-tile pair sn); pair pc takes column tile 2*sn + pc.
-    auto tile_of = [&](int t, int &mb, int &sn) {
-        const int per_group = kGroupM * num_sn;
+    // Tile t -> (row tile mb, column tile nb): bands of kGroupM row tiles, row
+    // tiles fastest inside a band, so pairs running at the same time share
+    // their B panels and A panels in L2.
+    auto tile_of = [&](int t, int &mb, int &nb) {
+        const int per_group = kGroupM * num_n;
         const int g = t / per_group;
         const int first = g * kGroupM;
         const int gm = min(kGroupM, num_m - first);
         const int local = t - g * per_group;
         mb = first + local % gm;
-        sn = local / gm;
+        nb = local / gm;
     };
     auto mmas_in = [&](int ks) { return min(kMmasPerStage, (p.K - ks * kBK) / kMmaK); };
     auto give_up = [&]() {
@@ -172,25 +167,21 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     if (warp == 0) {
         // ------------------------------------------------ TMA producer (every CTA)
         if (lane == 0) {
-            const uint16_t a_dest = static_cast<uint16_t>(0x5u << h);   // CTA h of both pairs
             int stage = 0;
             uint32_t phase = 0, issued = 0, issued_phase = 0;
             bool ok = true;
             for (int t = cl; t < total && ok; t += ncl) {
-                int mb, sn;
-                tile_of(t, mb, sn);
-                const int nb = 2 * sn + pc;
-                const int a_row = mb * kBM + h * kHalf + pc * kAPart;
+                int mb, nb;
+                tile_of(t, mb, nb);
+                const int a_row = mb * kBM + h * kHalf;
                 const int b_row = nb * kBN + h * kHalf;
                 const int rb_a = mb * 2 + h;               // this CTA's 128-row scale block of A
                 const int rb_b = nb * 2;                   // the tile's two B scale blocks
                 for (int ks = 0; ks < k_stages; ++ks) {
-                    // the slot is free once both pairs' MMAs have read it
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag) ||
-                        !mbar_wait(&empty[kStages + stage], phase ^ 1u, abort_flag)) { ok = false; break; }
+                    // the slot is free once the pair's MMAs have read it
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
                     mbar_arrive_expect_tx(&full[stage], p.stage_tx);
-                    tma_load_2d_multicast(stage_a(stage) + pc * (kAPart * kBKBytes), &tmA, &full[stage],
-                                          ks * kBKBytes, a_row, a_dest);
+                    tma_load_2d(stage_a(stage), &tmA, &full[stage], ks * kBKBytes, a_row);
                     tma_load_2d(stage_b(stage), &tmB, &full[stage], ks * kBKBytes, b_row);
                     const int atom = ks * kMmasPerStage;
                     tma_load_3d(stage_sfa(stage), &tmSFA, &full[stage], 0, 0, rb_a * p.atoms_per_rowblock + atom);
@@ -203,8 +194,7 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 }
             }
             for (int i = 0; i < kStages && ok; ++i) {
-                if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag) ||
-                    !mbar_wait(&empty[kStages + stage], phase ^ 1u, abort_flag)) ok = false;
+                if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) ok = false;
                 if (++stage == kStages) { stage = 0; phase ^= 1u; }
             }
             if (!ok) {
@@ -216,13 +206,12 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer (pair leaders)
+        // ------------------------------------------------ MMA issuer (pair leader)
         if (lane == 0 && h == 0) {
             int stage = 0, it = 0;
             uint32_t phase = 0;
             bool ok = true;
             const uint32_t d = tmem_base + kAccCol;
-            uint64_t *my_empty = empty + pc * kStages;
             for (int t = cl; t < total && ok; t += ncl, ++it) {
                 if (!mbar_wait(tempty, (it & 1) ^ 1u, abort_flag)) { ok = false; break; }
                 tc_fence_after();
@@ -235,15 +224,15 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     for (int j = 0; j < nk; ++j)
                         mma_nvf4_pair(d, sdesc_k_sw128(a0 + j * (kMmaK / 2)), sdesc_k_sw128(b0 + j * (kMmaK / 2)),
                                       kIdesc, sf + j * kSfColsPerMma, sf + j * kSfColsPerMma + 4, (ks | j) != 0);
-                    tc_commit_pair(&my_empty[stage], 0xF);
+                    tc_commit_pair(&empty[stage], 0x3);
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                tc_commit_pair(tfull, static_cast<uint16_t>(0x3u << lead));
+                tc_commit_pair(tfull, 0x3);
             }
             if (!ok) {
                 give_up();
-                tc_commit_pair(drain, static_cast<uint16_t>(1u << lead));
+                tc_commit_pair(drain, 0x1);
                 mbar_wait(drain, 0, nullptr);
             }
         }
@@ -255,7 +244,7 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         // four 32-bit columns of lane l for that atom.
         const int q = warp & 3;
         const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kSfCol;
-        const uint32_t ready_leader = mapa_shared(smem_u32(ready), lead);
+        const uint32_t ready_leader = mapa_shared(smem_u32(ready), 0);
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
@@ -297,15 +286,14 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         const int e = warp - 2 - kSfWarps;
         const int q = warp & 3;
         const int half = e / 4;                               // which 128 columns of the tile
-        const uint32_t tempty_leader = mapa_shared(smem_u32(tempty), lead);
+        const uint32_t tempty_leader = mapa_shared(smem_u32(tempty), 0);
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kAccCol + half * (kBN / 2);
         const uint32_t box = smem_u32(out_stage + e * kOutBytes);
         if (lane == 0) tma_prefetch_desc(&tmY);
         int it = 0;
         for (int t = cl; t < total; t += ncl, ++it) {
-            int mb, sn;
-            tile_of(t, mb, sn);
-            const int nb = 2 * sn + pc;
+            int mb, nb;
+            tile_of(t, mb, nb);
             int ok = 1;
             if (lane == 0) ok = mbar_wait(tfull, it & 1, abort_flag) ? 1 : 0;
             if (!__shfl_sync(0xffffffffu, ok, 0)) {
@@ -393,8 +381,8 @@ void plan_gemm_nvfp4(int64_t M, int64_t N, int64_t K, int clusters, bi_plan_t *p
     pl->smem_bytes = kSmem;
     pl->tiles_m = (M + kBM - 1) / kBM;
     pl->tiles_n = (N + kBN - 1) / kBN;
-    const int64_t supertiles = pl->tiles_m * ((pl->tiles_n + 1) / 2);
-    pl->grid = static_cast<int32_t>(kClusterCtas * (supertiles < clusters ? supertiles : clusters));
+    const int64_t tiles = pl->tiles_m * pl->tiles_n;
+    pl->grid = static_cast<int32_t>(kClusterCtas * (tiles < clusters ? tiles : clusters));
     pl->reduce_tree = 0;
 }
 
@@ -414,11 +402,11 @@ bi_status launch_gemm_nvfp4(const uint8_t *A, const uint8_t *A_sf, const uint8_t
     bi_status st = current_device(&dev, &info);
     if (st != BI_OK) return st;
     CUtensorMap ta, tb, tsa, tsb, ty;
-    // With fewer than 64 rows, each CTA copies only the A rows that can hold
-    // data (rounded up to 16) of its 64-row part; the MMA still multiplies the
-    // whole tile and the accumulator rows past M are never stored. Rows never
-    // interact, so no stored bit changes.
-    const int a_rows = M >= kAPart ? kAPart : static_cast<int>((M + 15) / 16 * 16);
+    // With fewer than 128 rows, each CTA copies only the A rows that can hold
+    // data (rounded up to 16); the MMA still multiplies the whole tile and the
+    // accumulator rows past M are never stored. Rows never interact, so no
+    // stored bit changes.
+    const int a_rows = M >= kHalf ? kHalf : static_cast<int>((M + 15) / 16 * 16);
     st = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K / 2, M, K / 2, kBKBytes, a_rows,
                       CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != BI_OK) return st;
@@ -444,7 +432,7 @@ bi_status launch_gemm_nvfp4(const uint8_t *A, const uint8_t *A_sf, const uint8_t
     p.N = static_cast<int32_t>(N);
     p.K = static_cast<int32_t>(K);
     p.atoms_per_rowblock = static_cast<int32_t>(K / 64);
-    p.stage_tx = kStageBytes - 2 * (kAPart - a_rows) * kBKBytes;   // both A parts it receives are a_rows high
+    p.stage_tx = kStageBytes - (kHalf - a_rows) * kBKBytes;   // the A box is a_rows high
     p.status = device_status_word();
     return launch_pdl(gemm_nvfp4_kernel, dim3(pl.grid), dim3(kThreads), kSmem, s, ta, tb, tsa, tsb, ty, p);
 }
