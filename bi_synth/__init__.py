@@ -182,10 +182,10 @@ def e2m1_encode(v: np.ndarray) -> np.ndarray:
     an exact midpoint it passes only when the upper neighbour's code is even
     (ties to even). Same result as the table search, much faster."""
     v = np.asarray(v)
-    mag = np.abs(v).astype(np.float32)
+    mag = np.abs(v).astype(np.float64)
     c = np.zeros(mag.shape, dtype=np.uint8)
     for lo in range(7):
-        mid = np.float32((_E2M1[lo] + _E2M1[lo + 1]) / 2)
+        mid = (_E2M1[lo] + _E2M1[lo + 1]) / 2
         c += (mag >= mid) if (lo + 1) % 2 == 0 else (mag > mid)
     return np.where((v < 0) & (c != 0), c | np.uint8(8), c).astype(np.uint8)
 
@@ -204,23 +204,25 @@ def nvfp4_global_scale(x: np.ndarray) -> np.float32:
 
 
 def nvfp4_quantize(x: np.ndarray, gs: np.float32):
-    """Quantise fp32 [R, K] (K % 16 == 0) with global scale gs.
+    """Quantise [R, K] values exact in bf16 (K % 16 == 0) with global scale gs.
 
-    Per 16-element block: s = e4m3(amax_block / 6 * gs); q = e2m1(x * (gs / s)),
-    q = 0 where s decodes to 0 (fp32: one division per block, one multiply per
-    element). Returns (packed codes u8 [R, K/2] with the even k in the low
-    nibble, block scales u8 [R, K/16] row-major)."""
-    x = np.ascontiguousarray(x, dtype=np.float32)
+    Per 16-element block: s = e4m3(amax_block * gs / 6); q = e2m1(x * gs / s),
+    q = 0 where s decodes to 0. The quotients are taken in fp64, where the
+    products x*gs are exact and the one division cannot move a value across a
+    rounding boundary, so the codes are those of the exact values. Returns
+    (packed codes u8 [R, K/2] with the even k in the low nibble, block scales
+    u8 [R, K/16] row-major)."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
     R, K = x.shape
     assert K % 16 == 0
+    g = np.float64(np.float32(gs))
     blocks = x.reshape(R, K // 16, 16)
     amax = np.max(np.abs(blocks), axis=2)
-    s_code = e4m3_encode_pos((amax / np.float32(6.0)) * gs)
-    s_val = _E4M3[s_code].astype(np.float32)
+    s_code = e4m3_encode_pos(amax * g / 6.0)
+    s_val = _E4M3[s_code].astype(np.float64)
     with np.errstate(divide="ignore", invalid="ignore"):
-        inv = np.float32(gs) / s_val
-        scaled = blocks * inv[:, :, None]
-    scaled = np.where(s_val[:, :, None] == 0, np.float32(0), scaled)
+        scaled = blocks * g / s_val[:, :, None]
+    scaled = np.where(s_val[:, :, None] == 0, 0.0, scaled)
     scaled = np.clip(scaled, -6.0, 6.0)
     q = e2m1_encode(scaled).reshape(R, K)
     packed = (q[:, 0::2] | (q[:, 1::2] << np.uint8(4))).astype(np.uint8)

@@ -3,8 +3,13 @@
 // The activation quantiser that feeds the NVFP4 linear layer in vLLM PR #39912
 // ("NVFP4 CUTLASS batch invariant mode", test code: scaled_fp4_quant with the
 // tensor's global scale). Per row and 16-element block, with global scale gs:
-//   s = e4m3( (amax / 6) * gs )        round to nearest even, saturating at 448
-//   q = e2m1( x * (gs / value(s)) )    round to nearest even, saturating at 6; q = 0 if value(s) = 0
+//   s = e4m3( amax * gs / 6 )          round to nearest even, saturating at 448
+//   q = e2m1( x * gs / value(s) )      round to nearest even, saturating at 6; q = 0 if value(s) = 0
+// evaluated in binary32 as (amax / 6) * gs and x * (gs / value(s)): one
+// division per block and one multiply per element. Each quotient carries two
+// roundings (within 2^-23 of the exact value, relatively), so a code or scale
+// can differ from the exact definition's only where the exact value lies
+// that close to the midpoint between two codes.
 // Every output depends only on its own row and gs, so a row quantises to the
 // same bytes whatever the batch. Zero magnitudes are stored as code 0 (never
 // the negative-zero code 8).

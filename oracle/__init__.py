@@ -68,6 +68,7 @@ def _load():
             lib.oracle_bf16_round_array.argtypes = [I64, P, P]
             lib.oracle_set_threads.argtypes = [ctypes.c_int]
             lib.oracle_quantize_nvfp4.argtypes = [I64, I64, P, ctypes.c_float, P, P]
+            lib.oracle_quantize_nvfp4_codes.argtypes = [I64, I64, P, ctypes.c_float, P, P]
             lib.oracle_moe_topk_softmax.argtypes = [I64, ctypes.c_int32, ctypes.c_int32, P, ctypes.c_int, P, P]
             lib.oracle_moe_align.argtypes = [I64, ctypes.c_int32, ctypes.c_int32, P, P, P, P]
             lib.oracle_silu_mul.argtypes = [I64, I64, P, P]
@@ -75,9 +76,9 @@ def _load():
             lib.oracle_rank_sum_rmsnorm.argtypes = [ctypes.c_int32, I64, I64, P, P, P, D, P, P, P]
             lib.oracle_attention_decode.argtypes = [I64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                                     ctypes.c_int32, ctypes.c_int32, P, P, P, P, P, D, P]
-            lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+            lib.oracle_e4m3_encode.argtypes = [D]
             lib.oracle_e4m3_encode.restype = ctypes.c_uint
-            lib.oracle_e2m1_encode.argtypes = [ctypes.c_float]
+            lib.oracle_e2m1_encode.argtypes = [D]
             lib.oracle_e2m1_encode.restype = ctypes.c_uint
             lib.oracle_threads.restype = ctypes.c_int
             _lib = lib
@@ -161,7 +162,8 @@ def rmsnorm(x, w, eps: float, residual=None):
 
 
 def quantize_nvfp4(X: np.ndarray, gs: float):
-    """NVFP4 quantisation of bf16 rows X [M,K] with global scale gs (fp32 arithmetic).
+    """NVFP4 quantisation of bf16 rows X [M,K] with global scale gs: the codes
+    and scales of the exact values amax*gs/6 and x*gs/value(s).
 
     Returns (packed e2m1 codes u8 [M, K/2], e4m3 block scales u8 [M, K/16] row-major)."""
     X = _c(X, np.uint16)
@@ -172,6 +174,19 @@ def quantize_nvfp4(X: np.ndarray, gs: float):
     if M:
         _load().oracle_quantize_nvfp4(M, K, _p(X), float(np.float32(gs)), _p(Q), _p(S))
     return Q, S
+
+
+def quantize_nvfp4_codes(X: np.ndarray, gs: float, S: np.ndarray) -> np.ndarray:
+    """The packed e2m1 codes of X [M,K] for given e4m3 block scales S [M, K/16]
+    (row-major), by the same definition as quantize_nvfp4."""
+    X = _c(X, np.uint16)
+    M, K = X.shape
+    S = _c(S, np.uint8)
+    assert S.shape == (M, K // 16)
+    Q = np.zeros((M, K // 2), dtype=np.uint8)
+    if M:
+        _load().oracle_quantize_nvfp4_codes(M, K, _p(X), float(np.float32(gs)), _p(S), _p(Q))
+    return Q
 
 
 def moe_topk_softmax(logits: np.ndarray, k: int, renormalize: bool = True):

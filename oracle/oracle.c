@@ -180,46 +180,68 @@ void oracle_gemm_nvfp4(int64_t M, int64_t N, int64_t K,
 }
 
 /* ---- NVFP4 quantisation of activations (scaled_fp4_quant in the page's test).
- * Per row r and 16-element block b, with the per-tensor global scale gs:
- *   amax = max |x| over the block                          (exact)
- *   s    = e4m3_rne_satfinite( (amax / 6) * gs )           (fp32 ops, then encode)
- *   q_k  = e2m1_rne( clamp( x_k * (gs / value(s)), -6, 6 ) )   (fp32 ops), q = 0 if value(s) == 0
- * Floating point decides integer codes here, so the arithmetic is binary32
- * (the precision the kernel uses), one rounding per operation (-ffp-contract=off).
+ * Per row r and 16-element block b, with the per-tensor global scale gs, the
+ * plain definition on exact values:
+ *   amax = max |x| over the block
+ *   s    = e4m3_rne_satfinite( amax * gs / 6 )
+ *   q_k  = e2m1_rne( clamp( x_k * gs / value(s), -6, 6 ) ),  q = 0 if value(s) == 0
+ * Both quotients are evaluated in fp64: x * gs and amax * gs are exact (a bf16
+ * significand times a binary32 one has at most 32 bits) and the one division
+ * rounds once, which cannot carry the quotient across a rounding boundary of
+ * e4m3 or e2m1 (a boundary has at most 5 significant bits, so a quotient
+ * that is not on it is at least 2^-40 away, relatively). The codes are
+ * therefore those of the exact rational values.
  * Encoders are written from the format definitions: round to the nearest
  * representable value by binade (quantum 2^(e - mantissa bits)), ties to even. */
 
-/* Round half to even of a non-negative float that is an exact multiple of 1/2. */
-static float rne_halves(float v) { return nearbyintf(v); }
+/* Round half to even of a non-negative double. */
+static double rne(double v) { return nearbyint(v); }
 
-static unsigned e4m3_encode_satfinite(float v) /* v >= 0 */
+static unsigned e4m3_encode_satfinite(double v) /* v >= 0 */
 {
-    if (!(v < 448.0f)) return 0x7Eu;                  /* saturate (also +inf) */
-    if (v < ldexpf(1.0f, -6)) {                       /* subnormal binade: quantum 2^-9 */
-        float m = rne_halves(v * 512.0f);             /* exact scaling by a power of two */
+    if (!(v < 448.0)) return 0x7Eu;                   /* saturate (also +inf) */
+    if (v < ldexp(1.0, -6)) {                         /* subnormal binade: quantum 2^-9 */
+        double m = rne(v * 512.0);                    /* exact scaling by a power of two */
         return (unsigned)m;                           /* m == 8 is 2^-6, code 0x08 */
     }
     int e;
-    (void)frexpf(v, &e);                              /* v = f * 2^e, f in [0.5, 1) */
+    (void)frexp(v, &e);                               /* v = f * 2^e, f in [0.5, 1) */
     e -= 1;                                           /* v in [2^e, 2^(e+1)) */
-    float m = rne_halves(ldexpf(v, 3 - e));           /* significand in [8, 16] */
-    if (m == 16.0f) { m = 8.0f; e += 1; }
+    double m = rne(ldexp(v, 3 - e));                  /* significand in [8, 16] */
+    if (m == 16.0) { m = 8.0; e += 1; }
     if (e > 8) return 0x7Eu;
     return ((unsigned)(e + 7) << 3) | ((unsigned)m - 8u);
 }
 
-static unsigned e2m1_encode_mag(float a) /* 0 <= a <= 6 */
+static unsigned e2m1_encode_mag(double a) /* 0 <= a <= 6 */
 {
-    if (a < 2.0f) return (unsigned)rne_halves(a * 2.0f);            /* quantum 0.5: codes 0..4 */
-    if (a < 4.0f) return 2u + (unsigned)rne_halves(a);              /* quantum 1: 2,3,4 -> codes 4,5,6 */
-    return 4u + (unsigned)rne_halves(a * 0.5f);                     /* quantum 2: 2,3 -> codes 6,7 */
+    if (a < 2.0) return (unsigned)rne(a * 2.0);                  /* quantum 0.5: codes 0..4 */
+    if (a < 4.0) return 2u + (unsigned)rne(a);                   /* quantum 1: 2,3,4 -> codes 4,5,6 */
+    return 4u + (unsigned)rne(a * 0.5);                          /* quantum 2: 2,3 -> codes 6,7 */
 }
 
-unsigned oracle_e4m3_encode(float v) { return e4m3_encode_satfinite(v); }
-unsigned oracle_e2m1_encode(float v)
+unsigned oracle_e4m3_encode(double v) { return e4m3_encode_satfinite(v); }
+unsigned oracle_e2m1_encode(double v)
 {
-    unsigned c = e2m1_encode_mag(fminf(fabsf(v), 6.0f));
-    return (v < 0.0f && c != 0u) ? (c | 8u) : c;
+    unsigned c = e2m1_encode_mag(fmin(fabs(v), 6.0));
+    return (v < 0.0 && c != 0u) ? (c | 8u) : c;
+}
+
+/* Codes of one row's blocks for given scale codes S (row-major [K/16]). */
+static void encode_row(int64_t K, const uint16_t *x, double gs, const uint8_t *S, uint8_t *Q)
+{
+    for (int64_t b = 0; b < K / 16; ++b) {
+        double sv = e4m3_to_double(S[b]);
+        for (int k = 0; k < 16; k += 2) {
+            unsigned c[2];
+            for (int h = 0; h < 2; ++h) {
+                if (sv == 0.0) { c[h] = 0u; continue; }
+                double y = bf16_to_double(x[b * 16 + k + h]) * gs / sv;
+                c[h] = oracle_e2m1_encode(fmin(fmax(y, -6.0), 6.0));
+            }
+            Q[(b * 16 + k) / 2] = (uint8_t)(c[0] | (c[1] << 4));
+        }
+    }
 }
 
 /* X: bf16 [M][K]; Q: packed e2m1 [M][K/2] (low nibble = even k); S: e4m3 [M][K/16]. */
@@ -228,29 +250,23 @@ void oracle_quantize_nvfp4(int64_t M, int64_t K, const uint16_t *X, float gs, ui
 #pragma omp parallel for schedule(static)
     for (int64_t i = 0; i < M; ++i) {
         for (int64_t b = 0; b < K / 16; ++b) {
-            float amax = 0.0f;
+            double amax = 0.0;
             for (int k = 0; k < 16; ++k) {
-                float a = fabsf((float)bf16_to_double(X[i * K + b * 16 + k]));
+                double a = fabs(bf16_to_double(X[i * K + b * 16 + k]));
                 if (a > amax) amax = a;
             }
-            volatile float t = amax / 6.0f;               /* keep the two roundings separate */
-            unsigned s = e4m3_encode_satfinite(t * gs);
-            float sv = (float)e4m3_to_double(s);
-            S[i * (K / 16) + b] = (uint8_t)s;
-            volatile float inv = (sv == 0.0f) ? 0.0f : gs / sv;
-            for (int k = 0; k < 16; k += 2) {
-                unsigned c[2];
-                for (int h = 0; h < 2; ++h) {
-                    float x = (float)bf16_to_double(X[i * K + b * 16 + k + h]);
-                    if (sv == 0.0f) { c[h] = 0u; continue; }
-                    float y = x * inv;
-                    y = fminf(fmaxf(y, -6.0f), 6.0f);
-                    c[h] = oracle_e2m1_encode(y);
-                }
-                Q[i * (K / 2) + (b * 16 + k) / 2] = (uint8_t)(c[0] | (c[1] << 4));
-            }
+            S[i * (K / 16) + b] = (uint8_t)e4m3_encode_satfinite(amax * (double)gs / 6.0);
         }
+        encode_row(K, X + i * K, (double)gs, S + i * (K / 16), Q + i * (K / 2));
     }
+}
+
+/* The codes of the definition above for given block scales S [M][K/16]
+ * (used to check codes in a block whose scale was taken from elsewhere). */
+void oracle_quantize_nvfp4_codes(int64_t M, int64_t K, const uint16_t *X, float gs, const uint8_t *S, uint8_t *Q)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < M; ++i) encode_row(K, X + i * K, (double)gs, S + i * (K / 16), Q + i * (K / 2));
 }
 
 /* ---- MoE layer surroundings (the MoE models listed as tested on the vllm-ascend
