@@ -252,7 +252,7 @@ bi_status bi_moe_combine(const void *Y_sorted, int64_t rows, const int32_t *pos,
 
 bi_status bi_rmsnorm(const void *x, void *residual, const void *w, void *out, int64_t M, int64_t H, float eps,
                      bi_stream stream) {
-    if (M < 0 || H < 8 || H > 65536 || !(eps >= 0.0f)) return BI_ERR_INVALID_ARG;
+    if (M < 0 || M >= kI32Max || H < 8 || H > 65536 || !(eps >= 0.0f)) return BI_ERR_INVALID_ARG;
     if (M == 0) return BI_OK;
     if (!x || !w || !out) return BI_ERR_INVALID_ARG;
     if (H % 8 != 0) return BI_ERR_UNSUPPORTED;

@@ -132,6 +132,7 @@ def test_other_calls_reject_bad_arguments(lib):
     assert so.bi_rmsnorm(FAKE, None, FAKE, FAKE, 4, 4, f(1e-6), None) == 1                 # H < 8
     assert so.bi_rmsnorm(FAKE, None, FAKE, FAKE, 4, 4100, f(1e-6), None) == 2              # H % 8
     assert so.bi_rmsnorm(FAKE, None, FAKE, FAKE, 4, 4096, f(-1.0), None) == 1              # eps < 0
+    assert so.bi_rmsnorm(FAKE, None, FAKE, FAKE, 1 << 31, 4096, f(1e-6), None) == 1        # M >= 2^31 - 1
     assert so.bi_rmsnorm(FAKE, FAKE + 8, FAKE, FAKE, 4, 4096, f(1e-6), None) == 3          # residual align
     assert so.bi_quantize_nvfp4(FAKE, 128, f(1.0), FAKE, FAKE, 4, 96, None) == 2           # K % 64
     assert so.bi_quantize_nvfp4(FAKE, 128, f(0.0), FAKE, FAKE, 4, 128, None) == 1          # scale <= 0
