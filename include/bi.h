@@ -156,8 +156,10 @@ BI_API bi_status bi_gemm_nvfp4(const uint8_t *A, const uint8_t *A_sf, const uint
  *
  * The activation quantiser of vLLM PR #39912's test (scaled_fp4_quant with
  * the tensor's global scale). Per row and 16-element block, with gs = global_scale:
- *   s = e4m3( (amax / 6) * gs )       fp32 arithmetic, round to nearest even, saturating at 448
- *   q = e2m1( x * (gs / value(s)) )   round to nearest even, saturating at 6; q = 0 where value(s) = 0
+ *   s = e4m3( amax * gs / 6 )         round to nearest even, saturating at 448
+ *   q = e2m1( x * gs / value(s) )     round to nearest even, saturating at 6; q = 0 where value(s) = 0
+ * with each quotient taken on the exact values (the codes are those of the
+ * exact rational numbers, ties included, not of a binary32 evaluation).
  * A zero magnitude is stored as code 0 (never code 8). Row-local: a row's
  * codes and scales do not depend on the other rows (the global scale is an
  * input, computed once for the whole tensor as in the page's test).
@@ -166,7 +168,8 @@ BI_API bi_status bi_gemm_nvfp4(const uint8_t *A, const uint8_t *A_sf, const uint
  *   Q     u8   [M][K/2]   packed e2m1 codes, element k in byte k/2, low nibble for even k
  *   Q_sf  u8              e4m3 scales in the interleaved 128x4 layout of bi_gemm_nvfp4;
  *                         the buffer holds ceil(M/128)*128 rows, rows >= M are not written
- * Requirements: K % 64 == 0, K > 0; ldx % 8 == 0, ldx >= K; global_scale finite and > 0.
+ * Requirements: K % 64 == 0, K > 0; ldx % 8 == 0, ldx >= K; 0 < global_scale <= 2^64
+ * (gs = 2688 / amax(tensor) stays below 2^64 for any tensor with amax >= 1.5e-16).
  */
 BI_API bi_status bi_quantize_nvfp4(const void *X, int64_t ldx, float global_scale, uint8_t *Q, uint8_t *Q_sf,
                                    int64_t M, int64_t K, bi_stream stream);

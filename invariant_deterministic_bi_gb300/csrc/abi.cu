@@ -181,7 +181,7 @@ bi_status bi_gemm_nvfp4(const uint8_t *A, const uint8_t *A_sf, const uint8_t *B,
 
 bi_status bi_quantize_nvfp4(const void *X, int64_t ldx, float global_scale, uint8_t *Q, uint8_t *Q_sf, int64_t M,
                             int64_t K, bi_stream stream) {
-    if (M < 0 || K <= 0 || M >= kI32Max || K >= kI32Max || !(global_scale > 0.0f) || !(global_scale < 3.5e38f))
+    if (M < 0 || K <= 0 || M >= kI32Max || K >= kI32Max || !(global_scale > 0.0f) || !(global_scale <= 0x1p64f))
         return BI_ERR_INVALID_ARG;
     if (M == 0) return BI_OK;
     if (!X || !Q || !Q_sf || ldx < K) return BI_ERR_INVALID_ARG;

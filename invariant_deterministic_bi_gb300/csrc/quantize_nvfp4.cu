@@ -5,11 +5,16 @@
 // tensor's global scale). Per row and 16-element block, with global scale gs:
 //   s = e4m3( amax * gs / 6 )          round to nearest even, saturating at 448
 //   q = e2m1( x * gs / value(s) )      round to nearest even, saturating at 6; q = 0 if value(s) = 0
-// evaluated in binary32 as (amax / 6) * gs and x * (gs / value(s)): one
-// division per block and one multiply per element. Each quotient carries two
-// roundings (within 2^-23 of the exact value, relatively), so a code or scale
-// can differ from the exact definition's only where the exact value lies
-// that close to the midpoint between two codes.
+// on the exact values. Each quotient is bracketed in binary32: a lower bound
+// (amax * gs times 1/6 rounded down, x times a lower bound of gs / value(s),
+// each product rounded toward zero) and an upper bound (the same rounded away
+// from zero), both converted with round-to-nearest-even. Rounding to a code
+// is monotone, so when the two codes agree the exact value has that code too.
+// When they differ (the exact value lies within a few binary32 ulps of the
+// midpoint between two codes, or on it: about 1 % of elements on N(0,1) data)
+// the side is decided exactly: the midpoint m times value(s) (or times 6) is
+// exact in binary32, and fma(|x|, gs, -m * value(s)) has the sign of the exact
+// difference; zero means a tie, which goes to the even code.
 // Every output depends only on its own row and gs, so a row quantises to the
 // same bytes whatever the batch. Zero magnitudes are stored as code 0 (never
 // the negative-zero code 8).
@@ -58,10 +63,33 @@ __device__ __forceinline__ uint32_t to_e2m1x8(const float (&y)[8]) {
         "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
         : "=r"(out)
         : "f"(y[0]), "f"(y[1]), "f"(y[2]), "f"(y[3]), "f"(y[4]), "f"(y[5]), "f"(y[6]), "f"(y[7]));
-    // clear the sign of every nibble whose magnitude is zero
-    const uint32_t mag = out & 0x77777777u;
-    const uint32_t nz = (mag | (mag >> 1) | (mag >> 2)) & 0x11111111u;
-    return mag | (out & (nz << 3));
+    return out;
+}
+
+// 1/6 rounded down and up to binary32.
+constexpr float kSixthDn = 0.166666656732559204f;   // 0x3E2AAAAA
+constexpr float kSixthUp = 0.166666671633720398f;   // 0x3E2AAAAB
+// 1 - 2^-21 and 1 + 2^-21: widen a quotient within 2 ulps (2^-23 relatively)
+// of the exact one into bounds.
+constexpr float kShrink = 0.99999952316284179688f;
+constexpr float kGrow = 1.00000047683715820312f;
+// Four times the midpoint between e2m1 magnitude codes a and a + 1, for
+// a = 0..6 (magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6): 1, 3, 5, 7, 10, 14, 20,
+// one byte each.
+constexpr unsigned long long kMid4 = 0x00140E0A07050301ull;
+
+// Of the neighbouring codes lo and lo + 1, the one the exact value a * gs / d
+// rounds to, given md = m * d exactly (m the midpoint of their values): the
+// sign of fma(a, gs, -md) is the sign of the exact difference a*gs - m*d, and
+// zero is a tie, which takes the even code.
+__device__ __forceinline__ uint32_t decide(float a, float gs, float md, uint32_t lo) {
+    const float diff = fmaf(a, gs, -md);
+    return (diff > 0.0f || (diff == 0.0f && (lo & 1u))) ? lo + 1u : lo;
+}
+
+// Magnitude with x's sign.
+__device__ __forceinline__ float with_sign_of(float mag, float x) {
+    return __uint_as_float(__float_as_uint(mag) | (__float_as_uint(x) & 0x80000000u));
 }
 
 __global__ void __launch_bounds__(kThreads)
@@ -88,16 +116,46 @@ quantize_nvfp4_kernel(const uint4 *__restrict__ X, int64_t ldx_vec, uint8_t *__r
         float amax = 0.0f;
 #pragma unroll
         for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
-        const uint32_t s = to_e4m3(__fmul_rn(__fdiv_rn(amax, 6.0f), gs));
+        // block scale: amax * gs / 6 bracketed by directed rounding
+        uint32_t s = to_e4m3(__fmul_rz(__fmul_rz(amax, gs), kSixthDn));
+        const uint32_t s_up = to_e4m3(__fmul_ru(__fmul_ru(amax, gs), kSixthUp));
+        if (s != s_up) s = decide(amax, gs, 3.0f * (from_e4m3(s) + from_e4m3(s_up)), s);
         const float sv = from_e4m3(s);
-        const float inv = sv == 0.0f ? 0.0f : __fdiv_rn(gs, sv);    // one division per block
+        // x * gs / sv bracketed: the fast division is within 2 ulps of gs / sv
+        // (sv is at least 2^-9), so inv * (1 -+ 2^-21), rounded outward, bound
+        // it (both zero when sv is zero)
+        const float inv = sv == 0.0f ? 0.0f : __fdividef(gs, sv);
+        const float inv_dn = __fmul_rz(inv, kShrink), inv_up = __fmul_ru(inv, kGrow);
+        const float sv4 = 0.25f * sv;
         uint32_t codes[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            float y[8];
+            float lo[8], hi[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) y[i] = __fmul_rn(x[8 * h + i], inv);
-            codes[h] = to_e2m1x8(y);
+            for (int i = 0; i < 8; ++i) {
+                const float xi = x[8 * h + i];
+                lo[i] = __fmul_rz(xi, inv_dn);
+                hi[i] = with_sign_of(__fmul_ru(fabsf(xi), inv_up), xi);
+            }
+            uint32_t cl = to_e2m1x8(lo);
+            const uint32_t ch = to_e2m1x8(hi);
+            uint32_t dm = (cl ^ ch) & 0x77777777u;   // nibbles within a few ulps of a midpoint
+            while (dm) {
+                const int sh = (__ffs(dm) - 1) & ~3;          // first bit of the nibble
+                dm &= ~(15u << sh);
+                const int j = sh >> 3;                        // bf16 word of the element within this half
+                const uint32_t wj = (j & 2) ? ((j & 1) ? w[4 * h + 3] : w[4 * h + 2]) : ((j & 1) ? w[4 * h + 1] : w[4 * h]);
+                const uint32_t xb = (sh & 4) ? (wj & 0xFFFF0000u) : (wj << 16);   // odd element: high half
+                const float xa = __uint_as_float(xb & 0x7FFFFFFFu);
+                const uint32_t a = (cl >> sh) & 7u;
+                const float m4 = static_cast<float>(static_cast<uint32_t>(kMid4 >> (8 * a)) & 0xFFu);
+                const uint32_t c = decide(xa, gs, m4 * sv4, a) | ((xb >> 28) & 8u);
+                cl = (cl & ~(15u << sh)) | (c << sh);
+            }
+            // clear the sign of every nibble whose magnitude is zero
+            const uint32_t mag = cl & 0x77777777u;
+            const uint32_t nz = (mag | (mag >> 1) | (mag >> 2)) & 0x11111111u;
+            codes[h] = mag | (cl & (nz << 3));
         }
         *reinterpret_cast<uint2 *>(Q + r * (K / 2) + c * 8) = make_uint2(codes[0], codes[1]);
         const int64_t atom = (r / 128) * atoms + c / 4;

@@ -136,6 +136,7 @@ def test_other_calls_reject_bad_arguments(lib):
     assert so.bi_rmsnorm(FAKE, FAKE + 8, FAKE, FAKE, 4, 4096, f(1e-6), None) == 3          # residual align
     assert so.bi_quantize_nvfp4(FAKE, 128, f(1.0), FAKE, FAKE, 4, 96, None) == 2           # K % 64
     assert so.bi_quantize_nvfp4(FAKE, 128, f(0.0), FAKE, FAKE, 4, 128, None) == 1          # scale <= 0
+    assert so.bi_quantize_nvfp4(FAKE, 128, f(2.0 ** 65), FAKE, FAKE, 4, 128, None) == 1    # scale > 2^64
     assert so.bi_quantize_nvfp4(FAKE, 100, f(1.0), FAKE, FAKE, 4, 128, None) == 1          # ldx < K
     assert so.bi_quantize_nvfp4(FAKE, 136, f(1.0), FAKE + 8, FAKE, 4, 128, None) == 3      # Q align
     assert so.bi_quantize_nvfp4(FAKE, 128, f(1.0), FAKE, FAKE, 0, 128, None) == 0          # empty

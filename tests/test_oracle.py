@@ -227,7 +227,7 @@ def test_quantize_golden_blocks():
             assert int(S[0, 0]) == int(sc, 16), (case, hex(int(S[0, 0])))
             assert [int(b) for b in Q[0]] == [int(v, 16) for v in qb.split(",")], (case, [hex(b) for b in Q[0]])
             n += 1
-    assert n == 6
+    assert n == 7
 
 
 def test_e4m3_encoder_roundtrip_ties_saturation():
