@@ -51,7 +51,7 @@ GATE_UP_TRAFFIC = {"source_sha256_16": "3a434c5bd9eca660", "bytes": 901581056 + 
 def gate_up_traffic():
     import hashlib
     h = hashlib.sha256()
-    for f in ("gemm_bf16_pair.cu", "bi_ptx.cuh"):
+    for f in ("gemm_bf16_dense.cu", "bi_ptx.cuh"):
         with open(os.path.join(ROOT, "invariant_deterministic_bi_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return GATE_UP_TRAFFIC["bytes"] if h.hexdigest()[:16] == GATE_UP_TRAFFIC["source_sha256_16"] else None

@@ -72,7 +72,16 @@ typedef void *bi_stream;
  *   X  bf16 [M][ldx]  row-major activations (first K columns used)
  *   W  bf16 [N][ldw]  row-major weights, nn.Linear layout (first K columns used)
  *   Y  bf16 [M][ldy]  output, first N columns written; RNE from the fp32 sum
- *   Y[i][j] = bf16( sum_{k ascending, 16-element MMA steps} X[i][k] * W[j][k] ), fp32 accumulate
+ *
+ * The fp32 reduction over k is fixed by (N, K) alone: K is cut into S
+ * segments of whole 64-wide steps (S in 1..4, reported as split_k by
+ * bi_plan; steps [s*T/S, (s+1)*T/S) of T = ceil(K/64)); each segment is summed
+ * in ascending 16-element MMA steps from zero, and the segment sums are added
+ * in segment order:
+ *   Y[i][j] = bf16( P_0 + P_1 + ... + P_{S-1} ),  P_s = sum_{k in segment s} X[i][k] * W[j][k]
+ * No part of this depends on M, on the row's position or on the other rows
+ * (with few rows the segments run on different SMs and the sums travel
+ * between them; that changes no operation).
  *
  * Requirements: M >= 0, N >= 0, K > 0; K % 8 == 0; N % 8 == 0; ldx, ldw, ldy
  * multiples of 8 and >= K (ldy >= N); M, N, K < 2^31. Y must not overlap X or W.
@@ -87,8 +96,10 @@ BI_API bi_status bi_gemm_bf16(const void *X, int64_t ldx, const void *W, int64_t
  * For the MoE models the pages list as tested (Qwen3-30B-A3B, Qwen3-235B-A22B;
  * vllm-ascend guide, Tested Models): rows are grouped by expert, and rows
  * offsets[e] .. offsets[e+1]-1 of X are multiplied by expert e's weight:
- *   Y[r][j] = bf16( sum_k X[r][k] * W[e][j][k] ),  same per-element order as bi_gemm_bf16,
- * so a token's expert output does not depend on which tokens share its expert.
+ *   Y[r][j] = bf16( sum_k X[r][k] * W[e][j][k] ),  k in ascending 16-element MMA
+ * steps from zero in one fp32 sum (bi_gemm_bf16's order when its plan has one
+ * segment), so a token's expert output does not depend on which tokens share
+ * its expert.
  *
  *   X        bf16 [rows][K]     expert-sorted activations (dense, ld = K)
  *   W        bf16 [E][N][K]     expert weights (dense)

@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 OBJDIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libbi.so")
-SOURCES = ["abi.cu", "gemm_bf16_pair.cu", "gemm_nvfp4.cu", "quantize_nvfp4.cu", "moe.cu", "attention.cu", "rmsnorm.cu"]
+SOURCES = ["abi.cu", "gemm_bf16_dense.cu", "gemm_bf16_pair.cu", "gemm_nvfp4.cu", "quantize_nvfp4.cu", "moe.cu", "attention.cu", "rmsnorm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-I", INCLUDE]

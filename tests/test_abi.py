@@ -61,9 +61,22 @@ def test_gemm_plan_independent_of_M(lib, N, K):
     for M in [1, 2, 7, 64, 127, 128, 129, 513, 4096, 8192, 65536]:
         p = _plan(lib, lib.OP_GEMM_BF16, M, N, K)
         assert {k: p[k] for k in keys} == {k: base[k] for k in keys}
-        assert p["tiles_m"] == -(-M // p["block_m"]) and p["split_k"] == 1
-        assert 2 <= p["grid"] <= 152 and p["grid"] % 2 == 0      # CTA pairs
+        assert p["tiles_m"] == -(-M // p["block_m"])
+        assert p["grid"] >= 2 and p["grid"] % 2 == 0             # CTA pairs
+        if M > 256 or p["split_k"] == 1:                          # one pair per tile, persistent
+            assert p["grid"] <= 152
+        else:                                                     # one cluster of split_k pairs per column tile
+            assert p["grid"] == 2 * p["split_k"] * p["tiles_n"]
     assert base["k_steps"] == -(-K // 64)
+    # the K reduction's segments are fixed by (N, K): each at least 16 steps of 64
+    assert 1 <= base["split_k"] <= 4 and (base["split_k"] == 1 or base["k_steps"] // base["split_k"] >= 16)
+
+
+def test_gemm_segments_for_the_qwen3_layers(lib):
+    """The fixed K segments of the Qwen3-8B linears and of the small config."""
+    seg = lambda N, K: _plan(lib, lib.OP_GEMM_BF16, 1, N, K)["split_k"]
+    assert (seg(6144, 4096), seg(24576, 4096), seg(4096, 12288)) == (2, 1, 3)
+    assert seg(512, 256) == 1 and seg(2048, 768) == 1
 
 
 def test_grouped_and_nvfp4_and_rmsnorm_plans_independent_of_M(lib):
