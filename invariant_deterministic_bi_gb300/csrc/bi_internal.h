@@ -69,6 +69,9 @@ inline bi_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, siz
 // Kernel launchers (defined in the .cu files); arguments already validated.
 bi_status launch_gemm_bf16(const void *X, int64_t ldx, const void *W, int64_t ldw, void *Y, int64_t ldy,
                            int64_t M, int64_t N, int64_t K, cudaStream_t s);
+// The dense layer with one K segment on the grouped layer's CTA-pair kernel.
+bi_status launch_gemm_bf16_one_segment(const void *X, int64_t ldx, const void *W, int64_t ldw, void *Y, int64_t ldy,
+                                       int64_t M, int64_t N, int64_t K, cudaStream_t s);
 bi_status launch_grouped_gemm_bf16(const void *X, const void *W, void *Y, const int32_t *offsets, int32_t E,
                                    int64_t rows, int64_t N, int64_t K, cudaStream_t s);
 bi_status launch_grouped_gemm_silu_bf16(const void *X, const void *W, void *act, const int32_t *offsets, int32_t E,
@@ -99,6 +102,7 @@ bi_status launch_wait_timeout_check(uint32_t limit_us, cudaStream_t s);
 
 // Plans (M-independent except tiles_m and grid).
 void plan_gemm_bf16(int64_t M, int64_t N, int64_t K, int sms, bi_plan_t *p);
+void plan_gemm_bf16_one_segment(int64_t M, int64_t N, int64_t K, int sms, bi_plan_t *p);
 void plan_grouped_gemm_bf16(int64_t rows, int64_t N, int64_t K, int sms, bi_plan_t *p);
 void plan_gemm_nvfp4(int64_t M, int64_t N, int64_t K, int clusters, bi_plan_t *p);
 // Clusters of the NVFP4 kernel resident at once on the current device (sms / 4 if the query fails).

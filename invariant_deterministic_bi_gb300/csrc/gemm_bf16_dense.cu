@@ -14,7 +14,9 @@
 // keeps one fixed reduction order for all M; here that order includes the
 // segments), so no M-dependent split-K, tile shape or stream-K appears.
 //
-// Two schedules perform exactly these operations:
+// With S = 1 the layer runs on the lean CTA-pair kernel of gemm_bf16_pair.cu
+// (one accumulation, 192 threads, no running sum to hold). With S > 1 two
+// schedules of this file's kernel perform exactly these operations:
 //   - one pair per 256 x 256 tile (any M, persistent grid): the pair runs
 //     the tile's S segments back to back, each into one of two tensor-memory
 //     accumulators, and the epilogue warps fold each finished partial into
@@ -485,6 +487,10 @@ int segments_for(int64_t N, int64_t K) {
 static bool use_chain(int64_t M, int segs) { return segs > 1 && M <= kChainMaxRows; }
 
 void plan_gemm_bf16(int64_t M, int64_t N, int64_t K, int sms, bi_plan_t *pl) {
+    if (segments_for(N, K) == 1) {      // one segment: the lean CTA-pair kernel of gemm_bf16_pair.cu
+        plan_gemm_bf16_one_segment(M, N, K, sms, pl);
+        return;
+    }
     pl->op = BI_OP_GEMM_BF16;
     pl->block_m = kBM; pl->block_n = kBN; pl->block_k = kBK;
     pl->mma_m = kBM; pl->mma_n = kBN; pl->mma_k = kMmaK;
@@ -507,6 +513,7 @@ void plan_gemm_bf16(int64_t M, int64_t N, int64_t K, int sms, bi_plan_t *pl) {
 
 bi_status launch_gemm_bf16(const void *X, int64_t ldx, const void *W, int64_t ldw, void *Y, int64_t ldy,
                            int64_t M, int64_t N, int64_t K, cudaStream_t s) {
+    if (segments_for(N, K) == 1) return launch_gemm_bf16_one_segment(X, ldx, W, ldw, Y, ldy, M, N, K, s);
     int dev;
     const DeviceInfo *info;
     bi_status st = current_device(&dev, &info);

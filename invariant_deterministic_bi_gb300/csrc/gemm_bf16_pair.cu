@@ -1,9 +1,11 @@
-// gemm_bf16_pair.cu -- the batch-invariant MoE-grouped bf16 linear layer on CTA
-// pairs (tcgen05 cta_group::2): for each expert e with rows [off[e], off[e+1])
-// of the expert-sorted X, Y_rows = X_rows W[e]^T (and the gate_up form with
-// SiLU-mul in the epilogue). The dense layer is in gemm_bf16_dense.cu; with one
-// K segment it runs the same tile, MMA instruction and K order, so an expert's
-// rows equal the dense layer's rows on the same input bit for bit.
+// gemm_bf16_pair.cu -- batch-invariant bf16 linear layers on CTA pairs (tcgen05 cta_group::2)
+// with one K segment: the dense layer Y = X W^T when its plan has one segment
+// (the plan and the segmented form are in gemm_bf16_dense.cu), and the
+// MoE-grouped layer (for each expert e with rows [off[e], off[e+1]) of the
+// expert-sorted X: Y_rows = X_rows W[e]^T, also with SiLU-mul fused).
+// This kernel holds no running sum: 192 threads of about 100 registers, so
+// under programmatic dependent launch its CTAs can take an SM while the
+// previous kernel's last CTAs (an RMSNorm, say) are still finishing there.
 //
 // 256 x 256 output tiles, each computed by a cluster of two CTAs on two SMs:
 //   - each CTA's warp 0 TMA-loads its own 128 rows of the A tile and its own
@@ -34,8 +36,8 @@
 //
 // Batch invariance: the tile shape, MMA instruction and K order (64-wide K
 // steps, four 16-wide MMA steps each, ascending, from zero) are the same for
-// every routing; rows never interact; only which pair computes which tile
-// depends on the routing.
+// every M and every routing, and the same in both modes; rows never interact;
+// only which pair computes which tile depends on M (or on the routing).
 #include <cuda_bf16.h>
 
 #include "bi_internal.h"
@@ -61,17 +63,18 @@ constexpr int kEpiWarps = 4;
 constexpr int kBarBytes = 256;
 constexpr int kMaxExperts = 1024;
 constexpr int kSchedBytes = 2 * (kMaxExperts + 1) * 4;
-// Modes of the kernel: the grouped layer, and the grouped gate_up layer with
-// SiLU-mul applied in the epilogue.
-constexpr int kGrouped = 1, kGroupedSilu = 2;
-// one staging box per epilogue warp, plus the tile map
+// Modes of the kernel: the dense layer, the grouped layer, and the grouped
+// gate_up layer with SiLU-mul applied in the epilogue.
+constexpr int kDense = 0, kGrouped = 1, kGroupedSilu = 2;
+// dense: two staging boxes per epilogue warp; grouped: one, plus the tile map
 template <int MODE>
-__host__ __device__ constexpr int out_boxes() { return 1; }
+__host__ __device__ constexpr int out_boxes() { return MODE == kDense ? 2 : 1; }
 template <int MODE>
 __host__ __device__ constexpr int smem_bytes() {
-    return 1024 + kStages * kStageBytes + kEpiWarps * out_boxes<MODE>() * kOutBytes + kBarBytes + kSchedBytes;
+    return 1024 + kStages * kStageBytes + kEpiWarps * out_boxes<MODE>() * kOutBytes + kBarBytes +
+           (MODE != kDense ? kSchedBytes : 0);
 }
-static_assert(smem_bytes<kGrouped>() <= 232448, "shared memory per CTA");
+static_assert(smem_bytes<kGrouped>() <= 232448 && smem_bytes<kDense>() <= 232448, "shared memory per CTA");
 
 // act = bf16(silu(g) * u) on bf16 g and u: the arithmetic of bi_silu_mul
 // (silu_mul_f32), so the fused layer gives the same bits.
@@ -83,11 +86,11 @@ __device__ __forceinline__ uint32_t silu_mul_bf16x2(uint32_t g2, uint32_t u2) {
 constexpr int kTmemCols = 512;
 
 struct Params {
-    int32_t M, N, K;           // M = offsets[E] (all rows)
-    int32_t a_bytes;           // A bytes each CTA loads per K step
-    const int32_t *offsets;    // device offsets [E+1]
-    int32_t E;                 // experts
-    uint8_t *Yg;               // Y (dense N-strided rows), for rows stored without TMA
+    int32_t M, N, K;           // dense: M rows; grouped: M = offsets[E] (all rows)
+    int32_t a_bytes;           // A bytes each CTA loads per K step (fewer rows when M < 128)
+    const int32_t *offsets;    // grouped: device offsets [E+1]
+    int32_t E;                 // grouped: experts
+    uint8_t *Yg;               // grouped: Y (dense N-strided rows), for rows stored without TMA
     unsigned *status;
 };
 
@@ -103,7 +106,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmY, const Params p) {
     constexpr uint32_t kIdesc = idesc_bf16(kBM, kBN);
-    constexpr bool GROUPED = true;
+    constexpr bool GROUPED = MODE != kDense;
     constexpr bool SILU = MODE == kGroupedSilu;
     // SILU: a tile's 256 accumulator columns are 128 gate columns (B rows from
     // the first half of the expert's weight) and the matching 128 up columns
@@ -393,6 +396,23 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
 
 }  // namespace
 
+void plan_gemm_bf16_one_segment(int64_t M, int64_t N, int64_t K, int sms, bi_plan_t *pl) {
+    pl->op = BI_OP_GEMM_BF16;
+    pl->block_m = kBM; pl->block_n = kBN; pl->block_k = kBK;
+    pl->mma_m = kBM; pl->mma_n = kBN; pl->mma_k = kMmaK;
+    pl->k_steps = static_cast<int32_t>((K + kBK - 1) / kBK);
+    pl->split_k = 1;
+    pl->stages = kStages;
+    pl->threads = kThreads;
+    pl->smem_bytes = smem_bytes<kDense>();
+    pl->tiles_m = (M + kBM - 1) / kBM;
+    pl->tiles_n = (N + kBN - 1) / kBN;
+    const int64_t tiles = pl->tiles_m * pl->tiles_n;
+    const int64_t pairs = sms / 2;
+    pl->grid = static_cast<int32_t>(2 * (tiles < pairs ? tiles : pairs));
+    pl->reduce_tree = 0;
+}
+
 void plan_grouped_gemm_bf16(int64_t rows, int64_t N, int64_t K, int sms, bi_plan_t *pl) {
     pl->op = BI_OP_GROUPED_GEMM_BF16;
     pl->block_m = kBM; pl->block_n = kBN; pl->block_k = kBK;
@@ -416,6 +436,36 @@ bi_status launch_pair(const CUtensorMap &ta, const CUtensorMap &tb, const CUtens
     if (ensure_smem_attr(reinterpret_cast<const void *>(kern), smem_bytes<MODE>(), &configured) != BI_OK)
         return BI_ERR_CUDA;
     return launch_pdl(kern, dim3(grid), dim3(kThreads), smem_bytes<MODE>(), s, ta, tb, ty, p);
+}
+
+bi_status launch_gemm_bf16_one_segment(const void *X, int64_t ldx, const void *W, int64_t ldw, void *Y, int64_t ldy,
+                                       int64_t M, int64_t N, int64_t K, cudaStream_t s) {
+    int dev;
+    const DeviceInfo *info;
+    bi_status st = current_device(&dev, &info);
+    if (st != BI_OK) return st;
+    // With fewer than 128 rows, each CTA copies only the A rows that can hold
+    // data (rounded up to 16); the MMA still multiplies 128 rows, and the
+    // accumulator rows past M -- computed from whatever the rest of the tile
+    // holds -- are never stored. Rows never interact, so this changes no bit
+    // of any stored row; it only spares the copy engine the zero rows.
+    const int a_rows = M >= kHalf ? kHalf : static_cast<int>((M + 15) / 16 * 16);
+    CUtensorMap ta, tb, ty;
+    st = make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, K, M, ldx * 2, kBK, a_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != BI_OK) return st;
+    st = make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, K, N, ldw * 2, kBK, kHalf, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != BI_OK) return st;
+    st = make_tmap_2d(&ty, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Y, N, M, ldy * 2, kOutCols, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != BI_OK) return st;
+    bi_plan_t pl;
+    plan_gemm_bf16_one_segment(M, N, K, info->sm_count, &pl);
+    Params p{};
+    p.a_bytes = a_rows * kBK * 2;
+    p.M = static_cast<int32_t>(M);
+    p.N = static_cast<int32_t>(N);
+    p.K = static_cast<int32_t>(K);
+    p.status = device_status_word();
+    return launch_pair<kDense>(ta, tb, ty, p, pl.grid, s);
 }
 
 // Grouped launch. silu == false: Y [rows][N] = X W[e]^T with W [E][N][K].
