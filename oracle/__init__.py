@@ -76,6 +76,8 @@ def _load():
             lib.oracle_rank_sum_rmsnorm.argtypes = [ctypes.c_int32, I64, I64, P, P, P, D, P, P, P]
             lib.oracle_attention_decode.argtypes = [I64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                                     ctypes.c_int32, ctypes.c_int32, P, P, P, P, P, D, P]
+            lib.oracle_attention_extend.argtypes = [I64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                                    ctypes.c_int32, ctypes.c_int32, P, P, P, P, P, P, D, P]
             lib.oracle_e4m3_encode.argtypes = [D]
             lib.oracle_e4m3_encode.restype = ctypes.c_uint
             lib.oracle_e2m1_encode.argtypes = [D]
@@ -276,6 +278,28 @@ def attention_decode(Q, K, V, table, lens, scale: float):
     O = np.zeros((B, Hq, D), dtype=np.float64)
     if B:
         _load().oracle_attention_decode(B, Hq, Hkv, D, bs, table.shape[1], _p(Q), _p(K), _p(V), _p(table),
+                                        _p(lens), float(scale), _p(O))
+    return O
+
+
+def attention_extend(Q, cu_q, K, V, table, lens, scale: float):
+    """Causal attention of each sequence's new query tokens over its paged KV
+    cache (fp64). Q bf16 [total_q, Hq, D]; cu_q int32 [B+1]; K, V bf16
+    [blocks, bs, Hkv, D]; table int32 [B, max_blocks]; lens int32 [B] (cached
+    length, the new tokens included). Token i of sequence b sits at position
+    lens[b] - q_len_b + i and sees tokens 0 .. that position. Returns O fp64
+    [total_q, Hq, D]."""
+    Q, K, V = _c(Q, np.uint16), _c(K, np.uint16), _c(V, np.uint16)
+    cu_q, table, lens = _c(cu_q, np.int32), _c(table, np.int32), _c(lens, np.int32)
+    T, Hq, D = Q.shape
+    _, bs, Hkv, D2 = K.shape
+    B = lens.shape[0]
+    assert D2 == D and V.shape == K.shape and Hq % Hkv == 0 and table.shape[0] == B
+    assert cu_q.shape == (B + 1,) and cu_q[0] == 0 and cu_q[-1] == T
+    assert np.all(np.diff(cu_q) >= 0) and np.all(np.diff(cu_q) <= lens)
+    O = np.zeros((T, Hq, D), dtype=np.float64)
+    if T:
+        _load().oracle_attention_extend(B, Hq, Hkv, D, bs, table.shape[1], _p(Q), _p(cu_q), _p(K), _p(V), _p(table),
                                         _p(lens), float(scale), _p(O))
     return O
 

@@ -438,6 +438,57 @@ void oracle_attention_decode(int64_t B, int32_t Hq, int32_t Hkv, int32_t D, int3
     }
 }
 
+/* ---- Extend (prefill) attention over a paged KV cache: q_len_b new query
+ * tokens of sequence b attend causally to its cache, which already holds
+ * their keys and values (the decode case is q_len_b = 1). Query token i of
+ * sequence b (0 <= i < q_len_b, row cu_q[b] + i of Q) sits at position
+ * p = L_b - q_len_b + i of the sequence, and sees the L_b - q_len_b + i + 1
+ * cached tokens j <= p:
+ *   s_j = scale * sum_d q[t][h][d] * k_j[g][d]
+ *   o[t][h][d] = sum_{j <= p} softmax(s)_j * v_j[g][d]     (fp64, exact softmax)
+ * Q: bf16 [total_q][Hq][D]; cu_q: int32 [B+1] (cu_q[0] = 0, rows of each
+ * sequence); K, V, table, lens as in oracle_attention_decode (lens = the
+ * cached length including the new tokens); O: fp64 [total_q][Hq][D]. */
+void oracle_attention_extend(int64_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t bs, int32_t max_blocks,
+                             const uint16_t *Q, const int32_t *cu_q, const uint16_t *K, const uint16_t *V,
+                             const int32_t *table, const int32_t *lens, double scale, double *O)
+{
+    const int64_t total_q = cu_q[B];
+#pragma omp parallel for schedule(dynamic)
+    for (int64_t th = 0; th < total_q * Hq; ++th) {
+        const int64_t t = th / Hq;
+        const int32_t h = (int32_t)(th % Hq), g = h / (Hq / Hkv);
+        int64_t b = 0;
+        while (cu_q[b + 1] <= t) ++b;
+        const int32_t qlen = cu_q[b + 1] - cu_q[b];
+        const int32_t pos = lens[b] - qlen + (int32_t)(t - cu_q[b]);
+        const uint16_t *q = Q + (t * Hq + h) * D;
+        double mx = -INFINITY;
+        for (int32_t j = 0; j <= pos; ++j) {
+            const int64_t blk = table[b * max_blocks + j / bs];
+            const uint16_t *k = K + ((blk * bs + j % bs) * (int64_t)Hkv + g) * D;
+            double s = 0.0;
+            for (int32_t d = 0; d < D; ++d) s += bf16_to_double(q[d]) * bf16_to_double(k[d]);
+            s *= scale;
+            if (s > mx) mx = s;
+        }
+        double den = 0.0;
+        double *o = O + (t * Hq + h) * D;
+        for (int32_t d = 0; d < D; ++d) o[d] = 0.0;
+        for (int32_t j = 0; j <= pos; ++j) {
+            const int64_t blk = table[b * max_blocks + j / bs];
+            const uint16_t *k = K + ((blk * bs + j % bs) * (int64_t)Hkv + g) * D;
+            const uint16_t *v = V + ((blk * bs + j % bs) * (int64_t)Hkv + g) * D;
+            double s = 0.0;
+            for (int32_t d = 0; d < D; ++d) s += bf16_to_double(q[d]) * bf16_to_double(k[d]);
+            const double pr = exp(s * scale - mx);
+            den += pr;
+            for (int32_t d = 0; d < D; ++d) o[d] += pr * bf16_to_double(v[d]);
+        }
+        for (int32_t d = 0; d < D; ++d) o[d] /= den;
+    }
+}
+
 /* RMSNorm with optional residual add, per row i:
  *   h = residual ? bf16(x + residual) : x         (the stored, rounded sum)
  *   y = h / sqrt( (1/H) sum_k h_k^2 + eps ) * w

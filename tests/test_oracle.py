@@ -411,6 +411,56 @@ def test_attention_block_placement_does_not_matter():
     assert np.array_equal(O, O2)
 
 
+def _extend_inputs(lens, qlens, Hq, Hkv, D, bs, seed):
+    B = len(lens)
+    K, V, table, lens = _paged(B, 0, Hkv, D, bs, seed=seed, lens=lens)
+    cu = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
+    Q = syn.to_bf16_bits(syn.normal_rows(seed + 1, 0, int(cu[-1]) * Hq, D)).reshape(int(cu[-1]), Hq, D)
+    return Q, cu, K, V, table, lens
+
+
+def test_attention_extend_matches_causal_numpy():
+    """Each new token attends to the tokens up to its own position (a causal
+    mask over the cached sequence), checked against scipy's softmax."""
+    scipy = pytest.importorskip("scipy.special")
+    Hq, Hkv, D, bs = 4, 2, 32, 8
+    lens, qlens = [19, 6, 40], [5, 6, 1]
+    Q, cu, K, V, table, lens = _extend_inputs(lens, qlens, Hq, Hkv, D, bs, seed=11)
+    scale = 1 / np.sqrt(D)
+    O = oracle.attention_extend(Q, cu, K, V, table, lens, scale)
+    for b in range(len(lens)):
+        kd, vd = _dense(K, V, table, lens, b)
+        kf, vf = (syn.bf16_bits_to_f32(a).astype(np.float64) for a in (kd, vd))
+        for i in range(qlens[b]):
+            t, pos = cu[b] + i, lens[b] - qlens[b] + i
+            for h in range(Hq):
+                q = syn.bf16_bits_to_f32(Q[t, h]).astype(np.float64)
+                pr = scipy.softmax(kf[:pos + 1, h // 2] @ q * scale)
+                assert np.allclose(O[t, h], pr @ vf[:pos + 1, h // 2], rtol=1e-12, atol=1e-14)
+
+
+def test_attention_extend_of_one_token_is_decode():
+    """One new token per sequence: extend is decode attention over the whole cache."""
+    Hq, Hkv, D, bs = 8, 2, 64, 16
+    lens = [37, 1, 130]
+    Q, cu, K, V, table, lens = _extend_inputs(lens, [1, 1, 1], Hq, Hkv, D, bs, seed=13)
+    O = oracle.attention_extend(Q, cu, K, V, table, lens, 0.1)
+    assert np.array_equal(O, oracle.attention_decode(Q, K, V, table, lens, 0.1))
+
+
+def test_attention_extend_is_causal():
+    """Changing the keys and values after a token's position leaves its output alone."""
+    Hq, Hkv, D, bs = 2, 1, 16, 4
+    Q, cu, K, V, table, lens = _extend_inputs([12], [12], Hq, Hkv, D, bs, seed=17)
+    O = oracle.attention_extend(Q, cu, K, V, table, lens, 0.3)
+    K2, V2 = K.copy(), V.copy()
+    late = table[0, 2]                       # block of positions 8 .. 11
+    K2[late] = syn.to_bf16_bits(syn.normal_rows(18, 0, bs, Hkv * D)).reshape(bs, Hkv, D)
+    V2[late] = syn.to_bf16_bits(syn.normal_rows(19, 0, bs, Hkv * D)).reshape(bs, Hkv, D)
+    O2 = oracle.attention_extend(Q, cu, K2, V2, table, lens, 0.3)
+    assert np.array_equal(O[:8], O2[:8]) and not np.array_equal(O[8:], O2[8:])
+
+
 # ----------------------------------------------------------------- RMSNorm
 
 def test_rmsnorm_golden_cases():
