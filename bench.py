@@ -642,6 +642,64 @@ def attention_sweep(bi, peaks):
     return rows
 
 
+EXT_CASES = [(1, 4096, 4096), (8, 512, 512), (4, 1024, 4096)]   # (sequences, new tokens each, cached length each)
+
+
+def extend_flops(q, L):
+    """Causal attention FLOPs of q new tokens ending a length-L cache, per query head:
+    token at position p costs 2*2*D*(p+1) (q.k and p.v)."""
+    D = ATTN_HEADS[2]
+    first = L - q
+    return 4.0 * D * (q * (first + 1) + q * (q - 1) / 2.0)
+
+
+def extend_sweep(bi, peaks):
+    """Extend (prefill) attention, Qwen3-8B heads, paged KV (block 16): TFLOP/s
+    of the causal attention, against torch's scaled_dot_product_attention on
+    the same data laid out contiguously (not paged, not batch-invariant;
+    informational)."""
+    import torch
+    Hq, Hkv, D, bs = ATTN_HEADS
+    rows = []
+    g = torch.Generator(device="cuda").manual_seed(0)
+    for B, q, L in EXT_CASES:
+        nb = L // bs
+        K = torch.randn((B * nb, bs, Hkv, D), device="cuda", generator=g).to(torch.bfloat16)
+        V = torch.randn((B * nb, bs, Hkv, D), device="cuda", generator=g).to(torch.bfloat16)
+        table = torch.randperm(B * nb, device="cuda", generator=g).to(torch.int32).view(B, nb)
+        lens = torch.full((B,), L, dtype=torch.int32, device="cuda")
+        cu = torch.arange(0, (B + 1) * q, q, dtype=torch.int32, device="cuda")
+        Q = torch.randn((B * q, Hq, D), device="cuda", generator=g).to(torch.bfloat16)
+        O = torch.empty_like(Q)
+        t = time_fn(lambda: bi.attention_extend(Q, cu, K, V, table, lens, L, q, D ** -0.5, O=O), 10)
+        flops = B * Hq * extend_flops(q, L)
+        row = {"B": B, "new_tokens": q, "cached": L, "us": round(t * 1e3, 2), "tflops": round(flops / (t * 1e-3) / 1e12, 1)}
+        try:     # the same attention by torch on contiguous K/V (causal with an offset: an explicit mask)
+            kc = K[table.view(-1).long()].view(B, L, Hkv, D).permute(0, 2, 1, 3).contiguous()
+            vc = V[table.view(-1).long()].view(B, L, Hkv, D).permute(0, 2, 1, 3).contiguous()
+            qc = Q.view(B, q, Hq, D).permute(0, 2, 1, 3).contiguous()
+            sdpa = torch.nn.functional.scaled_dot_product_attention
+            if q == L:    # plain causal: torch may use its flash kernel
+                mask = None
+                t2 = time_fn(lambda: sdpa(qc, kc, vc, is_causal=True, scale=D ** -0.5, enable_gqa=True), 10)
+            else:         # causal with an offset needs an explicit mask
+                pos = torch.arange(L - q, L, device="cuda")[:, None]
+                mask = torch.arange(L, device="cuda")[None, :] <= pos
+                t2 = time_fn(lambda: sdpa(qc, kc, vc, attn_mask=mask, scale=D ** -0.5, enable_gqa=True), 10)
+            row["torch_sdpa_us"] = round(t2 * 1e3, 2)
+            row["torch_sdpa_form"] = "is_causal" if mask is None else "explicit mask"
+            row["cost_vs_torch_sdpa"] = round(t / t2, 3)
+            del kc, vc, qc, mask
+        except (RuntimeError, TypeError) as exc:      # no GQA support in this torch: leave it out
+            if "CUDA" in str(exc) and "error" in str(exc).lower():
+                raise
+            row["torch_sdpa_us"] = None
+        rows.append(row)
+        del K, V, table, lens, cu, Q, O
+    torch.cuda.empty_cache()
+    return rows
+
+
 _STEP_WEIGHTS = {}
 
 
@@ -819,6 +877,7 @@ def run_ours(args, dist):
         breakdown["quantize_nvfp4"] = quant_sweep(bi, peaks)
         breakdown["moe_layer"] = moe_layer_sweep(bi, peaks)
         breakdown["attention_decode"] = attention_sweep(bi, peaks)
+        breakdown["attention_extend"] = extend_sweep(bi, peaks)
         if bi.device_status() != bi.BI_OK:
             raise RuntimeError("device status after breakdown")
         # the metric's per-M GEMM fractions and its RMSNorm half as flat numbers
@@ -897,7 +956,8 @@ def profile_case(spec: str, reps: int):
     """Run one kernel configuration `reps` times (for ncu captures); no output line.
     spec: gemm:<qkv|gate_up|down>:<M> | rmsnorm:<M>:<0|1 residual> | grouped:<gate_up|down>:<T> |
           nvfp4:<M> | quant:<M> | attention:<B> (decode, 4096 cached tokens per sequence) |
-          moe_layer:<T> (the whole MoE layer, gate_up with SiLU-mul fused)"""
+          moe_layer:<T> (the whole MoE layer, gate_up with SiLU-mul fused) |
+          extend:<B>:<new tokens>:<cached> (prefill attention)"""
     import torch
     import bi_synth as syn
     import invariant_deterministic_bi_gb300 as bi
@@ -961,6 +1021,19 @@ def profile_case(spec: str, reps: int):
         ws = torch.empty(bi.attention_decode_workspace_size(B, Hq, ATTN_L), dtype=torch.uint8, device="cuda")
         O = torch.empty_like(Q)
         fn = lambda: bi.attention_decode(Q, K, V, table, lens, ATTN_L, D ** -0.5, workspace=ws, O=O)
+    elif kind == "extend":
+        B, q, L = (int(v) for v in rest)
+        Hq, Hkv, D, bs = ATTN_HEADS
+        nb = -(-L // bs)
+        g = torch.Generator(device="cuda").manual_seed(0)
+        K = torch.randn((B * nb, bs, Hkv, D), device="cuda", generator=g).to(torch.bfloat16)
+        V = torch.randn((B * nb, bs, Hkv, D), device="cuda", generator=g).to(torch.bfloat16)
+        table = torch.randperm(B * nb, device="cuda", generator=g).to(torch.int32).view(B, nb)
+        lens = torch.full((B,), L, dtype=torch.int32, device="cuda")
+        cu = torch.arange(0, (B + 1) * q, q, dtype=torch.int32, device="cuda")
+        Q = torch.randn((B * q, Hq, D), device="cuda", generator=g).to(torch.bfloat16)
+        O = torch.empty_like(Q)
+        fn = lambda: bi.attention_extend(Q, cu, K, V, table, lens, L, q, D ** -0.5, O=O)
     else:
         raise SystemExit(f"unknown profile case {spec}")
     ms = time_fn(fn, reps, warm=1)

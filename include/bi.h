@@ -304,7 +304,8 @@ BI_API bi_status bi_rank_sum_rmsnorm(const void *const *parts, int32_t R, void *
  * Arithmetic: q.k and p.v are bf16 tensor-core products with fp32
  * accumulation; the probabilities enter p.v as a bf16 high part plus a bf16
  * low part (16 significant bits); softmax statistics and the chunk merge are
- * fp32.
+ * fp32. Chunks merge in order: m' = max(m, m_c), o = o e^(m-m') + o_c e^(m_c-m'),
+ * l likewise, then o / l.
  *
  *   Q         bf16 [B][Hq][128]
  *   K_cache   bf16 [num_blocks][block_size][Hkv][128]; V_cache likewise
@@ -325,6 +326,44 @@ BI_API bi_status bi_attention_decode(const void *Q, const void *K_cache, const v
                                      const int32_t *seq_lens, int64_t B, int32_t Hq, int32_t Hkv,
                                      int32_t head_dim, int32_t block_size, int32_t max_seq_len, float scale,
                                      void *workspace, int64_t workspace_bytes, void *O, bi_stream stream);
+
+/*
+ * bi_attention_extend -- batch-invariant extend (prefill) attention over a
+ * paged KV cache: the new query tokens of each sequence attend causally to
+ * the sequence's cache, which already holds their keys and values.
+ *
+ * The pages ask for batch-invariant attention backends (vLLM tracking issue
+ * #27433, TODO: FlashInfer, TRITON_MLA; vllm-ascend "Batch Invariance",
+ * Implementation Details: batch-invariant attention operators). With chunked
+ * prefill a sequence's new tokens share a batch with other sequences' tokens
+ * and are split across steps as the scheduler decides; here neither matters.
+ * Query token i of sequence b (row cu_q[b] + i of Q, 0 <= i < q_len_b =
+ * cu_q[b+1] - cu_q[b]) sits at position p = seq_lens[b] - q_len_b + i and sees
+ * the cached tokens 0..p:
+ *   O[t][h] = sum_{j <= p} softmax_j(scale * q.k_j) v_j
+ * computed exactly as bi_attention_decode computes the query of a sequence
+ * of length p + 1 (the same 128-token chunks by position, per-chunk
+ * arithmetic and chunk-order merge), so a token's output is the same bits
+ * whether it is decoded alone, prefilled in one call, prefilled in pieces of
+ * any size, or batched with any other sequences.
+ *
+ *   Q         bf16 [total_q][Hq][128]  the new tokens of all sequences, sequence by sequence
+ *   cu_q      int32 [B+1] (device)     cu_q[0] = 0, cu_q[b+1] - cu_q[b] = q_len_b, cu_q[B] <= total_q
+ *   K_cache, V_cache, block_table, block_size as in bi_attention_decode
+ *   seq_lens  int32 [B] (device)       cached length of each sequence, the new tokens included
+ *   O         bf16 [total_q][Hq][128]  rows of the sequences' new tokens written
+ * No workspace: each CTA merges its chunks in registers. A sequence whose
+ * q_len or seq_lens is out of range (q_len > max_q_len, q_len > seq_lens,
+ * seq_lens > max_seq_len or longer than its table, cu_q past total_q) is
+ * skipped and the device status becomes BI_ERR_INVALID_ARG.
+ * Requirements: head_dim == 128; Hq % Hkv == 0 and Hq / Hkv in {1, 2, 4, 8};
+ * 1 <= B <= 65535; 1 <= max_q_len; block_size >= 1; max_seq_len >= 1.
+ */
+BI_API bi_status bi_attention_extend(const void *Q, const int32_t *cu_q, int32_t total_q, const void *K_cache,
+                                     const void *V_cache, const int32_t *block_table, int32_t max_blocks_per_seq,
+                                     int64_t num_blocks, const int32_t *seq_lens, int64_t B, int32_t Hq,
+                                     int32_t Hkv, int32_t head_dim, int32_t block_size, int32_t max_seq_len,
+                                     int32_t max_q_len, float scale, void *O, bi_stream stream);
 
 /*
  * bi_attention_decode_noalloc -- bi_attention_decode for callers that cannot

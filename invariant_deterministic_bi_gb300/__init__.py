@@ -72,6 +72,7 @@ def load() -> ctypes.CDLL:
             "bi_attention_decode": [P, P, P, P, I32, I64, P, I64, I32, I32, I32, I32, I32, F, P, I64, P, P],
             "bi_attention_decode_workspace_size": [I64, I32, I32],
             "bi_attention_decode_noalloc": [P, P, P, P, I32, I64, P, I64, I32, I32, I32, I32, I32, F, P, P],
+            "bi_attention_extend": [P, P, I32, P, P, P, I32, I64, P, I64, I32, I32, I32, I32, I32, I32, F, P, P],
             "bi_plan": [I32, I64, I64, I64, I32, ctypes.POINTER(Plan)],
             "bi_device_status": [P],
             "bi_check_wait_timeout": [ctypes.c_uint32, P],
@@ -376,6 +377,32 @@ def attention_decode(Q, K_cache, V_cache, block_table, seq_lens, max_seq_len: in
                                       nblk, _ptr(seq_lens), B, Hq, Hkv, D, bs, max_seq_len, float(scale),
                                       _ptr(workspace), workspace.numel(), _ptr(O), _stream(stream)),
            "bi_attention_decode")
+    return O
+
+
+def attention_extend(Q, cu_q, K_cache, V_cache, block_table, seq_lens, max_seq_len: int, max_q_len: int,
+                     scale: float, O=None, stream=None):
+    """Batch-invariant causal extend (prefill) attention over a paged KV cache (see bi.h).
+
+    Q bf16 [total_q, Hq, 128] (each sequence's new tokens, in sequence order);
+    cu_q int32 [B+1]; K_cache, V_cache bf16 [blocks, block_size, Hkv, 128];
+    block_table int32 [B, max_blocks]; seq_lens int32 [B] (new tokens included)."""
+    import torch
+    _dev(Q, torch.bfloat16, "Q"), _dev(K_cache, torch.bfloat16, "K_cache"), _dev(V_cache, torch.bfloat16, "V_cache")
+    _dev(cu_q, torch.int32, "cu_q"), _dev(block_table, torch.int32, "block_table"), _dev(seq_lens, torch.int32, "seq_lens")
+    for t, n in ((Q, "Q"), (K_cache, "K_cache"), (V_cache, "V_cache"), (block_table, "block_table"), (cu_q, "cu_q")):
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    T, Hq, D = Q.shape
+    nblk, bs, Hkv, D2 = K_cache.shape
+    B = seq_lens.numel()
+    if D2 != D or V_cache.shape != K_cache.shape or block_table.shape[0] != B or cu_q.numel() != B + 1:
+        raise ValueError("shape mismatch")
+    if O is None:
+        O = torch.empty_like(Q)
+    _check(load().bi_attention_extend(_ptr(Q), _ptr(cu_q), T, _ptr(K_cache), _ptr(V_cache), _ptr(block_table),
+                                      block_table.shape[1], nblk, _ptr(seq_lens), B, Hq, Hkv, D, bs, max_seq_len,
+                                      max_q_len, float(scale), _ptr(O), _stream(stream)), "bi_attention_extend")
     return O
 
 

@@ -309,6 +309,29 @@ bi_status bi_attention_decode(const void *Q, const void *K_cache, const void *V_
                                    Hkv, head_dim, block_size, max_seq_len, scale, workspace, O, as_stream(stream));
 }
 
+bi_status bi_attention_extend(const void *Q, const int32_t *cu_q, int32_t total_q, const void *K_cache,
+                              const void *V_cache, const int32_t *block_table, int32_t max_blocks_per_seq,
+                              int64_t num_blocks, const int32_t *seq_lens, int64_t B, int32_t Hq, int32_t Hkv,
+                              int32_t head_dim, int32_t block_size, int32_t max_seq_len, int32_t max_q_len, float scale,
+                              void *O, bi_stream stream) {
+    if (B < 0 || B > 65535 || total_q < 0 || Hq < 1 || Hkv < 1 || block_size < 1 || max_seq_len < 1 ||
+        max_q_len < 1 || max_blocks_per_seq < 1 || num_blocks < 1 || !(scale == scale))
+        return BI_ERR_INVALID_ARG;
+    if (B == 0 || total_q == 0) return BI_OK;
+    if (!Q || !cu_q || !K_cache || !V_cache || !block_table || !seq_lens || !O) return BI_ERR_INVALID_ARG;
+    if (head_dim != 128 || Hq % Hkv != 0) return BI_ERR_UNSUPPORTED;
+    const int32_t G = Hq / Hkv;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return BI_ERR_UNSUPPORTED;
+    if (!aligned16(Q) || !aligned16(K_cache) || !aligned16(V_cache) || !aligned16(O) || !aligned4(block_table) ||
+        !aligned4(seq_lens) || !aligned4(cu_q))
+        return BI_ERR_MISALIGNED;
+    bi_status st = require_device();
+    if (st != BI_OK) return st;
+    return launch_attention_extend(Q, cu_q, total_q, K_cache, V_cache, block_table, max_blocks_per_seq, num_blocks,
+                                   seq_lens, B, Hq, Hkv, block_size, max_seq_len, max_q_len, scale, O,
+                                   as_stream(stream));
+}
+
 bi_status bi_plan(int32_t op, int64_t M, int64_t N, int64_t K, int32_t num_sms, bi_plan_t *out) {
     if (!out || M < 0 || N < 0 || K < 0 || num_sms < 0) return BI_ERR_INVALID_ARG;
     int sms = num_sms;

@@ -30,8 +30,22 @@
 //   - writes fp32 (m, l, o[0..127]) per head and chunk to the workspace.
 //   The MMA shapes and step orders are the same for every chunk of every
 //   batch, so the per-chunk results do not depend on the batch either.
-// Step 2, one CTA per (sequence, query head): M = max_c m_c; the output is
-//   sum_c e^{m_c - M} o_c / sum_c e^{m_c - M} l_c, chunks in order, rounded to bf16.
+// Step 2, one CTA per (sequence, query head): the chunk results are merged
+//   in chunk order by merge_chunk() below (running maximum m, with the
+//   running o and l rescaled by e^{m - m'} and the chunk's by e^{m_c - m'}),
+//   and o / l is rounded to bf16.
+//
+// Extend (prefill) attention, attn_extend_kernel: the new query tokens of a
+// sequence attend causally to its cache. Token i at position p sees tokens
+// 0..p, so its result is defined as the decode result of the sequence cut
+// after p: the same 128-token chunks by position, the same per-chunk
+// arithmetic (q.k on the tensor cores, max, e^(s-m), the lane-strided sum,
+// p.V with p as bf16 hi + lo) and the same chunk-order merge_chunk(). A
+// token's output is therefore the same bits whether it is decoded alone,
+// prefilled at once, prefilled in chunks of any size, or batched with other
+// sequences. One CTA per (sequence, KV head, 64 query rows = 64/G tokens x G
+// heads) walks the chunks in order and merges each into per-row running
+// state held in registers.
 #include <cuda_bf16.h>
 
 #include <mutex>
@@ -86,6 +100,19 @@ __device__ __forceinline__ void split_bf16x2(float p0, float p1, uint32_t &hi, u
     hi = pack_bf16x2(__float_as_uint(p0), __float_as_uint(p1));
     const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xFFFF0000u);
     lo = pack_bf16x2(__float_as_uint(p0 - h0), __float_as_uint(p1 - h1));
+}
+
+// Merge one chunk's (m_c, l_c, o_c) into the running (m, l, o) of a query
+// row, in chunk order: m' = max(m, m_c); o = o e^{m - m'} + o_c e^{m_c - m'},
+// l likewise (the first chunk finds m = -inf, l = o = 0). Decode and extend
+// attention both merge through this one definition.
+__device__ __forceinline__ void merge_factors(float m, float m_c, float &m_new, float &alpha, float &beta) {
+    m_new = fmaxf(m, m_c);
+    alpha = expf(__fsub_rn(m, m_new));
+    beta = expf(__fsub_rn(m_c, m_new));
+}
+__device__ __forceinline__ float merge_value(float run, float chunk, float alpha, float beta) {
+    return __fmaf_rn(chunk, beta, __fmul_rn(run, alpha));
 }
 
 struct AttnParams {
@@ -269,35 +296,43 @@ attn_combine_kernel(const AttnParams p) {
     grid_dep_wait();      // earlier work of the stream is complete and visible
     grid_dep_launch();
     // Chunk statistics go through shared memory in tiles of kCombineThreads
-    // chunks, loaded in parallel; the arithmetic is the sequential chunk-order
-    // merge described at the top of the file (the maximum is exact in any order).
-    __shared__ float red[kCombineThreads / 32];
-    __shared__ float fw[kCombineThreads];     // e^{m_c - M} for the tile's chunks
+    // chunks, loaded in parallel; the running maximum of the tile is a prefix
+    // maximum (exact in any order), so every chunk's merge factors are known
+    // before the sequential, chunk-order merge of the o values (thread d
+    // merges dimension d).
+    __shared__ float fm[kCombineThreads];     // m_c, then the running maximum after chunk c
+    __shared__ float fa[kCombineThreads];     // alpha of chunk c
+    __shared__ float fb[kCombineThreads];     // beta of chunk c
     __shared__ float fl[kCombineThreads];     // l_c
+    __shared__ float carry;                   // running maximum after the previous tile
     const int h = blockIdx.x;
     const int64_t b = blockIdx.y;
-    const int d = threadIdx.x, lane = d & 31, warp = d >> 5;
+    const int d = threadIdx.x;
     int L;
     if (!seq_ok(p, b, L)) return;
     const int nc = (L + kChunk - 1) / kChunk;
     const float *w = p.ws + (b * p.Hq + h) * p.chunks * (kD + 2);
-    float m = -INFINITY;
-    for (int c = d; c < nc; c += kCombineThreads) m = fmaxf(m, w[static_cast<int64_t>(c) * (kD + 2)]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (lane == 0) red[warp] = m;
-    __syncthreads();
-    float M = red[0];
-#pragma unroll
-    for (int i = 1; i < kCombineThreads / 32; ++i) M = fmaxf(M, red[i]);
-    float num = 0.0f, den = 0.0f;
+    if (d == 0) carry = -INFINITY;
+    float o = 0.0f, l = 0.0f;
     for (int c0 = 0; c0 < nc; c0 += kCombineThreads) {
         const int nt = min(kCombineThreads, nc - c0);
         __syncthreads();                                   // previous tile fully consumed
         if (d < nt) {
             const float *wc = w + static_cast<int64_t>(c0 + d) * (kD + 2);
-            fw[d] = expf(wc[0] - M);
+            fm[d] = wc[0];
             fl[d] = wc[1];
+        }
+        __syncthreads();
+        if (d == 0) {                                      // factors in chunk order
+            float m = carry;
+            for (int c = 0; c < nt; ++c) {
+                float mn, a, bt;
+                merge_factors(m, fm[c], mn, a, bt);
+                fa[c] = a;
+                fb[c] = bt;
+                m = mn;
+            }
+            carry = m;
         }
         __syncthreads();
         const float *oc = w + static_cast<int64_t>(c0) * (kD + 2) + 2 + d;
@@ -308,18 +343,275 @@ attn_combine_kernel(const AttnParams p) {
             for (int i = 0; i < 8; ++i) o8[i] = oc[static_cast<int64_t>(c + i) * (kD + 2)];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                num = __fmaf_rn(fw[c + i], o8[i], num);
-                den = __fmaf_rn(fw[c + i], fl[c + i], den);
+                o = merge_value(o, o8[i], fa[c + i], fb[c + i]);
+                l = merge_value(l, fl[c + i], fa[c + i], fb[c + i]);
             }
         }
         for (; c < nt; ++c) {
-            num = __fmaf_rn(fw[c], oc[static_cast<int64_t>(c) * (kD + 2)], num);
-            den = __fmaf_rn(fw[c], fl[c], den);
+            o = merge_value(o, oc[static_cast<int64_t>(c) * (kD + 2)], fa[c], fb[c]);
+            l = merge_value(l, fl[c], fa[c], fb[c]);
         }
     }
-    const float o = __fdiv_rn(num, den);
-    const uint32_t packed = pack_bf16x2(__float_as_uint(o), 0u);
+    const float r = __fdiv_rn(o, l);
+    const uint32_t packed = pack_bf16x2(__float_as_uint(r), 0u);
     p.O[(b * p.Hq + h) * kD + d] = static_cast<uint16_t>(packed & 0xFFFFu);
+}
+
+// ------------------------------------------------------------------ extend
+
+constexpr int kExtRows = 64;                   // query rows (token, head) per CTA: four m16 tiles
+constexpr int kExtThreads = 256;
+constexpr int kSStride = kChunk + 8;           // fp32 scores per row in shared memory (padded)
+// K and V tiles twice (the next chunk loads while this one is used), q rows,
+// scores, the K/V row offsets of two chunks, per-row count / m_c / l_c.
+constexpr int kExtSmem = 4 * kTileBytes + kExtRows * kD * 2 + kExtRows * kSStride * 4 + 2 * kChunk * 8 +
+                         kExtRows * 12;
+
+struct ExtParams {
+    const uint16_t *Q;       // [total_q][Hq][D]
+    const int32_t *cu_q;     // [B+1]
+    const uint16_t *K;       // [blocks][bs][Hkv][D]
+    const uint16_t *V;
+    const int32_t *table;    // [B][max_blocks]
+    const int32_t *lens;     // [B], cached length including the new tokens
+    uint16_t *O;             // [total_q][Hq][D]
+    int64_t num_blocks;
+    int32_t total_q, max_blocks, Hq, Hkv, bs, max_len, max_q;
+    float scale;
+    unsigned *status;
+};
+
+template <int G>
+__global__ void __launch_bounds__(kExtThreads, 1)
+attn_extend_kernel(const ExtParams p) {
+    constexpr int kTQ = kExtRows / G;                  // query tokens per CTA
+    grid_dep_wait();      // earlier work of the stream is complete and visible
+    grid_dep_launch();
+    extern __shared__ __align__(16) uint8_t smem[];
+    uint8_t *KV = smem;                                                    // [2][K, V] tiles, swizzled rows
+    uint16_t *qb = reinterpret_cast<uint16_t *>(smem + 4 * kTileBytes);   // [kExtRows][kD] bf16
+    float *S = reinterpret_cast<float *>(qb + kExtRows * kD);              // [kExtRows][kSStride]
+    int64_t *rowoff = reinterpret_cast<int64_t *>(S + kExtRows * kSStride); // [2][kChunk], -1: no row
+    int *nrow = reinterpret_cast<int *>(rowoff + 2 * kChunk);             // tokens of this chunk row r sees
+    float *mc = reinterpret_cast<float *>(nrow + kExtRows);
+    float *lc = mc + kExtRows;
+    const int g = blockIdx.y;
+    const int64_t b = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t q0 = p.cu_q[b], q1 = p.cu_q[b + 1];
+    const int L = p.lens[b];
+    const int64_t qlen = q1 - q0;
+    if (q0 < 0 || q1 < q0 || q1 > p.total_q || qlen > p.max_q || L < qlen || L > p.max_len ||
+        L > static_cast<int64_t>(p.max_blocks) * p.bs) {
+        if (tid == 0 && blockIdx.x == 0 && g == 0) atomicOr(p.status, kDevBadOffsets);
+        return;
+    }
+    const int i0 = blockIdx.x * kTQ;                   // first query token of this CTA
+    if (i0 >= qlen) return;
+    const int ntok = static_cast<int>(qlen - i0 < kTQ ? qlen - i0 : static_cast<int64_t>(kTQ));
+    const int base = L - static_cast<int>(qlen);       // position of query token 0
+    const int L_last = base + i0 + ntok;               // the last token's causal length
+    const int nchunks = (L_last + kChunk - 1) / kChunk;
+
+    // q rows: row r = token r / G, head g*G + r % G (zero rows past the tokens)
+    for (int i = tid; i < kExtRows * kD / 8; i += kExtThreads) {
+        const int r = i / (kD / 8), x = i % (kD / 8);
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (r / G < ntok)
+            v = *reinterpret_cast<const uint4 *>(p.Q + ((q0 + i0 + r / G) * p.Hq + g * G + r % G) * kD + x * 8);
+        *reinterpret_cast<uint4 *>(qb + r * kD + x * 8) = v;
+    }
+    auto load_chunk = [&](int c) {
+        const int j0 = c * kChunk, buf = c & 1;
+        const int nmax = min(kChunk, L_last - j0);
+        int64_t *ro = rowoff + buf * kChunk;
+        if (tid < kChunk) {
+            int64_t off = -1;
+            if (tid < nmax) {
+                const int j = j0 + tid;
+                const int64_t blk = p.table[b * p.max_blocks + j / p.bs];
+                if (blk >= 0 && blk < p.num_blocks)
+                    off = ((blk * p.bs + j % p.bs) * p.Hkv + g) * kD;
+                else
+                    atomicOr(p.status, kDevBadOffsets);
+            }
+            ro[tid] = off;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+            const uint16_t *src = which == 0 ? p.K : p.V;
+            const uint32_t dst0 = smem_u32(KV + (2 * buf + which) * kTileBytes);
+#pragma unroll
+            for (int r = 0; r < kChunk * 16 / kExtThreads; ++r) {
+                const int i = tid + r * kExtThreads;
+                const int t = i >> 4, x = i & 15;
+                const int64_t off = ro[t];
+                cp_async_16(dst0 + t * kRowBytes + ((x ^ (t & 7)) << 4), off >= 0 ? src + off + x * 8 : src,
+                            off >= 0 ? 16u : 0u);
+            }
+            cp_async_commit();
+        }
+    };
+    load_chunk(0);
+
+    const int gq = lane >> 2, cq = lane & 3;              // fragment row group, column pair
+    // running state of this thread's rows: tile rt, rows gq (h = 0) and gq + 8 (h = 1)
+    float o_run[4][2][4], m_run[4][2], l_run[4][2];
+#pragma unroll
+    for (int rt = 0; rt < 4; ++rt) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            m_run[rt][h] = -INFINITY;
+            l_run[rt][h] = 0.0f;
+        }
+#pragma unroll
+        for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o_run[rt][nb][e] = 0.0f;
+    }
+
+    for (int c = 0; c < nchunks; ++c) {
+        const int j0 = c * kChunk, buf = c & 1;
+        const int nmax = min(kChunk, L_last - j0);
+        const int64_t *ro = rowoff + buf * kChunk;
+        const uint8_t *Ks = KV + (2 * buf) * kTileBytes;
+        const uint8_t *Vs = KV + (2 * buf + 1) * kTileBytes;
+        const bool more = c + 1 < nchunks;
+        if (more) {
+            __syncthreads();                              // the other buffer's last readers are done
+            load_chunk(c + 1);
+            cp_async_wait<3>();                           // this chunk's K copies (of this thread)
+        } else {
+            cp_async_wait<1>();
+        }
+        __syncthreads();                                  // everyone's
+
+        // scores S[r][t] = scale * q_r . k_t: warp w takes tokens 16w .. 16w+15,
+        // every row tile, dimensions ascending in 16-dimension steps
+#pragma unroll
+        for (int rt = 0; rt < 4; ++rt) {
+            const uint16_t *qa = qb + (rt * 16 + gq) * kD + 2 * cq;
+#pragma unroll
+            for (int nb = 0; nb < 2; ++nb) {
+                const int n0 = warp * 16 + nb * 8;
+                const int t = n0 + gq;
+                const uint8_t *krow = Ks + t * kRowBytes + cq * 4;
+                float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                for (int ks = 0; ks < kD / 16; ++ks) {
+                    const uint32_t a0 = *reinterpret_cast<const uint32_t *>(qa + 16 * ks);
+                    const uint32_t a1 = *reinterpret_cast<const uint32_t *>(qa + 8 * kD + 16 * ks);
+                    const uint32_t a2 = *reinterpret_cast<const uint32_t *>(qa + 16 * ks + 8);
+                    const uint32_t a3 = *reinterpret_cast<const uint32_t *>(qa + 8 * kD + 16 * ks + 8);
+                    const uint32_t b0 = *reinterpret_cast<const uint32_t *>(krow + (((2 * ks) ^ (t & 7)) << 4));
+                    const uint32_t b1 = *reinterpret_cast<const uint32_t *>(krow + (((2 * ks + 1) ^ (t & 7)) << 4));
+                    mma_16816(acc, a0, a1, a2, a3, b0, b1);
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int tt = n0 + 2 * cq + (e & 1);
+                    const int r = rt * 16 + gq + 8 * (e >> 1);
+                    if (tt < nmax) S[r * kSStride + tt] = ro[tt] >= 0 ? __fmul_rn(acc[e], p.scale) : -INFINITY;
+                }
+            }
+        }
+        __syncthreads();
+
+        // per row: the tokens it sees in this chunk, max, exponentials, sum
+        for (int r = warp; r < kExtRows; r += kExtThreads / 32) {
+            const int ti = r / G;
+            const int n = ti < ntok ? min(kChunk, base + i0 + ti + 1 - j0) : 0;
+            float *Sr = S + r * kSStride;
+            if (n > 0) {
+                float m = -INFINITY;
+                for (int t = lane; t < n; t += 32) m = fmaxf(m, Sr[t]);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                float l = 0.0f;
+                for (int t = lane; t < n; t += 32) {
+                    const float e = expf(Sr[t] - m);
+                    Sr[t] = e;
+                    l += e;
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+                if (lane == 0) {
+                    mc[r] = m;
+                    lc[r] = l;
+                }
+            }
+            if (lane == 0) nrow[r] = n > 0 ? n : 0;
+        }
+        if (more) cp_async_wait<2>(); else cp_async_wait<0>();   // this chunk's V copies
+        __syncthreads();
+
+        // values: O_c[r][d] = sum_t p_t v_t[d], p = hi + lo (two bf16 MMAs per
+        // step; zero past the row's tokens); warp w takes dimensions
+        // 16w .. 16w+15, tokens ascending in 16-token steps
+        const int d0 = warp * 16;
+        const int mi = lane >> 3, mr = lane & 7;          // ldmatrix: matrix, row
+#pragma unroll
+        for (int rt = 0; rt < 4; ++rt) {
+            const int ra = rt * 16 + gq, rb = ra + 8;
+            const int na = nrow[ra], nb8 = nrow[rb];
+            // skip the tile only when none of its rows sees this chunk (the MMAs need the whole warp)
+            if (!__any_sync(0xffffffffu, na != 0 || nb8 != 0)) continue;
+            float acc[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
+            const float *Sa = S + ra * kSStride, *Sb = S + rb * kSStride;
+#pragma unroll 2
+            for (int ks = 0; ks < kChunk / 16; ++ks) {
+                const int k0 = ks * 16;
+                const int t0 = k0 + 2 * cq, t2 = t0 + 8;
+                uint32_t ph0, pl0, ph1, pl1, ph2, pl2, ph3, pl3;
+                split_bf16x2(t0 < na ? Sa[t0] : 0.0f, t0 + 1 < na ? Sa[t0 + 1] : 0.0f, ph0, pl0);
+                split_bf16x2(t0 < nb8 ? Sb[t0] : 0.0f, t0 + 1 < nb8 ? Sb[t0 + 1] : 0.0f, ph1, pl1);
+                split_bf16x2(t2 < na ? Sa[t2] : 0.0f, t2 + 1 < na ? Sa[t2 + 1] : 0.0f, ph2, pl2);
+                split_bf16x2(t2 < nb8 ? Sb[t2] : 0.0f, t2 + 1 < nb8 ? Sb[t2 + 1] : 0.0f, ph3, pl3);
+                const int tok = k0 + (mi & 1) * 8 + mr;
+                const int chunk = (d0 >> 3) + (mi >> 1);
+                uint32_t v0, v1, v2, v3;
+                ldmatrix_x4_trans(v0, v1, v2, v3, smem_u32(Vs + tok * kRowBytes + ((chunk ^ (tok & 7)) << 4)));
+                mma_16816(acc[0], ph0, ph1, ph2, ph3, v0, v1);
+                mma_16816(acc[0], pl0, pl1, pl2, pl3, v0, v1);
+                mma_16816(acc[1], ph0, ph1, ph2, ph3, v2, v3);
+                mma_16816(acc[1], pl0, pl1, pl2, pl3, v2, v3);
+            }
+            // merge this chunk into the rows' running state, in chunk order
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int r = h ? rb : ra;
+                if ((h ? nb8 : na) == 0) continue;
+                float mn, al, be;
+                merge_factors(m_run[rt][h], mc[r], mn, al, be);
+                m_run[rt][h] = mn;
+                l_run[rt][h] = merge_value(l_run[rt][h], lc[r], al, be);
+#pragma unroll
+                for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e)
+                        o_run[rt][nb][2 * h + e] = merge_value(o_run[rt][nb][2 * h + e], acc[nb][2 * h + e], al, be);
+            }
+        }
+    }
+
+    // o / l, rounded to bf16, for the rows that exist
+    const int d0 = warp * 16;
+#pragma unroll
+    for (int rt = 0; rt < 4; ++rt) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int r = rt * 16 + gq + 8 * h;
+            if (r / G >= ntok) continue;
+            uint16_t *orow = p.O + ((q0 + i0 + r / G) * p.Hq + g * G + r % G) * kD + d0 + 2 * cq;
+#pragma unroll
+            for (int nb = 0; nb < 2; ++nb) {
+                const float x0 = __fdiv_rn(o_run[rt][nb][2 * h], l_run[rt][h]);
+                const float x1 = __fdiv_rn(o_run[rt][nb][2 * h + 1], l_run[rt][h]);
+                *reinterpret_cast<uint32_t *>(orow + nb * 8) = pack_bf16x2(__float_as_uint(x0), __float_as_uint(x1));
+            }
+        }
+    }
 }
 
 }  // namespace
@@ -375,6 +667,48 @@ bi_status launch_attention_decode(const void *Q, const void *K, const void *V, c
         default: return BI_ERR_UNSUPPORTED;
     }
     return launch_pdl(attn_combine_kernel, dim3(Hq, static_cast<unsigned>(B)), dim3(kCombineThreads), 0, s, p);
+}
+
+template <int G>
+bi_status launch_extend_g(const dim3 &grid, const ExtParams &p, cudaStream_t s) {
+    static unsigned long long configured = 0;
+    if (ensure_smem_attr(reinterpret_cast<const void *>(attn_extend_kernel<G>), kExtSmem, &configured) != BI_OK)
+        return BI_ERR_CUDA;
+    return launch_pdl(attn_extend_kernel<G>, grid, dim3(kExtThreads), kExtSmem, s, p);
+}
+
+bi_status launch_attention_extend(const void *Q, const int32_t *cu_q, int32_t total_q, const void *K, const void *V,
+                                  const int32_t *table, int32_t max_blocks, int64_t num_blocks, const int32_t *lens,
+                                  int64_t B, int32_t Hq, int32_t Hkv, int32_t bs, int32_t max_len, int32_t max_q,
+                                  float scale, void *O, cudaStream_t s) {
+    ExtParams p{};
+    p.Q = static_cast<const uint16_t *>(Q);
+    p.cu_q = cu_q;
+    p.K = static_cast<const uint16_t *>(K);
+    p.V = static_cast<const uint16_t *>(V);
+    p.table = table;
+    p.lens = lens;
+    p.O = static_cast<uint16_t *>(O);
+    p.num_blocks = num_blocks;
+    p.total_q = total_q;
+    p.max_blocks = max_blocks;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.bs = bs;
+    p.max_len = max_len;
+    p.max_q = max_q;
+    p.scale = scale;
+    p.status = device_status_word();
+    const int G = Hq / Hkv;
+    const int tq = kExtRows / G;
+    const dim3 grid((max_q + tq - 1) / tq, Hkv, static_cast<unsigned>(B));
+    switch (G) {
+        case 1: return launch_extend_g<1>(grid, p, s);
+        case 2: return launch_extend_g<2>(grid, p, s);
+        case 4: return launch_extend_g<4>(grid, p, s);
+        case 8: return launch_extend_g<8>(grid, p, s);
+        default: return BI_ERR_UNSUPPORTED;
+    }
 }
 
 }  // namespace bi

@@ -98,6 +98,10 @@ bi_status launch_attention_decode(const void *Q, const void *K, const void *V, c
                                   int32_t max_blocks, int64_t num_blocks, const int32_t *lens, int64_t B, int32_t Hq,
                                   int32_t Hkv, int32_t D, int32_t bs, int32_t max_len, float scale, void *workspace,
                                   void *O, cudaStream_t s);
+bi_status launch_attention_extend(const void *Q, const int32_t *cu_q, int32_t total_q, const void *K, const void *V,
+                                  const int32_t *table, int32_t max_blocks, int64_t num_blocks, const int32_t *lens,
+                                  int64_t B, int32_t Hq, int32_t Hkv, int32_t bs, int32_t max_len, int32_t max_q,
+                                  float scale, void *O, cudaStream_t s);
 bi_status launch_wait_timeout_check(uint32_t limit_us, cudaStream_t s);
 
 // Plans (M-independent except tiles_m and grid).

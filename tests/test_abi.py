@@ -26,7 +26,7 @@ def declared_functions():
 
 def test_header_declares_the_calls():
     names = declared_functions()
-    for n in ["bi_gemm_bf16", "bi_grouped_gemm_bf16", "bi_grouped_gemm_silu_bf16", "bi_gemm_nvfp4", "bi_rmsnorm", "bi_plan", "bi_quantize_nvfp4", "bi_moe_topk_softmax", "bi_moe_align", "bi_moe_gather", "bi_silu_mul", "bi_moe_combine", "bi_rank_sum_rmsnorm", "bi_attention_decode", "bi_attention_decode_workspace_size",
+    for n in ["bi_gemm_bf16", "bi_grouped_gemm_bf16", "bi_grouped_gemm_silu_bf16", "bi_gemm_nvfp4", "bi_rmsnorm", "bi_plan", "bi_quantize_nvfp4", "bi_moe_topk_softmax", "bi_moe_align", "bi_moe_gather", "bi_silu_mul", "bi_moe_combine", "bi_rank_sum_rmsnorm", "bi_attention_decode", "bi_attention_decode_workspace_size", "bi_attention_extend",
               "bi_device_status", "bi_status_string", "bi_version", "bi_check_wait_timeout"]:
         assert n in names
 
