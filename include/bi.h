@@ -55,7 +55,8 @@ typedef enum {
     BI_ERR_MISALIGNED = 3,    /* pointer or leading dimension not 16-byte aligned */
     BI_ERR_ARCH = 4,          /* current device is not sm_103 */
     BI_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed */
-    BI_ERR_TIMEOUT = 6        /* a kernel's bounded wait ran out; its output is not valid */
+    BI_ERR_TIMEOUT = 6,       /* a kernel's bounded wait ran out; its output is not valid */
+    BI_ERR_BOUNDS = 7         /* debug build only: a bounds check failed and its access was skipped */
 } bi_status;
 
 /* Opaque CUDA stream handle (cudaStream_t). */
@@ -428,8 +429,10 @@ BI_API bi_status bi_plan(int32_t op, int64_t M, int64_t N, int64_t K, int32_t nu
 /*
  * bi_device_status -- synchronise `stream`, then read and clear the current
  * device's status word. Returns BI_OK, BI_ERR_TIMEOUT (a bounded wait in a
- * kernel ran out; that call's output is invalid), BI_ERR_INVALID_ARG (a
- * kernel found invalid device-side data, e.g. MoE offsets) or BI_ERR_CUDA.
+ * kernel ran out; that call's output is invalid), BI_ERR_BOUNDS (debug build:
+ * a bounds check failed; bi_last_bounds_line() names its source line),
+ * BI_ERR_INVALID_ARG (a kernel found invalid device-side data, e.g. MoE
+ * offsets) or BI_ERR_CUDA.
  */
 BI_API bi_status bi_device_status(bi_stream stream);
 
@@ -441,6 +444,28 @@ BI_API bi_status bi_device_status(bi_stream stream);
  * following bi_device_status(stream) returns BI_ERR_TIMEOUT.
  */
 BI_API bi_status bi_check_wait_timeout(uint32_t limit_us, bi_stream stream);
+
+/*
+ * The debug build (libbi_debug.so, compiled with BI_DEBUG): every kernel
+ * checks the indices and coordinates it computes -- TMA copy coordinates,
+ * tensor-memory columns, shared-memory areas, workspace and output rows --
+ * against the extents of its buffers before using them. A failed check skips
+ * the access and records BI_ERR_BOUNDS in the device status word (never a
+ * trap or an assert); the release build (libbi.so) compiles the checks away.
+ * Outputs of the two builds are identical when no check fails.
+ *
+ * bi_debug_build -- 1 in the debug build, 0 in the release build.
+ * bi_last_bounds_line -- the source line of the failed check that the last
+ *   bi_device_status call reported (0 if none).
+ * bi_check_bounds -- launch one thread that writes element `index` of a
+ *   library-owned 64-element array under a bounds check against `limit`
+ *   (1..64; index 0..63); in the debug build an index >= limit is skipped and
+ *   recorded, so a following bi_device_status returns BI_ERR_BOUNDS. It
+ *   exercises the check path without touching any caller memory.
+ */
+BI_API int32_t bi_debug_build(void);
+BI_API int32_t bi_last_bounds_line(void);
+BI_API bi_status bi_check_bounds(int32_t index, int32_t limit, bi_stream stream);
 
 /* Human-readable name of a status code (static string). */
 BI_API const char *bi_status_string(bi_status s);

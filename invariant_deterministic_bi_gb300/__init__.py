@@ -16,9 +16,11 @@ import os
 import threading
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libbi.so")
+# BI_LIBRARY=debug selects the debug build (bounds-checked kernels, same results)
+LIB_PATH = os.path.join(_HERE, "libbi_debug.so" if os.environ.get("BI_LIBRARY") == "debug" else "libbi.so")
 
-BI_OK, BI_ERR_INVALID_ARG, BI_ERR_UNSUPPORTED, BI_ERR_MISALIGNED, BI_ERR_ARCH, BI_ERR_CUDA, BI_ERR_TIMEOUT = range(7)
+(BI_OK, BI_ERR_INVALID_ARG, BI_ERR_UNSUPPORTED, BI_ERR_MISALIGNED, BI_ERR_ARCH, BI_ERR_CUDA, BI_ERR_TIMEOUT,
+ BI_ERR_BOUNDS) = range(8)
 OP_GEMM_BF16, OP_GROUPED_GEMM_BF16, OP_GEMM_NVFP4, OP_RMSNORM, OP_QUANTIZE_NVFP4, OP_GROUPED_GEMM_SILU_BF16 = range(6)
 
 _lock = threading.Lock()
@@ -72,6 +74,9 @@ def load() -> ctypes.CDLL:
             "bi_attention_decode": [P, P, P, P, I32, I64, P, I64, I32, I32, I32, I32, I32, F, P, I64, P, P],
             "bi_attention_decode_workspace_size": [I64, I32, I32],
             "bi_attention_decode_noalloc": [P, P, P, P, I32, I64, P, I64, I32, I32, I32, I32, I32, F, P, P],
+            "bi_debug_build": [],
+            "bi_last_bounds_line": [],
+            "bi_check_bounds": [I32, I32, P],
             "bi_attention_extend": [P, P, I32, P, P, P, I32, I64, P, I64, I32, I32, I32, I32, I32, I32, F, P, P],
             "bi_plan": [I32, I64, I64, I64, I32, ctypes.POINTER(Plan)],
             "bi_device_status": [P],
@@ -411,6 +416,23 @@ def plan(op: int, M: int, N: int, K: int, num_sms: int = 0) -> dict:
     p = Plan()
     _check(load().bi_plan(op, M, N, K, num_sms, ctypes.byref(p)), "bi_plan")
     return p.as_dict()
+
+
+def debug_build() -> bool:
+    """True when the loaded library is the bounds-checked debug build."""
+    return bool(load().bi_debug_build())
+
+
+def last_bounds_line() -> int:
+    """Source line of the failed bounds check the last device_status() reported (0 if none)."""
+    return int(load().bi_last_bounds_line())
+
+
+def check_bounds(index: int, limit: int, stream=None) -> None:
+    """Write element `index` of a library-owned 64-element array under a
+    bounds check against `limit` (debug build: index >= limit is skipped and
+    recorded; device_status() then returns BI_ERR_BOUNDS)."""
+    _check(load().bi_check_bounds(index, limit, _stream(stream)), "bi_check_bounds")
 
 
 def device_status(stream=None) -> int:

@@ -125,6 +125,7 @@ using namespace bi;
 
 namespace {
 constexpr int64_t kI32Max = 0x7FFFFFFF;
+int32_t g_last_bounds_line = 0;   // of the last bi_device_status that reported BI_ERR_BOUNDS
 inline cudaStream_t as_stream(bi_stream s) { return static_cast<cudaStream_t>(s); }
 }  // namespace
 
@@ -376,9 +377,24 @@ bi_status bi_device_status(bi_stream stream) {
     unsigned word = 0, zero = 0;
     if (cudaMemcpyFromSymbol(&word, g_status_word, sizeof word) != cudaSuccess) return BI_ERR_CUDA;
     if (word && cudaMemcpyToSymbol(g_status_word, &zero, sizeof zero) != cudaSuccess) return BI_ERR_CUDA;
+    g_last_bounds_line = (word & kDevBounds) ? static_cast<int32_t>(word >> 16) : 0;
     if (word & kDevTimeout) return BI_ERR_TIMEOUT;
+    if (word & kDevBounds) return BI_ERR_BOUNDS;
     if (word & kDevBadOffsets) return BI_ERR_INVALID_ARG;
     return BI_OK;
+}
+
+int32_t bi_debug_build(void) { return kDebugBuild ? 1 : 0; }
+
+int32_t bi_last_bounds_line(void) { return g_last_bounds_line; }
+
+bi_status bi_check_bounds(int32_t index, int32_t limit, bi_stream stream) {
+    if (limit < 1 || limit > 64 || index < 0 || index > 63) return BI_ERR_INVALID_ARG;
+    int dev;
+    const DeviceInfo *info;
+    bi_status st = current_device(&dev, &info);
+    if (st != BI_OK) return st;
+    return launch_bounds_check(index, limit, as_stream(stream));
 }
 
 bi_status bi_check_wait_timeout(uint32_t limit_us, bi_stream stream) {
@@ -399,6 +415,7 @@ const char *bi_status_string(bi_status s) {
         case BI_ERR_ARCH: return "BI_ERR_ARCH";
         case BI_ERR_CUDA: return "BI_ERR_CUDA";
         case BI_ERR_TIMEOUT: return "BI_ERR_TIMEOUT";
+        case BI_ERR_BOUNDS: return "BI_ERR_BOUNDS";
         default: return "BI_ERR_UNKNOWN";
     }
 }

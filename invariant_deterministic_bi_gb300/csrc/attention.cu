@@ -156,6 +156,7 @@ attn_split_kernel(const AttnParams p) {
     }
     const int j0 = c * kChunk;
     if (j0 >= L) return;                                  // this sequence has fewer chunks
+    if (!BI_IN_BOUNDS(c < p.chunks && b < gridDim.z, p.status)) return;   // debug build: inside the workspace
     const int n = min(kChunk, L - j0);
 
     // element offset of each token's K (and V) row for KV head g
@@ -311,6 +312,7 @@ attn_combine_kernel(const AttnParams p) {
     int L;
     if (!seq_ok(p, b, L)) return;
     const int nc = (L + kChunk - 1) / kChunk;
+    if (!BI_IN_BOUNDS(nc <= p.chunks, p.status)) return;   // debug build: inside the workspace
     const float *w = p.ws + (b * p.Hq + h) * p.chunks * (kD + 2);
     if (d == 0) carry = -INFINITY;
     float o = 0.0f, l = 0.0f;
@@ -602,7 +604,7 @@ attn_extend_kernel(const ExtParams p) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int r = rt * 16 + gq + 8 * h;
-            if (r / G >= ntok) continue;
+            if (r / G >= ntok || !BI_IN_BOUNDS(q0 + i0 + r / G < p.total_q, p.status)) continue;
             uint16_t *orow = p.O + ((q0 + i0 + r / G) * p.Hq + g * G + r % G) * kD + d0 + 2 * cq;
 #pragma unroll
             for (int nb = 0; nb < 2; ++nb) {

@@ -7,6 +7,7 @@
 #include <utility>
 
 #include "../../include/bi.h"
+#include "bi_debug.cuh"
 
 namespace bi {
 
@@ -102,6 +103,7 @@ bi_status launch_attention_extend(const void *Q, const int32_t *cu_q, int32_t to
                                   const int32_t *table, int32_t max_blocks, int64_t num_blocks, const int32_t *lens,
                                   int64_t B, int32_t Hq, int32_t Hkv, int32_t bs, int32_t max_len, int32_t max_q,
                                   float scale, void *O, cudaStream_t s);
+bi_status launch_bounds_check(int32_t index, int32_t limit, cudaStream_t s);
 bi_status launch_wait_timeout_check(uint32_t limit_us, cudaStream_t s);
 
 // Plans (M-independent except tiles_m and grid).

@@ -223,6 +223,11 @@ gemm_bf16_dense_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
                 const int a_row = mb * kBM + static_cast<int>(h) * kHalf;
                 const int b_row = nb * kBN + static_cast<int>(h) * kHalf;
                 for (int kb = kb_lo; kb < kb_hi; ++kb) {
+                    // debug build: the copy's coordinates lie inside the operands (padded to whole tiles)
+                    if (!BI_IN_BOUNDS(kb * kBK < p.K && a_row < num_m * kBM && b_row < num_n * kBN, p.status)) {
+                        ok = false;
+                        break;
+                    }
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
                     if (h == 0) mbar_arrive_expect_tx(&full[stage], 2 * (p.a_bytes + kBBytes));
                     const uint32_t bar = full_leader + stage * 8;
@@ -314,7 +319,7 @@ gemm_bf16_dense_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
                     break;
                 }
                 tc_fence_after();
-                if (rows) {
+                if (rows && BI_IN_BOUNDS(acc * kBN + hc * kColsPerWarp + kColsPerWarp <= kTmemCols, p.status)) {
                     const uint32_t taddr = lane_base + static_cast<uint32_t>(acc * kBN);
 #pragma unroll
                     for (int c = 0; c < kColsPerWarp / 16; ++c) {
@@ -341,6 +346,11 @@ gemm_bf16_dense_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
                 const int nrows = min(32, p.M - row0);
                 const uint32_t bytes = static_cast<uint32_t>(nrows) * 512u;
                 uint8_t *area = smem + e * kSumBytes;
+                // debug build: the running sum stays inside the operand ring, and the pairs of the chain exist
+                if (!BI_IN_BOUNDS(e * kSumBytes + static_cast<int>(bytes) <= kStages * kStageBytes &&
+                                      (my_seg == 0 || rank >= 2) && (my_seg == p.segs - 1 || static_cast<int>(rank) + 2 < csize),
+                                  p.status))
+                    continue;
                 if (my_seg > 0) {
                     if (lane == 0) {
                         mbar_arrive_expect_tx(&sum_full[e], bytes);

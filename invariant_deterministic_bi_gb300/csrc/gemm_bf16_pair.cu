@@ -210,6 +210,7 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                 if (pre_s[mid] <= x) lo = mid; else hi = mid - 1;
             }
             const int e = lo;
+            (void)BI_IN_BOUNDS(e >= 0 && e < p.E && x >= pre_s[e] && x < pre_s[e + 1], p.status);
             const int mt = pre_s[e + 1] - pre_s[e];
             const int local = t - pre_s[e] * num_n;
             const int mb = local % mt, nb = local / mt;
@@ -240,6 +241,9 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                 const int a_row = tl.a_row + static_cast<int>(rank) * kHalf;
                 const int b_row = tl.b_row + static_cast<int>(rank) * (SILU ? p.N : kHalf);
                 for (int kb = 0; kb < k_steps; ++kb) {
+                    // debug build: the copy's coordinates lie inside the operands (padded to whole tiles)
+                    if (!BI_IN_BOUNDS(kb * kBK < p.K && a_row >= 0 && a_row < num_m * kBM + (GROUPED ? p.E * kBM : 0) &&
+                                          b_row >= 0, p.status)) { ok = false; break; }
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
                     if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * (p.a_bytes + kBBytes));
                     const uint32_t bar = full_leader + stage * 8;
@@ -339,6 +343,9 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                     uint32_t r[32], w[32];
 #pragma unroll
                     for (int hf = 0; hf < 2; ++hf) {
+                        // debug build: the columns read lie inside this CTA's two accumulators
+                        (void)BI_IN_BOUNDS(acc * kBN + bx * kOutCols + hf * 32 + 32 + (SILU ? kOutTile : 0) <= kTmemCols,
+                                           p.status);
                         tmem_ld_32x32b_x32(taddr + bx * kOutCols + hf * 32, r);
                         tmem_wait_ld();
 #pragma unroll
@@ -368,7 +375,7 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                             tma_store_2d(&tmY, buf, n0 + bx * kOutCols, row0);
                             bulk_commit_group();
                         }
-                    } else if (row < tl.row_end) {
+                    } else if (row < tl.row_end && BI_IN_BOUNDS(row < p.M, p.status)) {
                         uint8_t *yrow = p.Yg + (row * p.N + n0 + bx * kOutCols) * 2;
 #pragma unroll
                         for (int c = 0; c < kOutCols / 8; ++c)

@@ -178,6 +178,9 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 const int rb_a = mb * 2 + h;               // this CTA's 128-row scale block of A
                 const int rb_b = nb * 2;                   // the tile's two B scale blocks
                 for (int ks = 0; ks < k_stages; ++ks) {
+                    // debug build: the copies' coordinates lie inside the operands and scale atoms
+                    if (!BI_IN_BOUNDS(ks * kBKBytes < p.K / 2 && a_row < num_m * kBM && b_row < num_n * kBN &&
+                                          ks * kMmasPerStage < p.atoms_per_rowblock, p.status)) { ok = false; break; }
                     // the slot is free once the pair's MMAs have read it
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
                     mbar_arrive_expect_tx(&full[stage], p.stage_tx);
@@ -267,6 +270,7 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     ld_shared_v4(sb + (kMmasPerStage + j) * kAtom, c[8], c[9], c[10], c[11]);
                 }
                 const uint32_t dst = lane_base + stage * kSfColsPerStage;
+                (void)BI_IN_BOUNDS(kSfCol + (stage + 1) * kSfColsPerStage <= kTmemCols, p.status);
 #pragma unroll
                 for (int o = 0; o < kSfColsPerStage; o += 16) tmem_st_32x32b_x16(dst + o, r, o);
                 tmem_wait_st();

@@ -94,7 +94,7 @@ __device__ __forceinline__ float with_sign_of(float mag, float x) {
 
 __global__ void __launch_bounds__(kThreads)
 quantize_nvfp4_kernel(const uint4 *__restrict__ X, int64_t ldx_vec, uint8_t *__restrict__ Q, uint8_t *__restrict__ SF,
-                      int64_t M, int K, float gs) {
+                      int64_t M, int K, float gs, unsigned *status) {
     grid_dep_wait();      // earlier work of the stream is complete and visible
     grid_dep_launch();
     const int blocks = K / 16;                       // 16-element scale blocks per row
@@ -159,7 +159,9 @@ quantize_nvfp4_kernel(const uint4 *__restrict__ X, int64_t ldx_vec, uint8_t *__r
         }
         *reinterpret_cast<uint2 *>(Q + r * (K / 2) + c * 8) = make_uint2(codes[0], codes[1]);
         const int64_t atom = (r / 128) * atoms + c / 4;
-        SF[atom * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4 + c % 4] = static_cast<uint8_t>(s);
+        const int64_t at = atom * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4 + c % 4;
+        // debug build: inside the interleaved scale buffer ((M rounded up to 128) x K/16 bytes)
+        if (BI_IN_BOUNDS(at < (M + 127) / 128 * 128 * blocks, status)) SF[at] = static_cast<uint8_t>(s);
     }
 }
 
@@ -176,7 +178,8 @@ bi_status launch_quantize_nvfp4(const void *X, int64_t ldx, float gs, uint8_t *Q
     const int64_t cap = static_cast<int64_t>(info->sm_count) * 16;
     if (grid > cap) grid = cap;
     return launch_pdl(quantize_nvfp4_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, s,
-                      static_cast<const uint4 *>(X), ldx / 8, Q, Q_sf, M, static_cast<int>(K), gs);
+                      static_cast<const uint4 *>(X), ldx / 8, Q, Q_sf, M, static_cast<int>(K), gs,
+                      device_status_word());
 }
 
 }  // namespace bi

@@ -274,6 +274,13 @@ __global__ void wait_timeout_check_kernel(unsigned *status, unsigned long long l
     if (threadIdx.x == 0 && !mbar_wait(&bar, 0, nullptr, limit_ns)) atomicOr(status, kDevTimeout);
 }
 
+// One thread writes element `index` of a 64-element array under the debug
+// build's bounds check against `limit` (an index >= limit is skipped and recorded).
+__device__ unsigned g_bounds_probe[64];
+__global__ void bounds_check_kernel(int index, int limit, unsigned *status) {
+    if (BI_IN_BOUNDS(index < limit, status)) g_bounds_probe[index & 63] = 1u;
+}
+
 }  // namespace
 
 void plan_rmsnorm(int64_t M, int64_t H, bi_plan_t *pl) {
@@ -306,6 +313,11 @@ bi_status launch_rank_sum_rmsnorm(const void *const *parts, int32_t R, void *res
     for (int r = 0; r < R; ++r) rp.p[r] = static_cast<const uint4 *>(parts[r]);
     return residual ? launch_rank_res<true>(rp, R, residual, w, sum_out, out, M, H, eps, s)
                     : launch_rank_res<false>(rp, R, residual, w, sum_out, out, M, H, eps, s);
+}
+
+bi_status launch_bounds_check(int32_t index, int32_t limit, cudaStream_t s) {
+    bounds_check_kernel<<<1, 1, 0, s>>>(index, limit, device_status_word());
+    return cudaGetLastError() == cudaSuccess ? BI_OK : BI_ERR_CUDA;
 }
 
 bi_status launch_wait_timeout_check(uint32_t limit_us, cudaStream_t s) {

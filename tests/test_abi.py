@@ -43,9 +43,24 @@ def test_every_declared_symbol_is_exported(lib):
     assert ours == set(declared_functions())
 
 
+def test_debug_library_builds_and_exports_the_same_calls(lib):
+    """libbi_debug.so (bounds-checked kernels) builds from the same sources and
+    exports exactly the calls bi.h declares; it says it is the debug build."""
+    from invariant_deterministic_bi_gb300 import _build
+    path = _build.build(debug=True)
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\sT\s(\w+)$", out, re.M))
+    assert {s for s in exported if s.startswith("bi_") or s.startswith("_ZN2bi")} == set(declared_functions())
+    dbg = ctypes.CDLL(path)
+    assert dbg.bi_debug_build() == 1
+    assert lib.load().bi_debug_build() == 0
+    assert dbg.bi_check_bounds(70, 10, None) == 1 and dbg.bi_check_bounds(5, 65, None) == 1   # argument checks
+
+
 def test_status_strings(lib):
     assert lib.status_string(lib.BI_OK) == "BI_OK"
     assert lib.status_string(lib.BI_ERR_TIMEOUT) == "BI_ERR_TIMEOUT"
+    assert lib.status_string(lib.BI_ERR_BOUNDS) == "BI_ERR_BOUNDS"
     assert lib.version() >= 100
 
 
