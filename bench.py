@@ -45,13 +45,13 @@ NOMINAL_HBM_GBS = 8000.0
 # DRAM bytes (read + write) of one gate_up launch at M=8192 from an ncu capture
 # of that launch, valid only for the kernel source it was taken on (checked by
 # hash at run time).
-GATE_UP_TRAFFIC = {"source_sha256_16": "3a434c5bd9eca660", "bytes": 901581056 + 384537088}
+GATE_UP_TRAFFIC = {"source_sha256_16": "e4f5879b289e86ec", "bytes": 885824768 + 385909248}
 
 
 def gate_up_traffic():
     import hashlib
     h = hashlib.sha256()
-    for f in ("gemm_bf16_dense.cu", "bi_ptx.cuh"):
+    for f in ("gemm_bf16_pair.cu", "bi_ptx.cuh"):
         with open(os.path.join(ROOT, "invariant_deterministic_bi_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return GATE_UP_TRAFFIC["bytes"] if h.hexdigest()[:16] == GATE_UP_TRAFFIC["source_sha256_16"] else None
