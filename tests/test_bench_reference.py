@@ -22,3 +22,6 @@ def test_reference_arm_prints_one_line():
     assert d["value"] > 0 and d["steps"] == 1 and d["warmup"] == 3
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    # the same workload as the GPU arm; the row sample is described in cpu_baseline
+    assert d["config"]["M"] == 8192 and "M=8192" in d["config"]["workload"]
+    assert "1 of the step's 8192 rows" in d["cpu_baseline"]["sample"]
