@@ -94,6 +94,12 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t &r0, uint32_t &r1, ui
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
 }
+// Four 8x8 bf16 matrices from shared memory (lanes 8i..8i+7 give the 16-byte
+// rows of matrix i); lane (g, c) receives row g, columns 2c and 2c+1 of each.
+__device__ __forceinline__ void ldmatrix_x4(uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3, uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
 // (p0, p1) = hi + lo, hi and lo packed bf16 pairs (round to nearest even);
 // hi + lo carries 16 significant bits of each p.
 __device__ __forceinline__ void split_bf16x2(float p0, float p1, uint32_t &hi, uint32_t &lo) {
@@ -458,19 +464,31 @@ attn_extend_kernel(const ExtParams p) {
     load_chunk(0);
 
     const int gq = lane >> 2, cq = lane & 3;              // fragment row group, column pair
-    // running state of this thread's rows: tile rt, rows gq (h = 0) and gq + 8 (h = 1)
-    float o_run[4][2][4], m_run[4][2], l_run[4][2];
+    const int rt = warp & 3;                              // this warp's 16-row tile
+    const int th = warp >> 2, dh = warp >> 2;             // its half of the chunk's tokens (scores), of the dimensions (values)
+    // running state of this thread's rows (gq: h = 0, gq + 8: h = 1) for the warp's 64 dimensions
+    float o_run[8][4], m_run[2], l_run[2];
 #pragma unroll
-    for (int rt = 0; rt < 4; ++rt) {
+    for (int h = 0; h < 2; ++h) {
+        m_run[h] = -INFINITY;
+        l_run[h] = 0.0f;
+    }
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            m_run[rt][h] = -INFINITY;
-            l_run[rt][h] = 0.0f;
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o_run[nt][e] = 0.0f;
+    __syncthreads();                                      // q rows in shared memory
+    // the warp's q fragments (A operand of q.k) for the whole kernel: rows gq and gq + 8 of tile rt
+    uint32_t qf[kD / 16][4];
+    {
+        const uint16_t *qa = qb + (rt * 16 + gq) * kD + 2 * cq;
+#pragma unroll
+        for (int ks = 0; ks < kD / 16; ++ks) {
+            qf[ks][0] = *reinterpret_cast<const uint32_t *>(qa + 16 * ks);
+            qf[ks][1] = *reinterpret_cast<const uint32_t *>(qa + 8 * kD + 16 * ks);
+            qf[ks][2] = *reinterpret_cast<const uint32_t *>(qa + 16 * ks + 8);
+            qf[ks][3] = *reinterpret_cast<const uint32_t *>(qa + 8 * kD + 16 * ks + 8);
         }
-#pragma unroll
-        for (int nb = 0; nb < 2; ++nb)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) o_run[rt][nb][e] = 0.0f;
     }
 
     for (int c = 0; c < nchunks; ++c) {
@@ -489,33 +507,28 @@ attn_extend_kernel(const ExtParams p) {
         }
         __syncthreads();                                  // everyone's
 
-        // scores S[r][t] = scale * q_r . k_t: warp w takes tokens 16w .. 16w+15,
-        // every row tile, dimensions ascending in 16-dimension steps
+        // scores S[r][t] = scale * q_r . k_t: warp w takes row tile rt = w % 4 and
+        // tokens 64 (w / 4) .. +63, dimensions ascending in 16-dimension steps (its
+        // q fragments stay in registers; K fragments by ldmatrix)
 #pragma unroll
-        for (int rt = 0; rt < 4; ++rt) {
-            const uint16_t *qa = qb + (rt * 16 + gq) * kD + 2 * cq;
+        for (int nt = 0; nt < 8; ++nt) {
+            const int n0 = th * 64 + nt * 8;
+            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            const int trow = n0 + (lane & 7);                      // the K row this lane addresses
+            const uint32_t kbase = smem_u32(Ks) + trow * kRowBytes;
 #pragma unroll
-            for (int nb = 0; nb < 2; ++nb) {
-                const int n0 = warp * 16 + nb * 8;
-                const int t = n0 + gq;
-                const uint8_t *krow = Ks + t * kRowBytes + cq * 4;
-                float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            for (int kp = 0; kp < kD / 32; ++kp) {                 // two 16-dimension steps per ldmatrix
+                const int chunk = 4 * kp + (lane >> 3);            // 16-byte chunk of matrix lane/8
+                uint32_t b0, b1, b2, b3;
+                ldmatrix_x4(b0, b1, b2, b3, kbase + ((chunk ^ (trow & 7)) << 4));
+                mma_16816(acc, qf[2 * kp][0], qf[2 * kp][1], qf[2 * kp][2], qf[2 * kp][3], b0, b1);
+                mma_16816(acc, qf[2 * kp + 1][0], qf[2 * kp + 1][1], qf[2 * kp + 1][2], qf[2 * kp + 1][3], b2, b3);
+            }
 #pragma unroll
-                for (int ks = 0; ks < kD / 16; ++ks) {
-                    const uint32_t a0 = *reinterpret_cast<const uint32_t *>(qa + 16 * ks);
-                    const uint32_t a1 = *reinterpret_cast<const uint32_t *>(qa + 8 * kD + 16 * ks);
-                    const uint32_t a2 = *reinterpret_cast<const uint32_t *>(qa + 16 * ks + 8);
-                    const uint32_t a3 = *reinterpret_cast<const uint32_t *>(qa + 8 * kD + 16 * ks + 8);
-                    const uint32_t b0 = *reinterpret_cast<const uint32_t *>(krow + (((2 * ks) ^ (t & 7)) << 4));
-                    const uint32_t b1 = *reinterpret_cast<const uint32_t *>(krow + (((2 * ks + 1) ^ (t & 7)) << 4));
-                    mma_16816(acc, a0, a1, a2, a3, b0, b1);
-                }
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int tt = n0 + 2 * cq + (e & 1);
-                    const int r = rt * 16 + gq + 8 * (e >> 1);
-                    if (tt < nmax) S[r * kSStride + tt] = ro[tt] >= 0 ? __fmul_rn(acc[e], p.scale) : -INFINITY;
-                }
+            for (int e = 0; e < 4; ++e) {
+                const int tt = n0 + 2 * cq + (e & 1);
+                const int r = rt * 16 + gq + 8 * (e >> 1);
+                if (tt < nmax) S[r * kSStride + tt] = ro[tt] >= 0 ? __fmul_rn(acc[e], p.scale) : -INFINITY;
             }
         }
         __syncthreads();
@@ -549,69 +562,71 @@ attn_extend_kernel(const ExtParams p) {
         __syncthreads();
 
         // values: O_c[r][d] = sum_t p_t v_t[d], p = hi + lo (two bf16 MMAs per
-        // step; zero past the row's tokens); warp w takes dimensions
-        // 16w .. 16w+15, tokens ascending in 16-token steps
-        const int d0 = warp * 16;
-        const int mi = lane >> 3, mr = lane & 7;          // ldmatrix: matrix, row
-#pragma unroll
-        for (int rt = 0; rt < 4; ++rt) {
+        // step; zero past the row's tokens); warp w takes row tile rt and
+        // dimensions 64 (w / 4) .. +63, tokens ascending in 16-token steps
+        {
             const int ra = rt * 16 + gq, rb = ra + 8;
             const int na = nrow[ra], nb8 = nrow[rb];
-            // skip the tile only when none of its rows sees this chunk (the MMAs need the whole warp)
-            if (!__any_sync(0xffffffffu, na != 0 || nb8 != 0)) continue;
-            float acc[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
-            const float *Sa = S + ra * kSStride, *Sb = S + rb * kSStride;
+            // skip only when none of the tile's rows sees this chunk (the MMAs need the whole warp)
+            if (__any_sync(0xffffffffu, na != 0 || nb8 != 0)) {
+                const int mi = lane >> 3, mr = lane & 7;          // ldmatrix: matrix, row
+                float acc[8][4];
+#pragma unroll
+                for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) acc[nt][e] = 0.0f;
+                const float *Sa = S + ra * kSStride, *Sb = S + rb * kSStride;
 #pragma unroll 2
-            for (int ks = 0; ks < kChunk / 16; ++ks) {
-                const int k0 = ks * 16;
-                const int t0 = k0 + 2 * cq, t2 = t0 + 8;
-                uint32_t ph0, pl0, ph1, pl1, ph2, pl2, ph3, pl3;
-                split_bf16x2(t0 < na ? Sa[t0] : 0.0f, t0 + 1 < na ? Sa[t0 + 1] : 0.0f, ph0, pl0);
-                split_bf16x2(t0 < nb8 ? Sb[t0] : 0.0f, t0 + 1 < nb8 ? Sb[t0 + 1] : 0.0f, ph1, pl1);
-                split_bf16x2(t2 < na ? Sa[t2] : 0.0f, t2 + 1 < na ? Sa[t2 + 1] : 0.0f, ph2, pl2);
-                split_bf16x2(t2 < nb8 ? Sb[t2] : 0.0f, t2 + 1 < nb8 ? Sb[t2 + 1] : 0.0f, ph3, pl3);
-                const int tok = k0 + (mi & 1) * 8 + mr;
-                const int chunk = (d0 >> 3) + (mi >> 1);
-                uint32_t v0, v1, v2, v3;
-                ldmatrix_x4_trans(v0, v1, v2, v3, smem_u32(Vs + tok * kRowBytes + ((chunk ^ (tok & 7)) << 4)));
-                mma_16816(acc[0], ph0, ph1, ph2, ph3, v0, v1);
-                mma_16816(acc[0], pl0, pl1, pl2, pl3, v0, v1);
-                mma_16816(acc[1], ph0, ph1, ph2, ph3, v2, v3);
-                mma_16816(acc[1], pl0, pl1, pl2, pl3, v2, v3);
-            }
-            // merge this chunk into the rows' running state, in chunk order
+                for (int ks = 0; ks < kChunk / 16; ++ks) {
+                    const int k0 = ks * 16;
+                    const int t0 = k0 + 2 * cq, t2 = t0 + 8;
+                    uint32_t ph0, pl0, ph1, pl1, ph2, pl2, ph3, pl3;
+                    split_bf16x2(t0 < na ? Sa[t0] : 0.0f, t0 + 1 < na ? Sa[t0 + 1] : 0.0f, ph0, pl0);
+                    split_bf16x2(t0 < nb8 ? Sb[t0] : 0.0f, t0 + 1 < nb8 ? Sb[t0 + 1] : 0.0f, ph1, pl1);
+                    split_bf16x2(t2 < na ? Sa[t2] : 0.0f, t2 + 1 < na ? Sa[t2 + 1] : 0.0f, ph2, pl2);
+                    split_bf16x2(t2 < nb8 ? Sb[t2] : 0.0f, t2 + 1 < nb8 ? Sb[t2 + 1] : 0.0f, ph3, pl3);
+                    const int tok = k0 + (mi & 1) * 8 + mr;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int r = h ? rb : ra;
-                if ((h ? nb8 : na) == 0) continue;
-                float mn, al, be;
-                merge_factors(m_run[rt][h], mc[r], mn, al, be);
-                m_run[rt][h] = mn;
-                l_run[rt][h] = merge_value(l_run[rt][h], lc[r], al, be);
+                    for (int np = 0; np < 4; ++np) {              // two 8-dimension tiles per ldmatrix
+                        const int chunk = ((dh * 64 + np * 16) >> 3) + (mi >> 1);
+                        uint32_t v0, v1, v2, v3;
+                        ldmatrix_x4_trans(v0, v1, v2, v3, smem_u32(Vs + tok * kRowBytes + ((chunk ^ (tok & 7)) << 4)));
+                        mma_16816(acc[2 * np], ph0, ph1, ph2, ph3, v0, v1);
+                        mma_16816(acc[2 * np], pl0, pl1, pl2, pl3, v0, v1);
+                        mma_16816(acc[2 * np + 1], ph0, ph1, ph2, ph3, v2, v3);
+                        mma_16816(acc[2 * np + 1], pl0, pl1, pl2, pl3, v2, v3);
+                    }
+                }
+                // merge this chunk into the rows' running state, in chunk order
 #pragma unroll
-                for (int nb = 0; nb < 2; ++nb)
+                for (int h = 0; h < 2; ++h) {
+                    const int r = h ? rb : ra;
+                    if ((h ? nb8 : na) == 0) continue;
+                    float mn, al, be;
+                    merge_factors(m_run[h], mc[r], mn, al, be);
+                    m_run[h] = mn;
+                    l_run[h] = merge_value(l_run[h], lc[r], al, be);
 #pragma unroll
-                    for (int e = 0; e < 2; ++e)
-                        o_run[rt][nb][2 * h + e] = merge_value(o_run[rt][nb][2 * h + e], acc[nb][2 * h + e], al, be);
+                    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e)
+                            o_run[nt][2 * h + e] = merge_value(o_run[nt][2 * h + e], acc[nt][2 * h + e], al, be);
+                }
             }
         }
     }
 
     // o / l, rounded to bf16, for the rows that exist
-    const int d0 = warp * 16;
 #pragma unroll
-    for (int rt = 0; rt < 4; ++rt) {
+    for (int h = 0; h < 2; ++h) {
+        const int r = rt * 16 + gq + 8 * h;
+        if (r / G >= ntok || !BI_IN_BOUNDS(q0 + i0 + r / G < p.total_q, p.status)) continue;
+        uint16_t *orow = p.O + ((q0 + i0 + r / G) * p.Hq + g * G + r % G) * kD + dh * 64 + 2 * cq;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int r = rt * 16 + gq + 8 * h;
-            if (r / G >= ntok || !BI_IN_BOUNDS(q0 + i0 + r / G < p.total_q, p.status)) continue;
-            uint16_t *orow = p.O + ((q0 + i0 + r / G) * p.Hq + g * G + r % G) * kD + d0 + 2 * cq;
-#pragma unroll
-            for (int nb = 0; nb < 2; ++nb) {
-                const float x0 = __fdiv_rn(o_run[rt][nb][2 * h], l_run[rt][h]);
-                const float x1 = __fdiv_rn(o_run[rt][nb][2 * h + 1], l_run[rt][h]);
-                *reinterpret_cast<uint32_t *>(orow + nb * 8) = pack_bf16x2(__float_as_uint(x0), __float_as_uint(x1));
-            }
+        for (int nt = 0; nt < 8; ++nt) {
+            const float x0 = __fdiv_rn(o_run[nt][2 * h], l_run[h]);
+            const float x1 = __fdiv_rn(o_run[nt][2 * h + 1], l_run[h]);
+            *reinterpret_cast<uint32_t *>(orow + nt * 8) = pack_bf16x2(__float_as_uint(x0), __float_as_uint(x1));
         }
     }
 }
