@@ -369,11 +369,9 @@ attn_combine_kernel(const AttnParams p) {
 
 constexpr int kExtRows = 64;                   // query rows (token, head) per CTA: four m16 tiles
 constexpr int kExtThreads = 256;
-constexpr int kSStride = kChunk + 8;           // fp32 scores per row in shared memory (padded)
 // K and V tiles twice (the next chunk loads while this one is used), q rows,
-// scores, the K/V row offsets of two chunks, per-row count / m_c / l_c.
-constexpr int kExtSmem = 4 * kTileBytes + kExtRows * kD * 2 + kExtRows * kSStride * 4 + 2 * kChunk * 8 +
-                         kExtRows * 12;
+// the K/V row offsets of three chunks.
+constexpr int kExtSmem = 4 * kTileBytes + kExtRows * kD * 2 + 3 * kChunk * 8;
 
 struct ExtParams {
     const uint16_t *Q;       // [total_q][Hq][D]
@@ -398,23 +396,22 @@ attn_extend_kernel(const ExtParams p) {
     extern __shared__ __align__(16) uint8_t smem[];
     uint8_t *KV = smem;                                                    // [2][K, V] tiles, swizzled rows
     uint16_t *qb = reinterpret_cast<uint16_t *>(smem + 4 * kTileBytes);   // [kExtRows][kD] bf16
-    float *S = reinterpret_cast<float *>(qb + kExtRows * kD);              // [kExtRows][kSStride]
-    int64_t *rowoff = reinterpret_cast<int64_t *>(S + kExtRows * kSStride); // [2][kChunk], -1: no row
-    int *nrow = reinterpret_cast<int *>(rowoff + 2 * kChunk);             // tokens of this chunk row r sees
-    float *mc = reinterpret_cast<float *>(nrow + kExtRows);
-    float *lc = mc + kExtRows;
-    const int g = blockIdx.y;
-    const int64_t b = blockIdx.z;
+    int64_t *rowoff = reinterpret_cast<int64_t *>(qb + kExtRows * kD);     // [3][kChunk], -1: no row
+    // blockIdx.x = (tile from the last, KV head): the tiles with the latest
+    // tokens (the most chunks) start first, so the light ones fill the tail
+    const int g = static_cast<int>(blockIdx.x % static_cast<unsigned>(p.Hkv));
+    const int tile = static_cast<int>(gridDim.x / static_cast<unsigned>(p.Hkv) - 1 - blockIdx.x / p.Hkv);
+    const int64_t b = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t q0 = p.cu_q[b], q1 = p.cu_q[b + 1];
     const int L = p.lens[b];
     const int64_t qlen = q1 - q0;
     if (q0 < 0 || q1 < q0 || q1 > p.total_q || qlen > p.max_q || L < qlen || L > p.max_len ||
         L > static_cast<int64_t>(p.max_blocks) * p.bs) {
-        if (tid == 0 && blockIdx.x == 0 && g == 0) atomicOr(p.status, kDevBadOffsets);
+        if (tid == 0 && tile == 0 && g == 0) atomicOr(p.status, kDevBadOffsets);
         return;
     }
-    const int i0 = blockIdx.x * kTQ;                   // first query token of this CTA
+    const int i0 = tile * kTQ;                         // first query token of this CTA
     if (i0 >= qlen) return;
     const int ntok = static_cast<int>(qlen - i0 < kTQ ? qlen - i0 : static_cast<int64_t>(kTQ));
     const int base = L - static_cast<int>(qlen);       // position of query token 0
@@ -429,23 +426,25 @@ attn_extend_kernel(const ExtParams p) {
             v = *reinterpret_cast<const uint4 *>(p.Q + ((q0 + i0 + r / G) * p.Hq + g * G + r % G) * kD + x * 8);
         *reinterpret_cast<uint4 *>(qb + r * kD + x * 8) = v;
     }
-    auto load_chunk = [&](int c) {
-        const int j0 = c * kChunk, buf = c & 1;
-        const int nmax = min(kChunk, L_last - j0);
-        int64_t *ro = rowoff + buf * kChunk;
+    // row offsets of chunk c's K/V rows (threads 0..127; buffer c % 3, so a
+    // buffer is rewritten only after every warp has left the chunk that used it)
+    auto chunk_rows = [&](int c) {
         if (tid < kChunk) {
+            const int j = c * kChunk + tid;
             int64_t off = -1;
-            if (tid < nmax) {
-                const int j = j0 + tid;
+            if (j < L_last) {
                 const int64_t blk = p.table[b * p.max_blocks + j / p.bs];
                 if (blk >= 0 && blk < p.num_blocks)
                     off = ((blk * p.bs + j % p.bs) * p.Hkv + g) * kD;
                 else
                     atomicOr(p.status, kDevBadOffsets);
             }
-            ro[tid] = off;
+            rowoff[(c % 3) * kChunk + tid] = off;
         }
-        __syncthreads();
+    };
+    auto issue_chunk = [&](int c) {                    // after chunk_rows(c) and a barrier
+        const int buf = c & 1;
+        const int64_t *ro = rowoff + (c % 3) * kChunk;
 #pragma unroll
         for (int which = 0; which < 2; ++which) {
             const uint16_t *src = which == 0 ? p.K : p.V;
@@ -458,15 +457,29 @@ attn_extend_kernel(const ExtParams p) {
                 cp_async_16(dst0 + t * kRowBytes + ((x ^ (t & 7)) << 4), off >= 0 ? src + off + x * 8 : src,
                             off >= 0 ? 16u : 0u);
             }
-            cp_async_commit();
         }
+        cp_async_commit();
     };
-    load_chunk(0);
+    chunk_rows(0);
+    __syncthreads();                                   // q rows and chunk 0's row offsets
+    issue_chunk(0);
 
-    const int gq = lane >> 2, cq = lane & 3;              // fragment row group, column pair
-    const int rt = warp & 3;                              // this warp's 16-row tile
-    const int th = warp >> 2, dh = warp >> 2;             // its half of the chunk's tokens (scores), of the dimensions (values)
-    // running state of this thread's rows (gq: h = 0, gq + 8: h = 1) for the warp's 64 dimensions
+    const int gq = lane >> 2, cq = lane & 3;           // fragment row group, column pair
+    const int rt = warp & 3, dh = warp >> 2;           // this warp's 16-row tile and 64-dimension half
+    const int ra = rt * 16 + gq, rb = ra + 8;          // this thread's two rows
+    // the warp's q fragments (A operand of q.k) for the whole kernel
+    uint32_t qf[kD / 16][4];
+    {
+        const uint16_t *qa = qb + ra * kD + 2 * cq;
+#pragma unroll
+        for (int ks = 0; ks < kD / 16; ++ks) {
+            qf[ks][0] = *reinterpret_cast<const uint32_t *>(qa + 16 * ks);
+            qf[ks][1] = *reinterpret_cast<const uint32_t *>(qa + 8 * kD + 16 * ks);
+            qf[ks][2] = *reinterpret_cast<const uint32_t *>(qa + 16 * ks + 8);
+            qf[ks][3] = *reinterpret_cast<const uint32_t *>(qa + 8 * kD + 16 * ks + 8);
+        }
+    }
+    // running state of rows ra (h = 0) and rb (h = 1) for the warp's 64 dimensions
     float o_run[8][4], m_run[2], l_run[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -477,44 +490,42 @@ attn_extend_kernel(const ExtParams p) {
     for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) o_run[nt][e] = 0.0f;
-    __syncthreads();                                      // q rows in shared memory
-    // the warp's q fragments (A operand of q.k) for the whole kernel: rows gq and gq + 8 of tile rt
-    uint32_t qf[kD / 16][4];
-    {
-        const uint16_t *qa = qb + (rt * 16 + gq) * kD + 2 * cq;
-#pragma unroll
-        for (int ks = 0; ks < kD / 16; ++ks) {
-            qf[ks][0] = *reinterpret_cast<const uint32_t *>(qa + 16 * ks);
-            qf[ks][1] = *reinterpret_cast<const uint32_t *>(qa + 8 * kD + 16 * ks);
-            qf[ks][2] = *reinterpret_cast<const uint32_t *>(qa + 16 * ks + 8);
-            qf[ks][3] = *reinterpret_cast<const uint32_t *>(qa + 8 * kD + 16 * ks + 8);
-        }
-    }
+    // the causal length of each row: position + 1 (0 for rows past the tokens)
+    const int len_a = ra / G < ntok ? base + i0 + ra / G + 1 : 0;
+    const int len_b = rb / G < ntok ? base + i0 + rb / G + 1 : 0;
 
     for (int c = 0; c < nchunks; ++c) {
-        const int j0 = c * kChunk, buf = c & 1;
-        const int nmax = min(kChunk, L_last - j0);
-        const int64_t *ro = rowoff + buf * kChunk;
-        const uint8_t *Ks = KV + (2 * buf) * kTileBytes;
-        const uint8_t *Vs = KV + (2 * buf + 1) * kTileBytes;
+        const int j0 = c * kChunk;
+        const int64_t *ro = rowoff + (c % 3) * kChunk;
+        const uint8_t *Ks = KV + (2 * (c & 1)) * kTileBytes;
+        const uint8_t *Vs = KV + (2 * (c & 1) + 1) * kTileBytes;
         const bool more = c + 1 < nchunks;
+        if (more) chunk_rows(c + 1);
+        // every warp has left chunk c - 1 (its K/V buffer is free) and chunk
+        // c + 1's row offsets are written
+        __syncthreads();
         if (more) {
-            __syncthreads();                              // the other buffer's last readers are done
-            load_chunk(c + 1);
-            cp_async_wait<3>();                           // this chunk's K copies (of this thread)
+            issue_chunk(c + 1);
+            cp_async_wait<1>();                        // this thread's copies of chunk c
         } else {
-            cp_async_wait<1>();
+            cp_async_wait<0>();
         }
-        __syncthreads();                                  // everyone's
+        __syncthreads();                               // everyone's
 
-        // scores S[r][t] = scale * q_r . k_t: warp w takes row tile rt = w % 4 and
-        // tokens 64 (w / 4) .. +63, dimensions ascending in 16-dimension steps (its
-        // q fragments stay in registers; K fragments by ldmatrix)
+        // tokens of this chunk each row sees (decode of the sequence cut after the row's token)
+        const int na = max(0, min(kChunk, len_a - j0)), nb = max(0, min(kChunk, len_b - j0));
+        // the MMAs need the whole warp: skip only when no row of the tile sees this chunk
+        if (!__any_sync(0xffffffffu, na > 0 || nb > 0)) continue;
+
+        // scores s = scale * q . k for the tile's 16 rows and all 128 tokens
+        // (both dimension-half warps of a tile compute them), dimensions
+        // ascending in 16-dimension steps; tokens a row does not see are -inf.
+        // s[nt][e]: row ra (e < 2) or rb, token 8 nt + 2 cq + (e & 1)
+        float s[kChunk / 8][4];
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
-            const int n0 = th * 64 + nt * 8;
+        for (int nt = 0; nt < kChunk / 8; ++nt) {
             float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            const int trow = n0 + (lane & 7);                      // the K row this lane addresses
+            const int trow = nt * 8 + (lane & 7);                  // the K row this lane addresses
             const uint32_t kbase = smem_u32(Ks) + trow * kRowBytes;
 #pragma unroll
             for (int kp = 0; kp < kD / 32; ++kp) {                 // two 16-dimension steps per ldmatrix
@@ -526,100 +537,108 @@ attn_extend_kernel(const ExtParams p) {
             }
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int tt = n0 + 2 * cq + (e & 1);
-                const int r = rt * 16 + gq + 8 * (e >> 1);
-                if (tt < nmax) S[r * kSStride + tt] = ro[tt] >= 0 ? __fmul_rn(acc[e], p.scale) : -INFINITY;
+                const int t = nt * 8 + 2 * cq + (e & 1);
+                s[nt][e] = t < (e < 2 ? na : nb) ? (ro[t] >= 0 ? __fmul_rn(acc[e], p.scale) : -INFINITY)
+                                                 : -INFINITY;
             }
         }
-        __syncthreads();
-
-        // per row: the tokens it sees in this chunk, max, exponentials, sum
-        for (int r = warp; r < kExtRows; r += kExtThreads / 32) {
-            const int ti = r / G;
-            const int n = ti < ntok ? min(kChunk, base + i0 + ti + 1 - j0) : 0;
-            float *Sr = S + r * kSStride;
-            if (n > 0) {
-                float m = -INFINITY;
-                for (int t = lane; t < n; t += 32) m = fmaxf(m, Sr[t]);
+        // per row: max (any order gives the same value), then e^(s - m) for the
+        // tokens it sees (0 past them)
+        float m[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-                float l = 0.0f;
-                for (int t = lane; t < n; t += 32) {
-                    const float e = expf(Sr[t] - m);
-                    Sr[t] = e;
-                    l += e;
-                }
+        for (int nt = 0; nt < kChunk / 8; ++nt)
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-                if (lane == 0) {
-                    mc[r] = m;
-                    lc[r] = l;
-                }
-            }
-            if (lane == 0) nrow[r] = n > 0 ? n : 0;
+            for (int e = 0; e < 4; ++e) m[e >> 1] = fmaxf(m[e >> 1], s[nt][e]);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            m[h] = fmaxf(m[h], __shfl_xor_sync(0xffffffffu, m[h], 1));
+            m[h] = fmaxf(m[h], __shfl_xor_sync(0xffffffffu, m[h], 2));
         }
-        if (more) cp_async_wait<2>(); else cp_async_wait<0>();   // this chunk's V copies
-        __syncthreads();
-
-        // values: O_c[r][d] = sum_t p_t v_t[d], p = hi + lo (two bf16 MMAs per
-        // step; zero past the row's tokens); warp w takes row tile rt and
-        // dimensions 64 (w / 4) .. +63, tokens ascending in 16-token steps
-        {
-            const int ra = rt * 16 + gq, rb = ra + 8;
-            const int na = nrow[ra], nb8 = nrow[rb];
-            // skip only when none of the tile's rows sees this chunk (the MMAs need the whole warp)
-            if (__any_sync(0xffffffffu, na != 0 || nb8 != 0)) {
-                const int mi = lane >> 3, mr = lane & 7;          // ldmatrix: matrix, row
-                float acc[8][4];
 #pragma unroll
-                for (int nt = 0; nt < 8; ++nt)
+        for (int nt = 0; nt < kChunk / 8; ++nt)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) acc[nt][e] = 0.0f;
-                const float *Sa = S + ra * kSStride, *Sb = S + rb * kSStride;
-#pragma unroll 2
-                for (int ks = 0; ks < kChunk / 16; ++ks) {
-                    const int k0 = ks * 16;
-                    const int t0 = k0 + 2 * cq, t2 = t0 + 8;
-                    uint32_t ph0, pl0, ph1, pl1, ph2, pl2, ph3, pl3;
-                    split_bf16x2(t0 < na ? Sa[t0] : 0.0f, t0 + 1 < na ? Sa[t0 + 1] : 0.0f, ph0, pl0);
-                    split_bf16x2(t0 < nb8 ? Sb[t0] : 0.0f, t0 + 1 < nb8 ? Sb[t0 + 1] : 0.0f, ph1, pl1);
-                    split_bf16x2(t2 < na ? Sa[t2] : 0.0f, t2 + 1 < na ? Sa[t2 + 1] : 0.0f, ph2, pl2);
-                    split_bf16x2(t2 < nb8 ? Sb[t2] : 0.0f, t2 + 1 < nb8 ? Sb[t2 + 1] : 0.0f, ph3, pl3);
-                    const int tok = k0 + (mi & 1) * 8 + mr;
-#pragma unroll
-                    for (int np = 0; np < 4; ++np) {              // two 8-dimension tiles per ldmatrix
-                        const int chunk = ((dh * 64 + np * 16) >> 3) + (mi >> 1);
-                        uint32_t v0, v1, v2, v3;
-                        ldmatrix_x4_trans(v0, v1, v2, v3, smem_u32(Vs + tok * kRowBytes + ((chunk ^ (tok & 7)) << 4)));
-                        mma_16816(acc[2 * np], ph0, ph1, ph2, ph3, v0, v1);
-                        mma_16816(acc[2 * np], pl0, pl1, pl2, pl3, v0, v1);
-                        mma_16816(acc[2 * np + 1], ph0, ph1, ph2, ph3, v2, v3);
-                        mma_16816(acc[2 * np + 1], pl0, pl1, pl2, pl3, v2, v3);
-                    }
-                }
-                // merge this chunk into the rows' running state, in chunk order
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int r = h ? rb : ra;
-                    if ((h ? nb8 : na) == 0) continue;
-                    float mn, al, be;
-                    merge_factors(m_run[h], mc[r], mn, al, be);
-                    m_run[h] = mn;
-                    l_run[h] = merge_value(l_run[h], lc[r], al, be);
-#pragma unroll
-                    for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-                        for (int e = 0; e < 2; ++e)
-                            o_run[nt][2 * h + e] = merge_value(o_run[nt][2 * h + e], acc[nt][2 * h + e], al, be);
-                }
+            for (int e = 0; e < 4; ++e) {
+                const int t = nt * 8 + 2 * cq + (e & 1);
+                s[nt][e] = t < (e < 2 ? na : nb) ? expf(s[nt][e] - m[e >> 1]) : 0.0f;
             }
+        // per row: the sum in decode's order. Lane L of decode sums tokens
+        // L, L + 32, L + 64, L + 96 in turn, then a butterfly over lanes xor
+        // 16, 8, 4, 2, 1. Here L = 8 (nt % 4) + 2 cq + (e & 1): the column
+        // steps (nt + 4k) and the butterfly steps 16 and 8 (nt ^ 2, nt ^ 1) and
+        // 1 (e ^ 1) are in this thread; steps 4 and 2 are lanes xor 2 and 1.
+        // Each butterfly step adds two equal-rank partials, and a + b = b + a,
+        // so every lane's total is the same bits as decode's.
+        float l[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float x[2];
+#pragma unroll
+            for (int e0 = 0; e0 < 2; ++e0) {
+                float col[4];
+#pragma unroll
+                for (int n4 = 0; n4 < 4; ++n4) {
+                    float acc = s[n4][2 * h + e0];
+#pragma unroll
+                    for (int k = 1; k < 4; ++k) acc += s[n4 + 4 * k][2 * h + e0];
+                    col[n4] = acc;
+                }
+                const float u0 = col[0] + col[2], u1 = col[1] + col[3];   // step 16
+                float v = u0 + u1;                                        // step 8
+                v += __shfl_xor_sync(0xffffffffu, v, 2);                  // step 4
+                v += __shfl_xor_sync(0xffffffffu, v, 1);                  // step 2
+                x[e0] = v;
+            }
+            l[h] = x[0] + x[1];                                           // step 1
+        }
+
+        // values: O_c = sum_t p_t v_t for the warp's 64 dimensions, p = hi + lo
+        // (two bf16 MMAs per step), tokens ascending in 16-token steps; the
+        // exponentials are already in the A-fragment layout
+        float acc[8][4];
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[nt][e] = 0.0f;
+        const int mi = lane >> 3, mr = lane & 7;       // ldmatrix: matrix, row
+#pragma unroll
+        for (int ks = 0; ks < kChunk / 16; ++ks) {
+            uint32_t ph0, pl0, ph1, pl1, ph2, pl2, ph3, pl3;
+            split_bf16x2(s[2 * ks][0], s[2 * ks][1], ph0, pl0);
+            split_bf16x2(s[2 * ks][2], s[2 * ks][3], ph1, pl1);
+            split_bf16x2(s[2 * ks + 1][0], s[2 * ks + 1][1], ph2, pl2);
+            split_bf16x2(s[2 * ks + 1][2], s[2 * ks + 1][3], ph3, pl3);
+            const int tok = ks * 16 + (mi & 1) * 8 + mr;
+#pragma unroll
+            for (int np = 0; np < 4; ++np) {           // two 8-dimension tiles per ldmatrix
+                const int chunk = ((dh * 64 + np * 16) >> 3) + (mi >> 1);
+                uint32_t v0, v1, v2, v3;
+                ldmatrix_x4_trans(v0, v1, v2, v3, smem_u32(Vs + tok * kRowBytes + ((chunk ^ (tok & 7)) << 4)));
+                mma_16816(acc[2 * np], ph0, ph1, ph2, ph3, v0, v1);
+                mma_16816(acc[2 * np], pl0, pl1, pl2, pl3, v0, v1);
+                mma_16816(acc[2 * np + 1], ph0, ph1, ph2, ph3, v2, v3);
+                mma_16816(acc[2 * np + 1], pl0, pl1, pl2, pl3, v2, v3);
+            }
+        }
+        // merge this chunk into the rows' running state, in chunk order
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            if ((h ? nb : na) == 0) continue;
+            float mn, al, be;
+            merge_factors(m_run[h], m[h], mn, al, be);
+            m_run[h] = mn;
+            l_run[h] = merge_value(l_run[h], l[h], al, be);
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e)
+                    o_run[nt][2 * h + e] = merge_value(o_run[nt][2 * h + e], acc[nt][2 * h + e], al, be);
         }
     }
 
     // o / l, rounded to bf16, for the rows that exist
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-        const int r = rt * 16 + gq + 8 * h;
+        const int r = h ? rb : ra;
         if (r / G >= ntok || !BI_IN_BOUNDS(q0 + i0 + r / G < p.total_q, p.status)) continue;
         uint16_t *orow = p.O + ((q0 + i0 + r / G) * p.Hq + g * G + r % G) * kD + dh * 64 + 2 * cq;
 #pragma unroll
@@ -718,7 +737,9 @@ bi_status launch_attention_extend(const void *Q, const int32_t *cu_q, int32_t to
     p.status = device_status_word();
     const int G = Hq / Hkv;
     const int tq = kExtRows / G;
-    const dim3 grid((max_q + tq - 1) / tq, Hkv, static_cast<unsigned>(B));
+    const int64_t ctas_x = (static_cast<int64_t>(max_q) + tq - 1) / tq * Hkv;   // (tile, KV head)
+    if (ctas_x > 0x7fffffff) return BI_ERR_UNSUPPORTED;
+    const dim3 grid(static_cast<unsigned>(ctas_x), static_cast<unsigned>(B));
     switch (G) {
         case 1: return launch_extend_g<1>(grid, p, s);
         case 2: return launch_extend_g<2>(grid, p, s);
