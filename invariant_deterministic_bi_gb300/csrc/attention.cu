@@ -428,19 +428,23 @@ attn_extend_kernel(const ExtParams p) {
     }
     // row offsets of chunk c's K/V rows (threads 0..127; buffer c % 3, so a
     // buffer is rewritten only after every warp has left the chunk that used it)
-    auto chunk_rows = [&](int c) {
+    auto chunk_rows = [&](int c) -> int {
+        int bad = 0;
         if (tid < kChunk) {
             const int j = c * kChunk + tid;
             int64_t off = -1;
             if (j < L_last) {
                 const int64_t blk = p.table[b * p.max_blocks + j / p.bs];
-                if (blk >= 0 && blk < p.num_blocks)
+                if (blk >= 0 && blk < p.num_blocks) {
                     off = ((blk * p.bs + j % p.bs) * p.Hkv + g) * kD;
-                else
+                } else {
                     atomicOr(p.status, kDevBadOffsets);
+                    bad = 1;
+                }
             }
             rowoff[(c % 3) * kChunk + tid] = off;
         }
+        return bad;
     };
     auto issue_chunk = [&](int c) {                    // after chunk_rows(c) and a barrier
         const int buf = c & 1;
@@ -460,8 +464,8 @@ attn_extend_kernel(const ExtParams p) {
         }
         cp_async_commit();
     };
-    chunk_rows(0);
-    __syncthreads();                                   // q rows and chunk 0's row offsets
+    // q rows and chunk 0's row offsets; bad_cur: chunk c has a token without a valid block
+    int bad_cur = __syncthreads_or(chunk_rows(0));
     issue_chunk(0);
 
     const int gq = lane >> 2, cq = lane & 3;           // fragment row group, column pair
@@ -500,10 +504,11 @@ attn_extend_kernel(const ExtParams p) {
         const uint8_t *Ks = KV + (2 * (c & 1)) * kTileBytes;
         const uint8_t *Vs = KV + (2 * (c & 1) + 1) * kTileBytes;
         const bool more = c + 1 < nchunks;
-        if (more) chunk_rows(c + 1);
         // every warp has left chunk c - 1 (its K/V buffer is free) and chunk
         // c + 1's row offsets are written
-        __syncthreads();
+        const int bad_next = __syncthreads_or(more ? chunk_rows(c + 1) : 0);
+        const bool bad = bad_cur != 0;
+        bad_cur = bad_next;
         if (more) {
             issue_chunk(c + 1);
             cp_async_wait<1>();                        // this thread's copies of chunk c
@@ -521,46 +526,69 @@ attn_extend_kernel(const ExtParams p) {
         // (both dimension-half warps of a tile compute them), dimensions
         // ascending in 16-dimension steps; tokens a row does not see are -inf.
         // s[nt][e]: row ra (e < 2) or rb, token 8 nt + 2 cq + (e & 1)
+        // The 16 n-tiles' MMA chains are interleaved (dimension step outer),
+        // each chain still in ascending dimension order.
         float s[kChunk / 8][4];
-#pragma unroll
-        for (int nt = 0; nt < kChunk / 8; ++nt) {
-            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            const int trow = nt * 8 + (lane & 7);                  // the K row this lane addresses
-            const uint32_t kbase = smem_u32(Ks) + trow * kRowBytes;
-#pragma unroll
-            for (int kp = 0; kp < kD / 32; ++kp) {                 // two 16-dimension steps per ldmatrix
-                const int chunk = 4 * kp + (lane >> 3);            // 16-byte chunk of matrix lane/8
-                uint32_t b0, b1, b2, b3;
-                ldmatrix_x4(b0, b1, b2, b3, kbase + ((chunk ^ (trow & 7)) << 4));
-                mma_16816(acc, qf[2 * kp][0], qf[2 * kp][1], qf[2 * kp][2], qf[2 * kp][3], b0, b1);
-                mma_16816(acc, qf[2 * kp + 1][0], qf[2 * kp + 1][1], qf[2 * kp + 1][2], qf[2 * kp + 1][3], b2, b3);
-            }
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int t = nt * 8 + 2 * cq + (e & 1);
-                s[nt][e] = t < (e < 2 ? na : nb) ? (ro[t] >= 0 ? __fmul_rn(acc[e], p.scale) : -INFINITY)
-                                                 : -INFINITY;
-            }
-        }
-        // per row: max (any order gives the same value), then e^(s - m) for the
-        // tokens it sees (0 past them)
-        float m[2] = {-INFINITY, -INFINITY};
 #pragma unroll
         for (int nt = 0; nt < kChunk / 8; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) m[e >> 1] = fmaxf(m[e >> 1], s[nt][e]);
+            for (int e = 0; e < 4; ++e) s[nt][e] = 0.0f;
+#pragma unroll
+        for (int kp = 0; kp < kD / 32; ++kp) {                     // two 16-dimension steps per ldmatrix
+#pragma unroll
+            for (int nt = 0; nt < kChunk / 8; ++nt) {
+                const int trow = nt * 8 + (lane & 7);              // the K row this lane addresses
+                const int chunk = 4 * kp + (lane >> 3);            // 16-byte chunk of matrix lane/8
+                uint32_t b0, b1, b2, b3;
+                ldmatrix_x4(b0, b1, b2, b3, smem_u32(Ks) + trow * kRowBytes + ((chunk ^ (trow & 7)) << 4));
+                mma_16816(s[nt], qf[2 * kp][0], qf[2 * kp][1], qf[2 * kp][2], qf[2 * kp][3], b0, b1);
+                mma_16816(s[nt], qf[2 * kp + 1][0], qf[2 * kp + 1][1], qf[2 * kp + 1][2], qf[2 * kp + 1][3], b2, b3);
+            }
+        }
+        // a chunk every row of the tile sees whole, with every block valid,
+        // needs no masks
+        const bool whole = !bad && __all_sync(0xffffffffu, na == kChunk && nb == kChunk);
+        float m[2] = {-INFINITY, -INFINITY};
+        if (whole) {
+#pragma unroll
+            for (int nt = 0; nt < kChunk / 8; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    s[nt][e] = __fmul_rn(s[nt][e], p.scale);
+                    m[e >> 1] = fmaxf(m[e >> 1], s[nt][e]);
+                }
+        } else {
+#pragma unroll
+            for (int nt = 0; nt < kChunk / 8; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int t = nt * 8 + 2 * cq + (e & 1);
+                    s[nt][e] = t < (e < 2 ? na : nb) ? (ro[t] >= 0 ? __fmul_rn(s[nt][e], p.scale) : -INFINITY)
+                                                     : -INFINITY;
+                    m[e >> 1] = fmaxf(m[e >> 1], s[nt][e]);
+                }
+        }
+        // per row: max (any order gives the same value), then e^(s - m) for the
+        // tokens it sees (0 past them)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             m[h] = fmaxf(m[h], __shfl_xor_sync(0xffffffffu, m[h], 1));
             m[h] = fmaxf(m[h], __shfl_xor_sync(0xffffffffu, m[h], 2));
         }
+        if (whole) {
 #pragma unroll
-        for (int nt = 0; nt < kChunk / 8; ++nt)
+            for (int nt = 0; nt < kChunk / 8; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int t = nt * 8 + 2 * cq + (e & 1);
-                s[nt][e] = t < (e < 2 ? na : nb) ? expf(s[nt][e] - m[e >> 1]) : 0.0f;
-            }
+                for (int e = 0; e < 4; ++e) s[nt][e] = expf(s[nt][e] - m[e >> 1]);
+        } else {
+#pragma unroll
+            for (int nt = 0; nt < kChunk / 8; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int t = nt * 8 + 2 * cq + (e & 1);
+                    s[nt][e] = t < (e < 2 ? na : nb) ? expf(s[nt][e] - m[e >> 1]) : 0.0f;
+                }
+        }
         // per row: the sum in decode's order. Lane L of decode sums tokens
         // L, L + 32, L + 64, L + 96 in turn, then a butterfly over lanes xor
         // 16, 8, 4, 2, 1. Here L = 8 (nt % 4) + 2 cq + (e & 1): the column
@@ -608,15 +636,23 @@ attn_extend_kernel(const ExtParams p) {
             split_bf16x2(s[2 * ks + 1][0], s[2 * ks + 1][1], ph2, pl2);
             split_bf16x2(s[2 * ks + 1][2], s[2 * ks + 1][3], ph3, pl3);
             const int tok = ks * 16 + (mi & 1) * 8 + mr;
+            uint32_t v[4][4];
 #pragma unroll
             for (int np = 0; np < 4; ++np) {           // two 8-dimension tiles per ldmatrix
                 const int chunk = ((dh * 64 + np * 16) >> 3) + (mi >> 1);
-                uint32_t v0, v1, v2, v3;
-                ldmatrix_x4_trans(v0, v1, v2, v3, smem_u32(Vs + tok * kRowBytes + ((chunk ^ (tok & 7)) << 4)));
-                mma_16816(acc[2 * np], ph0, ph1, ph2, ph3, v0, v1);
-                mma_16816(acc[2 * np], pl0, pl1, pl2, pl3, v0, v1);
-                mma_16816(acc[2 * np + 1], ph0, ph1, ph2, ph3, v2, v3);
-                mma_16816(acc[2 * np + 1], pl0, pl1, pl2, pl3, v2, v3);
+                ldmatrix_x4_trans(v[np][0], v[np][1], v[np][2], v[np][3],
+                                  smem_u32(Vs + tok * kRowBytes + ((chunk ^ (tok & 7)) << 4)));
+            }
+            // each accumulator takes hi, then lo (the chains interleaved)
+#pragma unroll
+            for (int np = 0; np < 4; ++np) {
+                mma_16816(acc[2 * np], ph0, ph1, ph2, ph3, v[np][0], v[np][1]);
+                mma_16816(acc[2 * np + 1], ph0, ph1, ph2, ph3, v[np][2], v[np][3]);
+            }
+#pragma unroll
+            for (int np = 0; np < 4; ++np) {
+                mma_16816(acc[2 * np], pl0, pl1, pl2, pl3, v[np][0], v[np][1]);
+                mma_16816(acc[2 * np + 1], pl0, pl1, pl2, pl3, v[np][2], v[np][3]);
             }
         }
         // merge this chunk into the rows' running state, in chunk order
