@@ -367,7 +367,7 @@ attn_combine_kernel(const AttnParams p) {
 
 // ------------------------------------------------------------------ extend
 
-constexpr int kExtRows = 64;                   // query rows (token, head) per CTA: four m16 tiles
+constexpr int kExtRows = 128;                  // query rows (token, head) per CTA: one m16 tile per warp
 constexpr int kExtThreads = 256;
 // K and V tiles twice (the next chunk loads while this one is used), q rows,
 // the K/V row offsets of three chunks.
@@ -418,13 +418,14 @@ attn_extend_kernel(const ExtParams p) {
     const int L_last = base + i0 + ntok;               // the last token's causal length
     const int nchunks = (L_last + kChunk - 1) / kChunk;
 
-    // q rows: row r = token r / G, head g*G + r % G (zero rows past the tokens)
+    // q rows: row r = token r / G, head g*G + r % G (zero rows past the
+    // tokens); 16-byte piece x of row r at piece x ^ (r % 8)
     for (int i = tid; i < kExtRows * kD / 8; i += kExtThreads) {
         const int r = i / (kD / 8), x = i % (kD / 8);
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (r / G < ntok)
             v = *reinterpret_cast<const uint4 *>(p.Q + ((q0 + i0 + r / G) * p.Hq + g * G + r % G) * kD + x * 8);
-        *reinterpret_cast<uint4 *>(qb + r * kD + x * 8) = v;
+        *reinterpret_cast<uint4 *>(qb + r * kD + ((x ^ (r & 7)) * 8)) = v;
     }
     // row offsets of chunk c's K/V rows (threads 0..127; buffer c % 3, so a
     // buffer is rewritten only after every warp has left the chunk that used it)
@@ -469,29 +470,22 @@ attn_extend_kernel(const ExtParams p) {
     issue_chunk(0);
 
     const int gq = lane >> 2, cq = lane & 3;           // fragment row group, column pair
-    const int rt = warp & 3, dh = warp >> 2;           // this warp's 16-row tile and 64-dimension half
+    const int rt = warp;                               // this warp's 16-row tile
     const int ra = rt * 16 + gq, rb = ra + 8;          // this thread's two rows
-    // the warp's q fragments (A operand of q.k) for the whole kernel
-    uint32_t qf[kD / 16][4];
-    {
-        const uint16_t *qa = qb + ra * kD + 2 * cq;
-#pragma unroll
-        for (int ks = 0; ks < kD / 16; ++ks) {
-            qf[ks][0] = *reinterpret_cast<const uint32_t *>(qa + 16 * ks);
-            qf[ks][1] = *reinterpret_cast<const uint32_t *>(qa + 8 * kD + 16 * ks);
-            qf[ks][2] = *reinterpret_cast<const uint32_t *>(qa + 16 * ks + 8);
-            qf[ks][3] = *reinterpret_cast<const uint32_t *>(qa + 8 * kD + 16 * ks + 8);
-        }
-    }
-    // running state of rows ra (h = 0) and rb (h = 1) for the warp's 64 dimensions
-    float o_run[8][4], m_run[2], l_run[2];
+    // the warp's q fragments (A operand of q.k) come from shared memory by
+    // ldmatrix: lane l addresses row (l / 8 % 2) * 8 + l % 8 of the tile,
+    // 16-byte piece 2 ks + l / 16
+    const int qrow = rt * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+    const uint32_t qaddr = smem_u32(qb) + qrow * kRowBytes;
+    // running state of rows ra (h = 0) and rb (h = 1), all 128 dimensions
+    float o_run[kD / 8][4], m_run[2], l_run[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         m_run[h] = -INFINITY;
         l_run[h] = 0.0f;
     }
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
+    for (int nt = 0; nt < kD / 8; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) o_run[nt][e] = 0.0f;
     // the causal length of each row: position + 1 (0 for rows past the tokens)
@@ -522,8 +516,8 @@ attn_extend_kernel(const ExtParams p) {
         // the MMAs need the whole warp: skip only when no row of the tile sees this chunk
         if (!__any_sync(0xffffffffu, na > 0 || nb > 0)) continue;
 
-        // scores s = scale * q . k for the tile's 16 rows and all 128 tokens
-        // (both dimension-half warps of a tile compute them), dimensions
+        // scores s = scale * q . k for the tile's 16 rows and all 128 tokens,
+        // dimensions
         // ascending in 16-dimension steps; tokens a row does not see are -inf.
         // s[nt][e]: row ra (e < 2) or rb, token 8 nt + 2 cq + (e & 1)
         // The 16 n-tiles' MMA chains are interleaved (dimension step outer),
@@ -535,14 +529,20 @@ attn_extend_kernel(const ExtParams p) {
             for (int e = 0; e < 4; ++e) s[nt][e] = 0.0f;
 #pragma unroll
         for (int kp = 0; kp < kD / 32; ++kp) {                     // two 16-dimension steps per ldmatrix
+            uint32_t qf[2][4];
+#pragma unroll
+            for (int k2 = 0; k2 < 2; ++k2) {
+                const int piece = 2 * (2 * kp + k2) + (lane >> 4);
+                ldmatrix_x4(qf[k2][0], qf[k2][1], qf[k2][2], qf[k2][3], qaddr + ((piece ^ (qrow & 7)) << 4));
+            }
 #pragma unroll
             for (int nt = 0; nt < kChunk / 8; ++nt) {
                 const int trow = nt * 8 + (lane & 7);              // the K row this lane addresses
                 const int chunk = 4 * kp + (lane >> 3);            // 16-byte chunk of matrix lane/8
                 uint32_t b0, b1, b2, b3;
                 ldmatrix_x4(b0, b1, b2, b3, smem_u32(Ks) + trow * kRowBytes + ((chunk ^ (trow & 7)) << 4));
-                mma_16816(s[nt], qf[2 * kp][0], qf[2 * kp][1], qf[2 * kp][2], qf[2 * kp][3], b0, b1);
-                mma_16816(s[nt], qf[2 * kp + 1][0], qf[2 * kp + 1][1], qf[2 * kp + 1][2], qf[2 * kp + 1][3], b2, b3);
+                mma_16816(s[nt], qf[0][0], qf[0][1], qf[0][2], qf[0][3], b0, b1);
+                mma_16816(s[nt], qf[1][0], qf[1][1], qf[1][2], qf[1][3], b2, b3);
             }
         }
         // a chunk every row of the tile sees whole, with every block valid,
@@ -619,12 +619,12 @@ attn_extend_kernel(const ExtParams p) {
             l[h] = x[0] + x[1];                                           // step 1
         }
 
-        // values: O_c = sum_t p_t v_t for the warp's 64 dimensions, p = hi + lo
+        // values: O_c = sum_t p_t v_t for all 128 dimensions, p = hi + lo
         // (two bf16 MMAs per step), tokens ascending in 16-token steps; the
         // exponentials are already in the A-fragment layout
-        float acc[8][4];
+        float acc[kD / 8][4];
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
+        for (int nt = 0; nt < kD / 8; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[nt][e] = 0.0f;
         const int mi = lane >> 3, mr = lane & 7;       // ldmatrix: matrix, row
@@ -636,23 +636,29 @@ attn_extend_kernel(const ExtParams p) {
             split_bf16x2(s[2 * ks + 1][0], s[2 * ks + 1][1], ph2, pl2);
             split_bf16x2(s[2 * ks + 1][2], s[2 * ks + 1][3], ph3, pl3);
             const int tok = ks * 16 + (mi & 1) * 8 + mr;
-            uint32_t v[4][4];
+            // dimensions in two halves of 64 (four ldmatrix each); each
+            // accumulator takes hi, then lo (the chains interleaved)
 #pragma unroll
-            for (int np = 0; np < 4; ++np) {           // two 8-dimension tiles per ldmatrix
-                const int chunk = ((dh * 64 + np * 16) >> 3) + (mi >> 1);
-                ldmatrix_x4_trans(v[np][0], v[np][1], v[np][2], v[np][3],
-                                  smem_u32(Vs + tok * kRowBytes + ((chunk ^ (tok & 7)) << 4)));
-            }
-            // each accumulator takes hi, then lo (the chains interleaved)
+            for (int half = 0; half < 2; ++half) {
+                uint32_t v[4][4];
 #pragma unroll
-            for (int np = 0; np < 4; ++np) {
-                mma_16816(acc[2 * np], ph0, ph1, ph2, ph3, v[np][0], v[np][1]);
-                mma_16816(acc[2 * np + 1], ph0, ph1, ph2, ph3, v[np][2], v[np][3]);
-            }
+                for (int q4 = 0; q4 < 4; ++q4) {       // two 8-dimension tiles per ldmatrix
+                    const int chunk = 2 * (4 * half + q4) + (mi >> 1);
+                    ldmatrix_x4_trans(v[q4][0], v[q4][1], v[q4][2], v[q4][3],
+                                      smem_u32(Vs + tok * kRowBytes + ((chunk ^ (tok & 7)) << 4)));
+                }
 #pragma unroll
-            for (int np = 0; np < 4; ++np) {
-                mma_16816(acc[2 * np], pl0, pl1, pl2, pl3, v[np][0], v[np][1]);
-                mma_16816(acc[2 * np + 1], pl0, pl1, pl2, pl3, v[np][2], v[np][3]);
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const int np = 4 * half + q4;
+                    mma_16816(acc[2 * np], ph0, ph1, ph2, ph3, v[q4][0], v[q4][1]);
+                    mma_16816(acc[2 * np + 1], ph0, ph1, ph2, ph3, v[q4][2], v[q4][3]);
+                }
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const int np = 4 * half + q4;
+                    mma_16816(acc[2 * np], pl0, pl1, pl2, pl3, v[q4][0], v[q4][1]);
+                    mma_16816(acc[2 * np + 1], pl0, pl1, pl2, pl3, v[q4][2], v[q4][3]);
+                }
             }
         }
         // merge this chunk into the rows' running state, in chunk order
@@ -664,7 +670,7 @@ attn_extend_kernel(const ExtParams p) {
             m_run[h] = mn;
             l_run[h] = merge_value(l_run[h], l[h], al, be);
 #pragma unroll
-            for (int nt = 0; nt < 8; ++nt)
+            for (int nt = 0; nt < kD / 8; ++nt)
 #pragma unroll
                 for (int e = 0; e < 2; ++e)
                     o_run[nt][2 * h + e] = merge_value(o_run[nt][2 * h + e], acc[nt][2 * h + e], al, be);
@@ -676,9 +682,9 @@ attn_extend_kernel(const ExtParams p) {
     for (int h = 0; h < 2; ++h) {
         const int r = h ? rb : ra;
         if (r / G >= ntok || !BI_IN_BOUNDS(q0 + i0 + r / G < p.total_q, p.status)) continue;
-        uint16_t *orow = p.O + ((q0 + i0 + r / G) * p.Hq + g * G + r % G) * kD + dh * 64 + 2 * cq;
+        uint16_t *orow = p.O + ((q0 + i0 + r / G) * p.Hq + g * G + r % G) * kD + 2 * cq;
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
+        for (int nt = 0; nt < kD / 8; ++nt) {
             const float x0 = __fdiv_rn(o_run[nt][2 * h], l_run[h]);
             const float x1 = __fdiv_rn(o_run[nt][2 * h + 1], l_run[h]);
             *reinterpret_cast<uint32_t *>(orow + nt * 8) = pack_bf16x2(__float_as_uint(x0), __float_as_uint(x1));
