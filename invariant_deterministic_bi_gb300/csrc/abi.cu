@@ -119,6 +119,19 @@ bi_status make_tmap_3d(CUtensorMap *map, CUtensorMapDataType dtype, const void *
     return r == CUDA_SUCCESS ? BI_OK : BI_ERR_CUDA;
 }
 
+bi_status make_tmap_4d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, const uint64_t dims[4],
+                       const uint64_t strides_bytes[3], const uint32_t box[4], CUtensorMapSwizzle swizzle) {
+    auto enc = encoder();
+    if (!enc) return BI_ERR_CUDA;
+    const cuuint64_t d[4] = {dims[0], dims[1], dims[2], dims[3]};
+    const cuuint64_t s[3] = {strides_bytes[0], strides_bytes[1], strides_bytes[2]};
+    const cuuint32_t b[4] = {box[0], box[1], box[2], box[3]};
+    const cuuint32_t e[4] = {1, 1, 1, 1};
+    CUresult r = enc(map, dtype, 4, const_cast<void *>(base), d, s, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? BI_OK : BI_ERR_CUDA;
+}
+
 }  // namespace bi
 
 using namespace bi;

@@ -63,12 +63,6 @@ constexpr int kCombineThreads = 128;           // one thread per output dimensio
 constexpr int kRowBytes = kD * 2;              // one token's K (or V) row of one KV head
 constexpr int kTileBytes = kChunk * kRowBytes; // 32 KB
 
-// K and V tiles, then q (G x kD fp32 of space, bf16 used), scores
-// (G x kChunk fp32) and the K/V row offset of every token of the chunk.
-template <int G>
-constexpr int split_smem_bytes() {
-    return 2 * kTileBytes + (G * kD + G * kChunk) * 4 + kChunk * 8;
-}
 
 // 16-byte global -> shared copy; src_bytes = 0 writes 16 zero bytes and reads nothing.
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes) {
@@ -129,8 +123,9 @@ struct AttnParams {
     const int32_t *lens;     // [B]
     float *ws;               // [B][Hq][chunks][kD + 2]
     uint16_t *O;             // [B][Hq][D]
-    int64_t num_blocks;
+    int64_t num_blocks, batch;
     int32_t max_blocks, Hq, Hkv, bs, chunks, max_len;
+    int32_t box_rows;        // tokens per TMA box of the decode loader; 0: per-row copies
     float scale;
     unsigned *status;
 };
@@ -140,161 +135,368 @@ __device__ __forceinline__ bool seq_ok(const AttnParams &p, int64_t b, int &L) {
     return L >= 1 && L <= p.max_len && L <= static_cast<int64_t>(p.max_blocks) * p.bs;
 }
 
+// Step 1 runs persistently: one CTA per SM walks the (sequence, KV head,
+// chunk) items blockIdx.x, blockIdx.x + gridDim.x, ... (which CTA computes an
+// item changes no arithmetic). A loading warp keeps up to kSlots chunks in
+// flight: per item it resolves the chunk's block-table entries and loads the
+// chunk's K and V rows of KV head g with TMA, one box per cache block (a 4-D
+// tensor map over [blocks][block size][KV heads][128], two 64-dimension
+// halves per box, 128-byte swizzle), plus the G q rows by a bulk copy, all
+// counted on the slot's "full" barrier. Block sizes that boxes cannot tile
+// (not a multiple of 128 and not 8, 16, 32 or 64) take 16-byte cp.async
+// copies per row instead. Blocks outside the cache arrive as zeros and their
+// tokens score -inf. Eight consumer warps compute the chunk and hand the slot
+// back through its "empty" barrier.
+constexpr int kHalfTile = kChunk * 128;                  // one 64-dimension half of a K or V tile (swizzled)
+constexpr int kSlots = 3;
+constexpr int kSlotBytes = 4 * kHalfTile + 8 * kRowBytes; // K, V, up to 8 q rows
+constexpr int kDecConsumers = kThreads / 32;             // 8 warps: two groups of four
+constexpr int NG = 2;                                    // consumer groups (items in compute at once)
+constexpr int kLoaders = 2;                              // loading warps: warp kDecConsumers + i loads items i, i + 2, ...
+constexpr int kDecThreads = kThreads + 32 * kLoaders;
+constexpr int kDecSStride = kChunk + 8;                 // scores of one head (padded)
+constexpr int kDecSFloats = 8 * kDecSStride;             // one score buffer: up to 8 heads
+constexpr int kDecSmem = 1024 + kSlots * kSlotBytes + 4 * kDecSFloats * 4 + kSlots * kChunk + 2 * kSlots * 8 + 16;
+static_assert(kSlotBytes % 1024 == 0, "slot alignment (128-byte swizzle atoms)");
+
+// Byte offset of 16-byte piece x (0..15) of token row t in a swizzled K or V tile.
+__device__ __forceinline__ int kv_piece(int t, int x) {
+    return (x >> 3) * kHalfTile + t * 128 + (((x & 7) ^ (t & 7)) << 4);
+}
+
+// bar.sync on the named barrier (1 + grp) of consumer group grp's GW warps
+template <int GW>
+__device__ __forceinline__ void group_sync(int grp) {
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "n"(32 * GW) : "memory");
+}
+// the same barrier with an OR vote over the group's threads
+template <int GW>
+__device__ __forceinline__ bool group_sync_or(int grp, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(1 + grp), "n"(32 * GW)
+        : "memory");
+    return r != 0;
+}
+
 template <int G>
-__global__ void __launch_bounds__(kThreads)
-attn_split_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(kDecThreads, 1)
+attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                  const AttnParams p) {
     grid_dep_wait();      // earlier work of the stream is complete and visible
     grid_dep_launch();
-    extern __shared__ __align__(16) uint8_t smem[];
-    uint8_t *Ks = smem;                                            // [kChunk][kD] bf16, 16-byte chunks swizzled
-    uint8_t *Vs = smem + kTileBytes;                               // [kChunk][kD] bf16, the same swizzle
-    float *qs = reinterpret_cast<float *>(smem + 2 * kTileBytes);  // [G][kD] bf16 (first half used)
-    uint16_t *qb = reinterpret_cast<uint16_t *>(qs);
-    float *S = qs + G * kD;                                        // [kChunk][G]
-    int64_t *rowoff = reinterpret_cast<int64_t *>(S + G * kChunk); // [kChunk], -1: no row
-    const int c = blockIdx.x, g = blockIdx.y;
-    const int64_t b = blockIdx.z;
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    float *S0 = reinterpret_cast<float *>(smem + kSlots * kSlotBytes);     // [group][2][G][kDecSStride] scores
+    uint8_t *valid = reinterpret_cast<uint8_t *>(S0 + 4 * kDecSFloats);     // [kSlots][kChunk]: row has K/V
+    uint64_t *full = reinterpret_cast<uint64_t *>(valid + kSlots * kChunk);
+    uint64_t *empty = full + kSlots;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + kSlots);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    int L;
-    if (!seq_ok(p, b, L)) {
-        if (tid == 0 && c == 0 && g == 0) atomicOr(p.status, kDevBadOffsets);
-        return;
-    }
-    const int j0 = c * kChunk;
-    if (j0 >= L) return;                                  // this sequence has fewer chunks
-    if (!BI_IN_BOUNDS(c < p.chunks && b < gridDim.z, p.status)) return;   // debug build: inside the workspace
-    const int n = min(kChunk, L - j0);
-
-    // element offset of each token's K (and V) row for KV head g
-    if (tid < kChunk) {
-        int64_t off = -1;
-        if (tid < n) {
-            const int j = j0 + tid;
-            const int64_t blk = p.table[b * p.max_blocks + j / p.bs];
-            if (blk >= 0 && blk < p.num_blocks)
-                off = ((blk * p.bs + j % p.bs) * p.Hkv + g) * kD;
-            else
-                atomicOr(p.status, kDevBadOffsets);
+    if (tid == 0) {
+        for (int s = 0; s < kSlots; ++s) {
+            mbar_init(&full[s], p.box_rows > 0 ? 32 : 64);
+            mbar_init(&empty[s], kDecConsumers / NG);
         }
-        rowoff[tid] = off;
+        *abort_flag = 0;
+        fence_mbar_init();
     }
-    for (int i = tid; i < G * kD; i += kThreads) qb[i] = p.Q[(b * p.Hq + g * G) * kD + i];
     __syncthreads();
-
-    // K rows, then V rows (16-byte chunk x of row t at chunk x ^ (t % 8));
-    // missing rows are zero-filled
-#pragma unroll
-    for (int which = 0; which < 2; ++which) {
-        const uint16_t *base = which == 0 ? p.K : p.V;
-        const uint32_t dst0 = smem_u32(which == 0 ? Ks : Vs);
-#pragma unroll
-        for (int r = 0; r < kChunk * 16 / kThreads; ++r) {
-            const int i = tid + r * kThreads;
-            const int t = i >> 4, x = i & 15;
-            const int64_t off = rowoff[t];
-            cp_async_16(dst0 + t * kRowBytes + ((x ^ (t & 7)) << 4), off >= 0 ? base + off + x * 8 : base,
-                        off >= 0 ? 16u : 0u);
+    const int64_t items = p.batch * p.Hkv * static_cast<int64_t>(p.chunks);
+    // item -> (sequence b, KV head g, chunk c) and the tokens n of the chunk;
+    // false when the chunk is past the sequence (or the sequence is invalid)
+    auto item = [&](int64_t it, int64_t &b, int &g, int &c, int &n) {
+        c = static_cast<int>(it % p.chunks);
+        const int64_t r = it / p.chunks;
+        g = static_cast<int>(r % p.Hkv);
+        b = r / p.Hkv;
+        int L;
+        if (!seq_ok(p, b, L)) {
+            if (warp == kDecConsumers && lane == 0 && c == 0 && g == 0) atomicOr(p.status, kDevBadOffsets);   // loader 0
+            return false;
         }
-        cp_async_commit();
-    }
-    const int gq = lane >> 2, cq = lane & 3;              // fragment row group, column pair
-    float *wsh = p.ws + ((b * p.Hq + g * G) * p.chunks + c) * static_cast<int64_t>(kD + 2);
-    const int64_t ws_head = static_cast<int64_t>(p.chunks) * (kD + 2);   // next query head's record
-    cp_async_wait<1>();                                   // this thread's K copies
-    __syncthreads();                                      // everyone's
+        n = min(kChunk, L - c * kChunk);
+        return n > 0;
+    };
 
-    // scores S[h][t] = q_h . k_t on the tensor cores: A = q (rows = the G heads,
-    // zero beyond), B = K^T; warp w takes tokens 16w .. 16w+15, K ascending
-    // in 16-dimension steps
-    {
-        uint32_t qa[kD / 16][2];
-#pragma unroll
-        for (int ks = 0; ks < kD / 16; ++ks) {
-            qa[ks][0] = gq < G ? *reinterpret_cast<const uint32_t *>(qb + gq * kD + 16 * ks + 2 * cq) : 0u;
-            qa[ks][1] = gq < G ? *reinterpret_cast<const uint32_t *>(qb + gq * kD + 16 * ks + 8 + 2 * cq) : 0u;
+    if (warp >= kDecConsumers) {
+        // ---- loading warps: each takes every kLoaders-th item (a table read and
+        // the copies' issue per item), so items are prepared kLoaders at a time
+        const int lw = warp - kDecConsumers;
+        if (lane == 0 && p.box_rows > 0) {
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
         }
-#pragma unroll
-        for (int nb = 0; nb < 2; ++nb) {
-            const int n0 = warp * 16 + nb * 8;
-            const int t = n0 + gq;                        // the K row of this lane's B fragment
-            const uint8_t *krow = Ks + t * kRowBytes + cq * 4;
-            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-            for (int ks = 0; ks < kD / 16; ++ks) {
-                const uint32_t b0 = *reinterpret_cast<const uint32_t *>(krow + (((2 * ks) ^ (t & 7)) << 4));
-                const uint32_t b1 = *reinterpret_cast<const uint32_t *>(krow + (((2 * ks + 1) ^ (t & 7)) << 4));
-                mma_16816(acc, qa[ks][0], 0u, qa[ks][1], 0u, b0, b1);
+        int k = 0;
+        for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
+            int64_t b;
+            int g, c, n;
+            if (!item(it, b, g, c, n)) continue;
+            if (k % kLoaders != lw) {
+                ++k;
+                continue;
             }
-            if (gq < G) {
+            // the block-table reads first: they do not touch the slot
+            const int j0 = c * kChunk;
+            int64_t off[kChunk / 32];                 // per-row copies: element offset of each row, -1: none
+            bool ok_row[kChunk / 32];                 // the row's block is inside the cache
+            int32_t box_blk = -1;                     // boxes: lane i < nbox holds box i's block
+            const int nbox = p.box_rows > 0 ? (n + p.box_rows - 1) / p.box_rows : 0;
+            if (p.box_rows > 0) {
+                if (lane < nbox) {
+                    box_blk = p.table[b * p.max_blocks + (j0 + lane * p.box_rows) / p.bs];
+                    if (box_blk < 0 || box_blk >= p.num_blocks) atomicOr(p.status, kDevBadOffsets);
+                }
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int tt = n0 + 2 * cq + e;
-                    if (tt < n) S[tt * G + gq] = rowoff[tt] >= 0 ? __fmul_rn(acc[e], p.scale) : -INFINITY;
+                for (int i = 0; i < kChunk / 32; ++i) {
+                    const int t = lane + 32 * i;
+                    const int32_t blk = __shfl_sync(0xffffffffu, box_blk, t / p.box_rows);
+                    ok_row[i] = t < n && blk >= 0 && blk < p.num_blocks;
+                    off[i] = -1;
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < kChunk / 32; ++i) {
+                    const int t = lane + 32 * i;
+                    off[i] = -1;
+                    if (t < n) {
+                        const int j = j0 + t;
+                        const int64_t blk = p.table[b * p.max_blocks + j / p.bs];
+                        if (blk >= 0 && blk < p.num_blocks)
+                            off[i] = ((blk * p.bs + j % p.bs) * p.Hkv + g) * kD;
+                        else
+                            atomicOr(p.status, kDevBadOffsets);
+                    }
+                    ok_row[i] = off[i] >= 0;
                 }
             }
-        }
-    }
-    __syncthreads();
-
-    // per head: max, exponentials, sum (head h on warp h); (m, l) to the workspace
-    if (warp < G) {
-        const int h = warp;
-        float m = -INFINITY;
-        for (int t = lane; t < n; t += 32) m = fmaxf(m, S[t * G + h]);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        float l = 0.0f;
-        for (int t = lane; t < n; t += 32) {
-            const float e = expf(S[t * G + h] - m);
-            S[t * G + h] = e;
-            l += e;
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-        if (lane == 0) {
-            wsh[h * ws_head] = m;
-            wsh[h * ws_head + 1] = l;
-        }
-    }
-    cp_async_wait<0>();                                   // this thread's V copies
-    __syncthreads();
-
-    // values O[h][d] = sum_t p_t v_t[d] on the tensor cores: A = p (rows = the
-    // G heads; p = hi + lo, two bf16 MMAs per step; zero past the chunk's
-    // tokens), B = V read transposed by ldmatrix; warp w takes dimensions
-    // 16w .. 16w+15, tokens ascending in 16-token steps
-    {
-        const int d0 = warp * 16;
-        const int mi = lane >> 3, mr = lane & 7;          // ldmatrix: matrix, row
-        float acc[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
-#pragma unroll 2
-        for (int ks = 0; ks < kChunk / 16; ++ks) {
-            const int k0 = ks * 16;
-            uint32_t ph0 = 0u, pl0 = 0u, ph2 = 0u, pl2 = 0u;
-            if (gq < G) {
-                const int t0 = k0 + 2 * cq, t2 = t0 + 8;
-                const float p00 = t0 < n ? S[t0 * G + gq] : 0.0f;
-                const float p01 = t0 + 1 < n ? S[(t0 + 1) * G + gq] : 0.0f;
-                const float p20 = t2 < n ? S[t2 * G + gq] : 0.0f;
-                const float p21 = t2 + 1 < n ? S[(t2 + 1) * G + gq] : 0.0f;
-                split_bf16x2(p00, p01, ph0, pl0);
-                split_bf16x2(p20, p21, ph2, pl2);
+            const int slot = k % kSlots;
+            if (k >= kSlots && !mbar_wait(&empty[slot], ((k / kSlots) - 1) & 1, abort_flag)) {
+                if (lane == 0) {
+                    atomicOr(p.status, kDevTimeout);
+                    *abort_flag = 1;
+                }
+                break;
             }
-            const int tok = k0 + (mi & 1) * 8 + mr;
-            const int chunk = (d0 >> 3) + (mi >> 1);
-            uint32_t v0, v1, v2, v3;
-            ldmatrix_x4_trans(v0, v1, v2, v3, smem_u32(Vs + tok * kRowBytes + ((chunk ^ (tok & 7)) << 4)));
-            mma_16816(acc[0], ph0, 0u, ph2, 0u, v0, v1);
-            mma_16816(acc[0], pl0, 0u, pl2, 0u, v0, v1);
-            mma_16816(acc[1], ph0, 0u, ph2, 0u, v2, v3);
-            mma_16816(acc[1], pl0, 0u, pl2, 0u, v2, v3);
-        }
-        if (gq < G) {
-            float *w = wsh + gq * ws_head + 2 + d0 + 2 * cq;
+            uint8_t *Ks = smem + slot * kSlotBytes;
+            uint8_t *Vs = Ks + 2 * kHalfTile;
+            uint8_t *qs = Vs + 2 * kHalfTile;
 #pragma unroll
-            for (int nb = 0; nb < 2; ++nb)
-                *reinterpret_cast<float2 *>(w + nb * 8) = make_float2(acc[nb][0], acc[nb][1]);
+            for (int i = 0; i < kChunk / 32; ++i) valid[slot * kChunk + lane + 32 * i] = ok_row[i];
+            const uint16_t *qsrc = p.Q + (b * p.Hq + g * G) * kD;
+            if (p.box_rows > 0) {
+                // V rows no box reaches (a chunk past the sequence's end) become
+                // zero, so that p = 0 meets finite values there
+                for (int r = nbox * p.box_rows + lane; r < kChunk; r += 32) {
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        uint4 *v = reinterpret_cast<uint4 *>(Vs + half * kHalfTile + r * 128);
+#pragma unroll
+                        for (int x = 0; x < 8; ++x) v[x] = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+                fence_proxy_async_smem();             // before later bulk copies into these rows
+                // one box per cache block (box_rows tokens), both halves, K and V
+                const int nbox = (n + p.box_rows - 1) / p.box_rows;
+                __syncwarp();
+                // each lane's arrival releases its shared-memory writes; lane 0
+                // also sets the bytes to expect, before any copy is issued
+                if (lane == 0)
+                    mbar_arrive_expect_tx(&full[slot], nbox * p.box_rows * 4 * 128 + G * kRowBytes);
+                else
+                    mbar_arrive(&full[slot]);
+                __syncwarp();
+                if (lane < nbox) {                    // a block outside the cache arrives as zeros
+                    const int tok = (j0 + lane * p.box_rows) % p.bs;
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        const int dst = half * kHalfTile + lane * p.box_rows * 128;
+                        tma_load_4d(Ks + dst, &tmK, &full[slot], half * 64, g, tok, box_blk);
+                        tma_load_4d(Vs + dst, &tmV, &full[slot], half * 64, g, tok, box_blk);
+                    }
+                }
+                if (lane == 0) bulk_load(qs, qsrc, G * kRowBytes, &full[slot]);
+            } else {
+                // 16-byte copies per row (rows without K/V zero-filled); each lane
+                // arrives twice: now, and once its copies have landed
+#pragma unroll
+                for (int i = 0; i < kChunk / 32; ++i) {
+                    const int t = lane + 32 * i;
+                    for (int x = 0; x < kRowBytes / 16; ++x) {
+                        const uint32_t so = kv_piece(t, x);
+                        cp_async_16(smem_u32(Ks) + so, off[i] >= 0 ? p.K + off[i] + x * 8 : p.K, off[i] >= 0 ? 16u : 0u);
+                        cp_async_16(smem_u32(Vs) + so, off[i] >= 0 ? p.V + off[i] + x * 8 : p.V, off[i] >= 0 ? 16u : 0u);
+                    }
+                }
+                for (int x = lane; x < G * kRowBytes / 16; x += 32) cp_async_16(smem_u32(qs) + x * 16, qsrc + x * 8, 16u);
+                mbar_arrive(&full[slot]);             // releases this lane's row flags
+                asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(&full[slot]))
+                             : "memory");
+            }
+            ++k;
         }
+        // the copies of the last items must land before the CTA exits (the
+        // consumers normally waited for them already)
+        for (int i = k > kSlots ? k - kSlots : 0; i < k; ++i)
+            if (i % kLoaders == lw) mbar_wait(&full[i % kSlots], (i / kSlots) & 1, nullptr);
+        return;
+    }
+
+    // ---- consumer warps 0..7: group grp (warps GW grp .. GW grp + GW - 1)
+    // computes the items k with k % NG == grp; how the warps share an item
+    // changes no arithmetic
+    constexpr int GW = kDecConsumers / NG;                // warps per group
+    constexpr int NT = kChunk / 8 / GW;                   // score n-tiles per warp
+    constexpr int DW = kD / GW;                           // value dimensions per warp
+    const int grp = warp / GW, gw = warp % GW;
+    const int gq = lane >> 2, cq = lane & 3;              // fragment row group, column pair
+    const int64_t ws_head = static_cast<int64_t>(p.chunks) * (kD + 2);   // next query head's record
+    int k = 0;
+    for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
+        int64_t b;
+        int g, c, n;
+        if (!item(it, b, g, c, n)) continue;
+        if (k % NG != grp) {
+            ++k;
+            continue;
+        }
+        const int slot = k % kSlots;
+        const bool ok = mbar_wait(&full[slot], (k / kSlots) & 1, abort_flag);
+        if (group_sync_or<GW>(grp, !ok)) {                    // the group's warps stop together
+            if (gw == 0 && lane == 0) {
+                atomicOr(p.status, kDevTimeout);
+                *abort_flag = 1;
+            }
+            break;
+        }
+        const uint8_t *Ks = smem + slot * kSlotBytes;
+        const uint8_t *Vs = Ks + 2 * kHalfTile;
+        const uint16_t *qb = reinterpret_cast<const uint16_t *>(Vs + 2 * kHalfTile);
+        const uint8_t *vrow = valid + slot * kChunk;
+        float *S = S0 + (grp * 2 + ((k / NG) & 1)) * kDecSFloats;
+        float *wsh = p.ws + ((b * p.Hq + g * G) * p.chunks + c) * static_cast<int64_t>(kD + 2);
+        if (!BI_IN_BOUNDS(b < p.batch && c < p.chunks, p.status)) break;
+
+        // scores S[h][t] = q_h . k_t on the tensor cores: A = q (rows = the G
+        // heads, zero beyond), B = K^T; warp gw of the group takes tokens
+        // 8 NT gw .. 8 NT gw + 8 NT - 1, K ascending in 16-dimension steps
+        {
+            uint32_t qa[kD / 16][2];
+#pragma unroll
+            for (int ks = 0; ks < kD / 16; ++ks) {
+                qa[ks][0] = gq < G ? *reinterpret_cast<const uint32_t *>(qb + gq * kD + 16 * ks + 2 * cq) : 0u;
+                qa[ks][1] = gq < G ? *reinterpret_cast<const uint32_t *>(qb + gq * kD + 16 * ks + 8 + 2 * cq) : 0u;
+            }
+            // the NT n-tiles' chains interleaved, each in ascending dimension order
+            float acc[NT][4] = {};
+#pragma unroll
+            for (int ks = 0; ks < kD / 16; ++ks) {
+                uint32_t bf[NT][2];
+#pragma unroll
+                for (int nb = 0; nb < NT; ++nb) {
+                    const int t = gw * 8 * NT + nb * 8 + gq;   // the K row of this lane's B fragment
+                    bf[nb][0] = *reinterpret_cast<const uint32_t *>(Ks + cq * 4 + kv_piece(t, 2 * ks));
+                    bf[nb][1] = *reinterpret_cast<const uint32_t *>(Ks + cq * 4 + kv_piece(t, 2 * ks + 1));
+                }
+#pragma unroll
+                for (int nb = 0; nb < NT; ++nb) mma_16816(acc[nb], qa[ks][0], 0u, qa[ks][1], 0u, bf[nb][0], bf[nb][1]);
+            }
+            if (gq < G) {
+#pragma unroll
+                for (int nb = 0; nb < NT; ++nb)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int tt = gw * 8 * NT + nb * 8 + 2 * cq + e;
+                        if (tt < n) S[gq * kDecSStride + tt] = vrow[tt] ? __fmul_rn(acc[nb][e], p.scale) : -INFINITY;
+                    }
+            }
+        }
+        group_sync<GW>(grp);
+
+        // per head: max, exponentials, sum (head h on warp h % GW); (m, l) to the workspace
+        for (int h = gw; h < G; h += GW) {
+            float m = -INFINITY;
+            const float *Sh = S + h * kDecSStride;
+            for (int t = lane; t < n; t += 32) m = fmaxf(m, Sh[t]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            float l = 0.0f;
+            for (int t = lane; t < n; t += 32) {
+                const float e = expf(Sh[t] - m);
+                S[h * kDecSStride + t] = e;
+                l += e;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+            if (lane == 0) {
+                wsh[h * ws_head] = m;
+                wsh[h * ws_head + 1] = l;
+            }
+        }
+        group_sync<GW>(grp);
+
+        // values O[h][d] = sum_t p_t v_t[d] on the tensor cores: A = p (rows =
+        // the G heads; p = hi + lo, two bf16 MMAs per step; zero past the
+        // chunk's tokens), B = V read transposed by ldmatrix; warp gw takes
+        // dimensions DW gw .. DW gw + DW - 1, tokens ascending in 16-token steps
+        {
+            const int d0 = gw * DW;
+            const int mi = lane >> 3, mr = lane & 7;      // ldmatrix: matrix, row
+            float acc[DW / 8][4] = {};
+            // p of every step first (independent loads), then the MMA chains
+            uint32_t ph[kChunk / 16][2], pl[kChunk / 16][2];
+#pragma unroll
+            for (int ks = 0; ks < kChunk / 16; ++ks) {
+                ph[ks][0] = ph[ks][1] = pl[ks][0] = pl[ks][1] = 0u;
+                if (gq < G) {
+                    const int t0 = ks * 16 + 2 * cq, t2 = t0 + 8;
+                    const float *Sq = S + gq * kDecSStride;
+                    const float p00 = t0 < n ? Sq[t0] : 0.0f;
+                    const float p01 = t0 + 1 < n ? Sq[t0 + 1] : 0.0f;
+                    const float p20 = t2 < n ? Sq[t2] : 0.0f;
+                    const float p21 = t2 + 1 < n ? Sq[t2 + 1] : 0.0f;
+                    split_bf16x2(p00, p01, ph[ks][0], pl[ks][0]);
+                    split_bf16x2(p20, p21, ph[ks][1], pl[ks][1]);
+                }
+            }
+#pragma unroll
+            for (int ks = 0; ks < kChunk / 16; ++ks) {
+                const int k0 = ks * 16;
+                const uint32_t ph0 = ph[ks][0], ph2 = ph[ks][1], pl0 = pl[ks][0], pl2 = pl[ks][1];
+                const int tok = k0 + (mi & 1) * 8 + mr;
+                uint32_t v[DW / 16][4];
+#pragma unroll
+                for (int hf = 0; hf < DW / 16; ++hf) {    // 16 dimensions per ldmatrix
+                    const int piece = ((d0 + 16 * hf) >> 3) + (mi >> 1);
+                    ldmatrix_x4_trans(v[hf][0], v[hf][1], v[hf][2], v[hf][3], smem_u32(Vs + kv_piece(tok, piece)));
+                }
+                // each accumulator takes hi, then lo
+#pragma unroll
+                for (int hf = 0; hf < DW / 16; ++hf) {
+                    mma_16816(acc[2 * hf], ph0, 0u, ph2, 0u, v[hf][0], v[hf][1]);
+                    mma_16816(acc[2 * hf + 1], ph0, 0u, ph2, 0u, v[hf][2], v[hf][3]);
+                }
+#pragma unroll
+                for (int hf = 0; hf < DW / 16; ++hf) {
+                    mma_16816(acc[2 * hf], pl0, 0u, pl2, 0u, v[hf][0], v[hf][1]);
+                    mma_16816(acc[2 * hf + 1], pl0, 0u, pl2, 0u, v[hf][2], v[hf][3]);
+                }
+            }
+            if (gq < G) {
+                float *w = wsh + gq * ws_head + 2 + d0 + 2 * cq;
+#pragma unroll
+                for (int nb = 0; nb < DW / 8; ++nb)
+                    *reinterpret_cast<float2 *>(w + nb * 8) = make_float2(acc[nb][0], acc[nb][1]);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);         // this warp is done with the slot
+        ++k;
     }
 }
 
@@ -700,17 +902,17 @@ int64_t attention_decode_workspace_bytes(int64_t B, int32_t Hq, int32_t max_len)
 }
 
 template <int G>
-bi_status launch_split(const dim3 &grid, const AttnParams &p, cudaStream_t s) {
+bi_status launch_split(const dim3 &grid, const CUtensorMap &tmK, const CUtensorMap &tmV, const AttnParams &p,
+                       cudaStream_t s) {
     static unsigned long long configured = 0;
-    if (ensure_smem_attr(reinterpret_cast<const void *>(attn_split_kernel<G>), split_smem_bytes<G>(), &configured) !=
-        BI_OK)
+    if (ensure_smem_attr(reinterpret_cast<const void *>(attn_split_kernel<G>), kDecSmem, &configured) != BI_OK)
         return BI_ERR_CUDA;
-    return launch_pdl(attn_split_kernel<G>, grid, dim3(kThreads), split_smem_bytes<G>(), s, p);
+    return launch_pdl(attn_split_kernel<G>, grid, dim3(kDecThreads), kDecSmem, s, tmK, tmV, p);
 }
-#define SPLIT_LAUNCH(G)                                    \
-    do {                                                   \
-        const bi_status st_ = launch_split<G>(grid1, p, s); \
-        if (st_ != BI_OK) return st_;                      \
+#define SPLIT_LAUNCH(G)                                              \
+    do {                                                             \
+        const bi_status st_ = launch_split<G>(grid1, tmK, tmV, p, s); \
+        if (st_ != BI_OK) return st_;                                \
     } while (0)
 
 bi_status launch_attention_decode(const void *Q, const void *K, const void *V, const int32_t *table,
@@ -727,6 +929,7 @@ bi_status launch_attention_decode(const void *Q, const void *K, const void *V, c
     p.ws = static_cast<float *>(workspace);
     p.O = static_cast<uint16_t *>(O);
     p.num_blocks = num_blocks;
+    p.batch = B;
     p.max_blocks = max_blocks;
     p.Hq = Hq;
     p.Hkv = Hkv;
@@ -736,7 +939,26 @@ bi_status launch_attention_decode(const void *Q, const void *K, const void *V, c
     p.scale = scale;
     p.status = device_status_word();
     const int G = Hq / Hkv;
-    const dim3 grid1(p.chunks, Hkv, static_cast<unsigned>(B));
+    int dev = 0;
+    const DeviceInfo *info = nullptr;
+    if (current_device(&dev, &info) != BI_OK) return BI_ERR_CUDA;
+    const int64_t items = B * Hkv * static_cast<int64_t>(p.chunks);
+    const dim3 grid1(static_cast<unsigned>(items < info->sm_count ? items : info->sm_count));
+    // TMA boxes of whole cache blocks (box start rows on 1024-byte swizzle atoms)
+    CUtensorMap tmK{}, tmV{};
+    p.box_rows = bs % kChunk == 0 ? kChunk : (kChunk % bs == 0 && bs >= 8 ? bs : 0);
+    if (p.box_rows > 0) {
+        const uint64_t dims[4] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(Hkv), static_cast<uint64_t>(bs),
+                                  static_cast<uint64_t>(num_blocks)};
+        const uint64_t strides[3] = {static_cast<uint64_t>(kRowBytes), static_cast<uint64_t>(Hkv) * kRowBytes,
+                                     static_cast<uint64_t>(bs) * Hkv * kRowBytes};
+        const uint32_t box[4] = {64, 1, static_cast<uint32_t>(p.box_rows), 1};
+        if (make_tmap_4d(&tmK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, dims, strides, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B) != BI_OK ||
+            make_tmap_4d(&tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, V, dims, strides, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B) != BI_OK)
+            p.box_rows = 0;                          // the per-row copies need no tensor map
+    }
     switch (G) {
         case 1: SPLIT_LAUNCH(1); break;
         case 2: SPLIT_LAUNCH(2); break;

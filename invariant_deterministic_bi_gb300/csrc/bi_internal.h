@@ -39,6 +39,10 @@ bi_status make_tmap_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *
 bi_status make_tmap_3d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, const uint64_t dims[3],
                        const uint64_t strides_bytes[2], const uint32_t box[3], CUtensorMapSwizzle swizzle);
 
+// Encode a 4-D tensor map (dims inner first; strides in bytes for dims 1..3).
+bi_status make_tmap_4d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, const uint64_t dims[4],
+                       const uint64_t strides_bytes[3], const uint32_t box[4], CUtensorMapSwizzle swizzle);
+
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Raise a kernel's dynamic shared-memory limit once per device. `done` is a

@@ -89,6 +89,17 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *m, uin
         : "memory");
 }
 
+// TMA 4-D load into this CTA's shared memory, counted on this CTA's barrier.
+__device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *m, uint64_t *bar, int32_t c0, int32_t c1,
+                                            int32_t c2, int32_t c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2),
+          "r"(c3)
+        : "memory");
+}
+
 // TMA 2-D store from this CTA's shared memory (bulk async-group completion).
 // Rows and columns outside the tensor map's extent are not written.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *m, const void *src, int32_t c0, int32_t c1) {

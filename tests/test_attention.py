@@ -100,3 +100,55 @@ def test_group_sizes(bi, hq, hkv):
         one = run(bi, Q[b:b + 1], K, V, table[b:b + 1], lens[b:b + 1], 512)
         assert np.array_equal(one[0], full[b]), f"Hq={hq} Hkv={hkv}: sequence {b} alone differs"
     assert bi.device_status() == bi.BI_OK
+
+
+def relayout(K, V, table, lens, bs, seed):
+    """The same sequences' K/V in a cache of block size bs (blocks in a
+    seeded random order, two spare blocks)."""
+    B, L = len(lens), int(lens.max())
+    nb = -(-L // bs)
+    blocks = B * nb + 2
+    K2 = np.zeros((blocks, bs) + K.shape[2:], K.dtype)
+    V2 = np.zeros_like(K2)
+    t2 = syn.rng(seed, 5).permutation(blocks)[: B * nb].astype(np.int32).reshape(B, nb)
+    for b in range(B):
+        for j in range(int(lens[b])):
+            K2[t2[b, j // bs], j % bs] = K[table[b, j // BS], j % BS]
+            V2[t2[b, j // bs], j % bs] = V[table[b, j // BS], j % BS]
+    return K2, V2, t2
+
+
+@pytest.mark.parametrize("bs", [1, 8, 24, 128, 256])
+def test_block_sizes(bi, bs):
+    """Block sizes the whole-block copies tile (8, 128, 256) and ones they do
+    not (1, 24): the same sequences give the same bits as with 16-token
+    blocks, and parity with the oracle."""
+    lens = np.asarray([300, 1, 129, 640], dtype=np.int32)
+    K, V, table, lens = make_cache(lens, seed=50)
+    Q = syn.to_bf16_bits(syn.normal_rows(51, 0, len(lens) * HQ, D)).reshape(len(lens), HQ, D)
+    base = run(bi, Q, K, V, table, lens, 640)
+    K2, V2, t2 = relayout(K, V, table, lens, bs, seed=bs)
+    got = run(bi, Q, K2, V2, t2, lens, 640)
+    assert np.array_equal(got, base), f"block size {bs} changed the bits"
+    ref = oracle.attention_decode(Q, K2, V2, t2, lens, SCALE)
+    assert_close_rel(syn.bf16_bits_to_f32(got).astype(np.float64), ref, 1e-2, 2e-3, f"bs={bs}")
+    assert bi.device_status() == bi.BI_OK
+
+
+@pytest.mark.parametrize("bs", [16, 24])
+def test_block_outside_the_cache_reported(bi, bs):
+    """A block-table entry outside the cache: its tokens are left out (score
+    -inf) and the device status reports it."""
+    import torch
+    lens = np.asarray([200, 50], dtype=np.int32)
+    K, V, table, lens = make_cache(lens, seed=60)
+    K2, V2, t2 = relayout(K, V, table, lens, bs, seed=61)
+    t2 = t2.copy()
+    t2[0, 1] = K2.shape[0] + 7
+    Q = syn.to_bf16_bits(syn.normal_rows(62, 0, 2 * HQ, D)).reshape(2, HQ, D)
+    got = run(bi, Q, K2, V2, t2, lens, 256)
+    torch.cuda.synchronize()
+    assert bi.device_status() == bi.BI_ERR_INVALID_ARG
+    good = run(bi, Q[1:], K2, V2, t2[1:], lens[1:], 256)
+    assert np.array_equal(got[1], good[0])
+    assert np.all(np.isfinite(syn.bf16_bits_to_f32(got)))

@@ -129,3 +129,29 @@ def test_group_sizes(bi, hq, hkv):
                                           to_dev(table[:1]), to_dev(np.array([pos + 1], np.int32)), 150, SCALE))
         assert np.array_equal(one[0], full[t]), f"Hq={hq} Hkv={hkv}: token {t}"
     assert bi.device_status() == bi.BI_OK
+
+
+@pytest.mark.parametrize("bs", [1, 24, 256])
+def test_block_sizes(bi, bs):
+    """The same cache in blocks of 1, 24 or 256 tokens gives the same bits as
+    in blocks of 16, and each token still equals its decode."""
+    lens, qlens = [300, 150], [300, 20]
+    Q, cu, K, V, table, lens = make(lens, qlens, seed=70)
+    base = extend(bi, Q, cu, K, V, table, lens)
+    B, L = len(lens), int(lens.max())
+    nb = -(-L // bs)
+    blocks = B * nb + 2
+    K2 = np.zeros((blocks, bs, HKV, D), K.dtype)
+    V2 = np.zeros_like(K2)
+    t2 = syn.rng(71, bs).permutation(blocks)[: B * nb].astype(np.int32).reshape(B, nb)
+    for b in range(B):
+        for j in range(int(lens[b])):
+            K2[t2[b, j // bs], j % bs] = K[table[b, j // BS], j % BS]
+            V2[t2[b, j // bs], j % bs] = V[table[b, j // BS], j % BS]
+    got = extend(bi, Q, cu, K2, V2, t2, lens)
+    assert np.array_equal(got, base), f"block size {bs} changed the bits"
+    for i in (0, 127, 299):
+        one = bits_of(bi.attention_decode(to_dev_bf16(Q[i:i + 1]), to_dev_bf16(K2), to_dev_bf16(V2),
+                                          to_dev(t2[:1]), to_dev(np.array([i + 1], np.int32)), L, SCALE))
+        assert np.array_equal(one[0], got[i]), f"bs={bs}: token {i} differs from decode"
+    assert bi.device_status() == bi.BI_OK
