@@ -10,42 +10,42 @@
 // chunk results are merged in chunk order. Nothing a sequence sees depends on
 // the other sequences in the batch.
 //
-// Step 1, one CTA per (sequence, KV head, chunk of kChunk = 128 tokens),
-//   256 threads, head_dim 128, the G = Hq/Hkv query heads of the KV head
-//   together (GQA):
-//   - every thread issues its share of the chunk's K rows, then V rows, as
-//     16-byte cp.async copies into shared memory (32 KB each, 16-byte chunks
-//     XOR-swizzled by row; rows past the sequence or in an invalid block are
-//     zero-filled), so the whole chunk is in flight at once and three CTAs
-//     share an SM;
-//   - scores, once K has landed, on the tensor cores (mma.sync m16n8k16, bf16
-//     operands, fp32 accumulation): the G q rows (zero rows up to 16) times
-//     K^T, warp w taking tokens 16w..16w+15, dimensions ascending in steps of
-//     16; s = scale * q.k;
-//   - per head (warp h): m = max s (exact), p = exp(s - m), l = sum p
-//     (lane-strided, then butterfly);
-//   - values, once V has landed, on the tensor cores: p (as bf16 hi + lo,
-//     two MMAs per step, 16 significant bits) times V, warp w taking
-//     dimensions 16w..16w+15, tokens ascending in steps of 16;
+// Step 1, per (sequence, KV head, chunk of kChunk = 128 tokens) item, head_dim
+//   128, the G = Hq/Hkv query heads of the KV head together (GQA), computed
+//   by a persistent kernel (one CTA per SM walking the items; details at
+//   attn_split_kernel):
+//   - the chunk's K and V rows arrive in shared memory by TMA (one box per
+//     cache block; blocks outside the cache arrive as zeros and score -inf);
+//   - scores on the tensor cores (mma.sync m16n8k16, bf16 operands, fp32
+//     accumulation): the G q rows (zero rows up to 16) times K^T, every
+//     8-token n-tile's chain of MMAs in ascending 16-dimension steps;
+//     s = scale * q.k;
+//   - per head (one warp): m = max s (exact), p = exp(s - m), l = sum p
+//     (lane L sums tokens L, L + 32, L + 64, L + 96 in turn, then a
+//     butterfly over lanes xor 16, 8, 4, 2, 1);
+//   - values on the tensor cores: p (as bf16 hi + lo, two MMAs per step, 16
+//     significant bits) times V, every 8-dimension tile's chain in
+//     ascending 16-token steps, hi before lo;
 //   - writes fp32 (m, l, o[0..127]) per head and chunk to the workspace.
 //   The MMA shapes and step orders are the same for every chunk of every
-//   batch, so the per-chunk results do not depend on the batch either.
+//   batch, and which warp or CTA computes a tile changes nothing, so the
+//   per-chunk results do not depend on the batch either.
 // Step 2, one CTA per (sequence, query head): the chunk results are merged
-//   in chunk order by merge_chunk() below (running maximum m, with the
-//   running o and l rescaled by e^{m - m'} and the chunk's by e^{m_c - m'}),
-//   and o / l is rounded to bf16.
+//   in chunk order by merge_factors() / merge_value() below (running maximum
+//   m, with the running o and l rescaled by e^{m - m'} and the chunk's by
+//   e^{m_c - m'}), and o / l is rounded to bf16.
 //
 // Extend (prefill) attention, attn_extend_kernel: the new query tokens of a
 // sequence attend causally to its cache. Token i at position p sees tokens
 // 0..p, so its result is defined as the decode result of the sequence cut
 // after p: the same 128-token chunks by position, the same per-chunk
-// arithmetic (q.k on the tensor cores, max, e^(s-m), the lane-strided sum,
-// p.V with p as bf16 hi + lo) and the same chunk-order merge_chunk(). A
-// token's output is therefore the same bits whether it is decoded alone,
-// prefilled at once, prefilled in chunks of any size, or batched with other
-// sequences. One CTA per (sequence, KV head, 64 query rows = 64/G tokens x G
-// heads) walks the chunks in order and merges each into per-row running
-// state held in registers.
+// arithmetic (the same MMA chains, max, e^(s-m), the same sum order, p.V with
+// p as bf16 hi + lo) and the same chunk-order merge. A token's output is
+// therefore the same bits whether it is decoded alone, prefilled at once,
+// prefilled in chunks of any size, or batched with other sequences. One CTA
+// per (sequence, KV head, 128 query rows = 128/G tokens x G heads) walks the
+// chunks in order; each warp keeps 16 rows' scores, exponentials and running
+// (m, l, o) in registers.
 #include <cuda_bf16.h>
 
 #include <mutex>
