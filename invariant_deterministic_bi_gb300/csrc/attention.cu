@@ -152,11 +152,11 @@ constexpr int kSlots = 3;
 constexpr int kSlotBytes = 4 * kHalfTile + 8 * kRowBytes; // K, V, up to 8 q rows
 constexpr int kDecConsumers = kThreads / 32;             // 8 warps: two groups of four
 constexpr int NG = 2;                                    // consumer groups (items in compute at once)
-constexpr int kLoaders = 2;                              // loading warps: warp kDecConsumers + i loads items i, i + 2, ...
+constexpr int kLoaders = kSlots;                         // loading warp kDecConsumers + i fills slot i (items i, i + 3, ...)
 constexpr int kDecThreads = kThreads + 32 * kLoaders;
 constexpr int kDecSStride = kChunk + 8;                 // scores of one head (padded)
 constexpr int kDecSFloats = 8 * kDecSStride;             // one score buffer: up to 8 heads
-constexpr int kDecSmem = 1024 + kSlots * kSlotBytes + 4 * kDecSFloats * 4 + kSlots * kChunk + 2 * kSlots * 8 + 16;
+constexpr int kDecSmem = 1024 + kSlots * kSlotBytes + 4 * kDecSFloats * 4 + kSlots * kChunk + 3 * kSlots * 8 + 16;
 static_assert(kSlotBytes % 1024 == 0, "slot alignment (128-byte swizzle atoms)");
 
 // Byte offset of 16-byte piece x (0..15) of token row t in a swizzled K or V tile.
@@ -194,15 +194,19 @@ attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     float *S0 = reinterpret_cast<float *>(smem + kSlots * kSlotBytes);     // [group][2][G][kDecSStride] scores
     uint8_t *valid = reinterpret_cast<uint8_t *>(S0 + 4 * kDecSFloats);     // [kSlots][kChunk]: row has K/V
-    uint64_t *full = reinterpret_cast<uint64_t *>(valid + kSlots * kChunk);
-    uint64_t *empty = full + kSlots;
+    // Barriers. Every waiter waits only for the phase right after one it has
+    // seen complete (a parity wait cannot tell a phase from the one two
+    // later): slot s is filled by one loading warp in item order, so one
+    // "empty" barrier per slot serves it; the items of a slot alternate
+    // between the consumer groups, so each (slot, group) has its own "full"
+    // barrier, whose phases are that group's items on that slot in order.
+    uint64_t *full = reinterpret_cast<uint64_t *>(valid + kSlots * kChunk);   // [kSlots][NG]
+    uint64_t *empty = full + kSlots * NG;                                     // [kSlots]
     volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + kSlots);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
-        for (int s = 0; s < kSlots; ++s) {
-            mbar_init(&full[s], p.box_rows > 0 ? 32 : 64);
-            mbar_init(&empty[s], kDecConsumers / NG);
-        }
+        for (int s = 0; s < kSlots * NG; ++s) mbar_init(&full[s], p.box_rows > 0 ? 32 : 64);
+        for (int s = 0; s < kSlots; ++s) mbar_init(&empty[s], kDecConsumers / NG);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -225,19 +229,20 @@ attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     };
 
     if (warp >= kDecConsumers) {
-        // ---- loading warps: each takes every kLoaders-th item (a table read and
-        // the copies' issue per item), so items are prepared kLoaders at a time
+        // ---- loading warps: warp lw fills slot lw with items lw, lw + 3, ... (a
+        // table read and the copies' issue per item), so three items are
+        // prepared at a time
         const int lw = warp - kDecConsumers;
         if (lane == 0 && p.box_rows > 0) {
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
         }
-        int k = 0;
+        int k = 0, last = -1;
         for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
             int64_t b;
             int g, c, n;
             if (!item(it, b, g, c, n)) continue;
-            if (k % kLoaders != lw) {
+            if (k % kSlots != lw) {
                 ++k;
                 continue;
             }
@@ -276,6 +281,7 @@ attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                 }
             }
             const int slot = k % kSlots;
+            uint64_t *fb = &full[slot * NG + k % NG];   // the consuming group's barrier for this slot
             if (k >= kSlots && !mbar_wait(&empty[slot], ((k / kSlots) - 1) & 1, abort_flag)) {
                 if (lane == 0) {
                     atomicOr(p.status, kDevTimeout);
@@ -307,20 +313,20 @@ attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                 // each lane's arrival releases its shared-memory writes; lane 0
                 // also sets the bytes to expect, before any copy is issued
                 if (lane == 0)
-                    mbar_arrive_expect_tx(&full[slot], nbox * p.box_rows * 4 * 128 + G * kRowBytes);
+                    mbar_arrive_expect_tx(fb, nbox * p.box_rows * 4 * 128 + G * kRowBytes);
                 else
-                    mbar_arrive(&full[slot]);
+                    mbar_arrive(fb);
                 __syncwarp();
                 if (lane < nbox) {                    // a block outside the cache arrives as zeros
                     const int tok = (j0 + lane * p.box_rows) % p.bs;
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         const int dst = half * kHalfTile + lane * p.box_rows * 128;
-                        tma_load_4d(Ks + dst, &tmK, &full[slot], half * 64, g, tok, box_blk);
-                        tma_load_4d(Vs + dst, &tmV, &full[slot], half * 64, g, tok, box_blk);
+                        tma_load_4d(Ks + dst, &tmK, fb, half * 64, g, tok, box_blk);
+                        tma_load_4d(Vs + dst, &tmV, fb, half * 64, g, tok, box_blk);
                     }
                 }
-                if (lane == 0) bulk_load(qs, qsrc, G * kRowBytes, &full[slot]);
+                if (lane == 0) bulk_load(qs, qsrc, G * kRowBytes, fb);
             } else {
                 // 16-byte copies per row (rows without K/V zero-filled); each lane
                 // arrives twice: now, and once its copies have landed
@@ -334,16 +340,16 @@ attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                     }
                 }
                 for (int x = lane; x < G * kRowBytes / 16; x += 32) cp_async_16(smem_u32(qs) + x * 16, qsrc + x * 8, 16u);
-                mbar_arrive(&full[slot]);             // releases this lane's row flags
-                asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(&full[slot]))
-                             : "memory");
+                mbar_arrive(fb);                      // releases this lane's row flags
+                asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(fb)) : "memory");
             }
+            last = k;
             ++k;
         }
-        // the copies of the last items must land before the CTA exits (the
-        // consumers normally waited for them already)
-        for (int i = k > kSlots ? k - kSlots : 0; i < k; ++i)
-            if (i % kLoaders == lw) mbar_wait(&full[i % kSlots], (i / kSlots) & 1, nullptr);
+        // the copies of this warp's last item must land before the CTA exits
+        // (the consumers normally waited for them already; every earlier item
+        // of the slot was consumed before the slot was filled again)
+        if (last >= 0) mbar_wait(&full[(last % kSlots) * NG + last % NG], (last / (kSlots * NG)) & 1, nullptr);
         return;
     }
 
@@ -366,7 +372,7 @@ attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             continue;
         }
         const int slot = k % kSlots;
-        const bool ok = mbar_wait(&full[slot], (k / kSlots) & 1, abort_flag);
+        const bool ok = mbar_wait(&full[slot * NG + grp], (k / (kSlots * NG)) & 1, abort_flag);
         if (group_sync_or<GW>(grp, !ok)) {                    // the group's warps stop together
             if (gw == 0 && lane == 0) {
                 atomicOr(p.status, kDevTimeout);
