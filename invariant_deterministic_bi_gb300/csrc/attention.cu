@@ -145,19 +145,28 @@ __device__ __forceinline__ bool seq_ok(const AttnParams &p, int64_t b, int &L) {
 // counted on the slot's "full" barrier. Block sizes that boxes cannot tile
 // (not a multiple of 128 and not 8, 16, 32 or 64) take 16-byte cp.async
 // copies per row instead. Blocks outside the cache arrive as zeros and their
-// tokens score -inf. Eight consumer warps compute the chunk and hand the slot
-// back through its "empty" barrier.
+// tokens score -inf. Eight consumer warps, in NG groups, compute the chunks
+// and hand each slot back through its "empty" barrier.
+//
+// Two shapes of the kernel, the same arithmetic per item:
+//   - many items: SLOTS = 3 ring slots, NG = 2 groups of four warps on
+//     alternate items (two items in compute while up to three load), one CTA
+//     per SM;
+//   - few items (at most two CTAs' worth per SM): SLOTS = 1, NG = 1, one item
+//     per CTA on all eight warps, two CTAs per SM.
 constexpr int kHalfTile = kChunk * 128;                  // one 64-dimension half of a K or V tile (swizzled)
-constexpr int kSlots = 3;
 constexpr int kSlotBytes = 4 * kHalfTile + 8 * kRowBytes; // K, V, up to 8 q rows
-constexpr int kDecConsumers = kThreads / 32;             // 8 warps: two groups of four
-constexpr int NG = 2;                                    // consumer groups (items in compute at once)
-constexpr int kLoaders = kSlots;                         // loading warp kDecConsumers + i fills slot i (items i, i + 3, ...)
-constexpr int kDecThreads = kThreads + 32 * kLoaders;
+constexpr int kDecConsumers = kThreads / 32;             // 8 warps
 constexpr int kDecSStride = kChunk + 8;                 // scores of one head (padded)
 constexpr int kDecSFloats = 8 * kDecSStride;             // one score buffer: up to 8 heads
-constexpr int kDecSmem = 1024 + kSlots * kSlotBytes + 4 * kDecSFloats * 4 + kSlots * kChunk + 3 * kSlots * 8 + 16;
+template <int SLOTS>
+constexpr int dec_threads() { return kThreads + 32 * SLOTS; }   // + one loading warp per slot
+template <int SLOTS, int NG>
+constexpr int dec_smem() {
+    return 1024 + SLOTS * kSlotBytes + 2 * NG * kDecSFloats * 4 + SLOTS * kChunk + (NG + 1) * SLOTS * 8 + 16;
+}
 static_assert(kSlotBytes % 1024 == 0, "slot alignment (128-byte swizzle atoms)");
+static_assert(2 * dec_smem<1, 1>() <= 232448, "two few-item CTAs per SM");
 
 // Byte offset of 16-byte piece x (0..15) of token row t in a swizzled K or V tile.
 __device__ __forceinline__ int kv_piece(int t, int x) {
@@ -184,8 +193,8 @@ __device__ __forceinline__ bool group_sync_or(int grp, bool pred) {
     return r != 0;
 }
 
-template <int G>
-__global__ void __launch_bounds__(kDecThreads, 1)
+template <int G, int kSlots, int NG>
+__global__ void __launch_bounds__(dec_threads<kSlots>(), kSlots == 1 ? 2 : 1)
 attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const AttnParams p) {
     grid_dep_wait();      // earlier work of the stream is complete and visible
@@ -193,7 +202,7 @@ attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     extern __shared__ __align__(16) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     float *S0 = reinterpret_cast<float *>(smem + kSlots * kSlotBytes);     // [group][2][G][kDecSStride] scores
-    uint8_t *valid = reinterpret_cast<uint8_t *>(S0 + 4 * kDecSFloats);     // [kSlots][kChunk]: row has K/V
+    uint8_t *valid = reinterpret_cast<uint8_t *>(S0 + 2 * NG * kDecSFloats); // [kSlots][kChunk]: row has K/V
     // Barriers. Every waiter waits only for the phase right after one it has
     // seen complete (a parity wait cannot tell a phase from the one two
     // later): slot s is filled by one loading warp in item order, so one
@@ -907,17 +916,26 @@ int64_t attention_decode_workspace_bytes(int64_t B, int32_t Hq, int32_t max_len)
     return B * Hq * chunks * (kD + 2) * static_cast<int64_t>(sizeof(float));
 }
 
-template <int G>
-bi_status launch_split(const dim3 &grid, const CUtensorMap &tmK, const CUtensorMap &tmV, const AttnParams &p,
-                       cudaStream_t s) {
+template <int G, int SLOTS, int NG>
+bi_status launch_split_shape(const dim3 &grid, const CUtensorMap &tmK, const CUtensorMap &tmV, const AttnParams &p,
+                             cudaStream_t s) {
     static unsigned long long configured = 0;
-    if (ensure_smem_attr(reinterpret_cast<const void *>(attn_split_kernel<G>), kDecSmem, &configured) != BI_OK)
+    constexpr int smem = dec_smem<SLOTS, NG>();
+    if (ensure_smem_attr(reinterpret_cast<const void *>(attn_split_kernel<G, SLOTS, NG>), smem, &configured) != BI_OK)
         return BI_ERR_CUDA;
-    return launch_pdl(attn_split_kernel<G>, grid, dim3(kDecThreads), kDecSmem, s, tmK, tmV, p);
+    return launch_pdl(attn_split_kernel<G, SLOTS, NG>, grid, dim3(dec_threads<SLOTS>()), smem, s, tmK, tmV, p);
+}
+// At most two items per SM: one item per CTA, two CTAs per SM; else the ring.
+template <int G>
+bi_status launch_split(int64_t items, int sms, const CUtensorMap &tmK, const CUtensorMap &tmV, const AttnParams &p,
+                       cudaStream_t s) {
+    if (items <= 2 * static_cast<int64_t>(sms))
+        return launch_split_shape<G, 1, 1>(dim3(static_cast<unsigned>(items)), tmK, tmV, p, s);
+    return launch_split_shape<G, 3, 2>(dim3(static_cast<unsigned>(sms)), tmK, tmV, p, s);
 }
 #define SPLIT_LAUNCH(G)                                              \
     do {                                                             \
-        const bi_status st_ = launch_split<G>(grid1, tmK, tmV, p, s); \
+        const bi_status st_ = launch_split<G>(items, info->sm_count, tmK, tmV, p, s); \
         if (st_ != BI_OK) return st_;                                \
     } while (0)
 
@@ -949,7 +967,6 @@ bi_status launch_attention_decode(const void *Q, const void *K, const void *V, c
     const DeviceInfo *info = nullptr;
     if (current_device(&dev, &info) != BI_OK) return BI_ERR_CUDA;
     const int64_t items = B * Hkv * static_cast<int64_t>(p.chunks);
-    const dim3 grid1(static_cast<unsigned>(items < info->sm_count ? items : info->sm_count));
     // TMA boxes of whole cache blocks (box start rows on 1024-byte swizzle atoms)
     CUtensorMap tmK{}, tmV{};
     p.box_rows = bs % kChunk == 0 ? kChunk : (kChunk % bs == 0 && bs >= 8 ? bs : 0);

@@ -19,10 +19,11 @@
 // same bytes whatever the batch. Zero magnitudes are stored as code 0 (never
 // the negative-zero code 8).
 //
-// One thread per 16-element block: a warp reads 1 KB of consecutive elements
-// (two 16-byte loads per thread) and writes 256 consecutive bytes of packed
-// codes; each thread stores its scale byte straight into the interleaved
-// 128x4 scale layout bi_gemm_nvfp4 reads.
+// One thread per 16-element block, a CTA per row at a time (two rows per
+// step): a warp reads 1 KB of consecutive elements (two 16-byte loads per
+// thread) and writes 256 consecutive bytes of packed codes; each thread stores
+// its scale byte straight into the interleaved 128x4 scale layout
+// bi_gemm_nvfp4 reads.
 #include <cuda_bf16.h>
 
 #include "bi_internal.h"
@@ -87,23 +88,16 @@ __device__ __forceinline__ uint32_t decide(float a, float gs, float md, uint32_t
     return (diff > 0.0f || (diff == 0.0f && (lo & 1u))) ? lo + 1u : lo;
 }
 
-// Magnitude with x's sign.
-__device__ __forceinline__ float with_sign_of(float mag, float x) {
-    return __uint_as_float(__float_as_uint(mag) | (__float_as_uint(x) & 0x80000000u));
-}
-
 __global__ void __launch_bounds__(kThreads)
 quantize_nvfp4_kernel(const uint4 *__restrict__ X, int64_t ldx_vec, uint8_t *__restrict__ Q, uint8_t *__restrict__ SF,
-                      int64_t M, int K, float gs, unsigned *status) {
+                      int M, int K, float gs, unsigned *status) {
     grid_dep_wait();      // earlier work of the stream is complete and visible
     grid_dep_launch();
     const int blocks = K / 16;                       // 16-element scale blocks per row
     const int atoms = K / 64;                        // 512-byte scale atoms per 128-row group
-    const int64_t total = M * blocks;
-    for (int64_t gid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; gid < total;
-         gid += static_cast<int64_t>(gridDim.x) * kThreads) {
-        const int64_t r = gid / blocks;
-        const int c = static_cast<int>(gid - r * blocks);
+    // rows over the grid, a row's blocks over the CTA's threads (no 64-bit
+    // division per block); two rows per step, so one thread has two blocks in flight
+    auto one = [&](int r, int c) {
         const uint4 *src = X + r * ldx_vec + c * 2;
         const uint4 v0 = __ldcs(src), v1 = __ldcs(src + 1);
         const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
@@ -135,7 +129,7 @@ quantize_nvfp4_kernel(const uint4 *__restrict__ X, int64_t ldx_vec, uint8_t *__r
             for (int i = 0; i < 8; ++i) {
                 const float xi = x[8 * h + i];
                 lo[i] = __fmul_rz(xi, inv_dn);
-                hi[i] = with_sign_of(__fmul_ru(fabsf(xi), inv_up), xi);
+                hi[i] = __fmul_ru(fabsf(xi), inv_up);   // magnitude only: the signs come from lo
             }
             uint32_t cl = to_e2m1x8(lo);
             const uint32_t ch = to_e2m1x8(hi);
@@ -157,12 +151,17 @@ quantize_nvfp4_kernel(const uint4 *__restrict__ X, int64_t ldx_vec, uint8_t *__r
             const uint32_t nz = (mag | (mag >> 1) | (mag >> 2)) & 0x11111111u;
             codes[h] = mag | (cl & (nz << 3));
         }
-        *reinterpret_cast<uint2 *>(Q + r * (K / 2) + c * 8) = make_uint2(codes[0], codes[1]);
-        const int64_t atom = (r / 128) * atoms + c / 4;
-        const int64_t at = atom * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4 + c % 4;
+        *reinterpret_cast<uint2 *>(Q + static_cast<int64_t>(r) * (K / 2) + c * 8) = make_uint2(codes[0], codes[1]);
+        const int64_t atom = static_cast<int64_t>(r >> 7) * atoms + (c >> 2);
+        const int64_t at = atom * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (c & 3);
         // debug build: inside the interleaved scale buffer ((M rounded up to 128) x K/16 bytes)
-        if (BI_IN_BOUNDS(at < (M + 127) / 128 * 128 * blocks, status)) SF[at] = static_cast<uint8_t>(s);
-    }
+        if (BI_IN_BOUNDS(at < (static_cast<int64_t>(M) + 127) / 128 * 128 * blocks, status)) SF[at] = static_cast<uint8_t>(s);
+    };
+    for (int r = blockIdx.x; r < M; r += 2 * gridDim.x)
+        for (int c = threadIdx.x; c < blocks; c += kThreads) {
+            one(r, c);
+            if (r + static_cast<int>(gridDim.x) < M) one(r + gridDim.x, c);
+        }
 }
 
 }  // namespace
@@ -173,12 +172,11 @@ bi_status launch_quantize_nvfp4(const void *X, int64_t ldx, float gs, uint8_t *Q
     const DeviceInfo *info;
     bi_status st = current_device(&dev, &info);
     if (st != BI_OK) return st;
-    const int64_t threads = M * (K / 16);
-    int64_t grid = (threads + kThreads - 1) / kThreads;
-    const int64_t cap = static_cast<int64_t>(info->sm_count) * 16;
-    if (grid > cap) grid = cap;
+    // one row per CTA at a time; 8 CTAs of 256 threads fill an SM
+    const int64_t cap = static_cast<int64_t>(info->sm_count) * 8;
+    const int64_t grid = M < cap ? M : cap;
     return launch_pdl(quantize_nvfp4_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, s,
-                      static_cast<const uint4 *>(X), ldx / 8, Q, Q_sf, M, static_cast<int>(K), gs,
+                      static_cast<const uint4 *>(X), ldx / 8, Q, Q_sf, static_cast<int>(M), static_cast<int>(K), gs,
                       device_status_word());
 }
 
