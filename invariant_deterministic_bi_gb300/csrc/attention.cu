@@ -604,6 +604,11 @@ struct ExtParams {
     unsigned *status;
 };
 
+// Tensor-pipe turns of the extend kernel's two warp groups (named barriers
+// 1 and 2, 256 threads: one group arrives, the other waits).
+__device__ __forceinline__ void turn_wait(int id) { asm volatile("bar.sync %0, 256;" ::"r"(id) : "memory"); }
+__device__ __forceinline__ void turn_pass(int id) { asm volatile("bar.arrive %0, 256;" ::"r"(id) : "memory"); }
+
 template <int G>
 __global__ void __launch_bounds__(kExtThreads, 1)
 attn_extend_kernel(const ExtParams p) {
@@ -688,6 +693,7 @@ attn_extend_kernel(const ExtParams p) {
 
     const int gq = lane >> 2, cq = lane & 3;           // fragment row group, column pair
     const int rt = warp;                               // this warp's 16-row tile
+    const int wg = warp >> 2;                          // warp group: 0 = A, 1 = B
     const int ra = rt * 16 + gq, rb = ra + 8;          // this thread's two rows
     // the warp's q fragments (A operand of q.k) come from shared memory by
     // ldmatrix: lane l addresses row (l / 8 % 2) * 8 + l % 8 of the tile,
@@ -730,8 +736,14 @@ attn_extend_kernel(const ExtParams p) {
 
         // tokens of this chunk each row sees (decode of the sequence cut after the row's token)
         const int na = max(0, min(kChunk, len_a - j0)), nb = max(0, min(kChunk, len_b - j0));
-        // the MMAs need the whole warp: skip only when no row of the tile sees this chunk
-        if (!__any_sync(0xffffffffu, na > 0 || nb > 0)) continue;
+        // The two warp groups (warps 0-3, 4-7; warp w and w + 4 share a
+        // scheduler) take turns on the tensor pipe: A's q.k, B's q.k, A's p.V,
+        // B's p.V, ..., each group's softmax and merge running under the other
+        // group's MMAs. Named barrier 1 hands the turn to A, 2 to B (bar.arrive
+        // by the group that finishes a phase, bar.sync by the one that starts).
+        // Every warp takes every turn and computes every chunk: rows that see
+        // nothing of it score -inf, get p = 0 and skip the merge.
+        if (wg == 1 || c > 0) turn_wait(wg == 0 ? 1 : 2);
 
         // scores s = scale * q . k for the tile's 16 rows and all 128 tokens,
         // dimensions
@@ -762,6 +774,7 @@ attn_extend_kernel(const ExtParams p) {
                 mma_16816(s[nt], qf[1][0], qf[1][1], qf[1][2], qf[1][3], b2, b3);
             }
         }
+        turn_pass(wg == 0 ? 2 : 1);
         // a chunk every row of the tile sees whole, with every block valid,
         // needs no masks
         const bool whole = !bad && __all_sync(0xffffffffu, na == kChunk && nb == kChunk);
@@ -836,6 +849,7 @@ attn_extend_kernel(const ExtParams p) {
             l[h] = x[0] + x[1];                                           // step 1
         }
 
+        turn_wait(wg == 0 ? 1 : 2);
         // values: O_c = sum_t p_t v_t for all 128 dimensions, p = hi + lo
         // (two bf16 MMAs per step), tokens ascending in 16-token steps; the
         // exponentials are already in the A-fragment layout
@@ -878,6 +892,7 @@ attn_extend_kernel(const ExtParams p) {
                 }
             }
         }
+        turn_pass(wg == 0 ? 2 : 1);
         // merge this chunk into the rows' running state, in chunk order
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -893,6 +908,8 @@ attn_extend_kernel(const ExtParams p) {
                     o_run[nt][2 * h + e] = merge_value(o_run[nt][2 * h + e], acc[nt][2 * h + e], al, be);
         }
     }
+
+    if (wg == 0) turn_wait(1);                            // B's hand-over after its last p.V
 
     // o / l, rounded to bf16, for the rows that exist
 #pragma unroll
