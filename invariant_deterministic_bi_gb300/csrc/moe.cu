@@ -24,7 +24,8 @@ __device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 
 // One warp per token. Lane l holds logits l, l+32, ...; max and the sum of
 // exponentials use fixed per-lane orders and xor butterflies; the k winners
 // come from k warp arg-max rounds under the total order (larger logit, then
-// lower expert index).
+// lower expert index), each round two warp reductions (redux.sync) on
+// order-preserving integer keys.
 template <int MAXJ>
 __global__ void __launch_bounds__(256)
 topk_softmax_kernel(const float *__restrict__ logits, int64_t T, int E, int k, int renorm, int32_t *__restrict__ ids,
@@ -53,33 +54,36 @@ topk_softmax_kernel(const float *__restrict__ logits, int64_t T, int E, int k, i
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
 
-    uint32_t taken = 0;
+    // each round: the lane's best untaken logit as an order-preserving key
+    // (zero of either sign as +0, so equal logits stay equal), the warp's
+    // largest key by one reduction, then the lowest expert holding it
+    uint32_t kv[MAXJ];
+#pragma unroll
+    for (int j = 0; j < MAXJ; ++j) {
+        const uint32_t u = __float_as_uint(v[j] == 0.0f ? 0.0f : v[j]);
+        kv[j] = lane + 32 * j < E ? ((u & 0x80000000u) ? ~u : (u | 0x80000000u)) : 0u;   // 0: no expert
+    }
     float my_w = 0.0f, wsum = 0.0f;
     for (int i = 0; i < k; ++i) {
-        float bv = -INFINITY;
-        int be = 0x7fffffff;
+        uint32_t lk = 0u, le = 0x7fffffffu;
 #pragma unroll
-        for (int j = 0; j < MAXJ; ++j) {
-            const int e = lane + 32 * j;
-            if (e < E && !((taken >> j) & 1u) && (v[j] > bv || be == 0x7fffffff)) {
-                bv = v[j];
-                be = e;
+        for (int j = 0; j < MAXJ; ++j)
+            if (kv[j] > lk) {                  // strict: the lane's lower expert wins a tie
+                lk = kv[j];
+                le = lane + 32 * j;
             }
-        }
+        const uint32_t mk = __reduce_max_sync(0xffffffffu, lk);
+        const uint32_t be = __reduce_min_sync(0xffffffffu, lk == mk ? le : 0x7fffffffu);
+        if ((be & 31u) == static_cast<uint32_t>(lane)) {
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-            if (ov > bv || (ov == bv && oe < be)) {
-                bv = ov;
-                be = oe;
-            }
+            for (int j = 0; j < MAXJ; ++j)
+                if (j == static_cast<int>(be >> 5)) kv[j] = 0u;   // taken
         }
-        if ((be & 31) == lane) taken |= 1u << (be >> 5);
+        const float bv = __uint_as_float((mk & 0x80000000u) ? (mk & 0x7fffffffu) : ~mk);
         const float wi = __fdiv_rn(expf(bv - mx), s);
         wsum += wi;
         if (lane == i) my_w = wi;
-        if (lane == 0) ids[t * k + i] = be;
+        if (lane == 0) ids[t * k + i] = static_cast<int32_t>(be);
     }
     if (lane < k) wout[t * k + lane] = renorm ? __fdiv_rn(my_w, wsum) : my_w;
 }
