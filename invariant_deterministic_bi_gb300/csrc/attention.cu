@@ -224,10 +224,10 @@ attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     // item -> (sequence b, KV head g, chunk c) and the tokens n of the chunk;
     // false when the chunk is past the sequence (or the sequence is invalid)
     auto item = [&](int64_t it, int64_t &b, int &g, int &c, int &n) {
-        c = static_cast<int>(it % p.chunks);
-        const int64_t r = it / p.chunks;
-        g = static_cast<int>(r % p.Hkv);
-        b = r / p.Hkv;
+        g = static_cast<int>(it % p.Hkv);               // KV head fastest: the heads of one
+        const int64_t r = it / p.Hkv;                    // cache block are read together
+        c = static_cast<int>(r % p.chunks);
+        b = r / p.chunks;
         int L;
         if (!seq_ok(p, b, L)) {
             if (warp == kDecConsumers && lane == 0 && c == 0 && g == 0) atomicOr(p.status, kDevBadOffsets);   // loader 0
