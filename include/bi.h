@@ -415,7 +415,7 @@ typedef struct {
     int32_t block_m, block_n, block_k;   /* CTA tile (rows, cols, K step); RMSNorm: 1 row per CTA, H, 8 */
     int32_t mma_m, mma_n, mma_k;         /* tcgen05.mma instruction shape (0 for RMSNorm) */
     int32_t k_steps;                     /* K steps per output tile (fixed by K); RMSNorm: vectors per thread */
-    int32_t split_k;                     /* always 1: no split of the K reduction */
+    int32_t split_k;                     /* bf16 GEMM: K segments S (1..4, fixed by N, K); others 1 */
     int32_t stages;                      /* shared-memory pipeline depth */
     int32_t threads;                     /* threads per CTA */
     int32_t smem_bytes;                  /* dynamic shared memory per CTA */
