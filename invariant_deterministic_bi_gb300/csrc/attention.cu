@@ -519,16 +519,17 @@ __global__ void __launch_bounds__(kCombineThreads)
 attn_combine_kernel(const AttnParams p) {
     grid_dep_wait();      // earlier work of the stream is complete and visible
     grid_dep_launch();
-    // Chunk statistics go through shared memory in tiles of kCombineThreads
-    // chunks, loaded in parallel; the running maximum of the tile is a prefix
-    // maximum (exact in any order), so every chunk's merge factors are known
-    // before the sequential, chunk-order merge of the o values (thread d
-    // merges dimension d).
-    __shared__ float fm[kCombineThreads];     // m_c, then the running maximum after chunk c
-    __shared__ float fa[kCombineThreads];     // alpha of chunk c
-    __shared__ float fb[kCombineThreads];     // beta of chunk c
-    __shared__ float fl[kCombineThreads];     // l_c
-    __shared__ float carry;                   // running maximum after the previous tile
+    // Chunks in tiles of 32. Every thread issues the tile's o loads of its
+    // dimension d at once; meanwhile warp 0 loads the tile's (m_c, l_c), one
+    // chunk per lane: the running maximum before chunk c is a prefix maximum
+    // (exact in any order: a shuffle scan), and chunk c's merge factors
+    // depend only on it and m_c, so each lane computes its chunk's factors.
+    // Then each thread merges its o values in chunk order: the same
+    // operations, in the same order, as a sequential walk over the chunks.
+    constexpr int kTile = 32;
+    __shared__ float fa[kTile];               // alpha of chunk c
+    __shared__ float fb[kTile];               // beta of chunk c
+    __shared__ float fl[kTile];               // l_c
     const int h = blockIdx.x;
     const int64_t b = blockIdx.y;
     const int d = threadIdx.x;
@@ -537,44 +538,42 @@ attn_combine_kernel(const AttnParams p) {
     const int nc = (L + kChunk - 1) / kChunk;
     if (!BI_IN_BOUNDS(nc <= p.chunks, p.status)) return;   // debug build: inside the workspace
     const float *w = p.ws + (b * p.Hq + h) * p.chunks * (kD + 2);
-    if (d == 0) carry = -INFINITY;
-    float o = 0.0f, l = 0.0f;
-    for (int c0 = 0; c0 < nc; c0 += kCombineThreads) {
-        const int nt = min(kCombineThreads, nc - c0);
-        __syncthreads();                                   // previous tile fully consumed
-        if (d < nt) {
-            const float *wc = w + static_cast<int64_t>(c0 + d) * (kD + 2);
-            fm[d] = wc[0];
-            fl[d] = wc[1];
-        }
-        __syncthreads();
-        if (d == 0) {                                      // factors in chunk order
-            float m = carry;
-            for (int c = 0; c < nt; ++c) {
-                float mn, a, bt;
-                merge_factors(m, fm[c], mn, a, bt);
-                fa[c] = a;
-                fb[c] = bt;
-                m = mn;
-            }
-            carry = m;
-        }
-        __syncthreads();
+    float o = 0.0f, l = 0.0f, m_run = -INFINITY;           // m_run: warp 0's copy of the running maximum
+    for (int c0 = 0; c0 < nc; c0 += kTile) {
+        const int nt = min(kTile, nc - c0);
         const float *oc = w + static_cast<int64_t>(c0) * (kD + 2) + 2 + d;
-        int c = 0;
-        for (; c + 8 <= nt; c += 8) {                      // 8 independent loads in flight
-            float o8[8];
+        float ov[kTile];                                   // in flight while warp 0 prepares the factors
 #pragma unroll
-            for (int i = 0; i < 8; ++i) o8[i] = oc[static_cast<int64_t>(c + i) * (kD + 2)];
+        for (int c = 0; c < kTile; ++c) ov[c] = c < nt ? oc[static_cast<int64_t>(c) * (kD + 2)] : 0.0f;
+        __syncthreads();                                   // previous tile fully consumed
+        if (d < 32) {
+            const float *wc = w + static_cast<int64_t>(c0 + d) * (kD + 2);
+            const float mc = d < nt ? wc[0] : -INFINITY;
+            const float lc = d < nt ? wc[1] : 0.0f;
+            float incl = mc;                               // max(m_c0 .. m_c) over the tile
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                o = merge_value(o, o8[i], fa[c + i], fb[c + i]);
-                l = merge_value(l, fl[c + i], fa[c + i], fb[c + i]);
+            for (int off = 1; off < 32; off <<= 1) {
+                const float v = __shfl_up_sync(0xffffffffu, incl, off);
+                if (d >= off) incl = fmaxf(incl, v);
             }
+            float before = __shfl_up_sync(0xffffffffu, incl, 1);
+            before = d == 0 ? m_run : fmaxf(m_run, before);   // running maximum before chunk c0 + d
+            float mn, a, bt;
+            merge_factors(before, mc, mn, a, bt);
+            if (d < nt) {
+                fa[d] = a;
+                fb[d] = bt;
+                fl[d] = lc;
+            }
+            m_run = fmaxf(m_run, __shfl_sync(0xffffffffu, incl, 31));
         }
-        for (; c < nt; ++c) {
-            o = merge_value(o, oc[static_cast<int64_t>(c) * (kD + 2)], fa[c], fb[c]);
-            l = merge_value(l, fl[c], fa[c], fb[c]);
+        __syncthreads();
+#pragma unroll
+        for (int c = 0; c < kTile; ++c) {
+            if (c < nt) {
+                o = merge_value(o, ov[c], fa[c], fb[c]);
+                l = merge_value(l, fl[c], fa[c], fb[c]);
+            }
         }
     }
     const float r = __fdiv_rn(o, l);
