@@ -130,6 +130,14 @@ struct AttnParams {
     unsigned *status;
 };
 
+// A read-only load issued where it stands (the table is not written while a
+// kernel of this file runs).
+__device__ __forceinline__ int32_t ld_nc_s32(const int32_t *ptr) {
+    int32_t v;
+    asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(v) : "l"(ptr));
+    return v;
+}
+
 __device__ __forceinline__ bool seq_ok(const AttnParams &p, int64_t b, int &L) {
     L = p.lens[b];
     return L >= 1 && L <= p.max_len && L <= static_cast<int64_t>(p.max_blocks) * p.bs;
@@ -248,6 +256,17 @@ attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         }
         int k = 0, last = -1;
         for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
+            // the item's block-table entries (boxes: lane i < kChunk / box_rows
+            // reads box i's) are requested before its sequence length is
+            // known, so the two reads overlap instead of following each other
+            int32_t spec_blk = -1;
+            if (p.box_rows > 0) {
+                const int64_t r = it / p.Hkv;
+                const int64_t bb = r / p.chunks;
+                const int64_t bi = ((r % p.chunks) * kChunk + lane * p.box_rows) / p.bs;
+                if (lane < kChunk / p.box_rows && bb < p.batch && bi < p.max_blocks)
+                    spec_blk = ld_nc_s32(p.table + bb * p.max_blocks + bi);
+            }
             int64_t b;
             int g, c, n;
             if (!item(it, b, g, c, n)) continue;
@@ -263,7 +282,7 @@ attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             const int nbox = p.box_rows > 0 ? (n + p.box_rows - 1) / p.box_rows : 0;
             if (p.box_rows > 0) {
                 if (lane < nbox) {
-                    box_blk = p.table[b * p.max_blocks + (j0 + lane * p.box_rows) / p.bs];
+                    box_blk = spec_blk;            // p.table[b][(j0 + lane * box_rows) / bs]
                     if (box_blk < 0 || box_blk >= p.num_blocks) atomicOr(p.status, kDevBadOffsets);
                 }
 #pragma unroll
