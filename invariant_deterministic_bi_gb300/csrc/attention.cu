@@ -254,6 +254,9 @@ attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
         }
+        // K and V rows are read once: evict them from L2 first, so that the
+        // chunk partials the combine step reads stay there
+        const uint64_t kv_policy = l2_policy_evict_first();
         int k = 0, last = -1;
         for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
             // the item's block-table entries (boxes: lane i < kChunk / box_rows
@@ -350,8 +353,8 @@ attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         const int dst = half * kHalfTile + lane * p.box_rows * 128;
-                        tma_load_4d(Ks + dst, &tmK, fb, half * 64, g, tok, box_blk);
-                        tma_load_4d(Vs + dst, &tmV, fb, half * 64, g, tok, box_blk);
+                        tma_load_4d_hint(Ks + dst, &tmK, fb, half * 64, g, tok, box_blk, kv_policy);
+                        tma_load_4d_hint(Vs + dst, &tmV, fb, half * 64, g, tok, box_blk, kv_policy);
                     }
                 }
                 if (lane == 0) bulk_load(qs, qsrc, G * kRowBytes, fb);

@@ -100,6 +100,25 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *m, uin
         : "memory");
 }
 
+// An L2 policy for data read once: its lines are the first to be evicted,
+// so a stream of them does not push out data that is read again soon.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// tma_load_4d with an L2 cache policy (from createpolicy).
+__device__ __forceinline__ void tma_load_4d_hint(void *dst, const CUtensorMap *m, uint64_t *bar, int32_t c0,
+                                                 int32_t c1, int32_t c2, int32_t c3, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2),
+          "r"(c3), "l"(policy)
+        : "memory");
+}
+
 // TMA 2-D store from this CTA's shared memory (bulk async-group completion).
 // Rows and columns outside the tensor map's extent are not written.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *m, const void *src, int32_t c0, int32_t c1) {
