@@ -343,6 +343,42 @@ def rmsnorm_sweep(bi, peaks):
     return rows
 
 
+RANK_SUM_R = [2, 4, 8]
+RANK_SUM_M = [1, 128, 16384]
+
+
+def rank_sum_sweep(bi, peaks):
+    """The tensor-parallel all-reduce + RMSNorm step (bi_rank_sum_rmsnorm) with R
+    ranks' partial rows resident on this GPU (as after a gather), residual
+    updated in place: HBM bytes = (2R + 6) M H (R parts and the residual read,
+    residual and output written)."""
+    import torch
+    import bi_synth as syn
+    rows = []
+    for R in RANK_SUM_R:
+        for M in RANK_SUM_M:
+            nbytes = (2 * R + 6) * M * H
+            sets = []
+            g = torch.Generator(device="cuda").manual_seed(R * 1000 + M)
+            _, _, w, _ = syn.rmsnorm_inputs(1, H, seed=0)
+            wd = bf16_dev(w)
+            for j in range(l2_sets(nbytes, cap=8)):   # values do not matter for the timing
+                parts = [torch.randn((M, H), device="cuda", generator=g).to(torch.bfloat16) for _ in range(R)]
+                res = torch.randn((M, H), device="cuda", generator=g).to(torch.bfloat16)
+                sets.append((parts, res, wd, torch.empty((M, H), dtype=torch.bfloat16, device="cuda")))
+            sel = rotate(sets)
+
+            def ours():
+                parts, res, w, out = sel()
+                bi.rank_sum_rmsnorm(parts, w, EPS, residual=res, out=out)
+            t = time_fn(ours, 200 if M <= 128 else 30)
+            gbs = nbytes / (t * 1e-3) / 1e9
+            rows.append({"R": R, "M": M, "H": H, "us": round(t * 1e3, 2), "gbs": round(gbs, 0),
+                         "frac_hbm_measured": round(gbs / peaks["hbm_gbs"], 3)})
+            del sets
+    return rows
+
+
 def torch_rmsnorm_row0_equal() -> bool:
     """Informational: is torch.nn.functional.rms_norm batch-invariant here, i.e.
     does row 0 of an M=16384 call equal the same row normalised alone?"""
@@ -883,6 +919,7 @@ def run_ours(args, dist):
         breakdown["cublas_row0_equal_M1_vs_M4096"] = cublas_inv
         breakdown["rmsnorm"] = rmsnorm_sweep(bi, peaks)
         breakdown["torch_rms_norm_row0_equal_M1_vs_M16384"] = torch_rmsnorm_row0_equal()
+        breakdown["rank_sum_rmsnorm"] = rank_sum_sweep(bi, peaks)
         breakdown["grouped_gemm_bf16_moe"] = moe_sweep(bi, peaks)
         breakdown["gemm_nvfp4"] = nvfp4_sweep(bi, peaks)
         breakdown["quantize_nvfp4"] = quant_sweep(bi, peaks)
@@ -965,6 +1002,7 @@ def profile_case(spec: str, reps: int):
     """Run one kernel configuration `reps` times (for ncu captures); no output line.
     spec: gemm:<qkv|gate_up|down>:<M> | rmsnorm:<M>:<0|1 residual> | grouped:<gate_up|down>:<T> |
           nvfp4:<M> | quant:<M> | attention:<B> (decode, 4096 cached tokens per sequence) |
+          rank_sum:<R>:<M> (all-reduce + RMSNorm over R resident parts) |
           moe_layer:<T> (the whole MoE layer, gate_up with SiLU-mul fused) |
           extend:<B>:<new tokens>:<cached> (prefill attention)"""
     import torch
@@ -985,6 +1023,14 @@ def profile_case(spec: str, reps: int):
         xd, rd, wd = bf16_dev(x), (bf16_dev(r) if res else None), bf16_dev(w)
         out = torch.empty_like(xd)
         fn = lambda: bi.rmsnorm(xd, wd, EPS, residual=rd, out=out)
+    elif kind == "rank_sum":
+        R, M = int(rest[0]), int(rest[1])
+        g = torch.Generator(device="cuda").manual_seed(0)
+        parts = [torch.randn((M, H), device="cuda", generator=g).to(torch.bfloat16) for _ in range(R)]
+        rd = torch.randn((M, H), device="cuda", generator=g).to(torch.bfloat16)
+        wd = bf16_dev(syn.rmsnorm_inputs(1, H, seed=0)[2])
+        out = torch.empty_like(rd)
+        fn = lambda: bi.rank_sum_rmsnorm(parts, wd, EPS, residual=rd, out=out)
     elif kind == "nvfp4":
         M = int(rest[0])
         d = syn.nvfp4_inputs(M, NVFP4_N, NVFP4_K, seed=0)

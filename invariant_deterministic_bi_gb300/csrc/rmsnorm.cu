@@ -146,28 +146,59 @@ rank_sum_rmsnorm_kernel(const RankParts parts, int R, uint4 *residual, const uin
     const int nvec = H >> 3;
     const int t = threadIdx.x;
     uint4 *rr = RESIDUAL ? residual + row * nvec : nullptr;
+    // Every element is summed over the ranks in order 0, 1, ..., R-1. Up to
+    // 8 vectors a thread, the rank loop is outside the row's vectors so that
+    // each thread has VPT (twice that, unrolled) independent loads in flight
+    // rather than one; longer rows keep one vector's sum at a time.
     uint4 h[VPT];
+    auto finish = [&](int i, int j, const float (&acc)[8]) {
+        uint4 a;
+        a.x = pack_bf16x2(__float_as_uint(acc[0]), __float_as_uint(acc[1]));
+        a.y = pack_bf16x2(__float_as_uint(acc[2]), __float_as_uint(acc[3]));
+        a.z = pack_bf16x2(__float_as_uint(acc[4]), __float_as_uint(acc[5]));
+        a.w = pack_bf16x2(__float_as_uint(acc[6]), __float_as_uint(acc[7]));
+        if (sum_out) __stcs(sum_out + row * nvec + j, a);
+        h[i] = RESIDUAL ? add_round(a, __ldcs(rr + j)) : a;
+    };
+    auto add8 = [](float (&acc)[8], const uint4 &v) {
+        const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int i = 0; i < VPT; ++i) {
-        const int j = t + T * i;
-        if (j < nvec) {
-            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            for (int r = 0; r < R; ++r) {
-                const uint4 v = __ldcs(parts.p[r] + row * nvec + j);
-                const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+        for (int q = 0; q < 4; ++q) {
+            acc[2 * q] = __fadd_rn(acc[2 * q], bf_lo(vw[q]));
+            acc[2 * q + 1] = __fadd_rn(acc[2 * q + 1], bf_hi(vw[q]));
+        }
+    };
+    if constexpr (VPT <= 8) {
+        float acc[VPT][8];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    acc[2 * q] = __fadd_rn(acc[2 * q], bf_lo(vw[q]));
-                    acc[2 * q + 1] = __fadd_rn(acc[2 * q + 1], bf_hi(vw[q]));
-                }
+        for (int i = 0; i < VPT; ++i)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[i][e] = 0.0f;
+#pragma unroll 2
+        for (int r = 0; r < R; ++r) {
+            uint4 v[VPT];
+#pragma unroll
+            for (int i = 0; i < VPT; ++i) {
+                const int j = t + T * i;
+                v[i] = j < nvec ? __ldcs(parts.p[r] + row * nvec + j) : make_uint4(0u, 0u, 0u, 0u);
             }
-            uint4 a;
-            a.x = pack_bf16x2(__float_as_uint(acc[0]), __float_as_uint(acc[1]));
-            a.y = pack_bf16x2(__float_as_uint(acc[2]), __float_as_uint(acc[3]));
-            a.z = pack_bf16x2(__float_as_uint(acc[4]), __float_as_uint(acc[5]));
-            a.w = pack_bf16x2(__float_as_uint(acc[6]), __float_as_uint(acc[7]));
-            if (sum_out) __stcs(sum_out + row * nvec + j, a);
-            h[i] = RESIDUAL ? add_round(a, __ldcs(rr + j)) : a;
+#pragma unroll
+            for (int i = 0; i < VPT; ++i) add8(acc[i], v[i]);
+        }
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+            const int j = t + T * i;
+            if (j < nvec) finish(i, j, acc[i]);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+            const int j = t + T * i;
+            if (j < nvec) {
+                float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                for (int r = 0; r < R; ++r) add8(acc, __ldcs(parts.p[r] + row * nvec + j));
+                finish(i, j, acc);
+            }
         }
     }
     float ss = 0.0f;
