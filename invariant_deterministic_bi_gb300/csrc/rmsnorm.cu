@@ -131,13 +131,15 @@ rmsnorm_kernel(const uint4 *x, uint4 *residual, const uint4 *__restrict__ w, uin
 // its fused all-reduce + RMSNorm under batch invariance because that kernel's
 // reduction order varies between runs; here the order is the rank index.
 constexpr int kMaxRanks = 16;
+// Passed as a __grid_constant__ kernel parameter: p[r] with a run-time r is
+// read from parameter space instead of from a per-thread local copy.
 struct RankParts {
     const uint4 *p[kMaxRanks];
 };
 
 template <int T, int VPT, bool RESIDUAL>
 __global__ void __launch_bounds__(T)
-rank_sum_rmsnorm_kernel(const RankParts parts, int R, uint4 *residual, const uint4 *__restrict__ w, uint4 *sum_out,
+rank_sum_rmsnorm_kernel(const __grid_constant__ RankParts parts, int R, uint4 *residual, const uint4 *__restrict__ w, uint4 *sum_out,
                         uint4 *out, int H, float eps) {
     grid_dep_wait();      // earlier work of the stream is complete and visible
     grid_dep_launch();
