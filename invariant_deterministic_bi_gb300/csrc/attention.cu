@@ -619,7 +619,7 @@ struct ExtParams {
     const int32_t *table;    // [B][max_blocks]
     const int32_t *lens;     // [B], cached length including the new tokens
     uint16_t *O;             // [total_q][Hq][D]
-    int64_t num_blocks;
+    int64_t num_blocks, batch;
     int32_t total_q, max_blocks, Hq, Hkv, bs, max_len, max_q;
     float scale;
     unsigned *status;
@@ -640,11 +640,13 @@ attn_extend_kernel(const ExtParams p) {
     uint8_t *KV = smem;                                                    // [2][K, V] tiles, swizzled rows
     uint16_t *qb = reinterpret_cast<uint16_t *>(smem + 4 * kTileBytes);   // [kExtRows][kD] bf16
     int64_t *rowoff = reinterpret_cast<int64_t *>(qb + kExtRows * kD);     // [3][kChunk], -1: no row
-    // blockIdx.x = (tile from the last, KV head): the tiles with the latest
-    // tokens (the most chunks) start first, so the light ones fill the tail
+    // blockIdx.x = (tile from the last, sequence, KV head): the tiles with the
+    // latest tokens (the most chunks) of every sequence start first, so the
+    // light ones fill the tail
+    const int64_t per_tile = static_cast<int64_t>(p.batch) * p.Hkv;
     const int g = static_cast<int>(blockIdx.x % static_cast<unsigned>(p.Hkv));
-    const int tile = static_cast<int>(gridDim.x / static_cast<unsigned>(p.Hkv) - 1 - blockIdx.x / p.Hkv);
-    const int64_t b = blockIdx.y;
+    const int64_t b = (blockIdx.x / static_cast<unsigned>(p.Hkv)) % p.batch;
+    const int tile = static_cast<int>(gridDim.x / per_tile - 1 - blockIdx.x / per_tile);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t q0 = p.cu_q[b], q1 = p.cu_q[b + 1];
     const int L = p.lens[b];
@@ -662,13 +664,13 @@ attn_extend_kernel(const ExtParams p) {
     const int nchunks = (L_last + kChunk - 1) / kChunk;
 
     // q rows: row r = token r / G, head g*G + r % G (zero rows past the
-    // tokens); 16-byte piece x of row r at piece x ^ (r % 8)
+    // tokens); 16-byte piece x of row r at piece x ^ (r % 8). Copied by
+    // cp.async in chunk 0's group, so they travel while the block table is read.
     for (int i = tid; i < kExtRows * kD / 8; i += kExtThreads) {
         const int r = i / (kD / 8), x = i % (kD / 8);
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (r / G < ntok)
-            v = *reinterpret_cast<const uint4 *>(p.Q + ((q0 + i0 + r / G) * p.Hq + g * G + r % G) * kD + x * 8);
-        *reinterpret_cast<uint4 *>(qb + r * kD + ((x ^ (r & 7)) * 8)) = v;
+        const bool v = r / G < ntok;
+        cp_async_16(smem_u32(qb + r * kD + ((x ^ (r & 7)) * 8)),
+                    v ? p.Q + ((q0 + i0 + r / G) * p.Hq + g * G + r % G) * kD + x * 8 : p.Q, v ? 16u : 0u);
     }
     // row offsets of chunk c's K/V rows (threads 0..127; buffer c % 3, so a
     // buffer is rewritten only after every warp has left the chunk that used it)
@@ -1051,6 +1053,7 @@ bi_status launch_attention_extend(const void *Q, const int32_t *cu_q, int32_t to
     p.lens = lens;
     p.O = static_cast<uint16_t *>(O);
     p.num_blocks = num_blocks;
+    p.batch = B;
     p.total_q = total_q;
     p.max_blocks = max_blocks;
     p.Hq = Hq;
@@ -1062,9 +1065,9 @@ bi_status launch_attention_extend(const void *Q, const int32_t *cu_q, int32_t to
     p.status = device_status_word();
     const int G = Hq / Hkv;
     const int tq = kExtRows / G;
-    const int64_t ctas_x = (static_cast<int64_t>(max_q) + tq - 1) / tq * Hkv;   // (tile, KV head)
+    const int64_t ctas_x = (static_cast<int64_t>(max_q) + tq - 1) / tq * B * Hkv;   // (tile, sequence, KV head)
     if (ctas_x > 0x7fffffff) return BI_ERR_UNSUPPORTED;
-    const dim3 grid(static_cast<unsigned>(ctas_x), static_cast<unsigned>(B));
+    const dim3 grid(static_cast<unsigned>(ctas_x));
     switch (G) {
         case 1: return launch_extend_g<1>(grid, p, s);
         case 2: return launch_extend_g<2>(grid, p, s);
