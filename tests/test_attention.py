@@ -29,7 +29,8 @@ def run(bi, Q, K, V, table, lens, max_len):
                                        to_dev(lens), max_len, SCALE))
 
 
-@pytest.mark.parametrize("lens", [[1, 300, 1000], [127, 128, 129, 255], [256, 257, 512, 513], [4096, 7]])
+@pytest.mark.parametrize("lens", [[1, 300, 1000], [127, 128, 129, 255], [256, 257, 512, 513], [4096, 7],
+                                  [4097, 8192, 8193, 33]])   # the merge takes chunks in tiles of 32
 def test_parity(bi, lens):
     K, V, table, lens = make_cache(lens, seed=len(lens))
     B = len(lens)
