@@ -37,6 +37,27 @@ def test_parity(bi, R, M):
     assert bi.device_status() == bi.BI_OK
 
 
+@pytest.mark.parametrize("R", [3, 5, 16])
+@pytest.mark.parametrize("H", [4096, 16384])
+def test_rank_order_is_the_stated_one(bi, R, H):
+    """The all-reduced row is bf16 of the fp32 sum in rank order 0, 1, ..., R-1
+    (each addition rounded to nearest even), bit for bit: numpy float32
+    additions in that order give the same bits. Odd R and R = 16 (the
+    largest), and a row long enough for the kernel's other loop order."""
+    import torch
+    M = 37
+    P = parts_for(R, M, H, seed=3)
+    _, _, w, _ = syn.rmsnorm_inputs(M, H, seed=4)
+    pd = [to_dev_bf16(P[r]) for r in range(R)]
+    a_out = torch.empty_like(pd[0])
+    bi.rank_sum_rmsnorm(pd, to_dev_bf16(w), EPS, sum_out=a_out)
+    acc = np.zeros((M, H), dtype=np.float32)
+    for r in range(R):
+        acc = (acc + syn.bf16_bits_to_f32(P[r])).astype(np.float32)
+    assert np.array_equal(bits_of(a_out), syn.to_bf16_bits(acc))
+    assert bi.device_status() == bi.BI_OK
+
+
 def test_one_rank_is_rmsnorm(bi):
     M, H = 300, 4096
     x, res, w, _ = syn.rmsnorm_inputs(M, H, seed=2)
