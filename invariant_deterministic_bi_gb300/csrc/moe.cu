@@ -182,6 +182,68 @@ align_rank_kernel(const int32_t *__restrict__ ids, int64_t P, int64_t seg, int S
     }
 }
 
+// Few pairs (at most kSmallAlign): the whole alignment in one block. The ids
+// are staged in shared memory by all threads; warp 0 walks the pairs in
+// order, 32 at a time: the lanes routed to the same
+// expert are grouped (__match_any_sync), a pair's rank is the expert's
+// running count plus the lanes before it in its group, and the group's
+// lowest lane advances the count. Then the counts are scanned into offsets
+// and every thread places its pairs. Integer only: the same unique stable
+// order as the multi-block path.
+constexpr int kSmallAlign = 128;
+__global__ void __launch_bounds__(1024)
+align_small_kernel(const int32_t *__restrict__ ids, int P, int k, int E, int32_t *__restrict__ offsets,
+                   int32_t *__restrict__ row_token, int32_t *__restrict__ pos, unsigned *status) {
+    grid_dep_wait();      // earlier work of the stream is complete and visible
+    grid_dep_launch();
+    __shared__ int cnt[1024];                 // per expert: pairs so far, then all its pairs
+    __shared__ int incl[1024];                // inclusive prefix of the counts
+    __shared__ int rank[kSmallAlign];         // a pair's rank within its expert; -1: id outside [0, E)
+    __shared__ int id_s[kSmallAlign];
+    const int t = threadIdx.x, lane = t & 31;
+    cnt[t] = 0;
+    for (int p = t; p < P; p += 1024) id_s[p] = ids[p];
+    __syncthreads();
+    if (t < 32) {
+        bool bad = false;
+        for (int p0 = 0; p0 < P; p0 += 32) {
+            const int p = p0 + lane;
+            int e = p < P ? id_s[p] : -1;
+            if (p < P && (e < 0 || e >= E)) {
+                bad = true;
+                e = -1;
+            }
+            const unsigned same = __match_any_sync(0xffffffffu, e);
+            const int before = __popc(same & ((1u << lane) - 1u));
+            const int base = e >= 0 ? cnt[e] : 0;
+            __syncwarp();
+            if (p < P) rank[p] = e >= 0 ? base + before : -1;
+            if (e >= 0 && before == 0) cnt[e] = base + __popc(same);
+            __syncwarp();
+        }
+        if (bad) atomicOr(status, kDevBadOffsets);
+    }
+    __syncthreads();
+    incl[t] = t < E ? cnt[t] : 0;
+    __syncthreads();
+    for (int d = 1; d < 1024; d <<= 1) {      // Hillis-Steele: integer adds, order-free
+        const int add = t >= d ? incl[t - d] : 0;
+        __syncthreads();
+        incl[t] += add;
+        __syncthreads();
+    }
+    if (t < E) offsets[t + 1] = incl[t];
+    if (t == 0) offsets[0] = 0;
+    for (int p = t; p < P; p += 1024) {
+        const int r = rank[p];
+        if (r < 0) continue;
+        const int e = id_s[p];
+        const int o = incl[e] - cnt[e] + r;
+        pos[p] = o;
+        row_token[o] = p / k;
+    }
+}
+
 // Step 2 (one block): offsets[1..E] counts -> inclusive prefix, in place.
 __global__ void __launch_bounds__(1024) align_scan_kernel(int32_t *offsets, int E) {
     grid_dep_wait();      // earlier work of the stream is complete and visible
@@ -348,6 +410,9 @@ bi_status launch_moe_align(const int32_t *ids, int64_t T, int32_t k, int32_t E, 
     bi_status st = current_device(&dev, &info);
     if (st != BI_OK) return st;
     const int64_t P = T * k;
+    if (P <= kSmallAlign)
+        return launch_pdl(align_small_kernel, dim3(1), dim3(1024), 0, s, ids, static_cast<int>(P), k, E, offsets,
+                          row_token, pos, device_status_word());
     // segments of whole 1024-pair passes, at most 32 per expert, E * S <= P;
     // below 16384 pairs one segment (no counting pass) is quicker
     int S = 1;

@@ -38,7 +38,7 @@ def test_topk_softmax(bi, T, renorm):
         assert np.array_equal(w1.cpu().numpy()[0], w.cpu().numpy()[t])
 
 
-@pytest.mark.parametrize("T", [1, 7, 512, 8192])
+@pytest.mark.parametrize("T", [1, 7, 16, 17, 512, 2048, 8192])   # one block up to 128 pairs, then the multi-block path
 def test_align_exact(bi, T):
     ids = oracle.moe_topk_softmax(logits_for(T, seed=1), TOPK)[0]
     off, row_token, pos = bi.moe_align(to_dev(ids), E)
@@ -48,10 +48,23 @@ def test_align_exact(bi, T):
     assert np.array_equal(pos.cpu().numpy(), o_pos)
 
 
-def test_align_with_unaligned_ids(bi):
-    """An id array that starts 4 bytes past a 16-byte boundary takes the scalar path: same result."""
+@pytest.mark.parametrize("E_,T,k", [(1, 100, 1), (1, 300, 1), (3, 60, 2), (3, 2000, 2), (1024, 4, 8), (1024, 16, 8),
+                                     (1024, 600, 4), (1024, 3000, 8)])
+def test_align_exact_expert_counts(bi, E_, T, k):
+    """Any ids in [0, E): one expert, few experts, the largest E, both paths."""
+    ids = np.random.default_rng(E_ * 7 + T).integers(0, E_, size=(T, k)).astype(np.int32)
+    off, row_token, pos = bi.moe_align(to_dev(ids), E_)
+    o_off, o_rt, o_pos = oracle.moe_align(ids, E_)
+    assert np.array_equal(off.cpu().numpy(), o_off)
+    assert np.array_equal(row_token.cpu().numpy(), o_rt)
+    assert np.array_equal(pos.cpu().numpy(), o_pos)
+
+
+@pytest.mark.parametrize("T", [300, 3000])
+def test_align_with_unaligned_ids(bi, T):
+    """An id array that starts 4 bytes past a 16-byte boundary (the multi-block
+    path's scalar loads at T = 3000): same result."""
     import torch
-    T = 300
     ids = oracle.moe_topk_softmax(logits_for(T, seed=3), TOPK)[0]
     buf = torch.zeros(T * TOPK + 1, dtype=torch.int32, device="cuda")
     buf[1:] = to_dev(ids).view(-1)
