@@ -153,3 +153,28 @@ def test_block_outside_the_cache_reported(bi, bs):
     good = run(bi, Q[1:], K2, V2, t2[1:], lens[1:], 256)
     assert np.array_equal(got[1], good[0])
     assert np.all(np.isfinite(syn.bf16_bits_to_f32(got)))
+
+
+def test_parity_at_the_bench_size_sampled(bi):
+    """The size the bench times: 64 sequences of 4096 cached tokens (the
+    persistent ring shape), Qwen3-8B heads, 16-token blocks in a random order;
+    two sequences cut short (a partial last chunk). Six sequences are checked
+    whole against the oracle, on their own blocks."""
+    import torch
+    B, L = 64, 4096
+    nb = L // BS
+    g = torch.Generator(device="cuda").manual_seed(5)
+    K = torch.randn((B * nb, BS, HKV, D), device="cuda", generator=g).to(torch.bfloat16)
+    V = torch.randn((B * nb, BS, HKV, D), device="cuda", generator=g).to(torch.bfloat16)
+    table = torch.randperm(B * nb, device="cuda", generator=g).to(torch.int32).view(B, nb)
+    lens = torch.full((B,), L, dtype=torch.int32, device="cuda")
+    lens[3], lens[40] = 4000, 129
+    Q = torch.randn((B, HQ, D), device="cuda", generator=g).to(torch.bfloat16)
+    got = bits_of(bi.attention_decode(Q, K, V, table, lens, L, SCALE))
+    assert bi.device_status() == bi.BI_OK
+    for b in [0, 3, 17, 40, 62, 63]:
+        blk = table[b].long()
+        n = int(lens[b].item())
+        ref = oracle.attention_decode(bits_of(Q[b:b + 1]), bits_of(K[blk]), bits_of(V[blk]),
+                                      np.arange(nb, dtype=np.int32)[None], np.array([n], dtype=np.int32), SCALE)
+        assert_close_rel(syn.bf16_bits_to_f32(got[b:b + 1]).astype(np.float64), ref, 1e-2, 2e-3, f"sequence {b}")

@@ -155,3 +155,26 @@ def test_block_sizes(bi, bs):
                                           to_dev(t2[:1]), to_dev(np.array([i + 1], np.int32)), L, SCALE))
         assert np.array_equal(one[0], got[i]), f"bs={bs}: token {i} differs from decode"
     assert bi.device_status() == bi.BI_OK
+
+
+def test_parity_at_the_bench_size_sampled(bi):
+    """The size the bench times: one 4096-token prefill over its 4096 cached
+    tokens (every query tile of the grid), Qwen3-8B heads. Sampled tokens
+    at chunk edges are checked against the oracle's decode of the sequence
+    cut after each."""
+    import torch
+    L = 4096
+    nb = L // BS
+    g = torch.Generator(device="cuda").manual_seed(6)
+    K = torch.randn((nb, BS, HKV, D), device="cuda", generator=g).to(torch.bfloat16)
+    V = torch.randn((nb, BS, HKV, D), device="cuda", generator=g).to(torch.bfloat16)
+    table = torch.randperm(nb, device="cuda", generator=g).to(torch.int32).view(1, nb)
+    lens = torch.tensor([L], dtype=torch.int32, device="cuda")
+    cu = torch.tensor([0, L], dtype=torch.int32, device="cuda")
+    Q = torch.randn((L, HQ, D), device="cuda", generator=g).to(torch.bfloat16)
+    got = bits_of(bi.attention_extend(Q, cu, K, V, table, lens, L, L, SCALE))
+    assert bi.device_status() == bi.BI_OK
+    Kb, Vb, tb = bits_of(K), bits_of(V), table.cpu().numpy()
+    for i in [0, 31, 127, 128, 1000, 2049, 4095]:
+        ref = oracle.attention_decode(bits_of(Q[i:i + 1]), Kb, Vb, tb, np.array([i + 1], dtype=np.int32), SCALE)
+        assert_close_rel(syn.bf16_bits_to_f32(got[i:i + 1]).astype(np.float64), ref, RTOL, ATOL, f"token {i}")
