@@ -44,6 +44,29 @@ def test_bit_exact_against_oracle(bi, M, K):
     assert np.array_equal(S_il, syn.swizzle_block_scales(So)), "scale padding"
 
 
+def test_bit_exact_at_the_bench_size_sampled(bi):
+    """The size the bench times (M=16384, K=4096: the multi-row grid, two rows
+    per step): codes and scales of sampled rows, bit-exact against the oracle
+    quantising those rows alone with the full tensor's global scale (the
+    quantiser is row-local)."""
+    import torch
+    M, K = 16384, 4096
+    g = torch.Generator(device="cuda").manual_seed(7)
+    X = torch.randn((M, K), device="cuda", generator=g).to(torch.bfloat16)
+    X[5000] *= 50.0                                     # an outlier row sets the global scale
+    Xb_all = bits_of(X)
+    gs = syn.nvfp4_global_scale(syn.bf16_bits_to_f32(Xb_all))
+    Q, S_il = bi.quantize_nvfp4(X, gs)
+    torch.cuda.synchronize()
+    Q, S_il = Q.cpu().numpy(), S_il.cpu().numpy()
+    S = unswizzle_block_scales(S_il, M, K // 16)
+    rows = [0, 1, 127, 128, 5000, 8191, 8192, 16383]
+    Qo, So = oracle.quantize_nvfp4(Xb_all[rows], gs)
+    assert np.array_equal(Q[rows], Qo), "codes differ"
+    assert np.array_equal(S[rows], So), "scales differ"
+    assert bi.device_status() == bi.BI_OK
+
+
 def test_special_values_and_ties(bi):
     """Golden blocks from tests/golden (hand-worked): ties, saturation, zero
     and subnormal scales, and block F, whose three scaled values lie within
