@@ -181,6 +181,31 @@ def test_fused_gate_up_silu_equals_unfused(bi, layer_weights, T):
     assert bi.device_status() == bi.BI_OK
 
 
+def test_full_layer_at_the_bench_size_sampled(bi, layer_weights):
+    """The size the bench times (T=8192 tokens, the fused gate_up): eight
+    sampled tokens against the oracle chain, and each sampled token alone
+    gives the same bits."""
+    W1, W2, W1d, W2d = layer_weights
+    T = 8192
+    hidden = syn.to_bf16_bits(syn.normal_rows(8, syn.TID_HIDDEN, T, HID))
+    logits = logits_for(T, seed=8)
+    out, _ = gpu_layer(bi, hidden, logits, W1d, W2d, fused=True)
+    ids, w = oracle.moe_topk_softmax(logits, TOPK)
+    for t in [0, 1, 777, 4096, 6000, 8191]:
+        ys = []
+        for i in range(TOPK):
+            e = ids[t, i]
+            gu = oracle.bf16_round_array(oracle.gemm_bf16(hidden[t:t + 1], W1[e]))
+            act = oracle.bf16_round_array(oracle.silu_mul(gu))
+            ys.append(oracle.bf16_round_array(oracle.gemm_bf16(act, W2[e]))[0])
+        ref = oracle.moe_combine(np.stack(ys), np.arange(TOPK, dtype=np.int32)[None],
+                                 w[t:t + 1].astype(np.float32).astype(np.float64))[0]
+        assert_close_abs1(syn.bf16_bits_to_f32(out[t]).astype(np.float64), ref, 2e-2, f"token {t}")
+        alone, _ = gpu_layer(bi, hidden[t:t + 1], logits[t:t + 1], W1d, W2d, fused=True)
+        assert np.array_equal(alone[0], out[t]), f"token {t}: differs alone"
+    assert bi.device_status() == bi.BI_OK
+
+
 def test_fused_layer_equals_unfused_layer(bi, layer_weights):
     W1, W2, W1d, W2d = layer_weights
     T = 300
