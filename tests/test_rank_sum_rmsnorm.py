@@ -58,6 +58,34 @@ def test_rank_order_is_the_stated_one(bi, R, H):
     assert bi.device_status() == bi.BI_OK
 
 
+def test_rank_order_at_the_bench_size(bi):
+    """The size the bench times (R=4 parts of 16384 x 4096, residual in place):
+    every all-reduced value bit-exact against float32 additions in rank order,
+    the residual update bf16(a + residual) likewise, and the normalised rows
+    against the oracle on a sample."""
+    import torch
+    R, M, H = 4, 16384, 4096
+    g = torch.Generator(device="cuda").manual_seed(9)
+    pd = [torch.randn((M, H), device="cuda", generator=g).to(torch.bfloat16) for _ in range(R)]
+    rd = torch.randn((M, H), device="cuda", generator=g).to(torch.bfloat16)
+    _, _, w, _ = syn.rmsnorm_inputs(1, H, seed=10)
+    res0 = bits_of(rd)
+    a_out = torch.empty_like(pd[0])
+    out = bits_of(bi.rank_sum_rmsnorm(pd, to_dev_bf16(w), EPS, residual=rd, sum_out=a_out))
+    assert bi.device_status() == bi.BI_OK
+    P = np.stack([bits_of(t) for t in pd])
+    acc = np.zeros((M, H), dtype=np.float32)
+    for r in range(R):
+        acc = (acc + syn.bf16_bits_to_f32(P[r])).astype(np.float32)
+    a = syn.to_bf16_bits(acc)
+    assert np.array_equal(bits_of(a_out), a)
+    h = syn.to_bf16_bits((syn.bf16_bits_to_f32(a) + syn.bf16_bits_to_f32(res0)).astype(np.float32))
+    assert np.array_equal(bits_of(rd), h), "residual update"
+    rows = [0, 1, 4097, 8191, 16383]
+    y, _, _ = oracle.rank_sum_rmsnorm(P[:, rows], w, EPS, residual=res0[rows])
+    assert_close_rel(syn.bf16_bits_to_f32(out[rows]).astype(np.float64), y, 1.6e-2, 1e-6, "out")
+
+
 def test_one_rank_is_rmsnorm(bi):
     M, H = 300, 4096
     x, res, w, _ = syn.rmsnorm_inputs(M, H, seed=2)
