@@ -113,3 +113,59 @@ def test_nvfp4_chain_back_to_back_equals_synchronised(bi):
     assert np.isfinite(syn.bf16_bits_to_f32(a)).all()
     assert np.array_equal(a, b)
     assert bi.device_status() == bi.BI_OK
+
+
+def _capture(fn):
+    """Run fn once eagerly (loads the library), then capture it in a CUDA graph
+    and replay; returns (eager result, replayed result)."""
+    import torch
+    eager = fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g):
+            out = fn()
+    torch.cuda.current_stream().wait_stream(side)
+    g.replay()
+    torch.cuda.synchronize()
+    return eager, out, g
+
+
+def test_attention_and_moe_calls_replay_from_a_graph(bi):
+    """Decode attention (with a caller workspace), extend attention and a whole
+    MoE layer allocate nothing and synchronise nothing inside the library: captured
+    in a CUDA graph and replayed, they give the eager calls' bits."""
+    import torch
+    g_ = torch.Generator(device="cuda").manual_seed(11)
+    Hq, Hkv, D, bs = 32, 8, 128, 16
+    lens = torch.tensor([700, 33, 1000], dtype=torch.int32, device="cuda")
+    nb = 1000 // bs + 1
+    K = torch.randn((3 * nb, bs, Hkv, D), device="cuda", generator=g_).to(torch.bfloat16)
+    V = torch.randn((3 * nb, bs, Hkv, D), device="cuda", generator=g_).to(torch.bfloat16)
+    table = torch.randperm(3 * nb, device="cuda", generator=g_).to(torch.int32).view(3, nb)
+    q = torch.randn((3, Hq, D), device="cuda", generator=g_).to(torch.bfloat16)
+    ws = torch.empty(bi.attention_decode_workspace_size(3, Hq, 1000), dtype=torch.uint8, device="cuda")
+    dec = lambda: bi.attention_decode(q, K, V, table, lens, 1000, D ** -0.5, workspace=ws, O=torch.empty_like(q))
+    a, b, keep1 = _capture(dec)
+    assert np.array_equal(bits_of(a), bits_of(b))
+    cu = torch.tensor([0, 100, 133, 333], dtype=torch.int32, device="cuda")
+    Q = torch.randn((333, Hq, D), device="cuda", generator=g_).to(torch.bfloat16)
+    ext = lambda: bi.attention_extend(Q, cu, K, V, table, lens, 1000, 200, D ** -0.5)
+    a, b, keep2 = _capture(ext)
+    assert np.array_equal(bits_of(a), bits_of(b))
+    E, k, T, HID, INTER = 128, 8, 64, 2048, 768
+    hidden = torch.randn((T, HID), device="cuda", generator=g_).to(torch.bfloat16)
+    logits = torch.randn((T, E), device="cuda", generator=g_)
+    W1 = (0.02 * torch.randn((E, 2 * INTER, HID), device="cuda", generator=g_)).to(torch.bfloat16)
+    W2 = (0.02 * torch.randn((E, HID, INTER), device="cuda", generator=g_)).to(torch.bfloat16)
+
+    def layer():
+        ids, w = bi.moe_topk_softmax(logits, k)
+        off, rt, pos = bi.moe_align(ids, E)
+        act = bi.grouped_gemm_silu_bf16(bi.moe_gather(hidden, rt), W1, off)
+        return bi.moe_combine(bi.grouped_gemm_bf16(act, W2, off), pos, w)
+    a, b, keep3 = _capture(layer)
+    assert np.array_equal(bits_of(a), bits_of(b))
+    assert bi.device_status() == bi.BI_OK
