@@ -910,7 +910,7 @@ def run_ours(args, dist):
                "ms_per_step": round(ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "pipelining": "3 buffer sets; later steps' host-to-device copies and earlier steps' "
                              "device-to-host copies run on their own streams while a step computes; the "
-                             "host link moves the two directions one after the other (~200 GB/s each)"}
+                             "host link moves ~200 GB/s each way, ~320 GB/s with both directions at once"}
 
     breakdown = {}
     if not args.no_breakdown and dist.rank == 0:
@@ -944,6 +944,31 @@ def run_ours(args, dist):
                 roofline[key + "_frac_hbm_measured"] = r["frac_hbm_measured"]
                 roofline[key + "_frac_hbm_nominal_8tbs"] = r["frac_hbm_nominal_8tbs"]
                 roofline[key + "_us"] = r["us"]
+        # the other hot-path rows' headline figures, also as flat numbers
+        for r in breakdown["gemm_nvfp4"]["rows"]:
+            if r["M"] in (1, 4096):
+                roofline[f"nvfp4_M{r['M']}_us"] = r["us"]
+                roofline[f"nvfp4_M{r['M']}_tflops"] = r["tflops"]
+                if "cost_vs_cublaslt" in r:
+                    roofline[f"nvfp4_M{r['M']}_cost_vs_cublaslt"] = r["cost_vs_cublaslt"]
+        qmax = max(x["M"] for x in breakdown["quantize_nvfp4"])
+        for r in breakdown["quantize_nvfp4"]:
+            if r["M"] == qmax:
+                roofline[f"quantize_nvfp4_M{r['M']}_us"] = r["us"]
+                roofline[f"quantize_nvfp4_M{r['M']}_frac_hbm_measured"] = r["frac_hbm_measured"]
+        for r in breakdown["rank_sum_rmsnorm"]:
+            if r["M"] == max(RANK_SUM_M) and r["R"] == 4:
+                roofline["rank_sum_rmsnorm_R4_M%d_us" % r["M"]] = r["us"]
+                roofline["rank_sum_rmsnorm_R4_M%d_frac_hbm_measured" % r["M"]] = r["frac_hbm_measured"]
+        for r in breakdown["moe_layer"]:
+            roofline[f"moe_layer_T{r['T']}_us_fused"] = r["us_total_fused"]
+        for r in breakdown["attention_decode"]:
+            roofline[f"attention_decode_B{r['B']}_L{r['L']}_us"] = r["us"]
+            roofline[f"attention_decode_B{r['B']}_L{r['L']}_frac_hbm_measured"] = r["frac_hbm_measured"]
+        for r in breakdown["attention_extend"]:
+            key = f"attention_extend_{r['B']}x{r['new_tokens']}_cached{r['cached']}"
+            roofline[key + "_us"] = r["us"]
+            roofline[key + "_tflops"] = r["tflops"]
 
     cpu = None
     if dist.rank == 0 and not args.no_cpu:
