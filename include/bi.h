@@ -216,7 +216,7 @@ BI_API bi_status bi_moe_topk_softmax(const float *logits, int64_t T, int32_t E, 
  * row_token[r] = token of sorted row r (T*k entries); pos[t][i] = sorted row
  * of pair (t, i) (T*k entries). Deterministic (block scans, no atomics).
  * An id outside [0, E) is skipped and the device status becomes
- * BI_ERR_INVALID_ARG. Requirements: 1 <= E <= 1024, k >= 1.
+ * BI_ERR_INVALID_ARG. Requirements: 1 <= E <= 1024, k >= 1, T * k < 2^31 - 1.
  */
 BI_API bi_status bi_moe_align(const int32_t *topk_ids, int64_t T, int32_t k, int32_t E, int32_t *expert_offsets,
                               int32_t *row_token, int32_t *pos, bi_stream stream);
@@ -319,8 +319,14 @@ BI_API bi_status bi_rank_sum_rmsnorm(const void *const *parts, int32_t R, void *
  * is skipped, a block index outside [0, num_blocks) is ignored, and the device
  * status becomes BI_ERR_INVALID_ARG.
  * Requirements: head_dim == 128; Hq % Hkv == 0 and Hq / Hkv in {1, 2, 4, 8};
- * 1 <= B <= 65535; block_size >= 1; max_seq_len >= 1.
+ * 1 <= B <= 65535; block_size >= 1; 1 <= max_seq_len <= BI_ATTENTION_MAX_SEQ_LEN;
+ * workspace_bytes >= bi_attention_decode_workspace_size(B, Hq, max_seq_len).
+ * bi_attention_decode_workspace_size returns -1 for arguments out of range
+ * (B < 0, Hq < 1, max_seq_len outside [1, BI_ATTENTION_MAX_SEQ_LEN]) or a size
+ * that does not fit in an int64_t; bi_attention_decode then refuses the call
+ * with BI_ERR_INVALID_ARG.
  */
+#define BI_ATTENTION_MAX_SEQ_LEN (1 << 30)
 BI_API int64_t bi_attention_decode_workspace_size(int64_t B, int32_t Hq, int32_t max_seq_len);
 BI_API bi_status bi_attention_decode(const void *Q, const void *K_cache, const void *V_cache,
                                      const int32_t *block_table, int32_t max_blocks_per_seq, int64_t num_blocks,
@@ -358,7 +364,8 @@ BI_API bi_status bi_attention_decode(const void *Q, const void *K_cache, const v
  * seq_lens > max_seq_len or longer than its table, cu_q past total_q) is
  * skipped and the device status becomes BI_ERR_INVALID_ARG.
  * Requirements: head_dim == 128; Hq % Hkv == 0 and Hq / Hkv in {1, 2, 4, 8};
- * 1 <= B <= 65535; 1 <= max_q_len; block_size >= 1; max_seq_len >= 1.
+ * 1 <= B <= 65535; 1 <= max_q_len; block_size >= 1;
+ * 1 <= max_seq_len <= BI_ATTENTION_MAX_SEQ_LEN.
  */
 BI_API bi_status bi_attention_extend(const void *Q, const int32_t *cu_q, int32_t total_q, const void *K_cache,
                                      const void *V_cache, const int32_t *block_table, int32_t max_blocks_per_seq,
@@ -380,8 +387,9 @@ BI_API bi_status bi_attention_extend(const void *Q, const int32_t *cu_q, int32_t
  * BI_ATTENTION_NOALLOC_SCRATCH_BYTES (16 MiB) that the library keeps in device
  * memory, on every GPU that loads it, until the process exits.
  *  - A problem whose partial results need more than that
- *    (bi_attention_decode_workspace_size(B, Hq, max_seq_len) > 16 MiB) is
- *    refused with BI_ERR_UNSUPPORTED before anything is launched.
+ *    (bi_attention_decode_workspace_size(B, Hq, max_seq_len) > 16 MiB, or -1
+ *    for a size past int64_t) is refused with BI_ERR_UNSUPPORTED before
+ *    anything is launched.
  *  - The first call on a device looks up the array's device address (once
  *    per device, with that device current); make that first call before any
  *    stream capture.

@@ -226,7 +226,7 @@ bi_status bi_moe_topk_softmax(const float *logits, int64_t T, int32_t E, int32_t
 
 bi_status bi_moe_align(const int32_t *topk_ids, int64_t T, int32_t k, int32_t E, int32_t *expert_offsets,
                        int32_t *row_token, int32_t *pos, bi_stream stream) {
-    if (T < 0 || k < 1 || E < 1 || E > 1024 || T * k >= kI32Max) return BI_ERR_INVALID_ARG;
+    if (T < 0 || T >= kI32Max || k < 1 || E < 1 || E > 1024 || T * k >= kI32Max) return BI_ERR_INVALID_ARG;
     if (!topk_ids || !expert_offsets || !row_token || !pos) return BI_ERR_INVALID_ARG;
     if (!aligned4(topk_ids) || !aligned4(expert_offsets) || !aligned4(row_token) || !aligned4(pos))
         return BI_ERR_MISALIGNED;
@@ -297,7 +297,7 @@ bi_status bi_rank_sum_rmsnorm(const void *const *parts, int32_t R, void *residua
 }
 
 int64_t bi_attention_decode_workspace_size(int64_t B, int32_t Hq, int32_t max_seq_len) {
-    if (B < 0 || Hq < 1 || max_seq_len < 1) return -1;
+    if (B < 0 || Hq < 1 || max_seq_len < 1 || max_seq_len > BI_ATTENTION_MAX_SEQ_LEN) return -1;
     return attention_decode_workspace_bytes(B, Hq, max_seq_len);
 }
 
@@ -305,15 +305,16 @@ bi_status bi_attention_decode(const void *Q, const void *K_cache, const void *V_
                               int32_t max_blocks_per_seq, int64_t num_blocks, const int32_t *seq_lens, int64_t B,
                               int32_t Hq, int32_t Hkv, int32_t head_dim, int32_t block_size, int32_t max_seq_len,
                               float scale, void *workspace, int64_t workspace_bytes, void *O, bi_stream stream) {
-    if (B < 0 || B > 65535 || Hq < 1 || Hkv < 1 || block_size < 1 || max_seq_len < 1 || max_blocks_per_seq < 1 ||
-        num_blocks < 1 || !(scale == scale))
+    if (B < 0 || B > 65535 || Hq < 1 || Hkv < 1 || block_size < 1 || max_seq_len < 1 ||
+        max_seq_len > BI_ATTENTION_MAX_SEQ_LEN || max_blocks_per_seq < 1 || num_blocks < 1 || !(scale == scale))
         return BI_ERR_INVALID_ARG;
     if (B == 0) return BI_OK;
     if (!Q || !K_cache || !V_cache || !block_table || !seq_lens || !workspace || !O) return BI_ERR_INVALID_ARG;
     if (head_dim != 128 || Hq % Hkv != 0) return BI_ERR_UNSUPPORTED;
     const int32_t G = Hq / Hkv;
     if (G != 1 && G != 2 && G != 4 && G != 8) return BI_ERR_UNSUPPORTED;
-    if (workspace_bytes < attention_decode_workspace_bytes(B, Hq, max_seq_len)) return BI_ERR_INVALID_ARG;
+    const int64_t need = attention_decode_workspace_bytes(B, Hq, max_seq_len);
+    if (need < 0 || workspace_bytes < need) return BI_ERR_INVALID_ARG;
     if (!aligned16(Q) || !aligned16(K_cache) || !aligned16(V_cache) || !aligned16(O) || !aligned16(workspace) ||
         !aligned4(block_table) || !aligned4(seq_lens))
         return BI_ERR_MISALIGNED;
@@ -329,7 +330,8 @@ bi_status bi_attention_extend(const void *Q, const int32_t *cu_q, int32_t total_
                               int32_t head_dim, int32_t block_size, int32_t max_seq_len, int32_t max_q_len, float scale,
                               void *O, bi_stream stream) {
     if (B < 0 || B > 65535 || total_q < 0 || Hq < 1 || Hkv < 1 || block_size < 1 || max_seq_len < 1 ||
-        max_q_len < 1 || max_blocks_per_seq < 1 || num_blocks < 1 || !(scale == scale))
+        max_seq_len > BI_ATTENTION_MAX_SEQ_LEN || max_q_len < 1 || max_blocks_per_seq < 1 || num_blocks < 1 ||
+        !(scale == scale))
         return BI_ERR_INVALID_ARG;
     if (B == 0 || total_q == 0) return BI_OK;
     if (!Q || !cu_q || !K_cache || !V_cache || !block_table || !seq_lens || !O) return BI_ERR_INVALID_ARG;

@@ -952,8 +952,13 @@ attn_extend_kernel(const ExtParams p) {
 }  // namespace
 
 int64_t attention_decode_workspace_bytes(int64_t B, int32_t Hq, int32_t max_len) {
-    const int64_t chunks = (max_len + kChunk - 1) / kChunk;
-    return B * Hq * chunks * (kD + 2) * static_cast<int64_t>(sizeof(float));
+    if (B < 0 || Hq < 1 || max_len < 1) return -1;
+    const int64_t chunks = (static_cast<int64_t>(max_len) + kChunk - 1) / kChunk;
+    constexpr int64_t kRecord = (kD + 2) * static_cast<int64_t>(sizeof(float));   // (m, l, o) of one head and chunk
+    // -1 when the size does not fit in an int64_t
+    const int64_t records_max = INT64_MAX / kRecord;
+    if (B > records_max / Hq || B * Hq > records_max / chunks) return -1;
+    return B * Hq * chunks * kRecord;
 }
 
 template <int G, int SLOTS, int NG>
@@ -998,7 +1003,7 @@ bi_status launch_attention_decode(const void *Q, const void *K, const void *V, c
     p.Hq = Hq;
     p.Hkv = Hkv;
     p.bs = bs;
-    p.chunks = (max_len + kChunk - 1) / kChunk;
+    p.chunks = static_cast<int32_t>((static_cast<int64_t>(max_len) + kChunk - 1) / kChunk);
     p.max_len = max_len;
     p.scale = scale;
     p.status = device_status_word();
@@ -1131,8 +1136,8 @@ extern "C" bi_status bi_attention_decode_noalloc(const void *Q, const void *K_ca
                                                  int32_t Hkv, int32_t head_dim, int32_t block_size,
                                                  int32_t max_seq_len, float scale, void *O, bi_stream stream) {
     using namespace bi;
-    if (B < 0 || B > 65535 || Hq < 1 || Hkv < 1 || block_size < 1 || max_seq_len < 1 || max_blocks_per_seq < 1 ||
-        num_blocks < 1 || !(scale == scale))
+    if (B < 0 || B > 65535 || Hq < 1 || Hkv < 1 || block_size < 1 || max_seq_len < 1 ||
+        max_seq_len > BI_ATTENTION_MAX_SEQ_LEN || max_blocks_per_seq < 1 || num_blocks < 1 || !(scale == scale))
         return BI_ERR_INVALID_ARG;
     if (B == 0) return BI_OK;
     if (!Q || !K_cache || !V_cache || !block_table || !seq_lens || !O) return BI_ERR_INVALID_ARG;
@@ -1140,8 +1145,8 @@ extern "C" bi_status bi_attention_decode_noalloc(const void *Q, const void *K_ca
     const int32_t G = Hq / Hkv;
     if (G != 1 && G != 2 && G != 4 && G != 8) return BI_ERR_UNSUPPORTED;
     // the problem's partial results must fit in the fixed array
-    if (attention_decode_workspace_bytes(B, Hq, max_seq_len) > static_cast<int64_t>(kNoAllocScratchBytes))
-        return BI_ERR_UNSUPPORTED;
+    const int64_t need = attention_decode_workspace_bytes(B, Hq, max_seq_len);
+    if (need < 0 || need > static_cast<int64_t>(kNoAllocScratchBytes)) return BI_ERR_UNSUPPORTED;
     const auto a16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
     const auto a4 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; };
     if (!a16(Q) || !a16(K_cache) || !a16(V_cache) || !a16(O) || !a4(block_table) || !a4(seq_lens))

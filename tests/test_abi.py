@@ -173,6 +173,7 @@ def test_other_calls_reject_bad_arguments(lib):
     assert so.bi_moe_topk_softmax(FAKE, 4, 4, 8, 1, FAKE, FAKE, None) == 1               # k > E
     assert so.bi_moe_topk_softmax(FAKE, 0, 128, 8, 1, FAKE, FAKE, None) == 0             # empty
     assert so.bi_moe_align(FAKE + 2, 4, 8, 128, FAKE, FAKE, FAKE, None) == 3
+    assert so.bi_moe_align(FAKE, 1 << 61, 8, 128, FAKE, FAKE, FAKE, None) == 1          # T * k past 2^31 - 1
     assert so.bi_moe_gather(FAKE, 4, 100, FAKE, 8, FAKE, None) == 2                      # H % 8
     assert so.bi_silu_mul(FAKE, 4, 12, FAKE, None) == 2                                  # I % 8
     assert so.bi_moe_combine(FAKE, 8, FAKE, FAKE, 4, 0, 64, FAKE, None) == 1              # k < 1
@@ -192,5 +193,16 @@ def test_other_calls_reject_bad_arguments(lib):
     assert call(ok_args(Q=FAKE + 8)) == 3
     assert call(ok_args(B=0)) == 0
     assert so.bi_attention_decode_workspace_size(4, 32, 300) == 4 * 32 * 3 * 130 * 4   # ceil(300 / 128) chunks
+    # the longest sequence bound, and sizes past int64_t, give -1 and refuse the calls
+    assert so.bi_attention_decode_workspace_size(1, 1, 1 << 30) == (1 << 23) * 130 * 4
+    assert so.bi_attention_decode_workspace_size(1, 1, (1 << 30) + 1) == -1
+    assert so.bi_attention_decode_workspace_size(65535, 1 << 30, 1 << 30) == -1
+    assert call(ok_args(L=(1 << 30) + 1)) == 1
+    assert call(ok_args(B=65535, Hq=1 << 30, Hkv=1 << 27, L=1 << 30)) == 1
+    N = so.bi_attention_decode_noalloc
+    assert N(FAKE, FAKE, FAKE, FAKE, 8, 64, FAKE, 65535, 1 << 30, 1 << 27, 128, 16, 1 << 30, f(0.1), FAKE,
+             None) == 2
+    assert so.bi_attention_extend(FAKE, FAKE, 4, FAKE, FAKE, FAKE, 8, 64, FAKE, 4, 32, 8, 128, 16, (1 << 30) + 1, 4,
+                                  f(0.1), FAKE, None) == 1
     assert so.bi_check_wait_timeout(0, None) == 1
     assert so.bi_plan(99, 1, 1, 1, 152, ctypes.byref(lib.Plan())) == 1
