@@ -161,7 +161,9 @@ __device__ __forceinline__ bool seq_ok(const AttnParams &p, int64_t b, int &L) {
 //     alternate items (two items in compute while up to three load), one CTA
 //     per SM;
 //   - few items (at most two CTAs' worth per SM): SLOTS = 1, NG = 1, one item
-//     per CTA on all eight warps, two CTAs per SM.
+//     per CTA on all eight warps, two CTAs per SM; the V rows are counted on
+//     a second "full" barrier, so that the scores start as soon as K and q
+//     have landed.
 constexpr int kHalfTile = kChunk * 128;                  // one 64-dimension half of a K or V tile (swizzled)
 constexpr int kSlotBytes = 4 * kHalfTile + 8 * kRowBytes; // K, V, up to 8 q rows
 constexpr int kDecConsumers = kThreads / 32;             // 8 warps
@@ -171,7 +173,7 @@ template <int SLOTS>
 constexpr int dec_threads() { return kThreads + 32 * SLOTS; }   // + one loading warp per slot
 template <int SLOTS, int NG>
 constexpr int dec_smem() {
-    return 1024 + SLOTS * kSlotBytes + 2 * NG * kDecSFloats * 4 + SLOTS * kChunk + (NG + 1) * SLOTS * 8 + 16;
+    return 1024 + SLOTS * kSlotBytes + 2 * NG * kDecSFloats * 4 + SLOTS * kChunk + (2 * NG + 1) * SLOTS * 8 + 16;
 }
 static_assert(kSlotBytes % 1024 == 0, "slot alignment (128-byte swizzle atoms)");
 static_assert(2 * dec_smem<1, 1>() <= 232448, "two few-item CTAs per SM");
@@ -217,12 +219,19 @@ attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     // "empty" barrier per slot serves it; the items of a slot alternate
     // between the consumer groups, so each (slot, group) has its own "full"
     // barrier, whose phases are that group's items on that slot in order.
+    // With one item per CTA (kSlots = 1) the V rows have a "full" barrier of
+    // their own (fullV); the ring counts them with the K rows.
+    constexpr bool kSplitKV = kSlots == 1;
     uint64_t *full = reinterpret_cast<uint64_t *>(valid + kSlots * kChunk);   // [kSlots][NG]
-    uint64_t *empty = full + kSlots * NG;                                     // [kSlots]
+    uint64_t *fullV = full + kSlots * NG;                                     // [kSlots][NG], kSplitKV only
+    uint64_t *empty = fullV + kSlots * NG;                                    // [kSlots]
     volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + kSlots);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
-        for (int s = 0; s < kSlots * NG; ++s) mbar_init(&full[s], p.box_rows > 0 ? 32 : 64);
+        for (int s = 0; s < kSlots * NG; ++s) {
+            mbar_init(&full[s], p.box_rows > 0 ? 32 : 64);
+            mbar_init(&fullV[s], p.box_rows > 0 ? 32 : 64);
+        }
         for (int s = 0; s < kSlots; ++s) mbar_init(&empty[s], kDecConsumers / NG);
         *abort_flag = 0;
         fence_mbar_init();
@@ -313,6 +322,7 @@ attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             }
             const int slot = k % kSlots;
             uint64_t *fb = &full[slot * NG + k % NG];   // the consuming group's barrier for this slot
+            uint64_t *fbv = kSplitKV ? &fullV[slot * NG + k % NG] : fb;   // the one counting the V rows
             if (k >= kSlots && !mbar_wait(&empty[slot], ((k / kSlots) - 1) & 1, abort_flag)) {
                 if (lane == 0) {
                     atomicOr(p.status, kDevTimeout);
@@ -327,40 +337,70 @@ attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             for (int i = 0; i < kChunk / 32; ++i) valid[slot * kChunk + lane + 32 * i] = ok_row[i];
             const uint16_t *qsrc = p.Q + (b * p.Hq + g * G) * kD;
             if (p.box_rows > 0) {
+                // one box per cache block (box_rows tokens), both halves
+                const int kv_bytes = nbox * p.box_rows * 2 * 128;   // the K rows, or the V rows
+                const int tok = (j0 + lane * p.box_rows) % p.bs;
                 // V rows no box reaches (a chunk past the sequence's end) become
-                // zero, so that p = 0 meets finite values there
-                for (int r = nbox * p.box_rows + lane; r < kChunk; r += 32) {
+                // zero, so that p = 0 meets finite values there; each lane's
+                // arrival on the barrier counting the V rows releases its zeros
+                auto zero_v_tail = [&] {
+                    for (int r = nbox * p.box_rows + lane; r < kChunk; r += 32) {
 #pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        uint4 *v = reinterpret_cast<uint4 *>(Vs + half * kHalfTile + r * 128);
+                        for (int half = 0; half < 2; ++half) {
+                            uint4 *v = reinterpret_cast<uint4 *>(Vs + half * kHalfTile + r * 128);
 #pragma unroll
-                        for (int x = 0; x < 8; ++x) v[x] = make_uint4(0u, 0u, 0u, 0u);
+                            for (int x = 0; x < 8; ++x) v[x] = make_uint4(0u, 0u, 0u, 0u);
+                        }
                     }
-                }
-                fence_proxy_async_smem();             // before later bulk copies into these rows
-                // one box per cache block (box_rows tokens), both halves, K and V
-                const int nbox = (n + p.box_rows - 1) / p.box_rows;
+                    fence_proxy_async_smem();         // before later bulk copies into these rows
+                    __syncwarp();
+                };
+                if (!kSplitKV) zero_v_tail();
                 __syncwarp();
                 // each lane's arrival releases its shared-memory writes; lane 0
                 // also sets the bytes to expect, before any copy is issued
                 if (lane == 0)
-                    mbar_arrive_expect_tx(fb, nbox * p.box_rows * 4 * 128 + G * kRowBytes);
+                    mbar_arrive_expect_tx(fb, (kSplitKV ? 1 : 2) * kv_bytes + G * kRowBytes);
                 else
                     mbar_arrive(fb);
                 __syncwarp();
-                if (lane < nbox) {                    // a block outside the cache arrives as zeros
-                    const int tok = (j0 + lane * p.box_rows) % p.bs;
+                if (kSplitKV) {
+                    // q and K first: the scores need them before p.V needs V
+                    if (lane == 0) bulk_load(qs, qsrc, G * kRowBytes, fb);
+                    if (lane < nbox) {                // a block outside the cache arrives as zeros
 #pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        const int dst = half * kHalfTile + lane * p.box_rows * 128;
-                        tma_load_4d_hint(Ks + dst, &tmK, fb, half * 64, g, tok, box_blk, kv_policy);
-                        tma_load_4d_hint(Vs + dst, &tmV, fb, half * 64, g, tok, box_blk, kv_policy);
+                        for (int half = 0; half < 2; ++half)
+                            tma_load_4d_hint(Ks + half * kHalfTile + lane * p.box_rows * 128, &tmK, fb, half * 64, g,
+                                             tok, box_blk, kv_policy);
                     }
+                    zero_v_tail();
+                    if (lane == 0)
+                        mbar_arrive_expect_tx(fbv, kv_bytes);
+                    else
+                        mbar_arrive(fbv);
+                    __syncwarp();
+                    if (lane < nbox) {
+#pragma unroll
+                        for (int half = 0; half < 2; ++half)
+                            tma_load_4d_hint(Vs + half * kHalfTile + lane * p.box_rows * 128, &tmV, fbv, half * 64, g,
+                                             tok, box_blk, kv_policy);
+                    }
+                } else {
+                    // the ring consumes a slot whole: K and V boxes in turn, then q
+                    if (lane < nbox) {
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) {
+                            const int dst = half * kHalfTile + lane * p.box_rows * 128;
+                            tma_load_4d_hint(Ks + dst, &tmK, fb, half * 64, g, tok, box_blk, kv_policy);
+                            tma_load_4d_hint(Vs + dst, &tmV, fb, half * 64, g, tok, box_blk, kv_policy);
+                        }
+                    }
+                    if (lane == 0) bulk_load(qs, qsrc, G * kRowBytes, fb);
                 }
-                if (lane == 0) bulk_load(qs, qsrc, G * kRowBytes, fb);
             } else {
                 // 16-byte copies per row (rows without K/V zero-filled); each lane
-                // arrives twice: now, and once its copies have landed
+                // arrives twice: now, and once its copies have landed (both on
+                // the V rows' barrier too, when it has its own)
 #pragma unroll
                 for (int i = 0; i < kChunk / 32; ++i) {
                     const int t = lane + 32 * i;
@@ -373,6 +413,10 @@ attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                 for (int x = lane; x < G * kRowBytes / 16; x += 32) cp_async_16(smem_u32(qs) + x * 16, qsrc + x * 8, 16u);
                 mbar_arrive(fb);                      // releases this lane's row flags
                 asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(fb)) : "memory");
+                if (kSplitKV) {
+                    mbar_arrive(fbv);
+                    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(fbv)) : "memory");
+                }
             }
             last = k;
             ++k;
@@ -380,7 +424,10 @@ attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         // the copies of this warp's last item must land before the CTA exits
         // (the consumers normally waited for them already; every earlier item
         // of the slot was consumed before the slot was filled again)
-        if (last >= 0) mbar_wait(&full[(last % kSlots) * NG + last % NG], (last / (kSlots * NG)) & 1, nullptr);
+        if (last >= 0) {
+            mbar_wait(&full[(last % kSlots) * NG + last % NG], (last / (kSlots * NG)) & 1, nullptr);
+            if (kSplitKV) mbar_wait(&fullV[(last % kSlots) * NG + last % NG], (last / (kSlots * NG)) & 1, nullptr);
+        }
         return;
     }
 
@@ -475,7 +522,18 @@ attn_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                 wsh[h * ws_head + 1] = l;
             }
         }
-        group_sync<GW>(grp);
+        if (kSplitKV) {
+            const bool ok_v = mbar_wait(&fullV[slot * NG + grp], (k / (kSlots * NG)) & 1, abort_flag);
+            if (group_sync_or<GW>(grp, !ok_v)) {              // the V rows did not land
+                if (gw == 0 && lane == 0) {
+                    atomicOr(p.status, kDevTimeout);
+                    *abort_flag = 1;
+                }
+                break;
+            }
+        } else {
+            group_sync<GW>(grp);
+        }
 
         // values O[h][d] = sum_t p_t v_t[d] on the tensor cores: A = p (rows =
         // the G heads; p = hi + lo, two bf16 MMAs per step; zero past the

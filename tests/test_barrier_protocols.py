@@ -16,7 +16,9 @@ kernels cannot time out, so their protocols are checked here before they run.
    own item's data, no copy lands in a slot that is still being read. The
    earlier form (one "full" barrier per slot shared by both groups, two
    loading warps taking alternate items) is shown to break, which pins the
-   model to a fault it must catch.
+   model to a fault it must catch. (The one-item-per-CTA shape counts its V
+   rows on a second "full" barrier; it fills its one slot once, so no phase
+   of either barrier is reused.)
 """
 import random
 
