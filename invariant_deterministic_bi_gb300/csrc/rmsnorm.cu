@@ -17,10 +17,13 @@
 //
 // Memory: 128-bit loads and stores, coalesced (thread t reads bytes 16t ..
 // 16t+15 of each 16T-byte segment). With 4 vectors per thread at H = 4096 the
-// kernel needs few registers, so 16 CTAs (64 warps) fit on an SM and every SM
-// keeps ~256 KB of loads in flight. x and residual are streamed (evict-first);
-// the weight row stays cached.
+// kernel needs few registers, so 10 to 16 CTAs (40 to 64 warps) fit on an SM
+// and every SM keeps 160-256 KB of loads in flight. x and residual are
+// streamed (evict-first); the weight row stays cached, and its vectors are
+// loaded together with the row's where that pays (launch_one below).
 #include <cuda_bf16.h>
+
+#include <atomic>
 
 #include "bi_internal.h"
 #include "bi_ptx.cuh"
@@ -85,8 +88,11 @@ __device__ __forceinline__ float row_scale(float ss, int H, float eps, float *re
     return red[T / 32];
 }
 
-// One row per CTA; VPT vectors per thread (H <= 8 * T * VPT).
-template <int T, int VPT, bool RESIDUAL>
+// One row per CTA; VPT vectors per thread (H <= 8 * T * VPT). WPRE: the
+// thread's weight vectors are loaded with the row, so the scaling after the
+// reduction waits for no load (VPT more registers a thread); otherwise they
+// are loaded after the reduction.
+template <int T, int VPT, bool RESIDUAL, bool WPRE>
 __global__ void __launch_bounds__(T)
 rmsnorm_kernel(const uint4 *x, uint4 *residual, const uint4 *__restrict__ w, uint4 *out, int H, float eps) {
     grid_dep_wait();      // earlier work of the stream is complete and visible
@@ -97,7 +103,14 @@ rmsnorm_kernel(const uint4 *x, uint4 *residual, const uint4 *__restrict__ w, uin
     const int t = threadIdx.x;
     const uint4 *xr = x + row * nvec;
     uint4 *rr = RESIDUAL ? residual + row * nvec : nullptr;
-    uint4 h[VPT];
+    uint4 h[VPT], wv[VPT];
+    if (WPRE) {
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+            const int j = t + T * i;
+            if (j < nvec) wv[i] = __ldg(w + j);
+        }
+    }
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
         const int j = t + T * i;
@@ -120,7 +133,7 @@ rmsnorm_kernel(const uint4 *x, uint4 *residual, const uint4 *__restrict__ w, uin
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
         const int j = t + T * i;
-        if (j < nvec) __stcs(orow + j, scale(h[i], __ldg(w + j), r));
+        if (j < nvec) __stcs(orow + j, scale(h[i], WPRE ? wv[i] : __ldg(w + j), r));
     }
 }
 
@@ -237,12 +250,30 @@ RowShape row_shape(int64_t H) {
     return {512, vpt};
 }
 
+// The weight vectors loaded with the row (WPRE) shorten every row's path
+// after its reduction. Without the residual that pays at every M. With it the
+// extra registers lower the CTAs an SM holds, which costs more than it saves
+// once the rows no longer fit on the GPU at once, so the form is taken only
+// while they do. Which form runs changes no arithmetic.
 template <int T, int VPT, bool RES>
 bi_status launch_one(const void *x, void *residual, const void *w, void *out, int64_t M, int64_t H, float eps,
                      cudaStream_t s) {
-    return launch_pdl(rmsnorm_kernel<T, VPT, RES>, dim3(static_cast<unsigned>(M)), dim3(T), 0, s,
-                      static_cast<const uint4 *>(x), static_cast<uint4 *>(residual), static_cast<const uint4 *>(w),
-                      static_cast<uint4 *>(out), static_cast<int>(H), eps);
+    auto kernel = rmsnorm_kernel<T, VPT, RES, true>;
+    if constexpr (RES) {
+        static std::atomic<int> per_sm{0};           // resident CTAs of the WPRE form per SM
+        int n = per_sm.load(std::memory_order_relaxed);
+        if (n == 0) {
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, T, 0) != cudaSuccess || n < 1) n = 1;
+            per_sm.store(n, std::memory_order_relaxed);
+        }
+        int dev;
+        const DeviceInfo *info;
+        if (current_device(&dev, &info) != BI_OK) return BI_ERR_CUDA;
+        if (M > static_cast<int64_t>(n) * info->sm_count) kernel = rmsnorm_kernel<T, VPT, RES, false>;
+    }
+    return launch_pdl(kernel, dim3(static_cast<unsigned>(M)), dim3(T), 0, s, static_cast<const uint4 *>(x),
+                      static_cast<uint4 *>(residual), static_cast<const uint4 *>(w), static_cast<uint4 *>(out),
+                      static_cast<int>(H), eps);
 }
 
 template <bool RES>
