@@ -150,7 +150,10 @@ struct RankParts {
     const uint4 *p[kMaxRanks];
 };
 
-template <int T, int VPT, bool RESIDUAL>
+// PRE: the row's residual and weight vectors are loaded before the rank sum
+// (2 VPT more registers a thread), so after the sum no load waits; otherwise
+// the residual is loaded after the sum and the weights after the reduction.
+template <int T, int VPT, bool RESIDUAL, bool PRE>
 __global__ void __launch_bounds__(T)
 rank_sum_rmsnorm_kernel(const __grid_constant__ RankParts parts, int R, uint4 *residual, const uint4 *__restrict__ w, uint4 *sum_out,
                         uint4 *out, int H, float eps) {
@@ -165,7 +168,17 @@ rank_sum_rmsnorm_kernel(const __grid_constant__ RankParts parts, int R, uint4 *r
     // 8 vectors a thread, the rank loop is outside the row's vectors so that
     // each thread has VPT (twice that, unrolled) independent loads in flight
     // rather than one; longer rows keep one vector's sum at a time.
-    uint4 h[VPT];
+    uint4 h[VPT], rv[VPT], wv[VPT];
+    if (PRE) {
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+            const int j = t + T * i;
+            if (j < nvec) {
+                wv[i] = __ldg(w + j);
+                if (RESIDUAL) rv[i] = __ldcs(rr + j);
+            }
+        }
+    }
     auto finish = [&](int i, int j, const float (&acc)[8]) {
         uint4 a;
         a.x = pack_bf16x2(__float_as_uint(acc[0]), __float_as_uint(acc[1]));
@@ -173,7 +186,7 @@ rank_sum_rmsnorm_kernel(const __grid_constant__ RankParts parts, int R, uint4 *r
         a.z = pack_bf16x2(__float_as_uint(acc[4]), __float_as_uint(acc[5]));
         a.w = pack_bf16x2(__float_as_uint(acc[6]), __float_as_uint(acc[7]));
         if (sum_out) __stcs(sum_out + row * nvec + j, a);
-        h[i] = RESIDUAL ? add_round(a, __ldcs(rr + j)) : a;
+        h[i] = RESIDUAL ? add_round(a, PRE ? rv[i] : __ldcs(rr + j)) : a;
     };
     auto add8 = [](float (&acc)[8], const uint4 &v) {
         const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
@@ -230,7 +243,7 @@ rank_sum_rmsnorm_kernel(const __grid_constant__ RankParts parts, int R, uint4 *r
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
         const int j = t + T * i;
-        if (j < nvec) __stcs(orow + j, scale(h[i], __ldg(w + j), r));
+        if (j < nvec) __stcs(orow + j, scale(h[i], PRE ? wv[i] : __ldg(w + j), r));
     }
 }
 
@@ -250,26 +263,45 @@ RowShape row_shape(int64_t H) {
     return {512, vpt};
 }
 
-// The weight vectors loaded with the row (WPRE) shorten every row's path
-// after its reduction. Without the residual that pays at every M. With it the
-// extra registers lower the CTAs an SM holds, which costs more than it saves
-// once the rows no longer fit on the GPU at once, so the form is taken only
-// while they do. Which form runs changes no arithmetic.
+// Resident CTAs per SM of a kernel launched with T threads, queried once.
+template <typename Kernel>
+int resident_per_sm(Kernel kernel, int T, std::atomic<int> &cache) {
+    int n = cache.load(std::memory_order_relaxed);
+    if (n == 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, T, 0) != cudaSuccess || n < 1) n = 1;
+        cache.store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
+
+// Whether M rows take a kernel's early-load form `pre` (more registers, no
+// load after the reduction) over its plain form: always while all M rows'
+// CTAs fit on the GPU at once, where a row's latency is the time; beyond,
+// only when `pre` keeps at least 3/4 of the plain form's CTAs per SM (the
+// loads in flight that set the rate), and only if `ratio_ok` allows it.
+template <typename Kernel>
+bool take_pre(Kernel pre, Kernel plain, int T, int64_t M, bool ratio_ok, std::atomic<int> (&cache)[2]) {
+    int dev;
+    const DeviceInfo *info;
+    if (current_device(&dev, &info) != BI_OK) return false;
+    const int np = resident_per_sm(pre, T, cache[0]);
+    if (M <= static_cast<int64_t>(np) * info->sm_count) return true;
+    return ratio_ok && 4 * np >= 3 * resident_per_sm(plain, T, cache[1]);
+}
+
+// RMSNorm: the form with the weight vectors loaded with the row (WPRE) for up
+// to 8 vectors a thread; measured at H = 4096 it is faster at every M without
+// the residual (48 against 38 registers: 10 against 13 CTAs an SM) and slower
+// beyond one wave with it (56 against 32: 9 against 16). Which form runs
+// changes no arithmetic.
 template <int T, int VPT, bool RES>
 bi_status launch_one(const void *x, void *residual, const void *w, void *out, int64_t M, int64_t H, float eps,
                      cudaStream_t s) {
-    auto kernel = rmsnorm_kernel<T, VPT, RES, true>;
-    if constexpr (RES) {
-        static std::atomic<int> per_sm{0};           // resident CTAs of the WPRE form per SM
-        int n = per_sm.load(std::memory_order_relaxed);
-        if (n == 0) {
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, T, 0) != cudaSuccess || n < 1) n = 1;
-            per_sm.store(n, std::memory_order_relaxed);
-        }
-        int dev;
-        const DeviceInfo *info;
-        if (current_device(&dev, &info) != BI_OK) return BI_ERR_CUDA;
-        if (M > static_cast<int64_t>(n) * info->sm_count) kernel = rmsnorm_kernel<T, VPT, RES, false>;
+    auto kernel = rmsnorm_kernel<T, VPT, RES, false>;
+    if constexpr (VPT <= 8) {
+        static std::atomic<int> cache[2];
+        if (take_pre(rmsnorm_kernel<T, VPT, RES, true>, kernel, T, M, true, cache))
+            kernel = rmsnorm_kernel<T, VPT, RES, true>;
     }
     return launch_pdl(kernel, dim3(static_cast<unsigned>(M)), dim3(T), 0, s, static_cast<const uint4 *>(x),
                       static_cast<uint4 *>(residual), static_cast<const uint4 *>(w), static_cast<uint4 *>(out),
@@ -298,12 +330,23 @@ bi_status launch_res(const void *x, void *residual, const void *w, void *out, in
     }
 }
 
+// The rank sum's early-load form (PRE) for up to 8 vectors a thread and up to
+// 4 ranks, while all M rows' CTAs fit on the GPU at once; the same operations
+// either way. Measured at H = 4096, M = 1 and 128: R = 2 3.1 -> 1.85 and
+// 4.0 -> 2.4 us, R = 4 3.85 -> 3.1 and 3.9 -> 3.2 us, but R = 8 5.3 -> 5.6
+// and 8.2 -> 9.3 us (the longer rank loop then holds fewer loads in flight).
 template <int T, int VPT, bool RES>
 bi_status launch_rank_one(const RankParts &parts, int R, void *residual, const void *w, void *sum_out, void *out,
                           int64_t M, int64_t H, float eps, cudaStream_t s) {
-    return launch_pdl(rank_sum_rmsnorm_kernel<T, VPT, RES>, dim3(static_cast<unsigned>(M)), dim3(T), 0, s, parts, R,
-                      static_cast<uint4 *>(residual), static_cast<const uint4 *>(w), static_cast<uint4 *>(sum_out),
-                      static_cast<uint4 *>(out), static_cast<int>(H), eps);
+    auto kernel = rank_sum_rmsnorm_kernel<T, VPT, RES, false>;
+    if constexpr (VPT <= 8) {
+        static std::atomic<int> cache[2];
+        if (R <= 4 && take_pre(rank_sum_rmsnorm_kernel<T, VPT, RES, true>, kernel, T, M, false, cache))
+            kernel = rank_sum_rmsnorm_kernel<T, VPT, RES, true>;
+    }
+    return launch_pdl(kernel, dim3(static_cast<unsigned>(M)), dim3(T), 0, s, parts, R, static_cast<uint4 *>(residual),
+                      static_cast<const uint4 *>(w), static_cast<uint4 *>(sum_out), static_cast<uint4 *>(out),
+                      static_cast<int>(H), eps);
 }
 
 template <bool RES>

@@ -106,3 +106,25 @@ def test_rows_independent_and_repeatable(bi):
     outs = {bits_of(bi.rank_sum_rmsnorm([to_dev_bf16(P[r]) for r in range(R)], wd, EPS)).tobytes()
             for _ in range(8)}
     assert len(outs) == 1
+
+
+@pytest.mark.parametrize("R", [2, 4])
+@pytest.mark.parametrize("with_res", [False, True])
+def test_row_alone_equals_row_in_a_large_batch(bi, R, with_res):
+    """A row reduced alone (M = 1) and among M = 4097 rows gives the same bits,
+    output and updated residual: the two sizes launch the kernel's two forms
+    (the row's residual and weight vectors loaded before or after the rank
+    sum), which compute the same operations."""
+    M, H = 4097, 4096
+    P = parts_for(R, M, H, seed=7)
+    _, res, w, _ = syn.rmsnorm_inputs(M, H, seed=8)
+    wd = to_dev_bf16(w)
+    rd = to_dev_bf16(res) if with_res else None
+    full = bits_of(bi.rank_sum_rmsnorm([to_dev_bf16(P[r]) for r in range(R)], wd, EPS, residual=rd))
+    for i in (0, 2048, 4096):
+        r1 = to_dev_bf16(res[i:i + 1]) if with_res else None
+        one = bits_of(bi.rank_sum_rmsnorm([to_dev_bf16(P[r][i:i + 1]) for r in range(R)], wd, EPS, residual=r1))
+        assert np.array_equal(one[0], full[i]), f"row {i}"
+        if with_res:
+            assert np.array_equal(bits_of(r1)[0], bits_of(rd)[i]), f"residual row {i}"
+    assert bi.device_status() == bi.BI_OK
