@@ -944,6 +944,8 @@ def run_ours(args, dist):
                 roofline[key + "_frac_hbm_measured"] = r["frac_hbm_measured"]
                 roofline[key + "_frac_hbm_nominal_8tbs"] = r["frac_hbm_nominal_8tbs"]
                 roofline[key + "_us"] = r["us"]
+            elif r["M"] == 1:                       # one decode token: latency
+                roofline["rmsnorm_M1_H%d_%s_us" % (r["H"], "res" if r["residual"] else "nores")] = r["us"]
         # the other hot-path rows' headline figures, also as flat numbers
         for r in breakdown["gemm_nvfp4"]["rows"]:
             if r["M"] in (1, 4096):
@@ -960,8 +962,11 @@ def run_ours(args, dist):
             if r["M"] == max(RANK_SUM_M) and r["R"] == 4:
                 roofline["rank_sum_rmsnorm_R4_M%d_us" % r["M"]] = r["us"]
                 roofline["rank_sum_rmsnorm_R4_M%d_frac_hbm_measured" % r["M"]] = r["frac_hbm_measured"]
+            elif r["M"] == 1 and r["R"] == 4:
+                roofline["rank_sum_rmsnorm_R4_M1_us"] = r["us"]
         for r in breakdown["moe_layer"]:
             roofline[f"moe_layer_T{r['T']}_us_fused"] = r["us_total_fused"]
+            roofline[f"moe_layer_T{r['T']}_us_unfused"] = r["us_total"]
         for r in breakdown["attention_decode"]:
             roofline[f"attention_decode_B{r['B']}_L{r['L']}_us"] = r["us"]
             roofline[f"attention_decode_B{r['B']}_L{r['L']}_frac_hbm_measured"] = r["frac_hbm_measured"]
