@@ -613,23 +613,28 @@ attn_combine_kernel(const AttnParams p) {
     const int h = blockIdx.x;
     const int64_t b = blockIdx.y;
     const int d = threadIdx.x;
+    const float *w = p.ws + (b * p.Hq + h) * p.chunks * (kD + 2);
+    // The first tile's loads go out before the sequence length is known: the
+    // workspace holds p.chunks records a head, and records past the
+    // sequence's chunks are loaded but never used.
+    const int nt0 = min(kTile, p.chunks);
+    float ov0[kTile];
+#pragma unroll
+    for (int c = 0; c < kTile; ++c) ov0[c] = c < nt0 ? w[static_cast<int64_t>(c) * (kD + 2) + 2 + d] : 0.0f;
+    const float mc0 = d < nt0 ? w[static_cast<int64_t>(d) * (kD + 2)] : -INFINITY;
+    const float lc0 = d < nt0 ? w[static_cast<int64_t>(d) * (kD + 2) + 1] : 0.0f;
     int L;
     if (!seq_ok(p, b, L)) return;
     const int nc = (L + kChunk - 1) / kChunk;
     if (!BI_IN_BOUNDS(nc <= p.chunks, p.status)) return;   // debug build: inside the workspace
-    const float *w = p.ws + (b * p.Hq + h) * p.chunks * (kD + 2);
     float o = 0.0f, l = 0.0f, m_run = -INFINITY;           // m_run: warp 0's copy of the running maximum
-    for (int c0 = 0; c0 < nc; c0 += kTile) {
-        const int nt = min(kTile, nc - c0);
-        const float *oc = w + static_cast<int64_t>(c0) * (kD + 2) + 2 + d;
-        float ov[kTile];                                   // in flight while warp 0 prepares the factors
-#pragma unroll
-        for (int c = 0; c < kTile; ++c) ov[c] = c < nt ? oc[static_cast<int64_t>(c) * (kD + 2)] : 0.0f;
+    // merge chunks c0 .. c0 + nt - 1 (their o values in ov; (m_c, l_c) of
+    // chunk c0 + d in warp 0's lane d)
+    auto merge_tile = [&](const float (&ov)[kTile], int nt, float mc, float lc) {
         __syncthreads();                                   // previous tile fully consumed
         if (d < 32) {
-            const float *wc = w + static_cast<int64_t>(c0 + d) * (kD + 2);
-            const float mc = d < nt ? wc[0] : -INFINITY;
-            const float lc = d < nt ? wc[1] : 0.0f;
+            mc = d < nt ? mc : -INFINITY;
+            lc = d < nt ? lc : 0.0f;
             float incl = mc;                               // max(m_c0 .. m_c) over the tile
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
@@ -655,6 +660,18 @@ attn_combine_kernel(const AttnParams p) {
                 l = merge_value(l, fl[c], fa[c], fb[c]);
             }
         }
+    };
+    merge_tile(ov0, min(kTile, nc), mc0, lc0);
+    for (int c0 = kTile; c0 < nc; c0 += kTile) {
+        const int nt = min(kTile, nc - c0);
+        const float *oc = w + static_cast<int64_t>(c0) * (kD + 2) + 2 + d;
+        float ov[kTile];                                   // in flight while warp 0 prepares the factors
+#pragma unroll
+        for (int c = 0; c < kTile; ++c) ov[c] = c < nt ? oc[static_cast<int64_t>(c) * (kD + 2)] : 0.0f;
+        const float *wc = w + static_cast<int64_t>(c0 + d) * (kD + 2);
+        const float mc = d < nt ? wc[0] : -INFINITY;       // read by warp 0 only
+        const float lc = d < nt ? wc[1] : 0.0f;
+        merge_tile(ov, nt, mc, lc);
     }
     const float r = __fdiv_rn(o, l);
     const uint32_t packed = pack_bf16x2(__float_as_uint(r), 0u);
