@@ -169,3 +169,78 @@ def test_attention_and_moe_calls_replay_from_a_graph(bi):
     a, b, keep3 = _capture(layer)
     assert np.array_equal(bits_of(a), bits_of(b))
     assert bi.device_status() == bi.BI_OK
+
+
+_FIRST_CALLS_IN_A_CAPTURE = r'''
+import sys
+import torch
+sys.path.insert(0, sys.argv[1])
+import invariant_deterministic_bi_gb300 as bi
+
+gen = torch.Generator(device="cuda").manual_seed(5)
+
+
+def bf(*shape, std=1.0):
+    return (std * torch.randn(*shape, device="cuda", generator=gen)).to(torch.bfloat16)
+
+
+x1, r1, w, p0, p1, X = bf(1, 4096), bf(1, 4096), bf(4096), bf(1, 4096), bf(1, 4096), bf(1, 4096)
+W = bf(6144, 4096, std=0.02)
+Hq, Hkv, L, bs = 32, 8, 4096, 16
+K, V = bf(L // bs, bs, Hkv, 128), bf(L // bs, bs, Hkv, 128)
+table = torch.arange(L // bs, dtype=torch.int32, device="cuda").view(1, -1)
+lens = torch.tensor([L], dtype=torch.int32, device="cuda")
+q = bf(1, Hq, 128)
+ws = torch.empty(bi.attention_decode_workspace_size(1, Hq, L), dtype=torch.uint8, device="cuda")
+
+
+def buffers():
+    return (r1.clone(), [torch.empty(1, 4096, dtype=torch.bfloat16, device="cuda") for _ in range(2)],
+            torch.empty(1, 6144, dtype=torch.bfloat16, device="cuda"), torch.empty_like(q))
+
+
+def calls(rr, outs, y, o):
+    bi.rmsnorm(x1, w, 1e-6, residual=rr, out=outs[0])
+    bi.rank_sum_rmsnorm([p0, p1], w, 1e-6, out=outs[1])
+    bi.gemm_bf16(X, W, Y=y)
+    bi.attention_decode(q, K, V, table, lens, L, 128 ** -0.5, workspace=ws, O=o)
+
+
+a = buffers()
+g = torch.cuda.CUDAGraph()
+side = torch.cuda.Stream()
+side.wait_stream(torch.cuda.current_stream())
+with torch.cuda.stream(side):
+    with torch.cuda.graph(g):
+        calls(*a)                      # the library's first launches
+torch.cuda.current_stream().wait_stream(side)
+g.replay()
+torch.cuda.synchronize()
+b = buffers()
+calls(*b)
+torch.cuda.synchronize()
+
+
+def same(u, v):
+    return torch.equal(u.view(torch.int16), v.view(torch.int16))
+
+
+assert same(a[0], b[0]) and all(same(u, v) for u, v in zip(a[1], b[1])) and same(a[2], b[2]) and same(a[3], b[3])
+assert bi.device_status() == bi.BI_OK
+print("ok")
+'''
+
+
+def test_first_calls_of_a_process_inside_a_capture(bi):
+    """A process whose first RMSNorm, rank-sum RMSNorm, GEMM and decode
+    attention launches happen inside a CUDA graph capture (the library's
+    one-time host queries then run during the capture) replays them with the
+    bits of the same calls made eagerly afterwards. A fresh process, so no
+    earlier call has done the one-time work."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _FIRST_CALLS_IN_A_CAPTURE, root], capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stderr[-3000:]
