@@ -291,7 +291,7 @@ bool take_pre(Kernel pre, Kernel plain, int T, int64_t M, bool ratio_ok, std::at
 
 // RMSNorm: the form with the weight vectors loaded with the row (WPRE) for up
 // to 8 vectors a thread; measured at H = 4096 it is faster at every M without
-// the residual (48 against 38 registers: 10 against 13 CTAs an SM) and slower
+// the residual (48 against 38 registers: 10 against 12 CTAs an SM) and slower
 // beyond one wave with it (56 against 32: 9 against 16). Which form runs
 // changes no arithmetic.
 template <int T, int VPT, bool RES>
