@@ -244,3 +244,73 @@ def test_first_calls_of_a_process_inside_a_capture(bi):
     r = subprocess.run([sys.executable, "-c", _FIRST_CALLS_IN_A_CAPTURE, root], capture_output=True, text=True,
                        timeout=600)
     assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stderr[-3000:]
+
+
+_FIRST_MOE_NVFP4_EXTEND_CALLS_IN_A_CAPTURE = r'''
+import sys
+import torch
+sys.path.insert(0, sys.argv[1])
+import invariant_deterministic_bi_gb300 as bi
+
+gen = torch.Generator(device="cuda").manual_seed(6)
+
+
+def bf(*shape, std=1.0):
+    return (std * torch.randn(*shape, device="cuda", generator=gen)).to(torch.bfloat16)
+
+
+T, E, k, H, I = 16, 128, 8, 2048, 768
+logits = torch.randn(T, E, device="cuda", generator=gen)
+hidden = bf(T, H)
+W1, W2 = bf(E, 2 * I, H, std=0.02), bf(E, H, I, std=0.02)
+Xq, Wq = bf(16, 256), bf(512, 256)
+Hq, Hkv, bs = 32, 8, 16
+K, V = bf(64, bs, Hkv, 128), bf(64, bs, Hkv, 128)
+table = torch.arange(64, dtype=torch.int32, device="cuda").view(2, 32)
+lens = torch.tensor([300, 129], dtype=torch.int32, device="cuda")
+cu = torch.tensor([0, 100, 129], dtype=torch.int32, device="cuda")
+Qe = bf(129, Hq, 128)
+
+
+def calls():
+    ids, wts = bi.moe_topk_softmax(logits, k)
+    off, row_token, pos = bi.moe_align(ids, E)
+    xs = bi.moe_gather(hidden, row_token)
+    act = bi.grouped_gemm_silu_bf16(xs, W1, off)
+    y = bi.grouped_gemm_bf16(act, W2, off)
+    out = bi.moe_combine(y, pos, wts)
+    qa, sa = bi.quantize_nvfp4(Xq, 1.0)
+    qb, sb = bi.quantize_nvfp4(Wq, 1.0)
+    yq = bi.gemm_nvfp4(qa, sa, qb, sb, 1.0)
+    oe = bi.attention_extend(Qe, cu, K, V, table, lens, 300, 100, 128 ** -0.5)
+    return [out, yq, oe]
+
+
+g = torch.cuda.CUDAGraph()
+side = torch.cuda.Stream()
+side.wait_stream(torch.cuda.current_stream())
+with torch.cuda.stream(side):
+    with torch.cuda.graph(g):
+        a = calls()                    # the library's first launches
+torch.cuda.current_stream().wait_stream(side)
+g.replay()
+torch.cuda.synchronize()
+b = calls()
+torch.cuda.synchronize()
+assert all(torch.equal(u.view(torch.int16), v.view(torch.int16)) for u, v in zip(a, b))
+assert bi.device_status() == bi.BI_OK
+print("ok")
+'''
+
+
+def test_first_moe_nvfp4_and_extend_calls_of_a_process_inside_a_capture(bi):
+    """The same for a process whose first launches are a whole MoE layer
+    (routing, alignment, gather, fused gate_up, down, combine), the NVFP4
+    quantiser and GEMM, and extend attention."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _FIRST_MOE_NVFP4_EXTEND_CALLS_IN_A_CAPTURE, root], capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stderr[-3000:]
