@@ -63,7 +63,8 @@ topk_softmax_kernel(const float *__restrict__ logits, int64_t T, int E, int k, i
         const uint32_t u = __float_as_uint(v[j] == 0.0f ? 0.0f : v[j]);
         kv[j] = lane + 32 * j < E ? ((u & 0x80000000u) ? ~u : (u | 0x80000000u)) : 0u;   // 0: no expert
     }
-    float my_w = 0.0f, wsum = 0.0f;
+    float my_v = 0.0f;                         // lane i < k: the logit of rank i
+    int32_t my_id = 0;                         // lane i < k: the expert of rank i
     for (int i = 0; i < k; ++i) {
         uint32_t lk = 0u, le = 0x7fffffffu;
 #pragma unroll
@@ -79,13 +80,20 @@ topk_softmax_kernel(const float *__restrict__ logits, int64_t T, int E, int k, i
             for (int j = 0; j < MAXJ; ++j)
                 if (j == static_cast<int>(be >> 5)) kv[j] = 0u;   // taken
         }
-        const float bv = __uint_as_float((mk & 0x80000000u) ? (mk & 0x7fffffffu) : ~mk);
-        const float wi = __fdiv_rn(expf(bv - mx), s);
-        wsum += wi;
-        if (lane == i) my_w = wi;
-        if (lane == 0) ids[t * k + i] = static_cast<int32_t>(be);
+        if (lane == i) {
+            my_v = __uint_as_float((mk & 0x80000000u) ? (mk & 0x7fffffffu) : ~mk);
+            my_id = static_cast<int32_t>(be);
+        }
     }
-    if (lane < k) wout[t * k + lane] = renorm ? __fdiv_rn(my_w, wsum) : my_w;
+    // rank i's weight e^(v - max) / sum on lane i, then the weights' sum in
+    // rank order 0, 1, ..., k-1 (every lane adds the same values in turn)
+    const float my_w = lane < k ? __fdiv_rn(expf(my_v - mx), s) : 0.0f;
+    float wsum = 0.0f;
+    for (int i = 0; i < k; ++i) wsum += __shfl_sync(0xffffffffu, my_w, i);
+    if (lane < k) {
+        ids[t * k + lane] = my_id;
+        wout[t * k + lane] = renorm ? __fdiv_rn(my_w, wsum) : my_w;
+    }
 }
 
 // ------------------------------------------------------------- alignment
