@@ -199,6 +199,32 @@ align_rank_kernel(const int32_t *__restrict__ ids, int64_t P, int64_t seg, int S
 // and every thread places its pairs. Integer only: the same unique stable
 // order as the multi-block path.
 constexpr int kSmallAlign = 128;
+
+// Inclusive prefix sum of one int per thread over a block of 1024 threads:
+// shuffle scans inside each warp, then over the 32 warp totals (integer adds,
+// so the order does not matter). `wsum` holds 32 ints.
+__device__ __forceinline__ int block_inclusive_scan_1024(int v, int *wsum) {
+    const int t = threadIdx.x, lane = t & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += y;
+    }
+    if (lane == 31) wsum[t >> 5] = v;
+    __syncthreads();
+    if (t < 32) {
+        int w = wsum[t];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        wsum[t] = w;
+    }
+    __syncthreads();
+    return t >= 32 ? v + wsum[(t >> 5) - 1] : v;
+}
+
 __global__ void __launch_bounds__(1024)
 align_small_kernel(const int32_t *__restrict__ ids, int P, int k, int E, int32_t *__restrict__ offsets,
                    int32_t *__restrict__ row_token, int32_t *__restrict__ pos, unsigned *status) {
@@ -232,14 +258,9 @@ align_small_kernel(const int32_t *__restrict__ ids, int P, int k, int E, int32_t
         if (bad) atomicOr(status, kDevBadOffsets);
     }
     __syncthreads();
-    incl[t] = t < E ? cnt[t] : 0;
+    __shared__ int wsum[32];
+    incl[t] = block_inclusive_scan_1024(t < E ? cnt[t] : 0, wsum);
     __syncthreads();
-    for (int d = 1; d < 1024; d <<= 1) {      // Hillis-Steele: integer adds, order-free
-        const int add = t >= d ? incl[t - d] : 0;
-        __syncthreads();
-        incl[t] += add;
-        __syncthreads();
-    }
     if (t < E) offsets[t + 1] = incl[t];
     if (t == 0) offsets[0] = 0;
     for (int p = t; p < P; p += 1024) {
@@ -256,17 +277,10 @@ align_small_kernel(const int32_t *__restrict__ ids, int P, int k, int E, int32_t
 __global__ void __launch_bounds__(1024) align_scan_kernel(int32_t *offsets, int E) {
     grid_dep_wait();      // earlier work of the stream is complete and visible
     grid_dep_launch();
-    __shared__ int buf[1024];
+    __shared__ int wsum[32];
     const int i = threadIdx.x;
-    buf[i] = i < E ? offsets[i + 1] : 0;
-    __syncthreads();
-    for (int d = 1; d < 1024; d <<= 1) {      // Hillis-Steele: integer adds, order-free
-        const int add = i >= d ? buf[i - d] : 0;
-        __syncthreads();
-        buf[i] += add;
-        __syncthreads();
-    }
-    if (i < E) offsets[i + 1] = buf[i];
+    const int v = block_inclusive_scan_1024(i < E ? offsets[i + 1] : 0, wsum);
+    if (i < E) offsets[i + 1] = v;
 }
 
 // Step 3: pos = offsets[expert] + rank; row_token[pos] = token.
