@@ -153,7 +153,8 @@ struct RankParts {
 // PRE: the row's residual and weight vectors are loaded before the rank sum
 // (2 VPT more registers a thread), so after the sum no load waits; otherwise
 // the residual is loaded after the sum and the weights after the reduction.
-template <int T, int VPT, bool RESIDUAL, bool PRE>
+// UNR: ranks whose loads are in flight together (the rank loop's unrolling).
+template <int T, int VPT, bool RESIDUAL, bool PRE, int UNR>
 __global__ void __launch_bounds__(T)
 rank_sum_rmsnorm_kernel(const __grid_constant__ RankParts parts, int R, uint4 *residual, const uint4 *__restrict__ w, uint4 *sum_out,
                         uint4 *out, int H, float eps) {
@@ -202,7 +203,7 @@ rank_sum_rmsnorm_kernel(const __grid_constant__ RankParts parts, int R, uint4 *r
         for (int i = 0; i < VPT; ++i)
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[i][e] = 0.0f;
-#pragma unroll 2
+#pragma unroll UNR
         for (int r = 0; r < R; ++r) {
             uint4 v[VPT];
 #pragma unroll
@@ -330,19 +331,33 @@ bi_status launch_res(const void *x, void *residual, const void *w, void *out, in
     }
 }
 
-// The rank sum's early-load form (PRE) for up to 8 vectors a thread and up to
-// 4 ranks, while all M rows' CTAs fit on the GPU at once; the same operations
-// either way. Measured at H = 4096, M = 1 and 128: R = 2 3.1 -> 1.85 and
-// 4.0 -> 2.4 us, R = 4 3.85 -> 3.1 and 3.9 -> 3.2 us, but R = 8 5.3 -> 5.6
-// and 8.2 -> 9.3 us (the longer rank loop then holds fewer loads in flight).
+// The rank sum's forms. Large M: the plain form, two ranks' loads in flight.
+// While all M rows' CTAs fit on the GPU at once (a row's latency is the time;
+// up to 8 vectors a thread): R <= 2 the early-load form (PRE), R = 3..4 PRE
+// with four ranks' loads in flight, R > 4 the plain form with four. The same
+// operations in the same order either way. Measured at H = 4096 (M = 1 and
+// 128): R = 2 3.1 -> 1.75 and 4.0 -> 2.4 us; R = 4 3.85 -> 2.0 and 3.9 ->
+// 2.25 us; R = 8 5.1 -> 3.7 and 8.4 -> 5.5 us. Four ranks in flight at
+// M = 16384 cost 6-23 % (fewer CTAs an SM), and at R = 2 PRE with four was
+// slower than with two (1.97 against 1.75 us).
 template <int T, int VPT, bool RES>
 bi_status launch_rank_one(const RankParts &parts, int R, void *residual, const void *w, void *sum_out, void *out,
                           int64_t M, int64_t H, float eps, cudaStream_t s) {
-    auto kernel = rank_sum_rmsnorm_kernel<T, VPT, RES, false>;
+    auto kernel = rank_sum_rmsnorm_kernel<T, VPT, RES, false, 2>;
     if constexpr (VPT <= 8) {
-        static std::atomic<int> cache[2];
-        if (R <= 4 && take_pre(rank_sum_rmsnorm_kernel<T, VPT, RES, true>, kernel, T, M, false, cache))
-            kernel = rank_sum_rmsnorm_kernel<T, VPT, RES, true>;
+        if (R <= 2) {
+            static std::atomic<int> cache[2];
+            if (take_pre(rank_sum_rmsnorm_kernel<T, VPT, RES, true, 2>, kernel, T, M, false, cache))
+                kernel = rank_sum_rmsnorm_kernel<T, VPT, RES, true, 2>;
+        } else if (R <= 4) {
+            static std::atomic<int> cache[2];
+            if (take_pre(rank_sum_rmsnorm_kernel<T, VPT, RES, true, 4>, kernel, T, M, false, cache))
+                kernel = rank_sum_rmsnorm_kernel<T, VPT, RES, true, 4>;
+        } else {
+            static std::atomic<int> cache[2];
+            if (take_pre(rank_sum_rmsnorm_kernel<T, VPT, RES, false, 4>, kernel, T, M, false, cache))
+                kernel = rank_sum_rmsnorm_kernel<T, VPT, RES, false, 4>;
+        }
     }
     return launch_pdl(kernel, dim3(static_cast<unsigned>(M)), dim3(T), 0, s, parts, R, static_cast<uint4 *>(residual),
                       static_cast<const uint4 *>(w), static_cast<uint4 *>(sum_out), static_cast<uint4 *>(out),
