@@ -108,13 +108,14 @@ def test_rows_independent_and_repeatable(bi):
     assert len(outs) == 1
 
 
-@pytest.mark.parametrize("R", [2, 4])
+@pytest.mark.parametrize("R", [2, 4, 8])
 @pytest.mark.parametrize("with_res", [False, True])
 def test_row_alone_equals_row_in_a_large_batch(bi, R, with_res):
     """A row reduced alone (M = 1) and among M = 4097 rows gives the same bits,
-    output and updated residual: the two sizes launch the kernel's two forms
-    (the row's residual and weight vectors loaded before or after the rank
-    sum), which compute the same operations."""
+    output and updated residual: the two sizes launch different forms of the
+    kernel (the row's residual and weight vectors loaded before or after the
+    rank sum; two or four ranks' loads in flight), which compute the same
+    operations in the same order."""
     M, H = 4097, 4096
     P = parts_for(R, M, H, seed=7)
     _, res, w, _ = syn.rmsnorm_inputs(M, H, seed=8)
