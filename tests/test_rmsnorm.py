@@ -78,3 +78,19 @@ def test_special_rows(bi):
     assert np.all(y[0] == 0)
     assert np.all(y[1] == 1.0)
     assert np.all(y[2] == -1.0)
+
+
+@pytest.mark.parametrize("H", [264, 8192])
+def test_row_alone_equals_row_in_a_large_batch_other_widths(bi, H):
+    """A row normalised alone (M = 1) and among M = 4097 rows gives the same
+    bits, output and updated residual, at a ragged width (33 vectors of 8)
+    and a long one (8 vectors a thread): with the residual the two sizes run
+    the kernel's two forms (weight vectors loaded with the row or after the
+    reduction), which compute the same operations."""
+    M = 4097
+    x, res, w, _ = syn.rmsnorm_inputs(M, H, seed=H + 1)
+    out, h = _run(bi, x, w, res)
+    for i in (0, 2048, 4096):
+        o1, h1 = _run(bi, x[i:i + 1], w, res[i:i + 1])
+        assert np.array_equal(o1[0], out[i]), f"row {i}"
+        assert np.array_equal(h1[0], h[i]), f"residual row {i}"
